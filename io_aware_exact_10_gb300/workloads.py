@@ -1,0 +1,94 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the smoke check.
+
+This module holds no attention arithmetic: it only draws random tensors.  Both
+the CUDA path and the fp64 oracle are fed from it, so the oracle never sees a
+value produced by the GPU.
+
+Recipe (the same for every workload): one CPU ``torch.Generator`` seeded with
+``seed`` draws Q, K, V and dO, in that order, as fp32 N(0, 1) tensors of shape
+[B, H, N, d]; Q and K are multiplied by ``qk_std``; when ``boost_every`` is set,
+key rows j with (j + 1) % boost_every == 0 (the 97th, 194th, ... row of each
+head, counting from one) are multiplied by ``boost``; then every tensor is
+rounded to bf16 (round to nearest even).  The default scale is 1/sqrt(d).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    qk_std: float = 1.0
+    boost_every: int = 0
+    boost: float = 1.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def fwd_flops(self) -> float:
+        """4*B*H*N^2*d, halved when causal (two N^2 d contractions, 2 flop/MAC)."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        """Five N^2 d contractions in the backward: 2.5x the forward."""
+        return 2.5 * self.fwd_flops()
+
+
+# The workloads the library is measured and checked on.
+SINGLE_HEAD = Workload("single_head_N128_d64", 1, 1, 128, 64, causal=False)
+GPT2_MEDIUM = Workload("gpt2_medium_B64_H16_N1024_d64", 64, 16, 1024, 64, causal=False)
+GPT2_MEDIUM_CAUSAL = Workload("gpt2_medium_B64_H16_N1024_d64_causal", 64, 16, 1024, 64,
+                              causal=True)
+LONG_CAUSAL = Workload("long_causal_B4_H32_N8192_d128", 4, 32, 8192, 128, causal=True)
+STRESS_CAUSAL = Workload("stress_B8_H16_N4096_d128_causal", 8, 16, 4096, 128, causal=True,
+                         qk_std=4.0, boost_every=97, boost=8.0)
+STRESS = Workload("stress_B8_H16_N4096_d128", 8, 16, 4096, 128, causal=False,
+                  qk_std=4.0, boost_every=97, boost=8.0)
+
+SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384, 32768)
+SWEEP_D = (64, 128)
+
+
+def sweep(N: int, d: int, causal: bool = True) -> Workload:
+    """Sequence-length sweep point: H=16, B*N = 65536 tokens."""
+    return Workload(f"sweep_N{N}_d{d}" + ("_causal" if causal else ""),
+                    65536 // N, 16, N, d, causal=causal)
+
+
+def make_inputs(w: Workload, device: str = "cpu", with_grad: bool = True):
+    """Draw (q, k, v, dO) as bf16 [B, H, N, d] tensors following the recipe."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    out = []
+    names = ("q", "k", "v", "dO") if with_grad else ("q", "k", "v")
+    for name in names:
+        t = torch.randn(shape, generator=g, dtype=torch.float32)
+        if name in ("q", "k") and w.qk_std != 1.0:
+            t.mul_(w.qk_std)
+        if name == "k" and w.boost_every:
+            rows = torch.arange(w.N)
+            sel = ((rows + 1) % w.boost_every) == 0
+            t[:, :, sel, :] *= w.boost
+        out.append(t.to(torch.bfloat16).to(device))
+    return tuple(out)
+
+
+def random_bf16(shape, seed: int, std: float = 1.0, device: str = "cpu"):
+    """One bf16 tensor drawn N(0, std^2) from its own seeded CPU generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    t = torch.randn(shape, generator=g, dtype=torch.float32) * std
+    return t.to(torch.bfloat16).to(device)

@@ -1,0 +1,221 @@
+/*
+ * attention_oracle.c -- plain fp64 CPU oracle for exact softmax attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header or table with the CUDA
+ * kernels of the library.
+ *
+ * What it computes is the plain definition of attention, not the tiled
+ * algorithm.  The tiled method reaches the same numbers up to rounding order
+ * ("exact attention": FlashAttention: exact attention made fast by counting
+ * memory traffic, "The method"; FlashAttention and IO-aware exact attention,
+ * "Common misconceptions").  So the oracle is the definition written out:
+ *
+ *   s_ij  = scale * sum_c q_ic k_jc, and s_ij = -inf when causal and j > i
+ *           (Flash Attention, "The Memory Wall Problem", step 1: S = Q K^T;
+ *            the scale and the causal rule are the library's documented
+ *            reading of an argument the pages leave open)
+ *   m_i   = max_j s_ij,  e_ij = exp(s_ij - m_i),  l_i = sum_j e_ij,
+ *   p_ij  = e_ij / l_i
+ *           (Flash Attention, "Online Softmax Algorithm", safe softmax)
+ *   o_ic  = sum_j p_ij v_jc
+ *           (Flash Attention, "The Memory Wall Problem", step 3: O = P V)
+ *   lse_i = m_i + log(l_i)   -- natural log of sum_j exp(s_ij)
+ *           (FlashAttention and IO-aware exact attention, "Core ideas":
+ *            one log-sum-exp per row is what the forward keeps)
+ *
+ * Backward, for a loss L with dL/dO = dO given.  The pages say the backward
+ * recomputes P from Q, K, V and the row statistics (paper review, "The
+ * method"; "Backward by recomputation" in the curriculum note) but print no
+ * gradient formulas; these are the chain rule through the three steps above
+ * (softmax Jacobian), pinned in the tests by finite differences:
+ *
+ *   dv_jc = sum_i p_ij dO_ic
+ *   dp_ij = sum_c dO_ic v_jc
+ *   D_i   = sum_j p_ij dp_ij          (equal to sum_c dO_ic o_ic)
+ *   ds_ij = p_ij (dp_ij - D_i)
+ *   dq_ic = scale * sum_j ds_ij k_jc
+ *   dk_jc = scale * sum_i ds_ij q_ic
+ *
+ * Layout: every tensor is a dense fp64 array [BH][N][d] (d innermost); lse
+ * and the per-row statistics are [BH][N].  BH = B*H independent heads.
+ * Parallelism: OpenMP over (head, row) for the row-wise passes and over
+ * (head, key) for the key-wise pass.  No blocking, no online softmax, no
+ * reordering beyond the loops of the definition.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* number of threads the oracle will use (for reporting) */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* key j is visible to query i: everything when not causal, j <= i when causal */
+static int visible(int causal, long i, long j) { return !causal || j <= i; }
+
+/* s_ij = scale * q_i . k_j (no masking here; callers skip invisible keys) */
+static double score(const double *qi, const double *kj, int d, double scale) {
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += qi[c] * kj[c];
+    return scale * acc;
+}
+
+/* Row statistics of the safe softmax of row i: m_i and l_i. */
+static void row_stats(const double *q, const double *k, long i, int N, int d,
+                      double scale, int causal, double *m_out, double *l_out) {
+    const double *qi = q + i * (long)d;
+    double m = -INFINITY;
+    for (long j = 0; j < N; ++j) {
+        if (!visible(causal, i, j)) continue;
+        double s = score(qi, k + j * (long)d, d, scale);
+        if (s > m) m = s;
+    }
+    double l = 0.0;
+    for (long j = 0; j < N; ++j) {
+        if (!visible(causal, i, j)) continue;
+        l += exp(score(qi, k + j * (long)d, d, scale) - m);
+    }
+    *m_out = m;
+    *l_out = l;
+}
+
+/*
+ * Forward: o = softmax(scale Q K^T [masked]) V and lse, per head.
+ * q, k, v, o: [BH][N][d]; lse: [BH][N].
+ */
+void oracle_attn_fwd(const double *q, const double *k, const double *v,
+                     double *o, double *lse, int BH, int N, int d,
+                     double scale, int causal) {
+    const long hs = (long)N * d;
+#pragma omp parallel for collapse(2) schedule(dynamic, 4)
+    for (int h = 0; h < BH; ++h) {
+        for (int i = 0; i < N; ++i) {
+            const double *qh = q + h * hs, *kh = k + h * hs, *vh = v + h * hs;
+            double m, l;
+            row_stats(qh, kh, i, N, d, scale, causal, &m, &l);
+            double *oi = o + h * hs + (long)i * d;
+            for (int c = 0; c < d; ++c) oi[c] = 0.0;
+            for (long j = 0; j < N; ++j) {
+                if (!visible(causal, i, j)) continue;
+                double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m) / l;
+                const double *vj = vh + j * d;
+                for (int c = 0; c < d; ++c) oi[c] += p * vj[c];
+            }
+            lse[(long)h * N + i] = m + log(l);
+        }
+    }
+}
+
+/*
+ * Backward: dq, dk, dv of L with dL/dO = dO, per head.
+ * All tensor arguments [BH][N][d].  Forward quantities are recomputed here
+ * from q, k, v (the oracle takes nothing produced by the GPU path).
+ * D_out (may be NULL): [BH][N], receives D_i = sum_j p_ij dp_ij.
+ */
+void oracle_attn_bwd(const double *q, const double *k, const double *v,
+                     const double *dO, double *dq, double *dk, double *dv,
+                     double *D_out, int BH, int N, int d, double scale,
+                     int causal) {
+    const long hs = (long)N * d;
+    double *m = (double *)malloc(sizeof(double) * (size_t)BH * N);
+    double *l = (double *)malloc(sizeof(double) * (size_t)BH * N);
+    double *D = (double *)malloc(sizeof(double) * (size_t)BH * N);
+
+    /* Pass over query rows: row statistics, D_i, and dq_i. */
+#pragma omp parallel for collapse(2) schedule(dynamic, 4)
+    for (int h = 0; h < BH; ++h) {
+        for (int i = 0; i < N; ++i) {
+            const double *qh = q + h * hs, *kh = k + h * hs, *vh = v + h * hs;
+            const double *dOi = dO + h * hs + (long)i * d;
+            const long r = (long)h * N + i;
+            row_stats(qh, kh, i, N, d, scale, causal, &m[r], &l[r]);
+            /* D_i = sum_j p_ij dp_ij */
+            double Di = 0.0;
+            for (long j = 0; j < N; ++j) {
+                if (!visible(causal, i, j)) continue;
+                double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m[r]) / l[r];
+                double dp = 0.0;
+                for (int c = 0; c < d; ++c) dp += dOi[c] * vh[j * d + c];
+                Di += p * dp;
+            }
+            D[r] = Di;
+            /* dq_i = scale * sum_j ds_ij k_j */
+            double *dqi = dq + h * hs + (long)i * d;
+            for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+            for (long j = 0; j < N; ++j) {
+                if (!visible(causal, i, j)) continue;
+                double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m[r]) / l[r];
+                double dp = 0.0;
+                for (int c = 0; c < d; ++c) dp += dOi[c] * vh[j * d + c];
+                double ds = p * (dp - Di);
+                for (int c = 0; c < d; ++c) dqi[c] += scale * ds * kh[j * d + c];
+            }
+        }
+    }
+
+    /* Pass over keys: dv_j = sum_i p_ij dO_i, dk_j = scale * sum_i ds_ij q_i. */
+#pragma omp parallel for collapse(2) schedule(dynamic, 4)
+    for (int h = 0; h < BH; ++h) {
+        for (int j = 0; j < N; ++j) {
+            const double *qh = q + h * hs, *kh = k + h * hs, *vh = v + h * hs;
+            const double *dOh = dO + h * hs;
+            double *dvj = dv + h * hs + (long)j * d;
+            double *dkj = dk + h * hs + (long)j * d;
+            for (int c = 0; c < d; ++c) { dvj[c] = 0.0; dkj[c] = 0.0; }
+            for (long i = 0; i < N; ++i) {
+                if (!visible(causal, i, j)) continue;
+                const long r = (long)h * N + i;
+                double p = exp(score(qh + i * d, kh + (long)j * d, d, scale) - m[r]) / l[r];
+                double dp = 0.0;
+                for (int c = 0; c < d; ++c) dp += dOh[i * d + c] * vh[(long)j * d + c];
+                double ds = p * (dp - D[r]);
+                for (int c = 0; c < d; ++c) {
+                    dvj[c] += p * dOh[i * d + c];
+                    dkj[c] += scale * ds * qh[i * d + c];
+                }
+            }
+        }
+    }
+
+    if (D_out) {
+        for (long r = 0; r < (long)BH * N; ++r) D_out[r] = D[r];
+    }
+    free(m);
+    free(l);
+    free(D);
+}
+
+/*
+ * Forward for a chosen subset of query rows of one head (for sampled checks
+ * at sizes where the full oracle would take too long).  rows: [R] indices.
+ * q, k, v: [N][d] of that head; o: [R][d]; lse: [R].
+ */
+void oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
+                          const int *rows, int R, double *o, double *lse,
+                          int N, int d, double scale, int causal) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < R; ++t) {
+        const long i = rows[t];
+        double m, l;
+        row_stats(q, k, i, N, d, scale, causal, &m, &l);
+        double *oi = o + (long)t * d;
+        for (int c = 0; c < d; ++c) oi[c] = 0.0;
+        for (long j = 0; j < N; ++j) {
+            if (!visible(causal, i, j)) continue;
+            double p = exp(score(q + i * d, k + j * d, d, scale) - m) / l;
+            for (int c = 0; c < d; ++c) oi[c] += p * v[j * d + c];
+        }
+        lse[t] = m + log(l);
+    }
+}

@@ -1,0 +1,163 @@
+"""ctypes wrapper around the fp64 C oracle (``attention_oracle.c``).
+
+Test infrastructure only: see the package docstring.  Arrays are numpy fp64,
+shaped [..., N, d] (flattened to BH heads); lse is [..., N].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "attention_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+
+def compile_c(src: str, out: str) -> str:
+    """gcc -O2 (with OpenMP when the compiler has it) into a shared object."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", src, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``oracle/_build/liboracle.so``."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(SOURCE)):
+        return _LIB_PATH
+    return compile_c(SOURCE, _LIB_PATH)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _heads(a: np.ndarray):
+    N, d = a.shape[-2], a.shape[-1]
+    return a.reshape(-1, N, d), N, d
+
+
+class OracleLib:
+    """The oracle's entry points, bound to one compiled shared object."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int)
+        ci, cd = ctypes.c_int, ctypes.c_double
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, cd, ci]
+        lib.oracle_attn_fwd.restype = None
+        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
+                                        ci, ci, ci, cd, ci]
+        lib.oracle_attn_bwd.restype = None
+        lib.oracle_attn_fwd_rows.argtypes = [dp, dp, dp, ip, ci, dp, dp,
+                                             ci, ci, cd, ci]
+        lib.oracle_attn_fwd_rows.restype = None
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ci
+        self._lib = lib
+
+    def num_threads(self) -> int:
+        return int(self._lib.oracle_num_threads())
+
+    def attn_fwd(self, q, k, v, scale: float, causal: bool):
+        """o = softmax(scale * q k^T [causal]) v and lse (natural log), fp64.
+
+        q, k, v: [..., N, d].  Returns (o shaped like q, lse shaped [..., N]).
+        """
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        lead = q.shape[:-2]
+        qh, N, d = _heads(q)
+        kh, _, _ = _heads(k)
+        vh, _, _ = _heads(v)
+        BH = qh.shape[0]
+        o = np.empty_like(qh)
+        lse = np.empty((BH, N), dtype=np.float64)
+        self._lib.oracle_attn_fwd(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(o),
+                                  _ptr(lse), BH, N, d, float(scale),
+                                  int(bool(causal)))
+        return o.reshape(*lead, N, d), lse.reshape(*lead, N)
+
+    def attn_bwd(self, q, k, v, dO, scale: float, causal: bool,
+                 return_D: bool = False):
+        """Gradients (dq, dk, dv) of L with dL/dO = dO, fp64.
+
+        With ``return_D`` also returns D = rowsum(P * dP) shaped [..., N].
+        """
+        q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+        lead = q.shape[:-2]
+        qh, N, d = _heads(q)
+        kh, _, _ = _heads(k)
+        vh, _, _ = _heads(v)
+        dOh, _, _ = _heads(dO)
+        BH = qh.shape[0]
+        dq = np.empty_like(qh)
+        dk = np.empty_like(qh)
+        dv = np.empty_like(qh)
+        D = np.empty((BH, N), dtype=np.float64)
+        self._lib.oracle_attn_bwd(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(dOh),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(D),
+                                  BH, N, d, float(scale), int(bool(causal)))
+        out = (dq.reshape(*lead, N, d), dk.reshape(*lead, N, d),
+               dv.reshape(*lead, N, d))
+        if return_D:
+            return out + (D.reshape(*lead, N),)
+        return out
+
+    def attn_fwd_rows(self, q, k, v, rows, scale: float, causal: bool):
+        """Forward for selected query rows of ONE head: q, k, v are [N, d].
+
+        Returns (o [R, d], lse [R]) for the rows listed in ``rows``.
+        """
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        N, d = q.shape
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        R = rows.shape[0]
+        o = np.empty((R, d), dtype=np.float64)
+        lse = np.empty((R,), dtype=np.float64)
+        self._lib.oracle_attn_fwd_rows(
+            _ptr(q), _ptr(k), _ptr(v),
+            rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), R,
+            _ptr(o), _ptr(lse), N, d, float(scale), int(bool(causal)))
+        return o, lse
+
+
+_default = None
+
+
+def default() -> OracleLib:
+    global _default
+    if _default is None:
+        _default = OracleLib(build())
+    return _default
+
+
+def num_threads() -> int:
+    return default().num_threads()
+
+
+def attn_fwd(q, k, v, scale, causal):
+    return default().attn_fwd(q, k, v, scale, causal)
+
+
+def attn_bwd(q, k, v, dO, scale, causal, return_D=False):
+    return default().attn_bwd(q, k, v, dO, scale, causal, return_D)
+
+
+def attn_fwd_rows(q, k, v, rows, scale, causal):
+    return default().attn_fwd_rows(q, k, v, rows, scale, causal)

@@ -1,0 +1,327 @@
+"""Checks that pin the fp64 oracle to facts other than itself.
+
+Each function takes an ``oracle.OracleLib`` and raises AssertionError when the
+oracle disagrees with a closed form, an invariant, brute force, an independent
+formulation or a library routine.  ``test_oracle_pins.py`` runs them on the
+real oracle; ``test_oracle_mutants.py`` runs them on oracles with planted
+mistakes and expects at least one of them to fail for every mistake.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def read_four_scores():
+    """Parse tests/golden/four_scores.txt into {key: [hand values...]}."""
+    out = {}
+    with open(os.path.join(GOLDEN, "four_scores.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            key = line.split()[0]
+            out[key] = line
+    scores = [float(x) for x in out["scores"].split()[1:]]
+    hand = {}
+    for key in ("block1_sum", "final_sum", "lse"):
+        hand[key] = float(out[key].split()[-1])
+    hand["softmax"] = [float(x) for x in out["softmax"].split()[-4:]]
+    return scores, hand
+
+
+# ----------------------------------------------------------------------------
+# forward pins
+# ----------------------------------------------------------------------------
+
+def check_four_scores(orc):
+    """The worked four-score example: oracle softmax row and LSE equal the
+    closed forms, which equal the hand values to 4 digits, and the online
+    recurrence over the two blocks reaches the same sum."""
+    x, hand = read_four_scores()
+    e = math.exp
+    final_sum = 1 + e(-1) + e(-2) + e(-3)
+    soft = [e(xi - 4) / final_sum for xi in x]
+    lse = 4 + math.log(final_sum)
+    # closed forms against the hand values written in the golden file
+    assert abs((1 + e(-1)) - hand["block1_sum"]) < 1e-4
+    assert abs(final_sum - hand["final_sum"]) < 1e-4
+    assert np.allclose(soft, hand["softmax"], atol=1e-4)
+    assert abs(lse - hand["lse"]) < 1e-4
+    # the recurrence of the page on the two blocks
+    m, s = -math.inf, 0.0
+    for blk in ((1.0, 2.0), (3.0, 4.0)):
+        for xi in blk:
+            m_new = max(m, xi)
+            s = s * (e(m - m_new) if m > -math.inf else 0.0) + e(xi - m_new)
+            m = m_new
+        if blk == (1.0, 2.0):
+            assert m == 2.0 and abs(s - (1 + e(-1))) < 1e-15
+    assert m == 4.0 and abs(s - final_sum) < 1e-15
+    # the oracle: d = 4, q_i = e_0, k_j = x_j e_0, v_j = e_j, so o_i = p_i
+    N = d = 4
+    q = np.zeros((N, d)); q[:, 0] = 1.0
+    k = np.zeros((N, d)); k[:, 0] = x
+    v = np.eye(N)
+    o, l = orc.attn_fwd(q, k, v, 1.0, False)
+    for i in range(N):
+        assert np.allclose(o[i], soft, rtol=0, atol=1e-14)
+        assert abs(l[i] - lse) < 1e-13
+
+
+def check_rows_sum_to_one(orc):
+    """With V = I (N <= d) the output is P itself: rows sum to 1, entries >= 0,
+    causal entries above the diagonal are exactly 0.  With V = ones, O = 1."""
+    r = _rng(1)
+    for causal in (False, True):
+        N, d = 16, 16
+        q, k = r.normal(size=(2, N, d)), r.normal(size=(2, N, d))
+        v = np.broadcast_to(np.eye(N), (2, N, d)).copy()
+        P, _ = orc.attn_fwd(q, k, v, 0.3, causal)
+        assert np.all(P >= 0)
+        assert np.allclose(P.sum(-1), 1.0, atol=1e-14)
+        if causal:
+            assert np.all(np.triu(P[0], 1) == 0) and np.all(np.triu(P[1], 1) == 0)
+        N, d = 40, 8
+        q, k = r.normal(size=(N, d)), r.normal(size=(N, d))
+        o, _ = orc.attn_fwd(q, k, np.ones((N, d)), 0.5, causal)
+        assert np.allclose(o, 1.0, atol=1e-13)
+
+
+def check_softmax_of_scores(orc):
+    """O = P with V = I equals the textbook softmax of scale*q.k computed by
+    brute force in numpy, and LSE equals log(sum(exp)) of the same scores."""
+    r = _rng(2)
+    for causal in (False, True):
+        N, d, scale = 12, 12, 0.7
+        q, k = r.normal(size=(N, d)), r.normal(size=(N, d))
+        P, lse = orc.attn_fwd(q, k, np.eye(N), scale, causal)
+        for i in range(N):
+            s = [scale * sum(q[i, c] * k[j, c] for c in range(d))
+                 for j in range(N) if (not causal or j <= i)]
+            ex = [math.exp(t) for t in s]
+            tot = sum(ex)
+            assert np.allclose(P[i, :len(ex)], [t / tot for t in ex], atol=1e-14)
+            assert abs(lse[i] - math.log(tot)) < 1e-12
+
+
+def check_identical_keys(orc):
+    """All k_j equal: p_ij = 1/N, O_i = mean_j V_j, LSE_i = scale q_i.k + ln N;
+    causal: O_i = mean_{j<=i} V_j, LSE_i = scale q_i.k + ln(i+1)."""
+    r = _rng(3)
+    N, d, scale = 24, 8, 0.25
+    q = r.normal(size=(N, d))
+    k = np.tile(r.normal(size=(1, d)), (N, 1))
+    v = r.normal(size=(N, d))
+    o, lse = orc.attn_fwd(q, k, v, scale, False)
+    assert np.allclose(o, v.mean(0, keepdims=True), atol=1e-13)
+    assert np.allclose(lse, scale * q @ k[0] + math.log(N), atol=1e-12)
+    o, lse = orc.attn_fwd(q, k, v, scale, True)
+    pref = np.cumsum(v, 0) / np.arange(1, N + 1)[:, None]
+    assert np.allclose(o, pref, atol=1e-13)
+    assert np.allclose(lse, scale * q @ k[0] + np.log(np.arange(1, N + 1)),
+                       atol=1e-12)
+
+
+def check_causal_row0(orc):
+    """Causal row 0 sees key 0 only: O_0 = V_0, LSE_0 = scale q_0.k_0."""
+    r = _rng(4)
+    N, d, scale = 32, 16, 0.125
+    q, k, v = (r.normal(size=(N, d)) for _ in range(3))
+    o, lse = orc.attn_fwd(q, k, v, scale, True)
+    assert np.allclose(o[0], v[0], atol=1e-15)
+    assert abs(lse[0] - scale * float(q[0] @ k[0])) < 1e-13
+
+
+def check_zero_queries(orc):
+    """Q = 0: all scores 0, O = column mean of V, LSE = ln N (causal: prefix)."""
+    r = _rng(5)
+    N, d = 20, 6
+    q = np.zeros((N, d))
+    k, v = r.normal(size=(N, d)), r.normal(size=(N, d))
+    o, lse = orc.attn_fwd(q, k, v, 1.0, False)
+    assert np.allclose(o, v.mean(0, keepdims=True), atol=1e-13)
+    assert np.allclose(lse, math.log(N), atol=1e-13)
+    o, lse = orc.attn_fwd(q, k, v, 1.0, True)
+    assert np.allclose(o, np.cumsum(v, 0) / np.arange(1, N + 1)[:, None], atol=1e-13)
+    assert np.allclose(lse, np.log(np.arange(1, N + 1)), atol=1e-13)
+
+
+def check_dominant_key(orc):
+    """One key whose score exceeds every other by >= 60: O_i = V_{j*} to
+    within e^-60 * N * max|V|, LSE_i = s_{i j*} up to the same."""
+    r = _rng(6)
+    N, d = 16, 4
+    q = np.zeros((N, d)); q[:, 0] = 1.0
+    k = r.uniform(-1, 1, size=(N, d)); k[:, 0] = r.uniform(-1, 1, size=N)
+    jstar = 11
+    k[jstar, 0] = 62.0
+    v = r.normal(size=(N, d))
+    o, lse = orc.attn_fwd(q, k, v, 1.0, False)
+    assert np.allclose(o, v[jstar][None, :], atol=1e-20 + N * math.exp(-60) * 4)
+    assert np.allclose(lse, 62.0, atol=1e-20 + N * math.exp(-60))
+
+
+def _online_blocked(q, k, v, scale, causal, bounds):
+    """Independent blocked forward: the per-block recurrence with an
+    unnormalised output and one final divide, per query row (Flash Attention,
+    "Core Flash Attention Algorithm", in the one-divide form its Flash
+    Attention 2 section describes).  Pure numpy, no oracle code."""
+    N, d = q.shape
+    o = np.zeros((N, d))
+    lse = np.zeros(N)
+    for i in range(N):
+        m, l, acc = -np.inf, 0.0, np.zeros(d)
+        for lo, hi in zip(bounds[:-1], bounds[1:]):
+            js = [j for j in range(lo, hi) if not causal or j <= i]
+            if not js:
+                continue
+            s = scale * (k[js] @ q[i])
+            m_new = max(m, s.max())
+            alpha = math.exp(m - m_new) if m > -np.inf else 0.0
+            p = np.exp(s - m_new)
+            l = l * alpha + p.sum()
+            acc = acc * alpha + p @ v[js]
+            m = m_new
+        o[i] = acc / l
+        lse[i] = m + math.log(l)
+    return o, lse
+
+
+def check_blocked_online_softmax(orc):
+    """Block-sum invariant: any partition of the keys into blocks, run through
+    the online recurrence, reproduces the oracle to 1e-12 (Flash Attention,
+    "Mathematical Correctness")."""
+    r = _rng(7)
+    for causal in (False, True):
+        for trial in range(4):
+            N, d = int(r.integers(5, 40)), int(r.integers(1, 9))
+            q, k, v = (r.normal(size=(N, d)) * 2 for _ in range(3))
+            cuts = sorted(set(r.integers(1, N, size=int(r.integers(0, 6))).tolist()))
+            bounds = [0] + cuts + [N]
+            ob, lb = _online_blocked(q, k, v, 0.6, causal, bounds)
+            o, l = orc.attn_fwd(q, k, v, 0.6, causal)
+            assert np.allclose(o, ob, atol=1e-12, rtol=0)
+            assert np.allclose(l, lb, atol=1e-12, rtol=0)
+
+
+def check_multi_head_independent(orc):
+    """Heads are independent: a [B, H] batch equals each head run alone."""
+    r = _rng(8)
+    B, H, N, d = 2, 3, 10, 4
+    q, k, v = (r.normal(size=(B, H, N, d)) for _ in range(3))
+    o, lse = orc.attn_fwd(q, k, v, 0.5, True)
+    for b in range(B):
+        for h in range(H):
+            o1, l1 = orc.attn_fwd(q[b, h], k[b, h], v[b, h], 0.5, True)
+            assert np.array_equal(o1, o[b, h]) and np.array_equal(l1, lse[b, h])
+
+
+def check_rows_entry(orc):
+    """The sampled-rows entry equals the full forward on those rows."""
+    r = _rng(9)
+    N, d = 33, 8
+    q, k, v = (r.normal(size=(N, d)) for _ in range(3))
+    rows = [0, 5, 17, 32]
+    for causal in (False, True):
+        o, lse = orc.attn_fwd(q, k, v, 0.4, causal)
+        o_r, l_r = orc.attn_fwd_rows(q, k, v, rows, 0.4, causal)
+        assert np.allclose(o_r, o[rows], atol=1e-14)
+        assert np.allclose(l_r, lse[rows], atol=1e-14)
+
+
+def check_torch_sdpa_fwd(orc):
+    """torch's CPU scaled_dot_product_attention in fp64 (a library routine
+    sharing no code with the oracle) agrees to 1e-12."""
+    import torch
+    import torch.nn.functional as F
+    r = _rng(10)
+    for causal in (False, True):
+        B, H, N, d = 2, 2, 37, 16
+        q, k, v = (r.normal(size=(B, H, N, d)) for _ in range(3))
+        o, _ = orc.attn_fwd(q, k, v, 0.3, causal)
+        ot = F.scaled_dot_product_attention(
+            torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v),
+            is_causal=causal, scale=0.3).numpy()
+        assert np.allclose(o, ot, atol=1e-12, rtol=0)
+
+
+# ----------------------------------------------------------------------------
+# backward pins
+# ----------------------------------------------------------------------------
+
+def _loss(orc, q, k, v, dO, scale, causal):
+    o, _ = orc.attn_fwd(q, k, v, scale, causal)
+    return float((o * dO).sum())
+
+
+def check_finite_differences(orc):
+    """Central differences of L = sum(dO * O) w.r.t. every entry of Q, K, V on
+    tiny shapes agree with the analytic gradients to 1e-6 relative."""
+    r = _rng(11)
+    h = 1e-6
+    for causal in (False, True):
+        for N, d in ((1, 1), (2, 2), (3, 4), (5, 1), (8, 2)):
+            q, k, v, dO = (r.normal(size=(N, d)) for _ in range(4))
+            scale = 0.9
+            g = orc.attn_bwd(q, k, v, dO, scale, causal)
+            for which, x in enumerate((q, k, v)):
+                num = np.zeros_like(x)
+                for idx in np.ndindex(x.shape):
+                    xp, xm = x.copy(), x.copy()
+                    xp[idx] += h
+                    xm[idx] -= h
+                    args_p = [q, k, v]; args_p[which] = xp
+                    args_m = [q, k, v]; args_m[which] = xm
+                    num[idx] = (_loss(orc, *args_p, dO, scale, causal)
+                                - _loss(orc, *args_m, dO, scale, causal)) / (2 * h)
+                err = np.abs(num - g[which]).max()
+                ref = max(np.abs(num).max(), 1e-3)
+                assert err / ref < 1e-6, (causal, N, d, which, err, ref)
+
+
+def check_gradient_invariants(orc):
+    """sum_j dk_j = 0 (softmax ignores a shift of all keys), sum_j dv_j =
+    sum_i dO_i (rows of P sum to 1), and D_i = dO_i . o_i."""
+    r = _rng(12)
+    for causal in (False, True):
+        B, H, N, d = 1, 2, 30, 8
+        q, k, v, dO = (r.normal(size=(B, H, N, d)) for _ in range(4))
+        dq, dk, dv, D = orc.attn_bwd(q, k, v, dO, 0.5, causal, return_D=True)
+        o, _ = orc.attn_fwd(q, k, v, 0.5, causal)
+        assert np.allclose(dk.sum(-2), 0.0, atol=1e-12)
+        assert np.allclose(dv.sum(-2), dO.sum(-2), atol=1e-12)
+        assert np.allclose(D, (dO * o).sum(-1), atol=1e-12)
+
+
+def check_torch_autograd(orc):
+    """torch autograd through fp64 CPU scaled_dot_product_attention agrees with
+    the oracle's gradients to 1e-11."""
+    import torch
+    import torch.nn.functional as F
+    r = _rng(13)
+    for causal in (False, True):
+        B, H, N, d = 1, 2, 29, 8
+        q, k, v, dO = (r.normal(size=(B, H, N, d)) for _ in range(4))
+        tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (q, k, v))
+        out = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=0.35)
+        out.backward(torch.from_numpy(dO))
+        dq, dk, dv = orc.attn_bwd(q, k, v, dO, 0.35, causal)
+        assert np.allclose(dq, tq.grad.numpy(), atol=1e-11, rtol=0)
+        assert np.allclose(dk, tk.grad.numpy(), atol=1e-11, rtol=0)
+        assert np.allclose(dv, tv.grad.numpy(), atol=1e-11, rtol=0)
+
+
+FWD_CHECKS = (check_four_scores, check_rows_sum_to_one, check_softmax_of_scores,
+              check_identical_keys, check_causal_row0, check_zero_queries,
+              check_dominant_key, check_blocked_online_softmax,
+              check_multi_head_independent, check_rows_entry, check_torch_sdpa_fwd)
+BWD_CHECKS = (check_finite_differences, check_gradient_invariants, check_torch_autograd)
+ALL_CHECKS = FWD_CHECKS + BWD_CHECKS

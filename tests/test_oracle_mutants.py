@@ -1,0 +1,56 @@
+"""Planted mistakes in the oracle must be caught by its pins (CPU only).
+
+Each case copies ``oracle/attention_oracle.c``, makes one plausible mistake in
+the copy (a dropped term, a wrong sign, a wrong index, a transposed operand, a
+wrong mask), compiles it to a temporary shared object and runs the pin checks
+on it.  The case passes when at least one pin fails on the mutant.  The real
+oracle source is never modified.
+"""
+import pytest
+
+import oracle
+from oracle_pin_checks import ALL_CHECKS
+
+MUTANTS = {
+    # forward
+    "max_wrong_direction": ("if (s > m) m = s;", "if (s < m) m = s;"),
+    "scale_dropped": ("return scale * acc;", "return acc;"),
+    "lse_sign": ("lse[(long)h * N + i] = m + log(l);", "lse[(long)h * N + i] = m - log(l);"),
+    "lse_log_dropped": ("lse[(long)h * N + i] = m + log(l);", "lse[(long)h * N + i] = m + l;"),
+    "value_row_index": ("const double *vj = vh + j * d;", "const double *vj = vh + i * d;"),
+    "causal_off_by_one": ("return !causal || j <= i;", "return !causal || j < i;"),
+    "causal_transposed": ("return !causal || j <= i;", "return !causal || j >= i;"),
+    "normaliser_dropped": (
+        "double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m) / l;",
+        "double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m);"),
+    # backward
+    "ds_D_sign": ("double ds = p * (dp - Di);", "double ds = p * (dp + Di);"),
+    "ds_D_dropped": ("double ds = p * (dp - Di);", "double ds = p * dp;"),
+    "dk_scale_dropped": ("dkj[c] += scale * ds * qh[i * d + c];", "dkj[c] += ds * qh[i * d + c];"),
+    "dv_transposed": ("dvj[c] += p * dOh[i * d + c];", "dvj[c] += p * dOh[(long)j * d + c];"),
+    "dq_wrong_operand": ("dqi[c] += scale * ds * kh[j * d + c];",
+                         "dqi[c] += scale * ds * qh[j * d + c];"),
+    "dp_transposed_in_key_pass": (
+        "dp += dOh[i * d + c] * vh[(long)j * d + c];",
+        "dp += dOh[(long)j * d + c] * vh[i * d + c];"),
+    "key_pass_D_dropped": ("double ds = p * (dp - D[r]);", "double ds = p * dp;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new)
+    c_path = tmp_path / f"mutant_{name}.c"
+    c_path.write_text(mutated)
+    lib = oracle.OracleLib(oracle.compile_c(str(c_path), str(tmp_path / f"mutant_{name}.so")))
+    failed = []
+    for check in ALL_CHECKS:
+        try:
+            check(lib)
+        except AssertionError:
+            failed.append(check.__name__)
+            break
+    assert failed, f"no pin caught the planted mistake {name}"
