@@ -1,0 +1,128 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * The library computes exact softmax attention FlashAttention-style: Q and
+ * K/V are tiled, an online softmax keeps a running row max and normaliser,
+ * and the N x N score matrix never reaches device memory.  Sources for the
+ * operations:
+ *   - attention itself: S = Q K^T, P = softmax(S), O = P V
+ *     (Flash Attention, ostralyan.com, "The Memory Wall Problem");
+ *   - the tiled, single-pass computation with running statistics
+ *     (FlashAttention: exact attention made fast by counting memory traffic,
+ *     "The method"; Flash Attention, "Online Softmax Algorithm" and
+ *     "Block-Wise Attention Computation");
+ *   - one log-sum-exp per row kept by the forward, and the backward that
+ *     recomputes P block by block from Q, K, V and that statistic
+ *     (FlashAttention and IO-aware exact attention, "Core ideas").
+ *
+ * Conventions shared by every entry point
+ *   - Tensors q, k, v, o, dO, dq, dk, dv are DEVICE pointers to contiguous
+ *     bf16 arrays of shape [B][H][N][d] (d innermost).  lse is a device
+ *     pointer to fp32 [B][H][N].  Every pointer must be 16-byte aligned.
+ *   - d must be 64 or 128.  N >= 1 is any length (the last tile is masked).
+ *     B, H >= 1.  B == 0, H == 0 or N == 0 is an empty problem: FA_OK, no work.
+ *   - scale multiplies Q K^T before the softmax; it must be finite and > 0
+ *     (usually 1/sqrt(d)).
+ *   - causal = 1: key j is visible to query i iff j <= i (N_q = N_k = N).
+ *     causal = 0: every key is visible.
+ *   - lse[i] = ln( sum over visible j of exp(scale * q_i . k_j) ).
+ *   - The caller owns every buffer, including the backward workspace.  The
+ *     library allocates no device memory per call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and run on the current device, which must be sm_103
+ *     (GB300).  Argument errors are reported before anything is launched.
+ *     A kernel whose internal pipeline wait exceeds the wait bound gives up
+ *     cleanly and records FA_ERR_TIMEOUT in a per-device error word that
+ *     fa_last_device_error() reads.
+ *   - Thread safety: calls on distinct streams may come from distinct host
+ *     threads.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st*` */
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, scale or flag */
+  FA_ERR_UNSUPPORTED = 2, /* d not in {64,128}, or device is not sm_103 */
+  FA_ERR_LAUNCH = 3,      /* a CUDA runtime call or kernel launch failed */
+  FA_ERR_TIMEOUT = 4,     /* a kernel gave up on a pipeline wait */
+  FA_ERR_NO_DEVICE = 5,   /* no CUDA device is current */
+  FA_ERR_DEVICE = 6       /* the stream reported an asynchronous CUDA error */
+} fa_status;
+
+/*
+ * Forward: o = softmax(scale * q k^T [causal]) v, and lse.
+ * Outputs o ([B][H][N][d] bf16) and lse ([B][H][N] fp32) are overwritten.
+ * Source: Flash Attention, "Core Flash Attention Algorithm" (tiled forward
+ * with running max and sum); FlashAttention and IO-aware exact attention,
+ * "Core ideas" (one log-sum-exp per row; only O and the row statistic are
+ * written).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, struct CUstream_st* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: fp32 D = rowsum(dO * o) of shape
+ * [B][H][N] followed by an fp32 dQ accumulator of shape [B][H][N][d], each
+ * region rounded up to 256 bytes.  0 for an empty problem or invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward: given dO = dL/do, writes dq, dk, dv (bf16 [B][H][N][d],
+ * overwritten).  o and lse must be the outputs of fa_fwd with the same
+ * q, k, v, B, H, N, d, scale and causal.  P is recomputed block by block
+ * from q, k and lse; no N x N matrix is stored (FlashAttention: exact
+ * attention made fast by counting memory traffic, "The method";
+ * FlashAttention and IO-aware exact attention, "Backward by recomputation").
+ * The gradient formulas are the chain rule through the softmax:
+ *   D_i = sum_c dO_ic o_ic,  dS_ij = P_ij (dO_i . v_j - D_i),
+ *   dq = scale dS k,  dk = scale dS^T q,  dv = P^T dO.
+ * workspace: device pointer, 256-byte aligned, at least
+ * fa_bwd_workspace_size(B, H, N, d) bytes; its contents on entry are
+ * ignored and on exit are unspecified.  Smaller => FA_ERR_INVALID_ARG.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, void* workspace, size_t workspace_bytes,
+                 struct CUstream_st* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up on a wait), or
+ * FA_ERR_DEVICE when the synchronisation itself reported a CUDA error.
+ */
+fa_status fa_last_device_error(struct CUstream_st* stream);
+
+/*
+ * Raw error word of the last recorded device error on the current device
+ * (code | site << 8 | block << 32), without clearing it; 0 if none.
+ * Synchronises `stream` first.  For diagnostics.
+ */
+unsigned long long fa_device_error_word(struct CUstream_st* stream);
+
+/*
+ * Bound, in nanoseconds, on every internal pipeline wait of kernels launched
+ * after this call (process-wide).  0 restores the default of 2 seconds.
+ */
+void fa_set_wait_timeout_ns(unsigned long long ns);
+
+/* Static description of a status code. */
+const char* fa_strerror(int status);
+
+/* Library version string. */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,130 @@
+"""Thin ctypes binding of the C ABI in ``include/fa.h``.
+
+Argument marshalling only: every step of the attention path runs in the CUDA
+kernels of ``libfa_gb300.so``.  The functions keep the C names.  Tensor
+arguments may be torch tensors (their ``data_ptr()`` is passed) or raw device
+addresses (ints).  There is no fallback: if the library has not been built,
+loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_LAUNCH = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_NO_DEVICE = 5
+FA_ERR_DEVICE = 6
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    """A non-zero fa_status returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({fa_strerror(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with `python -m io_aware_exact_10_gb300.build` "
+                "(the library has no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_fwd.restype = i
+        L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+        L.fa_bwd_workspace_size.restype = sz
+        L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+        L.fa_bwd.restype = i
+        L.fa_last_device_error.argtypes = [vp]
+        L.fa_last_device_error.restype = i
+        L.fa_device_error_word.argtypes = [vp]
+        L.fa_device_error_word.restype = ctypes.c_ulonglong
+        L.fa_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        L.fa_set_wait_timeout_ns.restype = None
+        L.fa_strerror.argtypes = [i]
+        L.fa_strerror.restype = ctypes.c_char_p
+        L.fa_version.argtypes = []
+        L.fa_version.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    """A torch stream, a raw cudaStream_t (int) or None (torch's current stream)."""
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def fa_strerror(status: int) -> str:
+    return lib().fa_strerror(int(status)).decode()
+
+
+def fa_version() -> str:
+    return lib().fa_version().decode()
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream=None, check=True) -> int:
+    """fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> status."""
+    s = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
+                     int(d), float(scale), int(causal), _stream(stream))
+    if check:
+        _check(s, "fa_fwd")
+    return s
+
+
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    return int(lib().fa_bwd_workspace_size(int(B), int(H), int(N), int(d)))
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+           workspace_bytes, stream=None, check=True) -> int:
+    """fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal,
+    workspace, workspace_bytes, stream) -> status."""
+    s = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                     _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), float(scale),
+                     int(causal), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if check:
+        _check(s, "fa_bwd")
+    return s
+
+
+def fa_last_device_error(stream=None) -> int:
+    return int(lib().fa_last_device_error(_stream(stream)))
+
+
+def fa_device_error_word(stream=None) -> int:
+    return int(lib().fa_device_error_word(_stream(stream)))
+
+
+def fa_set_wait_timeout_ns(ns: int) -> None:
+    lib().fa_set_wait_timeout_ns(int(ns))

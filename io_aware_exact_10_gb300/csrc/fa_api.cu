@@ -1,0 +1,264 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument validation,
+// tensor-map encoding, per-device state and kernel launches.  No device
+// memory is allocated here; the only device-resident state is one error word
+// per device (a file-scope __device__ variable).
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+
+namespace {
+
+__device__ unsigned long long g_fa_error_word;
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+
+struct DeviceState {
+  std::once_flag once;
+  bool supported = false;
+  unsigned long long* err = nullptr;  // device address of g_fa_error_word
+  cudaError_t init_error = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+std::atomic<unsigned long long> g_timeout_ns{0};
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+unsigned long long timeout_ns() {
+  unsigned long long t = g_timeout_ns.load(std::memory_order_relaxed);
+  if (t) return t;
+  static const unsigned long long env = [] {
+    const char* s = std::getenv("FA_WAIT_TIMEOUT_MS");
+    if (!s) return 0ull;
+    const double ms = std::atof(s);
+    return ms > 0 ? (unsigned long long)(ms * 1e6) : 0ull;
+  }();
+  return env ? env : kDefaultTimeoutNs;
+}
+
+// Resolve the current device: sm_103 check and the error word's address.
+fa_status current_device(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return FA_ERR_NO_DEVICE;
+  }
+  if (dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  DeviceState& st = g_dev[dev];
+  std::call_once(st.once, [&st, dev] {
+    cudaDeviceProp prop;
+    if ((st.init_error = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return;
+    st.supported = prop.major == 10 && prop.minor == 3;
+    void* p = nullptr;
+    if ((st.init_error = cudaGetSymbolAddress(&p, g_fa_error_word)) != cudaSuccess) return;
+    st.err = static_cast<unsigned long long*>(p);
+  });
+  if (st.init_error != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  if (!st.supported) return FA_ERR_UNSUPPORTED;
+  *out = &st;
+  return FA_OK;
+}
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode != nullptr;
+}
+
+// bf16 [BH][N][d] viewed as a 3-D tensor (d, N, BH); box of 64 columns x 128
+// rows, 128-byte swizzle (the layout the tcgen05 descriptors expect).
+bool encode_bf16_3d(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared validation of sizes and scalars.  *empty is set for a zero-size problem.
+fa_status check_common(int B, int H, int N, int d, float scale, int causal, bool* empty) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  *empty = (B == 0 || H == 0 || N == 0);
+  if (*empty) return FA_OK;
+  const long long BH = (long long)B * H;
+  if (BH > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;   // grid x
+  if ((N + 127) / 128 > 65535 * 2) return FA_ERR_INVALID_ARG;  // grid y
+  return FA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, struct CUstream_st* stream) {
+  bool empty = false;
+  fa_status s = check_common(B, H, N, d, scale, causal, &empty);
+  if (s != FA_OK || empty) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  if ((s = current_device(&dev)) != FA_OK) return s;
+  if (!get_encoder()) return FA_ERR_LAUNCH;
+  fa::FwdLaunch a;
+  const int BH = B * H;
+  if (!encode_bf16_3d(&a.tq, q, BH, N, d) || !encode_bf16_3d(&a.tk, k, BH, N, d) ||
+      !encode_bf16_3d(&a.tv, v, BH, N, d))
+    return FA_ERR_INVALID_ARG;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal;
+  a.ctl.err = dev->err;
+  a.ctl.timeout_ns = timeout_ns();
+  if (fa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  bool empty = false;
+  if (check_common(B, H, N, d, 1.0f, 0, &empty) != FA_OK || empty) return 0;
+  const size_t rows = (size_t)B * H * N;
+  return round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, void* workspace, size_t workspace_bytes,
+                 struct CUstream_st* stream) {
+  bool empty = false;
+  fa_status s = check_common(B, H, N, d, scale, causal, &empty);
+  if (s != FA_OK || empty) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < fa_bwd_workspace_size(B, H, N, d))
+    return FA_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  if ((s = current_device(&dev)) != FA_OK) return s;
+  if (!get_encoder()) return FA_ERR_LAUNCH;
+  fa::BwdLaunch a;
+  const int BH = B * H;
+  if (!encode_bf16_3d(&a.tq, q, BH, N, d) || !encode_bf16_3d(&a.tk, k, BH, N, d) ||
+      !encode_bf16_3d(&a.tv, v, BH, N, d) || !encode_bf16_3d(&a.tdo, dO, BH, N, d))
+    return FA_ERR_INVALID_ARG;
+  const size_t rows = (size_t)BH * N;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.D = static_cast<float*>(workspace);
+  a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)));
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal;
+  a.ctl.err = dev->err;
+  a.ctl.timeout_ns = timeout_ns();
+  if (fa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
+unsigned long long fa_device_error_word(struct CUstream_st* stream) {
+  DeviceState* dev = nullptr;
+  if (current_device(&dev) != FA_OK) return 0;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  unsigned long long w = 0;
+  if (cudaMemcpy(&w, dev->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return w;
+}
+
+fa_status fa_last_device_error(struct CUstream_st* stream) {
+  DeviceState* dev = nullptr;
+  fa_status s = current_device(&dev);
+  if (s != FA_OK) return s;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_DEVICE;
+  }
+  unsigned long long w = 0;
+  if (cudaMemcpy(&w, dev->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_DEVICE;
+  }
+  if (w == 0) return FA_OK;
+  const unsigned long long zero = 0;
+  if (cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_DEVICE;
+  }
+  switch (w & 0xFF) {
+    case fa::kErrTimeout: return FA_ERR_TIMEOUT;
+    default: return FA_ERR_DEVICE;
+  }
+}
+
+void fa_set_wait_timeout_ns(unsigned long long ns) {
+  g_timeout_ns.store(ns, std::memory_order_relaxed);
+}
+
+const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "success";
+    case FA_ERR_INVALID_ARG: return "invalid argument (pointer, alignment, size, scale, flag or workspace)";
+    case FA_ERR_UNSUPPORTED: return "unsupported (head dimension must be 64 or 128; device must be sm_103)";
+    case FA_ERR_LAUNCH: return "CUDA runtime call or kernel launch failed";
+    case FA_ERR_TIMEOUT: return "a kernel gave up on an internal pipeline wait";
+    case FA_ERR_NO_DEVICE: return "no CUDA device is current";
+    case FA_ERR_DEVICE: return "asynchronous CUDA error reported by the stream or device";
+    default: return "unknown status";
+  }
+}
+
+const char* fa_version(void) { return "io_aware_exact_10_gb300 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,511 @@
+// fa_bwd.cu -- exact softmax attention backward for sm_103a.
+//
+// The backward recomputes P block by block from Q, K and the saved per-row
+// log-sum-exp instead of storing it (FlashAttention: exact attention made fast
+// by counting memory traffic, "The method"; FlashAttention and IO-aware exact
+// attention, "Backward by recomputation").  The pages print no gradient
+// formulas; the ones used are the chain rule through S = scale Q K^T,
+// P = softmax(S), O = P V:
+//   D_i   = sum_c dO_ic O_ic
+//   dP    = dO V^T,   dS = P o (dP - D)
+//   dV    = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K
+//
+// Three kernels, all on the caller's stream:
+//   fa_bwd_pre_kernel   D = rowsum(dO o O) and dQacc = 0      (memory bound)
+//   fa_bwd_kernel       one CTA per 128-key tile of one head; loops over the
+//                       128-query tiles that see it; dK, dV accumulate in
+//                       TMEM; dQ contributions are added into dQacc (fp32)
+//   fa_bwd_dq_kernel    dq = bf16(scale * dQacc)                (memory bound)
+//
+// fa_bwd_kernel roles (320 threads):
+//   warps 0-3  P / dS warpgroup (thread = key row = TMEM lane)
+//   warps 4-7  dQ drain warpgroup (thread = query row = TMEM lane)
+//   warp  8    TMA producer (K, V once; then Q_i, dO_i through 2-slot rings)
+//   warp  9    tcgen05 MMA issuer and TMEM owner
+// Tensor memory (512 columns): ST (S^T, then P^T bf16) | DPT (dP^T, then dS^T
+// bf16, then dQ) | dV | dK.  Per query tile the MMA thread issues, in order:
+//   S^T = K Q_i^T -> ST;  dP^T = V dO_i^T -> DPT;  dV += P^T dO_i;
+//   dK += dS^T Q_i;  dQ_i = dS K -> DPT.
+// dS is also written to shared memory (query-major) as the A operand of dQ.
+#include <cuda_bf16.h>
+
+#include "fa_kernels.h"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// preprocess: D = rowsum(dO * O), dQacc = 0.  One warp per row.
+// ---------------------------------------------------------------------------
+template <int HD>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                         const __nv_bfloat16* __restrict__ dO,
+                                                         float* __restrict__ D,
+                                                         float* __restrict__ dq_acc, long rows) {
+  constexpr int PER = HD / 32;  // bf16 elements per lane (2 or 4)
+  const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const size_t base = (size_t)row * HD + lane * PER;
+  float acc = 0.f;
+  if constexpr (PER == 4) {
+    const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+    const uint2 b = *reinterpret_cast<const uint2*>(dO + base);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 fa2 = __bfloat1622float2(a2[i]), fb2 = __bfloat1622float2(b2[i]);
+      acc = fmaf(fa2.x, fb2.x, acc);
+      acc = fmaf(fa2.y, fb2.y, acc);
+    }
+    *reinterpret_cast<float4*>(dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dO + base);
+    const float2 fa2 = __bfloat1622float2(a), fb2 = __bfloat1622float2(b);
+    acc = fmaf(fa2.x, fb2.x, fmaf(fa2.y, fb2.y, 0.f));
+    *reinterpret_cast<float2*>(dq_acc + base) = make_float2(0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) D[row] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// dq = bf16(scale * dQacc).  8 elements per thread.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ dq_acc,
+                                                        __nv_bfloat16* __restrict__ dq,
+                                                        long n8, float scale) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+  uint4 out;
+  out.x = pack_bf16(a.x * scale, a.y * scale);
+  out.y = pack_bf16(a.z * scale, a.w * scale);
+  out.z = pack_bf16(b.x * scale, b.y * scale);
+  out.w = pack_bf16(b.z * scale, b.w * scale);
+  reinterpret_cast<uint4*>(dq)[i] = out;
+}
+
+// ---------------------------------------------------------------------------
+// main backward kernel
+// ---------------------------------------------------------------------------
+template <int HD>
+struct BwdCfg {
+  static constexpr int BQ = 128;              // queries per iteration
+  static constexpr int BK = 128;              // keys per CTA
+  static constexpr int KB = HD / 64;          // 64-column blocks per row
+  static constexpr int TILE = 128 * HD * 2;   // bytes of one 128-row bf16 tile
+  static constexpr int DS_BYTES = BQ * BK * 2;
+  // dynamic shared memory layout (offsets from a 1024-byte aligned base)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;        // 2 slots
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;   // 2 slots
+  static constexpr int OFF_DS = OFF_DO + 2 * TILE;
+  static constexpr int OFF_LSE = OFF_DS + DS_BYTES; // 2 x 128 floats (log2-scaled LSE)
+  static constexpr int OFF_D = OFF_LSE + 2 * BQ * 4;  // 2 x 128 floats
+  static constexpr int OFF_BAR = OFF_D + 2 * BQ * 4;
+  static constexpr int NBAR = 20;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + HD;
+};
+
+// barrier indices
+enum : int {
+  B_KV = 0, B_QF0 = 1, B_QF1 = 2, B_DOF0 = 3, B_DOF1 = 4, B_QE0 = 5, B_QE1 = 6, B_DOE0 = 7,
+  B_DOE1 = 8, B_ST = 9, B_DPT = 10, B_P = 11, B_DS = 12, B_DQF = 13, B_DQE = 14, B_FIN = 15,
+  B_DRAIN = 16, B_WG = 17
+};
+
+struct BwdParams {
+  const float* lse;
+  const float* D;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int N, nq;
+  float scale, scale2;
+  KernelCtl ctl;
+};
+
+__device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
+                                            volatile int* abort, uint32_t site) {
+  const bool ok = mbar_wait(bar, parity, ctl, abort, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int HD, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const BwdParams p) {
+  using C = BwdCfg<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // The swizzled tiles need a 1024-byte aligned base; with no static shared
+  // memory the dynamic window starts aligned.  Check rather than assume.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) record_error(p.ctl, kErrSmemAlign, 1);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int kt = blockIdx.y;                       // key tile (0 = most work when causal)
+  const int i0 = CAUSAL ? kt : 0;                  // first query tile that sees this key tile
+  const int nit = p.nq - i0;                       // query tiles to process
+
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
+                 sDO = s0 + C::OFF_DO, sDS = s0 + C::OFF_DS;
+  float* lse_sh = reinterpret_cast<float*>(smem + C::OFF_LSE);
+  float* d_sh = reinterpret_cast<float*>(smem + C::OFF_D);
+
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    const int counts[18] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 4, 1, 1, 128};
+    for (int i = 0; i < 18; ++i) mbar_init(bar(i), counts[i]);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_base_sh), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_sh;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tdo);
+      mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
+      for (int b = 0; b < C::KB; ++b) {
+        tma_load_3d(sK + b * 16384, &tk, bar(B_KV), b * 64, kt * C::BK, bh);
+        tma_load_3d(sV + b * 16384, &tv, bar(B_KV), b * 64, kt * C::BK, bh);
+      }
+      bool ok = true;
+      int u = 0;
+      for (; u < nit && ok; ++u) {
+        const int st = u & 1, use = u >> 1, qt = i0 + u;
+        if (use > 0 && !mbar_wait(bar(B_QE0 + st), (use - 1) & 1, p.ctl, abort, 10)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(B_QF0 + st), C::TILE);
+        for (int b = 0; b < C::KB; ++b)
+          tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, bh);
+        if (use > 0 && !mbar_wait(bar(B_DOE0 + st), (use - 1) & 1, p.ctl, abort, 11)) {
+          ok = false;
+          // the Q load above is in flight; wait for it below
+          mbar_wait_quiet(bar(B_QF0 + st), use & 1, 200000000ull);
+          break;
+        }
+        mbar_arrive_expect_tx(bar(B_DOF0 + st), C::TILE);
+        for (int b = 0; b < C::KB; ++b)
+          tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, bh);
+      }
+      if (!ok) {
+        // Abort: let every copy already issued land before the CTA exits.
+        mbar_wait_quiet(bar(B_KV), 0, 200000000ull);
+        for (int v = (u >= 2 ? u - 2 : 0); v < u; ++v) {
+          mbar_wait_quiet(bar(B_QF0 + (v & 1)), (v >> 1) & 1, 200000000ull);
+          mbar_wait_quiet(bar(B_DOF0 + (v & 1)), (v >> 1) & 1, 200000000ull);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, C::BQ, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdG = idesc_bf16(128, HD, false, true);      // dV, dK (A in TMEM)
+      constexpr uint32_t kIdQ = idesc_bf16(128, HD, true, true);       // dQ = dS K
+      const uint32_t tST = tmem + C::COL_ST, tDPT = tmem + C::COL_DPT, tDV = tmem + C::COL_DV,
+                     tDK = tmem + C::COL_DK;
+      bool ok = mbar_wait(bar(B_KV), 0, p.ctl, abort, 20);
+      for (int u = 0; u < nit && ok; ++u) {
+        const int st = u & 1, par = (u >> 1) & 1;
+        const uint32_t q0 = sQ + st * C::TILE, do0 = sDO + st * C::TILE;
+        if (!(ok = mbar_wait(bar(B_QF0 + st), par, p.ctl, abort, 21))) break;
+        tc_fence_after();
+        // S^T = K Q_i^T   (M = keys, N = queries, K = d; both K-major)
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          mma_ss(tST, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q0 + off, 16, 1024), kIdS, k > 0);
+        }
+        mma_commit(bar(B_ST));
+        if (!(ok = mbar_wait(bar(B_DOF0 + st), par, p.ctl, abort, 22))) break;
+        if (u > 0 && !(ok = mbar_wait(bar(B_DQE), (u - 1) & 1, p.ctl, abort, 23))) break;
+        tc_fence_after();
+        // dP^T = V dO_i^T
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          mma_ss(tDPT, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(do0 + off, 16, 1024), kIdS, k > 0);
+        }
+        mma_commit(bar(B_DPT));
+        // dV += P^T dO_i   (A = P^T bf16 in TMEM, B = dO_i query-major)
+        if (!(ok = mbar_wait(bar(B_P), u & 1, p.ctl, abort, 24))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::BQ / 16; ++k)
+          mma_ts(tDV, tST + k * 8, sdesc_sw128(do0 + k * 2048, 16384, 1024), kIdG, u > 0 || k > 0);
+        mma_commit(bar(B_DOE0 + st));
+        // dK += dS^T Q_i   (A = dS^T bf16 in TMEM)
+        if (!(ok = mbar_wait(bar(B_DS), u & 1, p.ctl, abort, 25))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::BQ / 16; ++k)
+          mma_ts(tDK, tDPT + k * 8, sdesc_sw128(q0 + k * 2048, 16384, 1024), kIdG, u > 0 || k > 0);
+        // dQ_i = dS K   (M = queries, N = d, K = keys; A = dS smem query-major, B = K key-major)
+#pragma unroll
+        for (int k = 0; k < C::BK / 16; ++k)
+          mma_ss(tDPT, sdesc_sw128(sDS + k * 2048, 16384, 1024),
+                 sdesc_sw128(sK + k * 2048, 16384, 1024), kIdQ, k > 0);
+        mma_commit(bar(B_DQF));
+        mma_commit(bar(B_QE0 + st));
+      }
+      if (ok) mma_commit(bar(B_FIN));
+      mma_commit(bar(B_DRAIN));
+      mbar_wait_quiet(bar(B_DRAIN), 0, 200000000ull);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------- P / dS warpgroup
+    const int r = warp * 32 + lane;                 // key row within the tile
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tST = tmem + lane_off + C::COL_ST, tDPT = tmem + lane_off + C::COL_DPT;
+    const float scale2 = p.scale2;
+    const size_t rowbase = (size_t)bh * p.N;
+    // stage the log2-scaled LSE and D of the first query tile
+    {
+      const int q = i0 * C::BQ + r;
+      lse_sh[r] = q < p.N ? p.lse[rowbase + q] * kLog2e : INFINITY;
+      d_sh[r] = q < p.N ? p.D[rowbase + q] : 0.f;
+    }
+    // The warpgroup synchronises on an mbarrier (128 arrivals per phase) so
+    // that the wait stays bounded if another warp gives up.
+    mbar_arrive(bar(B_WG));
+    bool ok = warp_wait_b(bar(B_WG), 0, p.ctl, abort, 34);
+    for (int u = 0; u < nit && ok; ++u) {
+      const int qt = i0 + u;
+      const float* lse_u = lse_sh + (u & 1) * C::BQ;
+      const float* d_u = d_sh + (u & 1) * C::BQ;
+      // prefetch the next tile's statistics
+      float nl = INFINITY, nd = 0.f;
+      if (u + 1 < nit) {
+        const int q = (qt + 1) * C::BQ + r;
+        if (q < p.N) {
+          nl = p.lse[rowbase + q] * kLog2e;
+          nd = p.D[rowbase + q];
+        }
+      }
+      if (!(ok = warp_wait_b(bar(B_ST), u & 1, p.ctl, abort, 30))) break;
+      tc_fence_after();
+      float pr[128];
+      {
+        uint32_t* pu = reinterpret_cast<uint32_t*>(pr);
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32)
+          tmem_ld32(tST + c0, *reinterpret_cast<uint32_t(*)[32]>(pu + c0));
+        tmem_wait_ld();
+      }
+      // P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query < key
+      const bool diag = CAUSAL && qt == blockIdx.y;
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float v = ex2(fmaf(pr[c0 + i], scale2, -lse_u[c0 + i]));
+          if (diag && (c0 + i) < r) v = 0.f;
+          pr[c0 + i] = v;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pr[c0 + 2 * i], pr[c0 + 2 * i + 1]);
+        tmem_st16(tST + c0 / 2, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_P));
+      // dS^T = P^T o (dP^T - D)
+      if (!(ok = warp_wait_b(bar(B_DPT), u & 1, p.ctl, abort, 31))) break;
+      if (u > 0 && !(ok = warp_wait_b(bar(B_DQF), (u - 1) & 1, p.ctl, abort, 32))) break;
+      tc_fence_after();
+      const uint32_t srow = sDS + r * 128;
+      const uint32_t sw = (uint32_t)(r & 7);
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t dp[32];
+        tmem_ld32(tDPT + c0, dp);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = pr[c0 + 2 * i] * (__uint_as_float(dp[2 * i]) - d_u[c0 + 2 * i]);
+          const float b = pr[c0 + 2 * i + 1] * (__uint_as_float(dp[2 * i + 1]) - d_u[c0 + 2 * i + 1]);
+          pk[i] = pack_bf16(a, b);
+        }
+        tmem_st16(tDPT + c0 / 2, pk);
+        // shared copy, query-major 128-byte swizzled: block c0/64, chunks of 8 queries
+        const uint32_t blk = sDS + (uint32_t)(c0 / 64) * 16384;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint32_t chunk = (uint32_t)((c0 % 64) / 8 + cc);
+          const uint32_t addr = blk + (srow - sDS) + ((chunk ^ sw) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * cc]),
+                       "r"(pk[4 * cc + 1]), "r"(pk[4 * cc + 2]), "r"(pk[4 * cc + 3])
+                       : "memory");
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DS));
+      // publish the next tile's statistics
+      lse_sh[((u + 1) & 1) * C::BQ + r] = nl;
+      d_sh[((u + 1) & 1) * C::BQ + r] = nd;
+      mbar_arrive(bar(B_WG));
+      if (!(ok = warp_wait_b(bar(B_WG), (u + 1) & 1, p.ctl, abort, 35))) break;
+    }
+    // epilogue: dV rows of this key tile
+    if (ok && warp_wait_b(bar(B_FIN), 0, p.ctl, abort, 33)) {
+      tc_fence_after();
+      const int key = kt * C::BK + r;
+      __nv_bfloat16* dst = p.dv + (rowbase + key) * HD;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + C::COL_DV + c0, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        if (key < p.N) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- dQ drain
+    const int sp = warp & 3;
+    const int r = sp * 32 + lane;  // query row within the tile (dQ) / key row (dK)
+    const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+    const size_t rowbase = (size_t)bh * p.N;
+    bool ok = true;
+    for (int u = 0; u < nit; ++u) {
+      if (!(ok = warp_wait_b(bar(B_DQF), u & 1, p.ctl, abort, 40))) break;
+      tc_fence_after();
+      const int q = (i0 + u) * C::BQ + r;
+      float* dst = p.dq_acc + (rowbase + q) * HD;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + C::COL_DPT + c0, v);
+        tmem_wait_ld();
+        if (q < p.N) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            atomicAdd(reinterpret_cast<float4*>(dst + c0) + i,
+                      make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DQE));
+    }
+    // epilogue: dK rows of this key tile (scaled)
+    if (ok && warp_wait_b(bar(B_FIN), 0, p.ctl, abort, 41)) {
+      tc_fence_after();
+      const int key = kt * C::BK + r;
+      __nv_bfloat16* dst = p.dk + (rowbase + key) * HD;
+      const float scale = p.scale;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + C::COL_DK + c0, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
+        if (key < p.N) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int HD, bool CAUSAL>
+cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
+  using C = BwdCfg<HD>;
+  auto kern = fa_bwd_kernel<HD, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  BwdParams p;
+  p.lse = a.lse;
+  p.D = a.D;
+  p.dq_acc = a.dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.N = a.N;
+  p.nq = (a.N + C::BQ - 1) / C::BQ;
+  p.scale = a.scale;
+  p.scale2 = a.scale * kLog2e;
+  p.ctl = a.ctl;
+  dim3 grid(a.BH, (a.N + C::BK - 1) / C::BK);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, p);
+  return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
+  const long rows = (long)a.BH * a.N;
+  fa_bwd_pre_kernel<HD><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.D,
+      a.dq_acc, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = a.causal ? launch_bwd_main<HD, true>(a, stream) : launch_bwd_main<HD, false>(a, stream);
+  if (e != cudaSuccess) return e;
+  const long n8 = rows * HD / 8;
+  fa_bwd_dq_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(
+      a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n8, a.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream) {
+  return a.d == 128 ? launch_bwd_t<128>(a, stream) : launch_bwd_t<64>(a, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,386 @@
+// fa_fwd.cu -- exact softmax attention forward for sm_103a.
+//
+// Computes O = softmax(scale * Q K^T [causal]) V and the per-row natural-log
+// log-sum-exp, tiled so the N x N score matrix never leaves the SM
+// (FlashAttention: exact attention made fast by counting memory traffic,
+// "The method"; Flash Attention (ostralyan.com), "Block-Wise Attention
+// Computation" and "Core Flash Attention Algorithm").
+//
+// One CTA owns two 128-row query tiles of one (batch, head) and streams the
+// head's 128-key K/V tiles through a TMA ring.  Roles (320 threads):
+//   warps 0-3  softmax for query tile 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer (Q tiles once, then K_0, V_0, K_1, V_1, ...)
+//   warp  9    tcgen05 MMA issuer (one thread) and TMEM owner
+// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1.  The softmax writes P as
+// bf16 pairs into the first 64 columns of its S region and the MMA reads it
+// from there as the A operand of O += P V.  The two query tiles alternate on
+// the tensor core: while one tile's softmax runs, the other tile's
+// O += P V and S = Q K^T run.
+//
+// Online softmax in base 2 with the scale folded into one FMA: the running
+// max m and normaliser l of each row follow the recurrence of Flash Attention,
+// "Online Softmax Algorithm"; O stays unnormalised and is divided by l once at
+// the end, and one log-sum-exp per row is written (FlashAttention and
+// IO-aware exact attention, "Core ideas").  The max is updated lazily: a new
+// max within TAU (log2 units) of the current one is not adopted, which keeps
+// P <= 2^TAU and skips the rescale of O in TMEM; the result is the same in
+// exact arithmetic because l and O always share one reference max.
+#include <cuda_bf16.h>
+
+#include "fa_kernels.h"
+
+namespace fa {
+namespace {
+
+constexpr float kTau = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int HD>
+struct FwdCfg {
+  static constexpr int BM = 128;                  // query rows per tile
+  static constexpr int BN = 128;                  // keys per K/V tile
+  static constexpr int KB = HD / 64;              // 64-column (128-byte) blocks per row
+  static constexpr int QTILE = BM * HD * 2;       // bytes of one Q tile
+  static constexpr int KVTILE = BN * HD * 2;      // bytes of one K or V tile
+  static constexpr int STAGES = HD == 128 ? 4 : 8;
+  static constexpr int SMEM = 2 * QTILE + STAGES * KVTILE + 1024;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+struct FwdParams {
+  __nv_bfloat16* o;
+  float* lse;
+  int N, nq, nkv;
+  float scale2;  // scale * log2(e)
+  KernelCtl ctl;
+};
+
+// Warp-uniform bounded wait: every lane polls, all agree on the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
+                                          volatile int* abort, uint32_t site) {
+  const bool ok = mbar_wait(bar, parity, ctl, abort, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int HD, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  using C = FwdCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+
+  __shared__ __align__(8) uint64_t bar_q[2];
+  __shared__ __align__(8) uint64_t bar_full[C::STAGES];
+  __shared__ __align__(8) uint64_t bar_empty[C::STAGES];
+  __shared__ __align__(8) uint64_t bar_s[2];
+  __shared__ __align__(8) uint64_t bar_p[2];
+  __shared__ __align__(8) uint64_t bar_o[2];
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  volatile int* abort = &abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int qt0 = 2 * (gridDim.y - 1 - blockIdx.y);  // heaviest causal tiles launch first
+  bool valid[2];
+  int nkv_t[2];
+  for (int t = 0; t < 2; ++t) {
+    valid[t] = qt0 + t < p.nq;
+    nkv_t[t] = !valid[t] ? 0 : (CAUSAL ? min(qt0 + t + 1, p.nkv) : p.nkv);
+  }
+  const int nmax = max(nkv_t[0], nkv_t[1]);
+
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sRing = sQ + 2 * C::QTILE;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bar_q[t]), 1);
+      mbar_init(smem_u32(&bar_s[t]), 1);
+      mbar_init(smem_u32(&bar_p[t]), 4);
+      mbar_init(smem_u32(&bar_o[t]), 1);
+    }
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&tmem_base_sh), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      for (int t = 0; t < 2; ++t) {
+        if (!valid[t]) continue;
+        const uint32_t bar = smem_u32(&bar_q[t]);
+        mbar_arrive_expect_tx(bar, C::QTILE);
+        for (int b = 0; b < C::KB; ++b)
+          tma_load_3d(sQ + t * C::QTILE + b * C::BM * 128, &tq, bar, b * 64, (qt0 + t) * C::BM, bh);
+      }
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; j < nmax && ok; ++j) {
+        for (int w = 0; w < 2; ++w, ++it) {
+          const int slot = it % C::STAGES, use = it / C::STAGES;
+          if (use > 0 && !mbar_wait(smem_u32(&bar_empty[slot]), (use - 1) & 1, p.ctl, abort, 10)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&bar_full[slot]);
+          mbar_arrive_expect_tx(bar, C::KVTILE);
+          const uint32_t dst = sRing + slot * C::KVTILE;
+          for (int b = 0; b < C::KB; ++b)
+            tma_load_3d(dst + b * C::BN * 128, w ? &tv : &tk, bar, b * 64, j * C::BN, bh);
+        }
+      }
+      if (!ok) {
+        // Abort: let the copies already issued land before the CTA exits.
+        for (int s = 0; s < C::STAGES && s < it; ++s)
+          mbar_wait_quiet(smem_u32(&bar_full[s]), ((it - 1 - s) / C::STAGES) & 1, 200000000ull);
+        for (int t = 0; t < 2; ++t)
+          if (valid[t]) mbar_wait_quiet(smem_u32(&bar_q[t]), 0, 200000000ull);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, C::BN, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(128, HD, false, true);
+      bool ok = true;
+      for (int t = 0; t < 2 && ok; ++t)
+        if (valid[t]) ok = mbar_wait(smem_u32(&bar_q[t]), 0, p.ctl, abort, 20);
+
+      // S_t = Q_t K^T for the K tile in ring slot `slot`.
+      auto issue_s = [&](int t, int slot) {
+        const uint32_t a0 = sQ + t * C::QTILE, b0 = sRing + slot * C::KVTILE;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k / 4) * (C::BM * 128) + (k % 4) * 32;
+          mma_ss(tmem + t * 128, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
+                 kIdS, k > 0);
+        }
+        mma_commit(smem_u32(&bar_s[t]));
+      };
+      // O_t (+)= P_t V for the V tile in ring slot `slot`.
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint32_t b0 = sRing + slot * C::KVTILE;
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k)
+          mma_ts(tmem + 256 + t * HD, tmem + t * 128 + k * 8,
+                 sdesc_sw128(b0 + k * 2048, C::BN * 128, 1024), kIdPV, acc || k > 0);
+      };
+
+      int it = 0;
+      if (ok) {
+        ok = mbar_wait(smem_u32(&bar_full[0]), 0, p.ctl, abort, 21);
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t)
+            if (valid[t]) issue_s(t, 0);
+          mma_commit(smem_u32(&bar_empty[0]));
+          it = 1;
+        }
+      }
+      for (int j = 1; j <= nmax && ok; ++j) {
+        const int vslot = it % C::STAGES;
+        ok = mbar_wait(smem_u32(&bar_full[vslot]), (it / C::STAGES) & 1, p.ctl, abort, 22);
+        ++it;
+        if (!ok) break;
+        tc_fence_after();
+        const bool have_k = j < nmax;
+        const int kslot = it % C::STAGES, kpar = (it / C::STAGES) & 1;
+        if (have_k) ++it;
+        bool k_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!valid[t] || j - 1 >= nkv_t[t]) continue;
+          ok = mbar_wait(smem_u32(&bar_p[t]), (j - 1) & 1, p.ctl, abort, 23);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, vslot, j - 1 > 0);
+          if (j - 1 == nkv_t[t] - 1) mma_commit(smem_u32(&bar_o[t]));
+          if (j < nkv_t[t]) {
+            if (!k_ready) {
+              ok = mbar_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 24);
+              if (!ok) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(t, kslot);
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bar_empty[vslot]));
+        if (have_k) {
+          if (!k_ready) {
+            ok = mbar_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 25);
+            if (!ok) break;
+          }
+          mma_commit(smem_u32(&bar_empty[kslot]));
+        }
+      }
+      // Drain: every MMA issued above completes before TMEM is released.
+      mma_commit(smem_u32(&bar_drain));
+      mbar_wait_quiet(smem_u32(&bar_drain), 0, 200000000ull);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int t = warp >> 2;           // query tile of this warpgroup
+    const int sp = warp & 3;           // TMEM lane quarter of this warp
+    const int r = sp * 32 + lane;      // row within the tile
+    if (valid[t]) {
+      const int qt = qt0 + t;
+      const int row = qt * C::BM + r;
+      const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+      const uint32_t tS = tmem + lane_off + t * 128;
+      const uint32_t tO = tmem + lane_off + 256 + t * HD;
+      const float scale2 = p.scale2;
+      const bool tail = (p.N % C::BN) != 0;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nkv_t[t]; ++j) {
+        if (!warp_wait(smem_u32(&bar_s[t]), j & 1, p.ctl, abort, 30)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[128];
+        {
+          uint32_t* su = reinterpret_cast<uint32_t*>(s);
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32)
+            tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(su + c0));
+          tmem_wait_ld();
+        }
+        if (CAUSAL && j == qt) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > r) s[c] = -INFINITY;
+        }
+        if (!CAUSAL && tail && j == p.nkv - 1) {
+          const int lim = p.N - j * C::BN;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        const float m_new = fmaxf(m, mx * scale2);
+        const bool need = m_new > m + kTau;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2(m - m_new) : 1.0f;
+          if (need) m = m_new;
+          l *= alpha;
+          if (j > 0) {
+            // O_t is complete here: S_t(j) was issued after PV_t(j-1) and its
+            // commit covers every earlier MMA of the issuing thread.
+#pragma unroll 1
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+              uint32_t ov[32];
+              tmem_ld32(tO + c0, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              tmem_st32(tO + c0, ov);
+            }
+          }
+        }
+        const float neg_m = -m;
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(s[c0 + 2 * i], scale2, neg_m));
+            const float p1 = ex2(fmaf(s[c0 + 2 * i + 1], scale2, neg_m));
+            pk[i] = pack_bf16(p0, p1);
+            // l sums the bf16-rounded values that O += P V multiplies, so O / l
+            // is an exact convex combination of V rows.
+            l += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+          }
+          tmem_st16(tS + c0 / 2, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_p[t]));
+      }
+      // Epilogue: O / l -> bf16, and LSE = ln 2 * (m + log2 l).
+      if (ok && warp_wait(smem_u32(&bar_o[t]), 0, p.ctl, abort, 31)) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
+        __nv_bfloat16* orow = p.o + ((size_t)bh * p.N + row) * HD;
+#pragma unroll 1
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c0, ov);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+          if (row < p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (row < p.N) p.lse[(size_t)bh * p.N + row] = (m + __log2f(l)) * kLn2;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int HD, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
+  using C = FwdCfg<HD>;
+  auto kern = fa_fwd_kernel<HD, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  FwdParams p;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.N = a.N;
+  p.nq = (a.N + C::BM - 1) / C::BM;
+  p.nkv = (a.N + C::BN - 1) / C::BN;
+  p.scale2 = a.scale * 1.4426950408889634f;
+  p.ctl = a.ctl;
+  dim3 grid(a.BH, (p.nq + 1) / 2);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.d == 128) return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+  return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+}
+
+}  // namespace fa
