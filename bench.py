@@ -1,0 +1,364 @@
+#!/usr/bin/env python3
+"""Benchmark: exact attention forward + backward on GB300 through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: fa_fwd (O, LSE) then
+fa_bwd (D preprocess, the backward kernel, dQ conversion).  The workload is the
+GPT-2-medium attention shape of the paper's Figure 2 (B=64, H=16, N=1024,
+d=64, non-causal, bf16, seeded synthetic N(0,1) inputs).  Its inputs (4 x 134
+MB) exceed the 129 MB L2, so no L2 flush is needed between steps.
+
+Printed (rank 0, one JSON line): fwd+bwd TFLOP/s with FLOPs counted as
+4*B*H*N^2*d for the forward and 2.5x that for the backward (recomputation
+included), the time per step, the roofline of the dominant call, the end-to-end
+figure through host buffers, the clocks seen while timing, and the fp64 oracle
+timed on the host cores as a baseline.
+
+With --gpus N > 1 (launched under torch.distributed.run) every rank processes
+its own copy of the workload (attention heads are independent: weak scaling,
+no data-path collective); the time is the max over ranks and the value sums
+the work of all ranks.  --impl reference times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# Main backward kernel share of the fa_bwd call, and DRAM bytes per launch,
+# from the ncu summaries committed under profiles/ (None until captured).
+NCU_TRAFFIC_BYTES = None
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_oracle_sample(w, cpu_inputs, n_heads: int):
+    """Time the fp64 oracle (fwd + bwd) on the first n_heads heads of the
+    workload's inputs; returns (seconds, flops of the sample, threads)."""
+    import oracle
+    from io_aware_exact_10_gb300 import workloads as W
+    oracle.build()
+    sub = W.Workload(w.name, 1, n_heads, w.N, w.d, causal=w.causal, seed=w.seed)
+    flat = lambda t: t.reshape(w.B * w.H, w.N, w.d)[:n_heads].double().numpy()
+    qs, ks, vs, dOs = (flat(t) for t in cpu_inputs)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(qs, ks, vs, w.scale, w.causal)
+    oracle.attn_bwd(qs, ks, vs, dOs, w.scale, w.causal)
+    dt = time.perf_counter() - t0
+    return dt, sub.fwd_flops() + sub.bwd_flops(), oracle.num_threads()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, w):
+    """The fp64 oracle timed on the host cores (rank 0 only)."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    heads_per_step = 8
+    import oracle
+    from io_aware_exact_10_gb300 import workloads as W
+    oracle.build()
+    q, k, v, dO = W.make_inputs(w)
+    flat = lambda t: t.reshape(w.B * w.H, w.N, w.d).double().numpy()
+    qs, ks, vs, dOs = flat(q), flat(k), flat(v), flat(dO)
+    sub = W.Workload(w.name, 1, heads_per_step, w.N, w.d, causal=w.causal)
+    flops_step = sub.fwd_flops() + sub.bwd_flops()
+
+    def step(i):
+        lo = (i * heads_per_step) % (w.B * w.H)
+        sl = slice(lo, lo + heads_per_step)
+        oracle.attn_fwd(qs[sl], ks[sl], vs[sl], w.scale, w.causal)
+        oracle.attn_bwd(qs[sl], ks[sl], vs[sl], dOs[sl], w.scale, w.causal)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = flops_step * args.steps / dt / 1e12
+    cores = oracle.num_threads()
+    sample = (f"{heads_per_step} heads (of {w.B * w.H}) of {w.name} per step, fwd+bwd, "
+              "fp64 C oracle with OpenMP")
+    line = {
+        "impl": "reference", "metric": "attention fwd+bwd TFLOP/s", "value": value,
+        "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": f"{w.name}, forward+backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+            "causal": w.causal, "scale": w.scale,
+            "l2": "inputs larger than L2 (4 x %.0f MB bf16), no flush" % (w.B * w.H * w.N * w.d * 2 / 1e6),
+            "flops": "fwd 4*B*H*N^2*d (x1/2 causal); bwd 2.5x fwd"}
+
+
+def run_ours(args, w):
+    import torch
+    import io_aware_exact_10_gb300 as fa
+    from io_aware_exact_10_gb300 import workloads as W
+    import __graft_entry__
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    __graft_entry__.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+
+    B, H, N, d = w.B, w.H, w.N, w.d
+    cpu_inputs = W.make_inputs(w)
+    q, k, v, dO = (t.to(dev) for t in cpu_inputs)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    causal = int(w.causal)
+
+    def fwd():
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, w.scale, causal, stream)
+
+    def bwd():
+        fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, w.scale, causal, ws, ws_bytes,
+                  stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    barrier()
+
+    # ---- timed region: K steps, device-resident inputs
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    if rank == 0:
+        clocks.start()
+    barrier()
+    e0, e1 = ev(), ev()
+    fwd_ev = [(ev(), ev()) for _ in range(args.steps)]
+    bwd_ev = [(ev(), ev()) for _ in range(args.steps)]
+    e0.record(stream)
+    for i in range(args.steps):
+        fwd_ev[i][0].record(stream)
+        fwd()
+        fwd_ev[i][1].record(stream)
+        bwd_ev[i][0].record(stream)
+        bwd()
+        bwd_ev[i][1].record(stream)
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop() if rank == 0 else None
+    ms_total = max_over_ranks(e0.elapsed_time(e1))
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
+    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in bwd_ev)
+    st = fa.fa_last_device_error(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device error after the timed region: {fa.fa_strerror(st)}")
+
+    flops_step = w.fwd_flops() + w.bwd_flops()
+    ms_step = ms_total / args.steps
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
+    bwd_tf = w.bwd_flops() / (bwd_ms * 1e-3) / 1e12
+    fwd_tf = w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device -> fwd + bwd -> host outputs
+    hq, hk, hv, hdO = (t.cpu().pin_memory() for t in (q, k, v, dO))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3))
+
+    def e2e_step():
+        for h, dd in ((hq, q), (hk, k), (hv, v), (hdO, dO)):
+            dd.copy_(h, non_blocking=True)
+        fwd()
+        bwd()
+        for h, dd in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            h.copy_(dd, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_step()
+    barrier()
+    a, b = ev(), ev()
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(a.elapsed_time(b)) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v, dO))
+    d2h = sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv))
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    # ---- CPU baseline: the oracle on a bounded sample of the same workload
+    cpu_heads = int(os.environ.get("FA_BENCH_CPU_HEADS", "128"))
+    cpu_s, cpu_flops, cores = cpu_oracle_sample(w, cpu_inputs, cpu_heads)
+
+    line = {
+        "metric": "attention fwd+bwd TFLOP/s",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) fp32 rounded to bf16)",
+        "config": config_of(w),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "pct_of_peak": 100 * fwd_tf / peak},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "pct_of_peak": 100 * bwd_tf / peak},
+        "roofline": {
+            "kernel": "fa_bwd call (D preprocess + backward kernel + dQ convert), timed with "
+                      "CUDA events per launch; its FLOPs are the backward's 5 N^2 d contractions",
+            "bound": "tensor",
+            "achieved": bwd_tf,
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": bwd_tf / peak,
+            "frac_sustained": bwd_tf / peak_sus,
+            "peak_source": f"{peak_src} bf16 burst ({PEAKS_PATH if peak_src == 'measured' else 'recipe fallback'})",
+            "traffic": NCU_TRAFFIC_BYTES,
+        },
+        "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": {"value": cpu_flops / cpu_s / 1e12, "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"first {cpu_heads} of {w.B * w.H} heads of {w.name}, "
+                                   f"fwd+bwd in fp64 ({cpu_s:.1f} s)"},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from io_aware_exact_10_gb300 import workloads as W
+    w = W.GPT2_MEDIUM
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

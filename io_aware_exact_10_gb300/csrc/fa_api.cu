@@ -98,6 +98,19 @@ bool encode_bf16_3d(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [BH][N][d] dQ accumulator; box of 32 columns x 32 rows, 128-byte
+// swizzle (one warp's slice of a tile, the unit of the bulk reductions).
+bool encode_f32_3d(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shared validation of sizes and scalars.  *empty is set for a zero-size problem.
@@ -108,9 +121,9 @@ fa_status check_common(int B, int H, int N, int d, float scale, int causal, bool
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   *empty = (B == 0 || H == 0 || N == 0);
   if (*empty) return FA_OK;
+  // one-dimensional grids of (query-tile pairs or key tiles) x heads
   const long long BH = (long long)B * H;
-  if (BH > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;   // grid x
-  if ((N + 127) / 128 > 65535 * 2) return FA_ERR_INVALID_ARG;  // grid y
+  if (BH * ((N + 127) / 128) > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 
@@ -185,6 +198,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.lse = lse;
   a.D = static_cast<float*>(workspace);
   a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)));
+  if (!encode_f32_3d(&a.tdq, a.dq_acc, BH, N, d)) return FA_ERR_INVALID_ARG;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;

@@ -122,16 +122,15 @@ struct BwdCfg {
 enum : int {
   B_KV = 0, B_QF0 = 1, B_QF1 = 2, B_DOF0 = 3, B_DOF1 = 4, B_QE0 = 5, B_QE1 = 6, B_DOE0 = 7,
   B_DOE1 = 8, B_ST = 9, B_DPT = 10, B_P = 11, B_DS = 12, B_DQF = 13, B_DQE = 14, B_FIN = 15,
-  B_DRAIN = 16, B_WG = 17
+  B_DRAIN = 16, B_WG = 17, B_DSF = 18
 };
 
 struct BwdParams {
   const float* lse;
   const float* D;
-  float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int N, nq;
+  int N, nq, nkv;
   float scale, scale2;
   KernelCtl ctl;
 };
@@ -146,7 +145,7 @@ template <int HD, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
   using C = BwdCfg<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // The swizzled tiles need a 1024-byte aligned base; with no static shared
@@ -161,8 +160,11 @@ __global__ void __launch_bounds__(320, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int kt = blockIdx.y;                       // key tile (0 = most work when causal)
+  // One-dimensional grid, key tiles of a head adjacent: the CTAs of one head
+  // run together, share its Q, dO in L2 and add into the same dQ rows (which
+  // then stay in L2).  Key tile 0 (the most work when causal) comes first.
+  const int bh = blockIdx.x / p.nkv;
+  const int kt = blockIdx.x % p.nkv;
   const int i0 = CAUSAL ? kt : 0;                  // first query tile that sees this key tile
   const int nit = p.nq - i0;                       // query tiles to process
 
@@ -174,8 +176,8 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     *abort = 0;
-    const int counts[18] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 4, 1, 1, 128};
-    for (int i = 0; i < 18; ++i) mbar_init(bar(i), counts[i]);
+    const int counts[19] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 4, 1, 1, 128, 4};
+    for (int i = 0; i < 19; ++i) mbar_init(bar(i), counts[i]);
     fence_barrier_init();
   }
   if (warp == 9) {
@@ -323,15 +325,21 @@ __global__ void __launch_bounds__(320, 1)
         tmem_wait_ld();
       }
       // P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query < key
-      const bool diag = CAUSAL && qt == blockIdx.y;
+      const bool diag = CAUSAL && qt == kt;
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = ex2(fmaf(pr[c0 + i], scale2, -lse_u[c0 + i]));
-          if (diag && (c0 + i) < r) v = 0.f;
-          pr[c0 + i] = v;
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 l4 = reinterpret_cast<const float4*>(lse_u + c0)[i4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * i4 + e;
+            float v = ex2(fmaf(pr[c0 + i], scale2, -lv[e]));
+            if (diag && (c0 + i) < r) v = 0.f;
+            pr[c0 + i] = v;
+          }
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pr[c0 + 2 * i], pr[c0 + 2 * i + 1]);
@@ -343,7 +351,9 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) mbar_arrive(bar(B_P));
       // dS^T = P^T o (dP^T - D)
       if (!(ok = warp_wait_b(bar(B_DPT), u & 1, p.ctl, abort, 31))) break;
-      if (u > 0 && !(ok = warp_wait_b(bar(B_DQF), (u - 1) & 1, p.ctl, abort, 32))) break;
+      // the dS buffer doubles as the dQ staging area: wait until the drain of
+      // the previous tile has been read out of it
+      if (u > 0 && !(ok = warp_wait_b(bar(B_DSF), (u - 1) & 1, p.ctl, abort, 32))) break;
       tc_fence_after();
       const uint32_t srow = sDS + r * 128;
       const uint32_t sw = (uint32_t)(r & 7);
@@ -354,10 +364,13 @@ __global__ void __launch_bounds__(320, 1)
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = pr[c0 + 2 * i] * (__uint_as_float(dp[2 * i]) - d_u[c0 + 2 * i]);
-          const float b = pr[c0 + 2 * i + 1] * (__uint_as_float(dp[2 * i + 1]) - d_u[c0 + 2 * i + 1]);
-          pk[i] = pack_bf16(a, b);
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 d4 = reinterpret_cast<const float4*>(d_u + c0)[i4];
+          const int i = 4 * i4;
+          pk[2 * i4] = pack_bf16(pr[c0 + i] * (__uint_as_float(dp[i]) - d4.x),
+                                 pr[c0 + i + 1] * (__uint_as_float(dp[i + 1]) - d4.y));
+          pk[2 * i4 + 1] = pack_bf16(pr[c0 + i + 2] * (__uint_as_float(dp[i + 2]) - d4.z),
+                                     pr[c0 + i + 3] * (__uint_as_float(dp[i + 3]) - d4.w));
         }
         tmem_st16(tDPT + c0 / 2, pk);
         // shared copy, query-major 128-byte swizzled: block c0/64, chunks of 8 queries
@@ -404,33 +417,59 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ---------------------------------------------------------- dQ drain
+    // dQ_i (128 query rows x d, fp32) leaves TMEM into registers, goes through
+    // this warp's 8 KB slice of the dS buffer as 32-row x 32-column boxes
+    // (128-byte swizzled), and is added into dQacc by TMA bulk reductions.
     const int sp = warp & 3;
     const int r = sp * 32 + lane;  // query row within the tile (dQ) / key row (dK)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const size_t rowbase = (size_t)bh * p.N;
+    const uint32_t stage = sDS + (uint32_t)sp * 8192u;
+    const uint32_t sw = (uint32_t)(lane & 7);
     bool ok = true;
     for (int u = 0; u < nit; ++u) {
       if (!(ok = warp_wait_b(bar(B_DQF), u & 1, p.ctl, abort, 40))) break;
       tc_fence_after();
-      const int q = (i0 + u) * C::BQ + r;
-      float* dst = p.dq_acc + (rowbase + q) * HD;
-#pragma unroll 1
-      for (int c0 = 0; c0 < HD; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + C::COL_DPT + c0, v);
-        tmem_wait_ld();
-        if (q < p.N) {
+      uint32_t v[HD];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            atomicAdd(reinterpret_cast<float4*>(dst + c0) + i,
-                      make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
-        }
-      }
+      for (int c0 = 0; c0 < HD; c0 += 32)
+        tmem_ld32(tmem + lane_off + C::COL_DPT + c0, *reinterpret_cast<uint32_t(*)[32]>(v + c0));
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DQE));
+      if (lane == 0) mbar_arrive(bar(B_DQE));  // dQ's TMEM columns are free again
+      const int y = (i0 + u) * C::BQ + sp * 32;
+#pragma unroll
+      for (int h = 0; h < HD / 64; ++h) {
+        if (h > 0) {
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const uint32_t row = stage + (uint32_t)bb * 4096u + (uint32_t)lane * 128u;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int col = h * 64 + bb * 32 + c * 4;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((uint32_t)c ^ sw) << 4)),
+                         "r"(v[col]), "r"(v[col + 1]), "r"(v[col + 2]), "r"(v[col + 3])
+                         : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tdq, stage, (2 * h) * 32, y, bh);
+          tma_reduce_add_3d(&tdq, stage + 4096u, (2 * h + 1) * 32, y, bh);
+          bulk_commit_group();
+        }
+      }
+      if (lane == 0) bulk_wait_group_read<0>();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DSF));  // staging slice read out
     }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
     // epilogue: dK rows of this key tile (scaled)
     if (ok && warp_wait_b(bar(B_FIN), 0, p.ctl, abort, 41)) {
       tc_fence_after();
@@ -473,16 +512,16 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   BwdParams p;
   p.lse = a.lse;
   p.D = a.D;
-  p.dq_acc = a.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.N = a.N;
   p.nq = (a.N + C::BQ - 1) / C::BQ;
+  p.nkv = (a.N + C::BK - 1) / C::BK;
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
-  dim3 grid(a.BH, (a.N + C::BK - 1) / C::BK);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, p);
+  dim3 grid((unsigned)((long)p.nkv * a.BH));
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();
 }
 

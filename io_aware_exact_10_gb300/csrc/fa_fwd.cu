@@ -52,7 +52,7 @@ struct FwdCfg {
 struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
-  int N, nq, nkv;
+  int N, nq, nkv, npairs;
   float scale2;  // scale * log2(e)
   KernelCtl ctl;
 };
@@ -84,8 +84,11 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort = &abort_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int qt0 = 2 * (gridDim.y - 1 - blockIdx.y);  // heaviest causal tiles launch first
+  // One-dimensional grid, query-tile pairs of a head adjacent: the CTAs that
+  // share a head's K and V run together and find them in L2.  Within a head
+  // the heaviest (causal) pair launches first.
+  const int bh = blockIdx.x / p.npairs;
+  const int qt0 = 2 * (p.npairs - 1 - (int)(blockIdx.x % p.npairs));
   bool valid[2];
   int nkv_t[2];
   for (int t = 0; t < 2; ++t) {
@@ -252,7 +255,10 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t tO = tmem + lane_off + 256 + t * HD;
       const float scale2 = p.scale2;
       const bool tail = (p.N % C::BN) != 0;
-      float m = -INFINITY, l = 0.f;
+      // l: sum of the fp32 P values (gives the LSE); lr: sum of the same
+      // values rounded to bf16, as O += P V multiplies them (normalises O,
+      // which then is an exact convex combination of V rows).
+      float m = -INFINITY, l = 0.f, lr = 0.f;
       bool ok = true;
       for (int j = 0; j < nkv_t[t]; ++j) {
         if (!warp_wait(smem_u32(&bar_s[t]), j & 1, p.ctl, abort, 30)) {
@@ -288,6 +294,7 @@ __global__ void __launch_bounds__(320, 1)
           const float alpha = need ? ex2(m - m_new) : 1.0f;
           if (need) m = m_new;
           l *= alpha;
+          lr *= alpha;
           if (j > 0) {
             // O_t is complete here: S_t(j) was issued after PV_t(j-1) and its
             // commit covers every earlier MMA of the issuing thread.
@@ -311,9 +318,8 @@ __global__ void __launch_bounds__(320, 1)
             const float p0 = ex2(fmaf(s[c0 + 2 * i], scale2, neg_m));
             const float p1 = ex2(fmaf(s[c0 + 2 * i + 1], scale2, neg_m));
             pk[i] = pack_bf16(p0, p1);
-            // l sums the bf16-rounded values that O += P V multiplies, so O / l
-            // is an exact convex combination of V rows.
-            l += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+            l += p0 + p1;
+            lr += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
           }
           tmem_st16(tS + c0 / 2, pk);
         }
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(320, 1)
       // Epilogue: O / l -> bf16, and LSE = ln 2 * (m + log2 l).
       if (ok && warp_wait(smem_u32(&bar_o[t]), 0, p.ctl, abort, 31)) {
         tc_fence_after();
-        const float inv_l = 1.0f / l;
+        const float inv_l = 1.0f / lr;
         __nv_bfloat16* orow = p.o + ((size_t)bh * p.N + row) * HD;
 #pragma unroll 1
         for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -369,9 +375,10 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   p.N = a.N;
   p.nq = (a.N + C::BM - 1) / C::BM;
   p.nkv = (a.N + C::BN - 1) / C::BN;
+  p.npairs = (p.nq + 1) / 2;
   p.scale2 = a.scale * 1.4426950408889634f;
   p.ctl = a.ctl;
-  dim3 grid(a.BH, (p.nq + 1) / 2);
+  dim3 grid((unsigned)((long)p.npairs * a.BH));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, p);
   return cudaGetLastError();
 }

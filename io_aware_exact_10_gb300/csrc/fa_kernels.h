@@ -24,6 +24,7 @@ struct FwdLaunch {
 // Everything a backward launch needs.
 struct BwdLaunch {
   CUtensorMap tq, tk, tv, tdo;  // bf16 [BH][N][d], box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tdq;              // fp32 dQacc [BH][N][d], box {32, 32, 1}, 128-byte swizzle
   const void* o;                // bf16 [BH][N][d]
   const void* dO;               // bf16 [BH][N][d]
   const float* lse;             // fp32 [BH][N]
