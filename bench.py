@@ -2,6 +2,7 @@
 """Benchmark: exact attention forward + backward on GB300 through the C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--sweep]
 
 A step is one pass of the whole hot path over one batch: fa_fwd (O, LSE) then
 fa_bwd (D preprocess, the backward kernel, dQ conversion).  The workload is the
@@ -19,6 +20,10 @@ With --gpus N > 1 (launched under torch.distributed.run) every rank processes
 its own copy of the workload (attention heads are independent: weak scaling,
 no data-path collective); the time is the max over ranks and the value sums
 the work of all ranks.  --impl reference times the fp64 CPU oracle instead.
+--workload picks another workload of io_aware_exact_10_gb300.workloads (the
+default line stays the GPT-2-medium one).  --sweep times the sequence-length
+sweep (N = 512 ... 32768, d = 64 and 128, H = 16, B*N = 65536, causal):
+forward and forward+backward TFLOP/s per point, printed as one JSON line.
 """
 from __future__ import annotations
 
@@ -343,17 +348,75 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """Forward and forward+backward TFLOP/s per sweep point (one JSON line)."""
+    import torch
+    import io_aware_exact_10_gb300 as fa
+    from io_aware_exact_10_gb300 import workloads as W
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peaks, _ = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    points = []
+    clocks = ClockSampler(0)
+    clocks.start()
+    for d in W.SWEEP_D:
+        for N in W.SWEEP_N:
+            w = W.sweep(N, d)
+            B, H = w.B, w.H
+            q, k, v, dO = W.make_inputs_on_device(w, dev)
+            o = torch.empty_like(q)
+            lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            wsb = fa.fa_bwd_workspace_size(B, H, N, d)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            f = lambda: fa.fa_fwd(q, k, v, o, lse, B, H, N, d, w.scale, 1, stream)
+            b = lambda: fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, w.scale, 1, ws,
+                                  wsb, stream)
+            res = {}
+            for name, fn, fl in (("fwd", f, w.fwd_flops()),
+                                 ("fwd_bwd", lambda: (f(), b()), w.fwd_flops() + w.bwd_flops())):
+                for _ in range(args.warmup):
+                    fn()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(args.steps):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / args.steps
+                res[name] = {"ms": ms, "tflops": fl / ms / 1e9, "pct_of_peak": 100 * fl / ms / 1e9 / peak}
+            if fa.fa_last_device_error(stream) != fa.FA_OK:
+                raise RuntimeError("device error during the sweep")
+            points.append({"N": N, "d": d, "B": B, "H": H, **res})
+            del q, k, v, dO, o, lse, dq, dk, dv, ws
+    clk = clocks.stop()
+    print(json.dumps({"metric": "attention fwd / fwd+bwd TFLOP/s vs N (causal, H=16, B*N=65536)",
+                      "unit": "TFLOP/s", "peak": peak, "steps": args.steps,
+                      "warmup": args.warmup, "data": "synthetic (seeded on the device)",
+                      "clocks": clk, "sweep": points}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="gpt2_medium")
+    ap.add_argument("--sweep", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from io_aware_exact_10_gb300 import workloads as W
-    w = W.GPT2_MEDIUM
+    if args.sweep:
+        run_sweep(args)
+        return
+    w = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
     else:

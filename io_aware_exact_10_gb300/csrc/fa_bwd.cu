@@ -17,13 +17,16 @@
 //                       TMEM; dQ contributions are added into dQacc (fp32)
 //   fa_bwd_dq_kernel    dq = bf16(scale * dQacc)                (memory bound)
 //
-// fa_bwd_kernel roles (320 threads):
-//   warps 0-3  P / dS warpgroup (thread = key row = TMEM lane)
-//   warps 4-7  dQ drain warpgroup (thread = query row = TMEM lane)
-//   warp  8    TMA producer (K, V once; then Q_i, dO_i through 2-slot rings)
-//   warp  9    tcgen05 MMA issuer and TMEM owner
+// fa_bwd_kernel roles (448 threads):
+//   warps 0-7   P / dS: thread = key row = TMEM lane; warps 0-3 take query
+//               columns 0-63 of the tile, warps 4-7 columns 64-127
+//   warps 8-11  dQ drain (thread = query row = TMEM lane), then dK epilogue
+//   warp  12    TMA producer (K, V once; then Q_i, dO_i through 2-slot rings)
+//   warp  13    tcgen05 MMA issuer and TMEM owner
 // Tensor memory (512 columns): ST (S^T, then P^T bf16) | DPT (dP^T, then dS^T
-// bf16, then dQ) | dV | dK.  Per query tile the MMA thread issues, in order:
+// bf16, then dQ) | dV | dK.  The bf16 pairs of P^T and dS^T for queries 0-63
+// sit in columns 0-31 of their region and those for queries 64-127 in
+// columns 64-95, inside the fp32 columns of the warpgroup that wrote them.  Per query tile the MMA thread issues, in order:
 //   S^T = K Q_i^T -> ST;  dP^T = V dO_i^T -> DPT;  dV += P^T dO_i;
 //   dK += dS^T Q_i;  dQ_i = dS K -> DPT.
 // dS is also written to shared memory (query-major) as the A operand of dQ.
@@ -113,7 +116,8 @@ struct BwdCfg {
   static constexpr int OFF_BAR = OFF_D + 2 * BQ * 4;
   static constexpr int NBAR = 20;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 448;
+  static constexpr int W_LOAD = 12, W_MMA = 13;  // warps 0-7: P / dS; 8-11: dQ drain
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + HD;
 };
@@ -122,8 +126,12 @@ struct BwdCfg {
 enum : int {
   B_KV = 0, B_QF0 = 1, B_QF1 = 2, B_DOF0 = 3, B_DOF1 = 4, B_QE0 = 5, B_QE1 = 6, B_DOE0 = 7,
   B_DOE1 = 8, B_ST = 9, B_DPT = 10, B_P = 11, B_DS = 12, B_DQF = 13, B_DQE = 14, B_FIN = 15,
-  B_DRAIN = 16, B_WG = 17, B_DSF = 18
+  B_DRAIN = 16, B_WG = 17, B_DSF = 18, B_COUNT = 19
 };
+// arrival counts: TMA / commit barriers take one arrival; B_P and B_DS one
+// per P/dS warp; B_DQE and B_DSF one per drain warp; B_WG every P/dS thread.
+__device__ __constant__ const uint32_t kBarCount[B_COUNT] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 8, 8,
+                                                             1, 4, 1, 1, 256, 4};
 
 struct BwdParams {
   const float* lse;
@@ -135,6 +143,12 @@ struct BwdParams {
   KernelCtl ctl;
 };
 
+// TMEM column, relative to the S^T (or dP^T) region, of the packed bf16 pairs
+// of P^T (or dS^T) for MMA K-step k (16 queries).  Each P/dS warpgroup packs
+// its 64 queries into the first 32 columns of its own 64-column half, which it
+// has already read: queries 0-63 -> columns 0-31, queries 64-127 -> 64-95.
+__device__ __forceinline__ uint32_t pcol(int k) { return (uint32_t)((k >> 2) * 64 + (k & 3) * 8); }
+
 __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
                                             volatile int* abort, uint32_t site) {
   const bool ok = mbar_wait(bar, parity, ctl, abort, site);
@@ -142,7 +156,7 @@ __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, const
 }
 
 template <int HD, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
@@ -176,11 +190,10 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     *abort = 0;
-    const int counts[19] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 4, 1, 1, 128, 4};
-    for (int i = 0; i < 19; ++i) mbar_init(bar(i), counts[i]);
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), kBarCount[i]);
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == C::W_MMA) {
     tmem_alloc(smem_u32(tmem_base_sh), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -189,13 +202,14 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_sh;
 
-  if (warp == 8) {
+  if (warp == C::W_LOAD) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
       tma_prefetch_desc(&tdo);
+      tma_prefetch_desc(&tdq);
       mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
       for (int b = 0; b < C::KB; ++b) {
         tma_load_3d(sK + b * 16384, &tk, bar(B_KV), b * 64, kt * C::BK, bh);
@@ -228,7 +242,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == C::W_MMA) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, C::BQ, false, false);  // S^T, dP^T
@@ -264,14 +278,14 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
-          mma_ts(tDV, tST + k * 8, sdesc_sw128(do0 + k * 2048, 16384, 1024), kIdG, u > 0 || k > 0);
+          mma_ts(tDV, tST + pcol(k), sdesc_sw128(do0 + k * 2048, 16384, 1024), kIdG, u > 0 || k > 0);
         mma_commit(bar(B_DOE0 + st));
         // dK += dS^T Q_i   (A = dS^T bf16 in TMEM)
         if (!(ok = mbar_wait(bar(B_DS), u & 1, p.ctl, abort, 25))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
-          mma_ts(tDK, tDPT + k * 8, sdesc_sw128(q0 + k * 2048, 16384, 1024), kIdG, u > 0 || k > 0);
+          mma_ts(tDK, tDPT + pcol(k), sdesc_sw128(q0 + k * 2048, 16384, 1024), kIdG, u > 0 || k > 0);
         // dQ_i = dS K   (M = queries, N = d, K = keys; A = dS smem query-major, B = K key-major)
 #pragma unroll
         for (int k = 0; k < C::BK / 16; ++k)
@@ -284,30 +298,34 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(bar(B_DRAIN));
       mbar_wait_quiet(bar(B_DRAIN), 0, 200000000ull);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------- P / dS warpgroup
-    const int r = warp * 32 + lane;                 // key row within the tile
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  } else if (warp < 8) {
+    // --------------------------------------------- P / dS warpgroups (x2)
+    // Thread = key row r (TMEM lane); warpgroup h takes query columns
+    // [64h, 64h + 64) of the tile.
+    const int h = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tST = tmem + lane_off + C::COL_ST, tDPT = tmem + lane_off + C::COL_DPT;
+    const int cb = 64 * h;                          // first query column of this thread
     const float scale2 = p.scale2;
     const size_t rowbase = (size_t)bh * p.N;
-    // stage the log2-scaled LSE and D of the first query tile
-    {
+    // warpgroup 0 stages the log2-scaled LSE and D of the first query tile
+    if (h == 0) {
       const int q = i0 * C::BQ + r;
       lse_sh[r] = q < p.N ? p.lse[rowbase + q] * kLog2e : INFINITY;
       d_sh[r] = q < p.N ? p.D[rowbase + q] : 0.f;
     }
-    // The warpgroup synchronises on an mbarrier (128 arrivals per phase) so
+    // Both warpgroups synchronise on an mbarrier (256 arrivals per phase) so
     // that the wait stays bounded if another warp gives up.
     mbar_arrive(bar(B_WG));
     bool ok = warp_wait_b(bar(B_WG), 0, p.ctl, abort, 34);
     for (int u = 0; u < nit && ok; ++u) {
       const int qt = i0 + u;
-      const float* lse_u = lse_sh + (u & 1) * C::BQ;
-      const float* d_u = d_sh + (u & 1) * C::BQ;
+      const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
+      const float* d_u = d_sh + (u & 1) * C::BQ + cb;
       // prefetch the next tile's statistics
       float nl = INFINITY, nd = 0.f;
-      if (u + 1 < nit) {
+      if (h == 0 && u + 1 < nit) {
         const int q = (qt + 1) * C::BQ + r;
         if (q < p.N) {
           nl = p.lse[rowbase + q] * kLog2e;
@@ -316,18 +334,14 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (!(ok = warp_wait_b(bar(B_ST), u & 1, p.ctl, abort, 30))) break;
       tc_fence_after();
-      float pr[128];
-      {
-        uint32_t* pu = reinterpret_cast<uint32_t*>(pr);
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32)
-          tmem_ld32(tST + c0, *reinterpret_cast<uint32_t(*)[32]>(pu + c0));
-        tmem_wait_ld();
-      }
+      float pr[64];
+      tmem_ld32(tST + cb, *reinterpret_cast<uint32_t(*)[32]>(pr));
+      tmem_ld32(tST + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(pr + 32));
+      tmem_wait_ld();
       // P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query < key
       const bool diag = CAUSAL && qt == kt;
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
@@ -335,15 +349,15 @@ __global__ void __launch_bounds__(320, 1)
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int i = 4 * i4 + e;
-            float v = ex2(fmaf(pr[c0 + i], scale2, -lv[e]));
-            if (diag && (c0 + i) < r) v = 0.f;
-            pr[c0 + i] = v;
+            const int i = c0 + 4 * i4 + e;
+            float v = ex2(fmaf(reinterpret_cast<float*>(pr)[i], scale2, -lv[e]));
+            if (diag && cb + i < r) v = 0.f;
+            pr[i] = v;
           }
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pr[c0 + 2 * i], pr[c0 + 2 * i + 1]);
-        tmem_st16(tST + c0 / 2, pk);
+        tmem_st16(tST + cb + c0 / 2, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -355,12 +369,12 @@ __global__ void __launch_bounds__(320, 1)
       // the previous tile has been read out of it
       if (u > 0 && !(ok = warp_wait_b(bar(B_DSF), (u - 1) & 1, p.ctl, abort, 32))) break;
       tc_fence_after();
-      const uint32_t srow = sDS + r * 128;
+      const uint32_t srow = sDS + (uint32_t)h * 16384u + (uint32_t)r * 128u;
       const uint32_t sw = (uint32_t)(r & 7);
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t dp[32];
-        tmem_ld32(tDPT + c0, dp);
+        tmem_ld32(tDPT + cb + c0, dp);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
@@ -372,15 +386,13 @@ __global__ void __launch_bounds__(320, 1)
           pk[2 * i4 + 1] = pack_bf16(pr[c0 + i + 2] * (__uint_as_float(dp[i + 2]) - d4.z),
                                      pr[c0 + i + 3] * (__uint_as_float(dp[i + 3]) - d4.w));
         }
-        tmem_st16(tDPT + c0 / 2, pk);
-        // shared copy, query-major 128-byte swizzled: block c0/64, chunks of 8 queries
-        const uint32_t blk = sDS + (uint32_t)(c0 / 64) * 16384;
+        tmem_st16(tDPT + cb + c0 / 2, pk);
+        // shared copy, query-major 128-byte swizzled: block h, chunks of 8 queries
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          const uint32_t chunk = (uint32_t)((c0 % 64) / 8 + cc);
-          const uint32_t addr = blk + (srow - sDS) + ((chunk ^ sw) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * cc]),
-                       "r"(pk[4 * cc + 1]), "r"(pk[4 * cc + 2]), "r"(pk[4 * cc + 3])
+          const uint32_t chunk = (uint32_t)(c0 / 8 + cc);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + ((chunk ^ sw) << 4)),
+                       "r"(pk[4 * cc]), "r"(pk[4 * cc + 1]), "r"(pk[4 * cc + 2]), "r"(pk[4 * cc + 3])
                        : "memory");
         }
       }
@@ -390,18 +402,20 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS));
       // publish the next tile's statistics
-      lse_sh[((u + 1) & 1) * C::BQ + r] = nl;
-      d_sh[((u + 1) & 1) * C::BQ + r] = nd;
+      if (h == 0) {
+        lse_sh[((u + 1) & 1) * C::BQ + r] = nl;
+        d_sh[((u + 1) & 1) * C::BQ + r] = nd;
+      }
       mbar_arrive(bar(B_WG));
       if (!(ok = warp_wait_b(bar(B_WG), (u + 1) & 1, p.ctl, abort, 35))) break;
     }
-    // epilogue: dV rows of this key tile
+    // epilogue: dV rows of this key tile, columns [h*HD/2, (h+1)*HD/2)
     if (ok && warp_wait_b(bar(B_FIN), 0, p.ctl, abort, 33)) {
       tc_fence_after();
       const int key = kt * C::BK + r;
       __nv_bfloat16* dst = p.dv + (rowbase + key) * HD;
 #pragma unroll 1
-      for (int c0 = 0; c0 < HD; c0 += 32) {
+      for (int c0 = h * (HD / 2); c0 < (h + 1) * (HD / 2); c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + C::COL_DV + c0, v);
         tmem_wait_ld();
@@ -417,9 +431,10 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ---------------------------------------------------------- dQ drain
-    // dQ_i (128 query rows x d, fp32) leaves TMEM into registers, goes through
-    // this warp's 8 KB slice of the dS buffer as 32-row x 32-column boxes
-    // (128-byte swizzled), and is added into dQacc by TMA bulk reductions.
+    // dQ_i (128 query rows x d, fp32) leaves TMEM 64 columns at a time, goes
+    // through this warp's 8 KB slice of the dS buffer as two 32-row x
+    // 32-column boxes (128-byte swizzled), and is added into dQacc by TMA
+    // bulk reductions.
     const int sp = warp & 3;
     const int r = sp * 32 + lane;  // query row within the tile (dQ) / key row (dK)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
@@ -430,18 +445,19 @@ __global__ void __launch_bounds__(320, 1)
     for (int u = 0; u < nit; ++u) {
       if (!(ok = warp_wait_b(bar(B_DQF), u & 1, p.ctl, abort, 40))) break;
       tc_fence_after();
-      uint32_t v[HD];
-#pragma unroll
-      for (int c0 = 0; c0 < HD; c0 += 32)
-        tmem_ld32(tmem + lane_off + C::COL_DPT + c0, *reinterpret_cast<uint32_t(*)[32]>(v + c0));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DQE));  // dQ's TMEM columns are free again
       const int y = (i0 + u) * C::BQ + sp * 32;
 #pragma unroll
-      for (int h = 0; h < HD / 64; ++h) {
-        if (h > 0) {
+      for (int hh = 0; hh < HD / 64; ++hh) {
+        uint32_t v[64];
+        tmem_ld32(tmem + lane_off + C::COL_DPT + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32(tmem + lane_off + C::COL_DPT + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_wait_ld();
+        if (hh == HD / 64 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_DQE));  // dQ's TMEM columns are free again
+        }
+        if (hh > 0) {
           if (lane == 0) bulk_wait_group_read<0>();
           __syncwarp();
         }
@@ -450,7 +466,7 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t row = stage + (uint32_t)bb * 4096u + (uint32_t)lane * 128u;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const int col = h * 64 + bb * 32 + c * 4;
+            const int col = bb * 32 + c * 4;
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((uint32_t)c ^ sw) << 4)),
                          "r"(v[col]), "r"(v[col + 1]), "r"(v[col + 2]), "r"(v[col + 3])
                          : "memory");
@@ -459,8 +475,8 @@ __global__ void __launch_bounds__(320, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(&tdq, stage, (2 * h) * 32, y, bh);
-          tma_reduce_add_3d(&tdq, stage + 4096u, (2 * h + 1) * 32, y, bh);
+          tma_reduce_add_3d(&tdq, stage, (2 * hh) * 32, y, bh);
+          tma_reduce_add_3d(&tdq, stage + 4096u, (2 * hh + 1) * 32, y, bh);
           bulk_commit_group();
         }
       }
@@ -496,7 +512,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::W_MMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);

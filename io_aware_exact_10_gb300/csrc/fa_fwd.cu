@@ -123,7 +123,6 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
@@ -242,7 +241,7 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(smem_u32(&bar_drain));
       mbar_wait_quiet(smem_u32(&bar_drain), 0, 200000000ull);
     }
-  } else {
+  } else if (warp < 8) {
     // -------------------------------------------------------------- softmax
     const int t = warp >> 2;           // query tile of this warpgroup
     const int sp = warp & 3;           // TMEM lane quarter of this warp
@@ -285,9 +284,14 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= lim) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // row max: four independent chains of three-input max
+        float mc[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 4; c < 128; c += 8) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) mc[e] = fmax3(mc[e], s[c + 2 * e], s[c + 2 * e + 1]);
+        }
+        const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
         const float m_new = fmaxf(m, mx * scale2);
         const bool need = m_new > m + kTau;
         if (__any_sync(0xffffffffu, need)) {
@@ -309,19 +313,30 @@ __global__ void __launch_bounds__(320, 1)
             }
           }
         }
-        const float neg_m = -m;
+        // P = exp2(scale2 * s - m), two elements per paired FMA and add
+        const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-m, -m);
+        uint64_t l2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(s[c0 + 2 * i], scale2, neg_m));
-            const float p1 = ex2(fmaf(s[c0 + 2 * i + 1], scale2, neg_m));
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), sc2, nm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
             pk[i] = pack_bf16(p0, p1);
-            l += p0 + p1;
-            lr += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+            l2 = f2_add(l2, f2_pack(p0, p1));
+            lr2 = f2_add(lr2, f2_pack(__uint_as_float(pk[i] << 16),
+                                      __uint_as_float(pk[i] & 0xFFFF0000u)));
           }
           tmem_st16(tS + c0 / 2, pk);
+        }
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(l2, a0, a1);
+          f2_unpack(lr2, b0, b1);
+          l += a0 + a1;
+          lr += b0 + b1;
         }
         tmem_wait_st();
         tc_fence_before();

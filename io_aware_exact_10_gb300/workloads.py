@@ -86,6 +86,34 @@ def make_inputs(w: Workload, device: str = "cpu", with_grad: bool = True):
     return tuple(out)
 
 
+WORKLOADS = {w.name: w for w in (SINGLE_HEAD, GPT2_MEDIUM, GPT2_MEDIUM_CAUSAL, LONG_CAUSAL,
+                                  STRESS_CAUSAL, STRESS)}
+WORKLOADS.update({sweep(N, d).name: sweep(N, d) for N in SWEEP_N for d in SWEEP_D})
+# short aliases
+WORKLOADS.update({"gpt2_medium": GPT2_MEDIUM, "gpt2_medium_causal": GPT2_MEDIUM_CAUSAL,
+                  "long_causal": LONG_CAUSAL, "stress": STRESS, "stress_causal": STRESS_CAUSAL,
+                  "single_head": SINGLE_HEAD})
+
+
+def make_inputs_on_device(w: Workload, device, with_grad: bool = True):
+    """The same recipe drawn by a seeded generator on `device` (a different
+    random stream than make_inputs; used where only timing matters and the
+    host-side draw of a large workload would dominate)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    out = []
+    for name in (("q", "k", "v", "dO") if with_grad else ("q", "k", "v")):
+        t = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
+        if name in ("q", "k") and w.qk_std != 1.0:
+            t.mul_(w.qk_std)
+        if name == "k" and w.boost_every:
+            rows = torch.arange(w.N, device=device)
+            t[:, :, ((rows + 1) % w.boost_every) == 0, :] *= w.boost
+        out.append(t.to(torch.bfloat16))
+    return tuple(out)
+
+
 def random_bf16(shape, seed: int, std: float = 1.0, device: str = "cpu"):
     """One bf16 tensor drawn N(0, std^2) from its own seeded CPU generator."""
     g = torch.Generator(device="cpu")
