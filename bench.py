@@ -218,13 +218,10 @@ def run_ours(args, w):
             dist.barrier()
         torch.cuda.synchronize()
 
+    from io_aware_exact_10_gb300.replicas import max_over_ranks as _max_over_ranks
+
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return _max_over_ranks(x, device=dev)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
@@ -260,7 +257,8 @@ def run_ours(args, w):
 
     flops_step = w.fwd_flops() + w.bwd_flops()
     ms_step = ms_total / args.steps
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    from io_aware_exact_10_gb300.replicas import whole_job_rate
+    value = whole_job_rate(flops_step, world, ms_step * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     peak_sus = float(peaks.get("bf16_tflops_sustained", peak))

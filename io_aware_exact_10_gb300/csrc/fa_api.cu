@@ -24,6 +24,7 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 struct DeviceState {
   std::once_flag once;
   bool supported = false;
+  int num_sms = 0;
   unsigned long long* err = nullptr;  // device address of g_fa_error_word
   cudaError_t init_error = cudaSuccess;
 };
@@ -58,6 +59,7 @@ fa_status current_device(DeviceState** out) {
     cudaDeviceProp prop;
     if ((st.init_error = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return;
     st.supported = prop.major == 10 && prop.minor == 3;
+    st.num_sms = prop.multiProcessorCount;
     void* p = nullptr;
     if ((st.init_error = cudaGetSymbolAddress(&p, g_fa_error_word)) != cudaSuccess) return;
     st.err = static_cast<unsigned long long*>(p);
@@ -155,6 +157,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   a.d = d;
   a.scale = scale;
   a.causal = causal;
+  a.num_sms = dev->num_sms;
   a.ctl.err = dev->err;
   a.ctl.timeout_ns = timeout_ns();
   if (fa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
@@ -207,6 +210,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.d = d;
   a.scale = scale;
   a.causal = causal;
+  a.num_sms = dev->num_sms;
   a.ctl.err = dev->err;
   a.ctl.timeout_ns = timeout_ns();
   if (fa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {

@@ -138,7 +138,7 @@ struct BwdParams {
   const float* D;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int N, nq, nkv;
+  int N, nq, nkv, BH, group;
   float scale, scale2;
   KernelCtl ctl;
 };
@@ -174,11 +174,13 @@ __global__ void __launch_bounds__(448, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One-dimensional grid, key tiles of a head adjacent: the CTAs of one head
-  // run together, share its Q, dO in L2 and add into the same dQ rows (which
-  // then stay in L2).  Key tile 0 (the most work when causal) comes first.
-  const int bh = blockIdx.x / p.nkv;
-  const int kt = blockIdx.x % p.nkv;
+  // One-dimensional grid over (head group, key tile, head): the CTAs of a
+  // group's heads run together, share their Q, dO in L2 and add into the same
+  // dQ rows (which then stay in L2).  Key tile 0 (the most work when causal)
+  // of every head in the group comes first.
+  const GridPos gp = decode_grid((int)blockIdx.x, p.BH, p.nkv, p.group);
+  const int bh = gp.bh;
+  const int kt = gp.rank;
   const int i0 = CAUSAL ? kt : 0;                  // first query tile that sees this key tile
   const int nit = p.nq - i0;                       // query tiles to process
 
@@ -533,6 +535,8 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   p.N = a.N;
   p.nq = (a.N + C::BQ - 1) / C::BQ;
   p.nkv = (a.N + C::BK - 1) / C::BK;
+  p.BH = a.BH;
+  p.group = head_group(a.BH, p.nkv, a.num_sms);
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;

@@ -52,7 +52,7 @@ struct FwdCfg {
 struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
-  int N, nq, nkv, npairs;
+  int N, nq, nkv, npairs, BH, group;
   float scale2;  // scale * log2(e)
   KernelCtl ctl;
 };
@@ -84,11 +84,12 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort = &abort_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One-dimensional grid, query-tile pairs of a head adjacent: the CTAs that
-  // share a head's K and V run together and find them in L2.  Within a head
-  // the heaviest (causal) pair launches first.
-  const int bh = blockIdx.x / p.npairs;
-  const int qt0 = 2 * (p.npairs - 1 - (int)(blockIdx.x % p.npairs));
+  // One-dimensional grid over (head group, pair rank, head): the CTAs that
+  // share a head's K and V run together and find them in L2, and within a
+  // group the heaviest (causal) query-tile pairs launch first.
+  const GridPos gp = decode_grid((int)blockIdx.x, p.BH, p.npairs, p.group);
+  const int bh = gp.bh;
+  const int qt0 = 2 * (p.npairs - 1 - gp.rank);
   bool valid[2];
   int nkv_t[2];
   for (int t = 0; t < 2; ++t) {
@@ -391,6 +392,8 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   p.nq = (a.N + C::BM - 1) / C::BM;
   p.nkv = (a.N + C::BN - 1) / C::BN;
   p.npairs = (p.nq + 1) / 2;
+  p.BH = a.BH;
+  p.group = head_group(a.BH, p.npairs, a.num_sms);
   p.scale2 = a.scale * 1.4426950408889634f;
   p.ctl = a.ctl;
   dim3 grid((unsigned)((long)p.npairs * a.BH));

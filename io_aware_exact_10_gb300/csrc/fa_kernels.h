@@ -16,6 +16,7 @@ struct FwdLaunch {
   void* o;                      // bf16 [BH][N][d]
   float* lse;                   // fp32 [BH][N]
   int BH, N, d;
+  int num_sms;                  // multiprocessors of the device (grid ordering)
   float scale;
   int causal;
   KernelCtl ctl;
@@ -34,10 +35,35 @@ struct BwdLaunch {
   void* dk;                     // bf16 [BH][N][d]
   void* dv;                     // bf16 [BH][N][d]
   int BH, N, d;
+  int num_sms;                  // multiprocessors of the device (grid ordering)
   float scale;
   int causal;
   KernelCtl ctl;
 };
+
+// Heads per scheduling group: enough tiles for about two waves of CTAs, so a
+// group's heads stay resident in L2 while its heaviest tiles start first.
+inline int head_group(int BH, int tiles_per_head, int num_sms) {
+  int g = (2 * num_sms + tiles_per_head - 1) / tiles_per_head;
+  return g < 1 ? 1 : (g > BH ? BH : g);
+}
+
+// Decode a one-dimensional grid index into (head, tile rank): heads come in
+// groups of `group`; inside a group the tile rank varies slowest, so rank 0
+// (the heaviest tile when causal) of every head in the group comes first.
+struct GridPos {
+  int bh, rank;
+};
+__host__ __device__ inline GridPos decode_grid(int L, int BH, int tiles, int group) {
+  const int per_group = group * tiles;
+  const int g = L / per_group;
+  const int idx = L - g * per_group;
+  const int gh = (BH - g * group) < group ? (BH - g * group) : group;
+  GridPos r;
+  r.rank = idx / gh;
+  r.bh = g * group + (idx - r.rank * gh);
+  return r;
+}
 
 // Each returns cudaSuccess or the launch error; nothing is synchronised.
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
