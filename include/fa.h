@@ -96,6 +96,35 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  struct CUstream_st* stream);
 
 /*
+ * Backward with no workspace argument and no allocation.  The paper has no
+ * counterpart; this entry point exists for callers that cannot allocate
+ * device memory: plugins inside a host framework that owns all device memory
+ * and gives them none, and latency-critical loops that must not call
+ * cudaMalloc (it may synchronise the device and takes unbounded time).
+ *
+ * Same arguments, semantics and outputs as fa_bwd minus the workspace: the
+ * scratch (D and the fp32 dQ accumulator) lives in a 64 MiB array that the
+ * library holds on every device that loads it, until the process exits.
+ *   - Capacity: fa_bwd_workspace_size(B, H, N, d) must be <= 64 MiB
+ *     (67108864 bytes): up to about 130,000 rows (B*H*N) at d=128 and
+ *     258,000 at d=64; larger problems return FA_ERR_INVALID_ARG before
+ *     anything is launched.
+ *   - The first call on a device looks up the array's device address (a
+ *     one-time runtime query, with that device current); make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one array.  Each call rewrites D and
+ *     re-zeroes the accumulator before use, so earlier contents never leak
+ *     into a result, but calls that overlap on the GPU (on different streams
+ *     without ordering between them) race on the array and give wrong
+ *     gradients.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal,
+                         struct CUstream_st* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up on a wait), or
  * FA_ERR_DEVICE when the synchronisation itself reported a CUDA error.

@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     FA_OK,
     FAError,
     fa_bwd,
+    fa_bwd_noalloc,
     fa_bwd_workspace_size,
     fa_device_error_word,
     fa_fwd,

@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_workspace_size.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
         L.fa_bwd.restype = i
+        L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd_noalloc.restype = i
         L.fa_last_device_error.argtypes = [vp]
         L.fa_last_device_error.restype = i
         L.fa_device_error_word.argtypes = [vp]
@@ -115,6 +117,19 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace
                      int(causal), _ptr(workspace), int(workspace_bytes), _stream(stream))
     if check:
         _check(s, "fa_bwd")
+    return s
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, stream=None,
+                   check=True) -> int:
+    """fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal,
+    stream) -> status: the backward for callers that cannot allocate a
+    workspace; its scratch is a fixed 64 MiB array inside the library."""
+    s = lib().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                             _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), float(scale),
+                             int(causal), _stream(stream))
+    if check:
+        _check(s, "fa_bwd_noalloc")
     return s
 
 

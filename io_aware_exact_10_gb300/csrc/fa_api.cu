@@ -280,3 +280,65 @@ const char* fa_strerror(int status) {
 const char* fa_version(void) { return "io_aware_exact_10_gb300 0.1.0 (sm_103a)"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward without a caller-provided workspace.
+//
+// Some callers cannot hand the library a workspace: a plugin running inside a
+// host framework that owns all device memory and gives the plugin none, or a
+// latency-critical loop that must never call cudaMalloc (which may
+// synchronise the device and takes unbounded time).  For them the backward's
+// scratch (D and the fp32 dQ accumulator) lives in one file-scope device array
+// that every GPU loading the library holds until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = 64ull << 20;  // 64 MiB per device
+static __device__ __align__(256) unsigned char g_fa_bwd_static_scratch[kStaticScratchBytes];
+
+struct StaticScratch {
+  std::once_flag once;
+  void* ptr = nullptr;  // device address of g_fa_bwd_static_scratch on this device
+  cudaError_t err = cudaSuccess;
+};
+StaticScratch g_static_scratch[kMaxDevices];
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal,
+                         struct CUstream_st* stream) {
+  bool empty = false;
+  fa_status s = check_common(B, H, N, d, scale, causal, &empty);
+  if (s != FA_OK || empty) return s;
+  // Problems whose D + dQ accumulator exceed the static array are refused.
+  if (fa_bwd_workspace_size(B, H, N, d) > kStaticScratchBytes) return FA_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  if ((s = current_device(&dev)) != FA_OK) return s;
+  int id = -1;
+  if (cudaGetDevice(&id) != cudaSuccess || id < 0 || id >= kMaxDevices) {
+    cudaGetLastError();
+    return FA_ERR_NO_DEVICE;
+  }
+  // Once per device, with that device current: the host-side name of the
+  // array is not a device address, so ask the runtime for the real one.
+  StaticScratch& sc = g_static_scratch[id];
+  std::call_once(sc.once, [&sc] {
+    void* p = nullptr;
+    sc.err = cudaGetSymbolAddress(&p, g_fa_bwd_static_scratch);
+    if (sc.err == cudaSuccess) sc.ptr = p;
+  });
+  if (sc.err != cudaSuccess || !sc.ptr) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  // The preprocess kernel of fa_bwd rewrites D and zeroes the dQ accumulator
+  // on every call, so nothing left in the array by an earlier call leaks in.
+  return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, sc.ptr,
+                kStaticScratchBytes, stream);
+}
+
+}  // extern "C"
