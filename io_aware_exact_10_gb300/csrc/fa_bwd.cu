@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P));
-      // dS^T = P^T o (dP^T - D)
+      // dS^T = P^T o (dP^T - D), with P^T the bf16 values dV multiplied
       if (!(ok = warp_wait_b(bar(B_DPT), u & 1, p.ctl, abort, 31))) break;
       // the dS buffer doubles as the dQ staging area: wait until the drain of
       // the previous tile has been read out of it
@@ -375,18 +375,21 @@ __global__ void __launch_bounds__(448, 1)
       const uint32_t sw = (uint32_t)(r & 7);
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t dp[32];
+        // dP^T of 32 queries, and the bf16 pairs of P^T that dV used for them
+        uint32_t dp[32], pp[16];
         tmem_ld32(tDPT + cb + c0, dp);
+        tmem_ld16(tST + cb + c0 / 2, pp);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
           const float4 d4 = reinterpret_cast<const float4*>(d_u + c0)[i4];
           const int i = 4 * i4;
-          pk[2 * i4] = pack_bf16(pr[c0 + i] * (__uint_as_float(dp[i]) - d4.x),
-                                 pr[c0 + i + 1] * (__uint_as_float(dp[i + 1]) - d4.y));
-          pk[2 * i4 + 1] = pack_bf16(pr[c0 + i + 2] * (__uint_as_float(dp[i + 2]) - d4.z),
-                                     pr[c0 + i + 3] * (__uint_as_float(dp[i + 3]) - d4.w));
+          const uint32_t w0 = pp[2 * i4], w1 = pp[2 * i4 + 1];
+          pk[2 * i4] = pack_bf16(__uint_as_float(w0 << 16) * (__uint_as_float(dp[i]) - d4.x),
+                                 __uint_as_float(w0 & 0xFFFF0000u) * (__uint_as_float(dp[i + 1]) - d4.y));
+          pk[2 * i4 + 1] = pack_bf16(__uint_as_float(w1 << 16) * (__uint_as_float(dp[i + 2]) - d4.z),
+                                     __uint_as_float(w1 & 0xFFFF0000u) * (__uint_as_float(dp[i + 3]) - d4.w));
         }
         tmem_st16(tDPT + cb + c0 / 2, pk);
         // shared copy, query-major 128-byte swizzled: block h, chunks of 8 queries

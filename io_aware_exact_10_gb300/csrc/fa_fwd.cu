@@ -266,31 +266,30 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after();
-        float s[128];
-        {
-          uint32_t* su = reinterpret_cast<uint32_t*>(s);
+        // Keys c >= lim of this row are masked in this tile (causal diagonal,
+        // or the ragged last tile).
+        int lim = 128;
+        if (CAUSAL && j == qt) lim = r + 1;
+        if (!CAUSAL && tail && j == p.nkv - 1) lim = p.N - j * C::BN;
+        // Pass 1: row max, 64 columns at a time (the whole row is never held
+        // in registers; pass 2 reads it again chunk by chunk).
+        float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32)
-            tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(su + c0));
+        for (int h = 0; h < 128; h += 64) {
+          float sv[64];
+          tmem_ld32(tS + h, *reinterpret_cast<uint32_t(*)[32]>(sv));
+          tmem_ld32(tS + h + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
           tmem_wait_ld();
-        }
-        if (CAUSAL && j == qt) {
+          if (lim < 128) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > r) s[c] = -INFINITY;
-        }
-        if (!CAUSAL && tail && j == p.nkv - 1) {
-          const int lim = p.N - j * C::BN;
+            for (int c = 0; c < 64; ++c)
+              if (h + c >= lim) sv[c] = -INFINITY;
+          }
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= lim) s[c] = -INFINITY;
-        }
-        // row max: four independent chains of three-input max
-        float mc[4] = {s[0], s[1], s[2], s[3]};
+          for (int c = 0; c < 64; c += 8) {
 #pragma unroll
-        for (int c = 4; c < 128; c += 8) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) mc[e] = fmax3(mc[e], s[c + 2 * e], s[c + 2 * e + 1]);
+            for (int e = 0; e < 4; ++e) mc[e] = fmax3(mc[e], sv[c + 2 * e], sv[c + 2 * e + 1]);
+          }
         }
         const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
         const float m_new = fmaxf(m, mx * scale2);
@@ -314,16 +313,29 @@ __global__ void __launch_bounds__(320, 1)
             }
           }
         }
-        // P = exp2(scale2 * s - m), two elements per paired FMA and add
+        // Pass 2: P = exp2(scale2 * s - m), two elements per paired FMA and
+        // add, 32 columns at a time with the next chunk's load in flight.  P
+        // of chunk c lands in columns [c/2, c/2 + 16), all already read.
         const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-m, -m);
         uint64_t l2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
+        float sbuf[2][32];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sbuf[0]));
+        tmem_wait_ld();
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
+          float* sv = sbuf[(c0 / 32) & 1];
+          if (c0 + 32 < 128)
+            tmem_ld32(tS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sbuf[((c0 / 32) + 1) & 1]));
+          if (lim < 128) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c0 + c >= lim) sv[c] = -INFINITY;
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float x0, x1;
-            f2_unpack(f2_fma(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), sc2, nm2), x0, x1);
+            f2_unpack(f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), sc2, nm2), x0, x1);
             const float p0 = ex2(x0), p1 = ex2(x1);
             pk[i] = pack_bf16(p0, p1);
             l2 = f2_add(l2, f2_pack(p0, p1));
@@ -331,6 +343,7 @@ __global__ void __launch_bounds__(320, 1)
                                       __uint_as_float(pk[i] & 0xFFFF0000u)));
           }
           tmem_st16(tS + c0 / 2, pk);
+          if (c0 + 32 < 128) tmem_wait_ld();
         }
         {
           float a0, a1, b0, b1;
