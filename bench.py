@@ -40,9 +40,31 @@ sys.path.insert(0, ROOT)
 
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-# Main backward kernel share of the fa_bwd call, and DRAM bytes per launch,
-# from the ncu summaries committed under profiles/ (None until captured).
-NCU_TRAFFIC_BYTES = None
+# DRAM bytes (read + write) of one fa_bwd call on the default workload, summed
+# over its three launches, from one ncu capture (profiles/
+# launches_gpt2_medium_fwd_bwd.md), and the commit of the kernels it measured.
+# The bench line reports it only while the kernel sources are unchanged.
+NCU_TRAFFIC_BYTES = 2148.0e6
+NCU_TRAFFIC_COMMIT = "6955ff5"
+NCU_TRAFFIC_SOURCES_SHA256 = None
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "io_aware_exact_10_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic():
+    """The captured traffic if the kernel sources still match the capture."""
+    if NCU_TRAFFIC_SOURCES_SHA256 and kernel_sources_sha256() == NCU_TRAFFIC_SOURCES_SHA256:
+        return NCU_TRAFFIC_BYTES
+    return None
 
 
 def load_peaks():
@@ -329,7 +351,7 @@ def run_ours(args, w):
             "frac": bwd_tf / peak,
             "frac_sustained": bwd_tf / peak_sus,
             "peak_source": f"{peak_src} bf16 burst ({PEAKS_PATH if peak_src == 'measured' else 'recipe fallback'})",
-            "traffic": NCU_TRAFFIC_BYTES,
+            "traffic": ncu_traffic(),
         },
         "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
