@@ -34,9 +34,10 @@ namespace fa {
 namespace {
 
 constexpr float kTau = 8.0f;
+constexpr int kSplit = 1;  // softmax warpgroups per query tile (2 measured no faster)
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int HD>
+template <int HD, int NH>
 struct FwdCfg {
   static constexpr int BM = 128;                  // query rows per tile
   static constexpr int BN = 128;                  // keys per K/V tile
@@ -45,7 +46,13 @@ struct FwdCfg {
   static constexpr int KVTILE = BN * HD * 2;      // bytes of one K or V tile
   static constexpr int STAGES = HD == 128 ? 4 : 8;
   static constexpr int SMEM = 2 * QTILE + STAGES * KVTILE + 1024;
-  static constexpr int THREADS = 320;
+  // NH warpgroups share each query tile's softmax, each taking 128 / NH of
+  // the key columns; then come the TMA warp and the MMA warp.
+  static constexpr int WS = 8 * NH;               // softmax warps
+  static constexpr int W_LOAD = WS, W_MMA = WS + 1;
+  static constexpr int THREADS = (WS + 2) * 32;
+  static constexpr int CPT = 128 / NH;            // key columns per softmax thread
+  static constexpr int OCPT = HD / NH;            // O columns per softmax thread
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -64,11 +71,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const K
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int HD, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+// TMEM column (relative to S_t) of the bf16 pairs of P for K-step k (16 keys
+// of the P V contraction).  Each softmax warpgroup packs its keys into the
+// first half of its own, already read, column range.
+template <int NH>
+__device__ __forceinline__ uint32_t p_col(int k) {
+  return NH == 1 ? (uint32_t)(k * 8) : (uint32_t)(k * 8 + (k >= 4 ? 32 : 0));
+}
+
+template <int HD, bool CAUSAL, int NH>
+__global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  using C = FwdCfg<HD>;
+  using C = FwdCfg<HD, NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
@@ -79,6 +94,8 @@ __global__ void __launch_bounds__(320, 1)
   __shared__ __align__(8) uint64_t bar_p[2];
   __shared__ __align__(8) uint64_t bar_o[2];
   __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ __align__(8) uint64_t bar_x[2][4];  // partner-warp exchange (NH == 2)
+  __shared__ float xch[2][2][2][128];             // [tile][parity][half][row]
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   volatile int* abort = &abort_sh;
@@ -106,7 +123,8 @@ __global__ void __launch_bounds__(320, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bar_q[t]), 1);
       mbar_init(smem_u32(&bar_s[t]), 1);
-      mbar_init(smem_u32(&bar_p[t]), 4);
+      mbar_init(smem_u32(&bar_p[t]), 4 * NH);
+      for (int sp = 0; sp < 4; ++sp) mbar_init(smem_u32(&bar_x[t][sp]), 64);
       mbar_init(smem_u32(&bar_o[t]), 1);
     }
     for (int s = 0; s < C::STAGES; ++s) {
@@ -116,7 +134,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(smem_u32(&bar_drain), 1);
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == C::W_MMA) {
     tmem_alloc(smem_u32(&tmem_base_sh), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -124,7 +142,7 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  if (warp == 8) {
+  if (warp == C::W_LOAD) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
       tma_prefetch_desc(&tq);
@@ -161,7 +179,7 @@ __global__ void __launch_bounds__(320, 1)
           if (valid[t]) mbar_wait_quiet(smem_u32(&bar_q[t]), 0, 200000000ull);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == C::W_MMA) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, C::BN, false, false);
@@ -186,7 +204,7 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t b0 = sRing + slot * C::KVTILE;
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts(tmem + 256 + t * HD, tmem + t * 128 + k * 8,
+          mma_ts(tmem + 256 + t * HD, tmem + t * 128 + p_col<NH>(k),
                  sdesc_sw128(b0 + k * 2048, C::BN * 128, 1024), kIdPV, acc || k > 0);
       };
 
@@ -242,11 +260,17 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(smem_u32(&bar_drain));
       mbar_wait_quiet(smem_u32(&bar_drain), 0, 200000000ull);
     }
-  } else if (warp < 8) {
+  } else if (warp < C::WS) {
     // -------------------------------------------------------------- softmax
-    const int t = warp >> 2;           // query tile of this warpgroup
-    const int sp = warp & 3;           // TMEM lane quarter of this warp
-    const int r = sp * 32 + lane;      // row within the tile
+    // Thread = (query row r, column half h): warps [4*NH*t, 4*NH*(t+1)) serve
+    // query tile t; warp w covers TMEM lanes 32*(w % 4) and key columns
+    // [h*CPT, (h+1)*CPT) of the tile.
+    const int t = warp / (4 * NH);
+    const int h = (warp % (4 * NH)) / 4;
+    const int sp = warp & 3;
+    const int r = sp * 32 + lane;
+    const int cb = h * C::CPT;          // first key column of this thread
+    const int ob = h * C::OCPT;         // first O column of this thread
     if (valid[t]) {
       const int qt = qt0 + t;
       const int row = qt * C::BM + r;
@@ -255,9 +279,24 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t tO = tmem + lane_off + 256 + t * HD;
       const float scale2 = p.scale2;
       const bool tail = (p.N % C::BN) != 0;
+      const uint32_t xbar = smem_u32(&bar_x[t][sp]);
+      int xph = 0;
+      // Exchange one value per row with the partner warp (the other column
+      // half of the same rows); bounded like every other wait.  Slots
+      // alternate with every exchange: a value is overwritten only after the
+      // partner has arrived at the next exchange, i.e. after it read it.
+      auto exchange = [&](float v) -> float {
+        const int slot = xph & 1;
+        xch[t][slot][h][r] = v;
+        mbar_arrive(xbar);  // every lane: releases its own write
+        const bool okx = warp_wait(xbar, xph & 1, p.ctl, abort, 32);
+        ++xph;
+        return okx ? xch[t][slot][h ^ 1][r] : NAN;
+      };
       // l: sum of the fp32 P values (gives the LSE); lr: sum of the same
       // values rounded to bf16, as O += P V multiplies them (normalises O,
-      // which then is an exact convex combination of V rows).
+      // which then is an exact convex combination of V rows).  With NH = 2
+      // each half keeps partial sums, combined once at the end.
       float m = -INFINITY, l = 0.f, lr = 0.f;
       bool ok = true;
       for (int j = 0; j < nkv_t[t]; ++j) {
@@ -271,19 +310,19 @@ __global__ void __launch_bounds__(320, 1)
         int lim = 128;
         if (CAUSAL && j == qt) lim = r + 1;
         if (!CAUSAL && tail && j == p.nkv - 1) lim = p.N - j * C::BN;
-        // Pass 1: row max, 64 columns at a time (the whole row is never held
-        // in registers; pass 2 reads it again chunk by chunk).
+        // Pass 1: max over this thread's columns, 64 at a time (pass 2 reads
+        // them again chunk by chunk).
         float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int h = 0; h < 128; h += 64) {
+        for (int c64 = 0; c64 < C::CPT; c64 += 64) {
           float sv[64];
-          tmem_ld32(tS + h, *reinterpret_cast<uint32_t(*)[32]>(sv));
-          tmem_ld32(tS + h + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+          tmem_ld32(tS + cb + c64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+          tmem_ld32(tS + cb + c64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
           tmem_wait_ld();
           if (lim < 128) {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
-              if (h + c >= lim) sv[c] = -INFINITY;
+              if (cb + c64 + c >= lim) sv[c] = -INFINITY;
           }
 #pragma unroll
           for (int c = 0; c < 64; c += 8) {
@@ -291,7 +330,14 @@ __global__ void __launch_bounds__(320, 1)
             for (int e = 0; e < 4; ++e) mc[e] = fmax3(mc[e], sv[c + 2 * e], sv[c + 2 * e + 1]);
           }
         }
-        const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+        float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+        if (NH == 2) {
+          mx = fmaxf(mx, exchange(mx));
+          if (__any_sync(0xffffffffu, mx != mx)) {  // the exchange gave up
+            ok = false;
+            break;
+          }
+        }
         const float m_new = fmaxf(m, mx * scale2);
         const bool need = m_new > m + kTau;
         if (__any_sync(0xffffffffu, need)) {
@@ -303,33 +349,34 @@ __global__ void __launch_bounds__(320, 1)
             // O_t is complete here: S_t(j) was issued after PV_t(j-1) and its
             // commit covers every earlier MMA of the issuing thread.
 #pragma unroll 1
-            for (int c0 = 0; c0 < HD; c0 += 32) {
+            for (int c0 = 0; c0 < C::OCPT; c0 += 32) {
               uint32_t ov[32];
-              tmem_ld32(tO + c0, ov);
+              tmem_ld32(tO + ob + c0, ov);
               tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-              tmem_st32(tO + c0, ov);
+              tmem_st32(tO + ob + c0, ov);
             }
           }
         }
         // Pass 2: P = exp2(scale2 * s - m), two elements per paired FMA and
         // add, 32 columns at a time with the next chunk's load in flight.  P
-        // of chunk c lands in columns [c/2, c/2 + 16), all already read.
+        // of chunk c lands in columns [cb + c/2, cb + c/2 + 16), all already
+        // read by this thread.
         const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-m, -m);
         uint64_t l2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
         float sbuf[2][32];
-        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sbuf[0]));
+        tmem_ld32(tS + cb, *reinterpret_cast<uint32_t(*)[32]>(sbuf[0]));
         tmem_wait_ld();
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int c0 = 0; c0 < C::CPT; c0 += 32) {
           float* sv = sbuf[(c0 / 32) & 1];
-          if (c0 + 32 < 128)
-            tmem_ld32(tS + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sbuf[((c0 / 32) + 1) & 1]));
+          if (c0 + 32 < C::CPT)
+            tmem_ld32(tS + cb + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sbuf[((c0 / 32) + 1) & 1]));
           if (lim < 128) {
 #pragma unroll
             for (int c = 0; c < 32; ++c)
-              if (c0 + c >= lim) sv[c] = -INFINITY;
+              if (cb + c0 + c >= lim) sv[c] = -INFINITY;
           }
           uint32_t pk[16];
 #pragma unroll
@@ -342,8 +389,8 @@ __global__ void __launch_bounds__(320, 1)
             lr2 = f2_add(lr2, f2_pack(__uint_as_float(pk[i] << 16),
                                       __uint_as_float(pk[i] & 0xFFFF0000u)));
           }
-          tmem_st16(tS + c0 / 2, pk);
-          if (c0 + 32 < 128) tmem_wait_ld();
+          tmem_st16(tS + cb + c0 / 2, pk);
+          if (c0 + 32 < C::CPT) tmem_wait_ld();
         }
         {
           float a0, a1, b0, b1;
@@ -357,35 +404,43 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_p[t]));
       }
-      // Epilogue: O / l -> bf16, and LSE = ln 2 * (m + log2 l).
+      // Epilogue: O / lr -> bf16, and LSE = ln 2 * (m + log2 l).
+      if (ok && NH == 2) {
+        // the two halves' partial sums (one exchange slot each)
+        const float lo = exchange(l);
+        const float lro = exchange(lr);
+        if (__any_sync(0xffffffffu, lo != lo || lro != lro)) ok = false;
+        l += lo;
+        lr += lro;
+      }
       if (ok && warp_wait(smem_u32(&bar_o[t]), 0, p.ctl, abort, 31)) {
         tc_fence_after();
         const float inv_l = 1.0f / lr;
         __nv_bfloat16* orow = p.o + ((size_t)bh * p.N + row) * HD;
 #pragma unroll 1
-        for (int c0 = 0; c0 < HD; c0 += 32) {
+        for (int c0 = 0; c0 < C::OCPT; c0 += 32) {
           uint32_t ov[32];
-          tmem_ld32(tO + c0, ov);
+          tmem_ld32(tO + ob + c0, ov);
           tmem_wait_ld();
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
           if (row < p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+            uint4* dst = reinterpret_cast<uint4*>(orow + ob + c0);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
         }
-        if (row < p.N) p.lse[(size_t)bh * p.N + row] = (m + __log2f(l)) * kLn2;
+        if (h == 0 && row < p.N) p.lse[(size_t)bh * p.N + row] = (m + __log2f(l)) * kLn2;
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::W_MMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -394,8 +449,9 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int HD, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
-  using C = FwdCfg<HD>;
-  auto kern = fa_fwd_kernel<HD, CAUSAL>;
+  constexpr int NH = kSplit;
+  using C = FwdCfg<HD, NH>;
+  auto kern = fa_fwd_kernel<HD, CAUSAL, NH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   FwdParams p;
