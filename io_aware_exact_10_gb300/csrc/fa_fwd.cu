@@ -293,10 +293,11 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         ++xph;
         return okx ? xch[t][slot][h ^ 1][r] : NAN;
       };
-      // l: sum of the fp32 P values (gives the LSE); lr: sum of the same
-      // values rounded to bf16, as O += P V multiplies them (normalises O,
-      // which then is an exact convex combination of V rows).  With NH = 2
-      // each half keeps partial sums, combined once at the end.
+      // l: sum of the fp32 P values (gives the LSE).  lr normalises O: l plus,
+      // for each tile, the bf16 rounding error of the row's largest P (the
+      // value O += P V multiplied), so a row dominated by one key gets that
+      // key's V row exactly.  With NH = 2 each half keeps partial sums,
+      // combined once at the end.
       float m = -INFINITY, l = 0.f, lr = 0.f;
       bool ok = true;
       for (int j = 0; j < nkv_t[t]; ++j) {
@@ -331,6 +332,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           }
         }
         float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+        const float mxh = mx;  // max over this thread's own columns
         if (NH == 2) {
           mx = fmaxf(mx, exchange(mx));
           if (__any_sync(0xffffffffu, mx != mx)) {  // the exchange gave up
@@ -359,12 +361,18 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
             }
           }
         }
+        // Rounding error of this tile's largest P (mx is the max over this
+        // thread's columns, which holds the row's maximum in one half).
+        {
+          const float pmax = ex2(fmaf(mxh, scale2, -m));
+          lr += __uint_as_float(pack_bf16(pmax, 0.f) << 16) - pmax;
+        }
         // Pass 2: P = exp2(scale2 * s - m), two elements per paired FMA and
         // add, 32 columns at a time with the next chunk's load in flight.  P
         // of chunk c lands in columns [cb + c/2, cb + c/2 + 16), all already
         // read by this thread.
         const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-m, -m);
-        uint64_t l2 = f2_pack(0.f, 0.f), lr2 = f2_pack(0.f, 0.f);
+        uint64_t l2 = f2_pack(0.f, 0.f);
         float sbuf[2][32];
         tmem_ld32(tS + cb, *reinterpret_cast<uint32_t(*)[32]>(sbuf[0]));
         tmem_wait_ld();
@@ -386,18 +394,15 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
             const float p0 = ex2(x0), p1 = ex2(x1);
             pk[i] = pack_bf16(p0, p1);
             l2 = f2_add(l2, f2_pack(p0, p1));
-            lr2 = f2_add(lr2, f2_pack(__uint_as_float(pk[i] << 16),
-                                      __uint_as_float(pk[i] & 0xFFFF0000u)));
           }
           tmem_st16(tS + cb + c0 / 2, pk);
           if (c0 + 32 < C::CPT) tmem_wait_ld();
         }
         {
-          float a0, a1, b0, b1;
+          float a0, a1;
           f2_unpack(l2, a0, a1);
-          f2_unpack(lr2, b0, b1);
           l += a0 + a1;
-          lr += b0 + b1;
+          lr += a0 + a1;
         }
         tmem_wait_st();
         tc_fence_before();
