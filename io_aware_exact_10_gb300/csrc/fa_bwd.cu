@@ -29,7 +29,8 @@
 // columns 64-95, inside the fp32 columns of the warpgroup that wrote them.  Per query tile the MMA thread issues, in order:
 //   S^T = K Q_i^T -> ST;  dP^T = V dO_i^T -> DPT;  dV += P^T dO_i;
 //   dK += dS^T Q_i;  dQ_i = dS K -> DPT.
-// dS is also written to shared memory (query-major) as the A operand of dQ.
+// dS is also written to shared memory (query-major) as the A operand of dQ;
+// dQ is staged for its bulk reductions in the Q_u and dO_u ring slots.
 #include <cuda_bf16.h>
 
 #include "fa_kernels.h"
@@ -126,12 +127,13 @@ struct BwdCfg {
 enum : int {
   B_KV = 0, B_QF0 = 1, B_QF1 = 2, B_DOF0 = 3, B_DOF1 = 4, B_QE0 = 5, B_QE1 = 6, B_DOE0 = 7,
   B_DOE1 = 8, B_ST = 9, B_DPT = 10, B_P = 11, B_DS = 12, B_DQF = 13, B_DQE = 14, B_FIN = 15,
-  B_DRAIN = 16, B_WG = 17, B_DSF = 18, B_COUNT = 19
+  B_DRAIN = 16, B_WG = 17, B_COUNT = 18
 };
 // arrival counts: TMA / commit barriers take one arrival; B_P and B_DS one
-// per P/dS warp; B_DQE and B_DSF one per drain warp; B_WG every P/dS thread.
-__device__ __constant__ const uint32_t kBarCount[B_COUNT] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 8, 8,
-                                                             1, 4, 1, 1, 256, 4};
+// per P/dS warp; B_QE*, B_DOE* and B_DQE one per drain warp (the drain frees
+// the Q and dO slots: it stages dQ in them); B_WG every P/dS thread.
+__device__ __constant__ const uint32_t kBarCount[B_COUNT] = {1, 1, 1, 1, 1, 4, 4, 4, 4, 1, 1, 8, 8,
+                                                             1, 4, 1, 1, 256};
 
 struct BwdParams {
   const float* lse;
@@ -281,7 +283,6 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
           mma_ts(tDV, tST + pcol(k), sdesc_sw128(do0 + k * 2048, 16384, 1024), kIdG, u > 0 || k > 0);
-        mma_commit(bar(B_DOE0 + st));
         // dK += dS^T Q_i   (A = dS^T bf16 in TMEM)
         if (!(ok = mbar_wait(bar(B_DS), u & 1, p.ctl, abort, 25))) break;
         tc_fence_after();
@@ -294,7 +295,6 @@ __global__ void __launch_bounds__(448, 1)
           mma_ss(tDPT, sdesc_sw128(sDS + k * 2048, 16384, 1024),
                  sdesc_sw128(sK + k * 2048, 16384, 1024), kIdQ, k > 0);
         mma_commit(bar(B_DQF));
-        mma_commit(bar(B_QE0 + st));
       }
       if (ok) mma_commit(bar(B_FIN));
       mma_commit(bar(B_DRAIN));
@@ -367,9 +367,8 @@ __global__ void __launch_bounds__(448, 1)
       if (lane == 0) mbar_arrive(bar(B_P));
       // dS^T = P^T o (dP^T - D), with P^T the bf16 values dV multiplied
       if (!(ok = warp_wait_b(bar(B_DPT), u & 1, p.ctl, abort, 31))) break;
-      // the dS buffer doubles as the dQ staging area: wait until the drain of
-      // the previous tile has been read out of it
-      if (u > 0 && !(ok = warp_wait_b(bar(B_DSF), (u - 1) & 1, p.ctl, abort, 32))) break;
+      // the dS buffer is the A operand of dQ_{u-1}: wait until it is read
+      if (u > 0 && !(ok = warp_wait_b(bar(B_DQF), (u - 1) & 1, p.ctl, abort, 32))) break;
       tc_fence_after();
       const uint32_t srow = sDS + (uint32_t)h * 16384u + (uint32_t)r * 128u;
       const uint32_t sw = (uint32_t)(r & 7);
@@ -436,20 +435,25 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else {
     // ---------------------------------------------------------- dQ drain
-    // dQ_i (128 query rows x d, fp32) leaves TMEM 64 columns at a time, goes
-    // through this warp's 8 KB slice of the dS buffer as two 32-row x
-    // 32-column boxes (128-byte swizzled), and is added into dQacc by TMA
-    // bulk reductions.
+    // dQ_u (128 query rows x d, fp32) leaves TMEM 64 columns at a time and is
+    // added into dQacc by TMA bulk reductions of 32-row x 32-column boxes
+    // (128-byte swizzled).  The boxes are staged in the ring slots of Q_u and
+    // dO_u, which no MMA reads once dQ_u is complete: this warp's quarter of
+    // the dO_u slot holds the first HD/64 boxes, its quarter of the Q_u slot
+    // the rest.  The drain then releases both slots to the TMA producer.
     const int sp = warp & 3;
     const int r = sp * 32 + lane;  // query row within the tile (dQ) / key row (dK)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const size_t rowbase = (size_t)bh * p.N;
-    const uint32_t stage = sDS + (uint32_t)sp * 8192u;
     const uint32_t sw = (uint32_t)(lane & 7);
+    constexpr int BOXES_PER_SLOT = HD / 64;          // 4 KB boxes in a warp's quarter
     bool ok = true;
     for (int u = 0; u < nit; ++u) {
       if (!(ok = warp_wait_b(bar(B_DQF), u & 1, p.ctl, abort, 40))) break;
       tc_fence_after();
+      const int st = u & 1;
+      const uint32_t quarter = (uint32_t)sp * (uint32_t)(C::TILE / 4);
+      const uint32_t stage_do = sDO + st * C::TILE + quarter, stage_q = sQ + st * C::TILE + quarter;
       const int y = (i0 + u) * C::BQ + sp * 32;
 #pragma unroll
       for (int hh = 0; hh < HD / 64; ++hh) {
@@ -462,13 +466,12 @@ __global__ void __launch_bounds__(448, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_DQE));  // dQ's TMEM columns are free again
         }
-        if (hh > 0) {
-          if (lane == 0) bulk_wait_group_read<0>();
-          __syncwarp();
-        }
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
-          const uint32_t row = stage + (uint32_t)bb * 4096u + (uint32_t)lane * 128u;
+          const int box = 2 * hh + bb;             // columns [32 box, 32 box + 32)
+          const uint32_t base = (box < BOXES_PER_SLOT ? stage_do : stage_q) +
+                                (uint32_t)(box % BOXES_PER_SLOT) * 4096u;
+          const uint32_t row = base + (uint32_t)lane * 128u;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const int col = bb * 32 + c * 4;
@@ -480,14 +483,23 @@ __global__ void __launch_bounds__(448, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(&tdq, stage, (2 * hh) * 32, y, bh);
-          tma_reduce_add_3d(&tdq, stage + 4096u, (2 * hh + 1) * 32, y, bh);
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb) {
+            const int box = 2 * hh + bb;
+            const uint32_t base = (box < BOXES_PER_SLOT ? stage_do : stage_q) +
+                                  (uint32_t)(box % BOXES_PER_SLOT) * 4096u;
+            tma_reduce_add_3d(&tdq, base, box * 32, y, bh);
+          }
           bulk_commit_group();
         }
       }
-      if (lane == 0) bulk_wait_group_read<0>();
+      // once the boxes have been read, the Q_u and dO_u slots may be refilled
+      if (lane == 0) {
+        bulk_wait_group_read<0>();
+        mbar_arrive(bar(B_QE0 + st));
+        mbar_arrive(bar(B_DOE0 + st));
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DSF));  // staging slice read out
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
