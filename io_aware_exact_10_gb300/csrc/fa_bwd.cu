@@ -112,8 +112,8 @@ struct BwdCfg {
   static constexpr int OFF_Q = OFF_V + TILE;        // 2 slots
   static constexpr int OFF_DO = OFF_Q + 2 * TILE;   // 2 slots
   static constexpr int OFF_DS = OFF_DO + 2 * TILE;
-  static constexpr int OFF_LSE = OFF_DS + DS_BYTES; // 2 x 128 floats (log2-scaled LSE)
-  static constexpr int OFF_D = OFF_LSE + 2 * BQ * 4;  // 2 x 128 floats
+  static constexpr int OFF_LSE = OFF_DS + DS_BYTES; // 2 x 128 floats (-LSE * log2 e)
+  static constexpr int OFF_D = OFF_LSE + 2 * BQ * 4;  // 2 x 128 floats (-D)
   static constexpr int OFF_BAR = OFF_D + 2 * BQ * 4;
   static constexpr int NBAR = 20;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
@@ -310,12 +310,14 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t tST = tmem + lane_off + C::COL_ST, tDPT = tmem + lane_off + C::COL_DPT;
     const int cb = 64 * h;                          // first query column of this thread
     const float scale2 = p.scale2;
+    const uint64_t sc2 = f2_pack(scale2, scale2);
     const size_t rowbase = (size_t)bh * p.N;
-    // warpgroup 0 stages the log2-scaled LSE and D of the first query tile
+    // warpgroup 0 stages the negated log2-scaled LSE and negated D of the
+    // first query tile
     if (h == 0) {
       const int q = i0 * C::BQ + r;
-      lse_sh[r] = q < p.N ? p.lse[rowbase + q] * kLog2e : INFINITY;
-      d_sh[r] = q < p.N ? p.D[rowbase + q] : 0.f;
+      lse_sh[r] = q < p.N ? -p.lse[rowbase + q] * kLog2e : -INFINITY;
+      d_sh[r] = q < p.N ? -p.D[rowbase + q] : 0.f;
     }
     // Both warpgroups synchronise on an mbarrier (256 arrivals per phase) so
     // that the wait stays bounded if another warp gives up.
@@ -326,12 +328,12 @@ __global__ void __launch_bounds__(448, 1)
       const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
       const float* d_u = d_sh + (u & 1) * C::BQ + cb;
       // prefetch the next tile's statistics
-      float nl = INFINITY, nd = 0.f;
+      float nl = -INFINITY, nd = 0.f;
       if (h == 0 && u + 1 < nit) {
         const int q = (qt + 1) * C::BQ + r;
         if (q < p.N) {
-          nl = p.lse[rowbase + q] * kLog2e;
-          nd = p.D[rowbase + q];
+          nl = -p.lse[rowbase + q] * kLog2e;
+          nd = -p.D[rowbase + q];
         }
       }
       if (!(ok = warp_wait_b(bar(B_ST), u & 1, p.ctl, abort, 30))) break;
@@ -345,20 +347,18 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t pk[16];
+        // two queries per paired FMA: scale2 * s - LSE2 (the shared copy holds -LSE2)
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 l4 = reinterpret_cast<const float4*>(lse_u + c0)[i4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = c0 + 4 * i4 + e;
-            float v = ex2(fmaf(reinterpret_cast<float*>(pr)[i], scale2, -lv[e]));
-            if (diag && cb + i < r) v = 0.f;
-            pr[i] = v;
-          }
+        for (int i = 0; i < 16; ++i) {
+          const int q = c0 + 2 * i;
+          const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(lse_u + q);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(pr[q], pr[q + 1]), sc2, nl2), x0, x1);
+          float p0 = ex2(x0), p1 = ex2(x1);
+          if (diag && cb + q < r) p0 = 0.f;
+          if (diag && cb + q + 1 < r) p1 = 0.f;
+          pk[i] = pack_bf16(p0, p1);
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pr[c0 + 2 * i], pr[c0 + 2 * i + 1]);
         tmem_st16(tST + cb + c0 / 2, pk);
       }
       tmem_wait_st();
@@ -380,15 +380,16 @@ __global__ void __launch_bounds__(448, 1)
         tmem_ld16(tST + cb + c0 / 2, pp);
         tmem_wait_ld();
         uint32_t pk[16];
+        // two queries per paired add and multiply: (dP - D) * P (the shared
+        // copy holds -D)
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 d4 = reinterpret_cast<const float4*>(d_u + c0)[i4];
-          const int i = 4 * i4;
-          const uint32_t w0 = pp[2 * i4], w1 = pp[2 * i4 + 1];
-          pk[2 * i4] = pack_bf16(__uint_as_float(w0 << 16) * (__uint_as_float(dp[i]) - d4.x),
-                                 __uint_as_float(w0 & 0xFFFF0000u) * (__uint_as_float(dp[i + 1]) - d4.y));
-          pk[2 * i4 + 1] = pack_bf16(__uint_as_float(w1 << 16) * (__uint_as_float(dp[i + 2]) - d4.z),
-                                     __uint_as_float(w1 & 0xFFFF0000u) * (__uint_as_float(dp[i + 3]) - d4.w));
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(d_u + c0 + 2 * i);
+          const uint32_t w = pp[i];
+          const uint64_t pv = f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+          float a, b;
+          f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), nd2), pv), a, b);
+          pk[i] = pack_bf16(a, b);
         }
         tmem_st16(tDPT + cb + c0 / 2, pk);
         // shared copy, query-major 128-byte swizzled: block h, chunks of 8 queries
