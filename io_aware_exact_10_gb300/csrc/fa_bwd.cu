@@ -14,7 +14,10 @@
 //   fa_bwd_pre_kernel   D = rowsum(dO o O) and dQacc = 0      (memory bound)
 //   fa_bwd_kernel       one CTA per 128-key tile of one head; loops over the
 //                       128-query tiles that see it; dK, dV accumulate in
-//                       TMEM; dQ contributions are added into dQacc (fp32)
+//                       TMEM; dQ contributions are added into dQacc (fp32).
+//                       d = 128 uses the kernel below; d = 64 a software-
+//                       pipelined variant (fa_bwd_d64.cu) that the smaller
+//                       operands leave room for
 //   fa_bwd_dq_kernel    dq = bf16(scale * dQacc)                (memory bound)
 //
 // fa_bwd_kernel roles (448 threads):
@@ -569,7 +572,10 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
       a.dq_acc, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = a.causal ? launch_bwd_main<HD, true>(a, stream) : launch_bwd_main<HD, false>(a, stream);
+  if constexpr (HD == 64)
+    e = launch_bwd_main_d64(a, stream);
+  else
+    e = a.causal ? launch_bwd_main<HD, true>(a, stream) : launch_bwd_main<HD, false>(a, stream);
   if (e != cudaSuccess) return e;
   const long n8 = rows * HD / 8;
   fa_bwd_dq_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(

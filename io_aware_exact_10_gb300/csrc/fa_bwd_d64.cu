@@ -1,0 +1,509 @@
+// fa_bwd_d64.cu -- main attention backward kernel for head dimension 64.
+//
+// Same arithmetic as the general backward kernel (FlashAttention: exact
+// attention made fast by counting memory traffic, "The method"; FlashAttention
+// and IO-aware exact attention, "Backward by recomputation"): one CTA per
+// 128-key tile of one head, looping over the 128-query tiles that see it,
+//   S^T = K Q_i^T,  P^T = exp2(scale2 S^T - LSE2_i),
+//   dP^T = V dO_i^T,  dS^T = P^T o (dP^T - D_i),
+//   dV += P^T dO_i,  dK += dS^T Q_i,  dQ_i = dS K  (added into dQacc).
+//
+// At d = 64 the operands are small enough to software-pipeline the loop:
+// tensor memory holds S^T, dP^T, P^T (bf16), dV, dK and dQ in separate
+// columns, so S^T of the next query tile is computed while the P/dS warps
+// work on the current one, and dP^T of the next tile as soon as the current
+// dP^T has been read.  The tensor pipe then runs
+//   ... S^T(u+1), dV(u), dP^T(u+1), dK(u), dQ(u), S^T(u+2) ...
+// while the P/dS warps run P(u), dS(u), P(u+1), ... back to back.  dK takes
+// dS from shared memory (key rows, query-contiguous: a K-major operand) and
+// dQ takes the same buffer as an M-major operand, so dS^T is never written to
+// tensor memory.  dS is double-buffered in shared memory, Q goes through a
+// 3-slot ring (its next tile is needed early), dO through a 2-slot ring, and
+// the dQ drain stages its reductions in a buffer of its own.
+//
+// Roles (448 threads):
+//   warps 0-7   P / dS: thread = key row = TMEM lane; warps 0-3 take query
+//               columns 0-63 of the tile, warps 4-7 columns 64-127
+//   warps 8-11  dQ drain (thread = query row), then the dK epilogue
+//   warp  12    TMA producer
+//   warp  13    tcgen05 MMA issuer and TMEM owner
+#include <cuda_bf16.h>
+
+#include "fa_kernels.h"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Cfg64 {
+  static constexpr int HD = 64;
+  static constexpr int BQ = 128;              // queries per iteration
+  static constexpr int BK = 128;              // keys per CTA
+  static constexpr int TILE = 128 * HD * 2;   // one 128-row bf16 tile: 16 KB
+  static constexpr int DS_BYTES = BQ * BK * 2;
+  static constexpr int QSLOTS = 3, DOSLOTS = 2;
+  // dynamic shared memory layout (offsets from a 1024-byte aligned base)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;
+  static constexpr int OFF_DO = OFF_Q + QSLOTS * TILE;
+  static constexpr int OFF_DS = OFF_DO + DOSLOTS * TILE;     // 2 buffers
+  static constexpr int OFF_STAGE = OFF_DS + 2 * DS_BYTES;    // dQ boxes, 8 KB per drain warp
+  static constexpr int OFF_LSE = OFF_STAGE + BQ * HD * 4;    // 2 x 128 floats (-LSE * log2 e)
+  static constexpr int OFF_D = OFF_LSE + 2 * BQ * 4;         // 2 x 128 floats (-D)
+  static constexpr int OFF_BAR = OFF_D + 2 * BQ * 4;
+  static constexpr int NBAR = 32;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int THREADS = 448;
+  static constexpr int W_LOAD = 12, W_MMA = 13;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_PT = 256, COL_DV = 320, COL_DK = 384,
+                            COL_DQ = 448;
+};
+static_assert(Cfg64::SMEM <= 232448, "shared memory budget");
+static_assert(Cfg64::QSLOTS >= 2 && Cfg64::QSLOTS <= 3 && Cfg64::DOSLOTS == 2, "ring sizes");
+
+// barrier indices
+enum : int {
+  B_K = 0, B_V, B_QF0, B_QF1, B_QF2, B_QE0, B_QE1, B_QE2, B_DOF0, B_DOF1, B_DOE0, B_DOE1,
+  B_ST, B_STF, B_P, B_PV, B_DPT, B_DPTF, B_DS0, B_DS1, B_DSF0, B_DSF1, B_DQF, B_DQE,
+  B_FIN, B_DRAIN, B_WG, B_COUNT
+};
+static_assert(B_COUNT <= Cfg64::NBAR, "barrier area");
+// arrival counts: TMA and tcgen05.commit barriers take one arrival; the
+// P/dS hand-offs (STF, P, DPTF, DS*) one per P/dS warp; DQE one per drain
+// warp; WG every P/dS thread.
+__device__ __constant__ const uint32_t kBarCount64[B_COUNT] = {
+    1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1,   // K, V, QF*, QE*, DOF*, DOE*
+    1, 8, 8, 1, 1, 8, 8, 8, 1, 1, 1, 4,   // ST, STF, P, PV, DPT, DPTF, DS*, DSF*, DQF, DQE
+    1, 1, 256};                           // FIN, DRAIN, WG
+
+struct BwdParams64 {
+  const float* lse;
+  const float* D;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int N, nq, nkv, BH, group;
+  float scale, scale2;
+  KernelCtl ctl;
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
+                                          volatile int* abort, uint32_t site) {
+  const bool ok = mbar_wait(bar, parity, ctl, abort, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(448, 1)
+    fa_bwd_d64_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                      const __grid_constant__ CUtensorMap tdq, const BwdParams64 p) {
+  using C = Cfg64;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) record_error(p.ctl, kErrSmemAlign, 2);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const GridPos gp = decode_grid((int)blockIdx.x, p.BH, p.nkv, p.group);
+  const int bh = gp.bh;
+  const int kt = gp.rank;
+  const int i0 = CAUSAL ? kt : 0;                  // first query tile that sees this key tile
+  const int nit = p.nq - i0;                       // query tiles to process
+
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
+                 sDO = s0 + C::OFF_DO, sDS = s0 + C::OFF_DS;
+  float* lse_sh = reinterpret_cast<float*>(smem + C::OFF_LSE);
+  float* d_sh = reinterpret_cast<float*>(smem + C::OFF_D);
+
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), kBarCount64[i]);
+    fence_barrier_init();
+  }
+  if (warp == C::W_MMA) {
+    tmem_alloc(smem_u32(tmem_base_sh), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_sh;
+
+  if (warp == C::W_LOAD) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tdo);
+      tma_prefetch_desc(&tdq);
+      // K and Q_0 first: S^T of the first tile needs only those two
+      mbar_arrive_expect_tx(bar(B_K), C::TILE);
+      tma_load_3d(sK, &tk, bar(B_K), 0, kt * C::BK, bh);
+      bool ok = true;
+      int nq_issued = 0, ndo_issued = 0;
+      for (int u = 0; u < nit; ++u) {
+        const int qt = i0 + u;
+        const int qs = u % C::QSLOTS, qn = u / C::QSLOTS;
+        if (qn > 0 && !(ok = mbar_wait(bar(B_QE0 + qs), (qn - 1) & 1, p.ctl, abort, 50))) break;
+        mbar_arrive_expect_tx(bar(B_QF0 + qs), C::TILE);
+        tma_load_3d(sQ + qs * C::TILE, &tq, bar(B_QF0 + qs), 0, qt * C::BQ, bh);
+        ++nq_issued;
+        if (u == 0) {
+          mbar_arrive_expect_tx(bar(B_V), C::TILE);
+          tma_load_3d(sV, &tv, bar(B_V), 0, kt * C::BK, bh);
+        }
+        const int ds = u % C::DOSLOTS, dn = u / C::DOSLOTS;
+        if (dn > 0 && !(ok = mbar_wait(bar(B_DOE0 + ds), (dn - 1) & 1, p.ctl, abort, 51))) break;
+        mbar_arrive_expect_tx(bar(B_DOF0 + ds), C::TILE);
+        tma_load_3d(sDO + ds * C::TILE, &tdo, bar(B_DOF0 + ds), 0, qt * C::BQ, bh);
+        ++ndo_issued;
+      }
+      if (!ok) {
+        // Abort: let every copy already issued land before the CTA exits.
+        mbar_wait_quiet(bar(B_K), 0, 200000000ull);
+        if (nq_issued > 0) mbar_wait_quiet(bar(B_V), 0, 200000000ull);
+        for (int v = (nq_issued > C::QSLOTS ? nq_issued - C::QSLOTS : 0); v < nq_issued; ++v)
+          mbar_wait_quiet(bar(B_QF0 + v % C::QSLOTS), (v / C::QSLOTS) & 1, 200000000ull);
+        for (int v = (ndo_issued > C::DOSLOTS ? ndo_issued - C::DOSLOTS : 0); v < ndo_issued; ++v)
+          mbar_wait_quiet(bar(B_DOF0 + v % C::DOSLOTS), (v / C::DOSLOTS) & 1, 200000000ull);
+      }
+    }
+  } else if (warp == C::W_MMA) {
+    // ------------------------------------------------------------------ MMA
+    // The whole warp runs the issue loop; one elected lane issues.
+    {
+      const uint32_t lead = elect_one();
+      constexpr uint32_t kIdS = idesc_bf16(128, C::BQ, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdG = idesc_bf16(128, C::HD, false, true);   // dV, dK
+      constexpr uint32_t kIdQ = idesc_bf16(128, C::HD, true, true);    // dQ = dS K
+      const uint32_t tST = tmem + C::COL_ST, tDPT = tmem + C::COL_DPT, tPT = tmem + C::COL_PT,
+                     tDV = tmem + C::COL_DV, tDK = tmem + C::COL_DK, tDQ = tmem + C::COL_DQ;
+      // Descriptor low halves of every operand tile (sdesc_lo): K-major
+      // operands with lbo 16, M/N-major ones with lbo 16384 (the distance
+      // between 64-element blocks); the high half is the same for all.
+      constexpr uint32_t HI = sdesc_hi(1024);
+      constexpr uint32_t TILE16 = C::TILE >> 4, DS16 = C::DS_BYTES >> 4;
+      const uint32_t kK = sdesc_lo(sK, 16), kMN = sdesc_lo(sK, 16384), vK = sdesc_lo(sV, 16);
+      const uint32_t qK = sdesc_lo(sQ, 16), qMN = sdesc_lo(sQ, 16384);
+      const uint32_t doK = sdesc_lo(sDO, 16), doMN = sdesc_lo(sDO, 16384);
+      const uint32_t dsK = sdesc_lo(sDS, 16), dsMN = sdesc_lo(sDS, 16384);
+      // S^T = K Q_v^T   (M = keys, N = queries, K = d; both K-major)
+      auto issue_st = [&](uint32_t qo) {
+#pragma unroll
+        for (int k = 0; k < C::HD / 16; ++k)
+          mma_ss_e(lead, tST, kK + 2 * k, HI, qK + qo + 2 * k, HI, kIdS, k > 0);
+        mma_commit_e(lead, bar(B_ST));
+      };
+      // dP^T = V dO_v^T
+      auto issue_dpt = [&](uint32_t dof) {
+#pragma unroll
+        for (int k = 0; k < C::HD / 16; ++k)
+          mma_ss_e(lead, tDPT, vK + 2 * k, HI, doK + dof + 2 * k, HI, kIdS, k > 0);
+        mma_commit_e(lead, bar(B_DPT));
+      };
+      bool ok = warp_wait(bar(B_K), 0, p.ctl, abort, 60) && warp_wait(bar(B_QF0), 0, p.ctl, abort, 61);
+      if (ok) {
+        tc_fence_after();
+        issue_st(0);
+        ok = warp_wait(bar(B_V), 0, p.ctl, abort, 62) && warp_wait(bar(B_DOF0), 0, p.ctl, abort, 63);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dpt(0);
+      }
+      // ring positions: Q slot and phase of tile u + 1, Q slot offset of tile u
+      int qs_v = 1;
+      uint32_t qph_v = 0, qo_u = 0;
+      for (int u = 0; u < nit && ok; ++u) {
+        const uint32_t qo_v = (uint32_t)qs_v * TILE16;
+        const uint32_t dof_u = (uint32_t)(u & 1) * TILE16, dof_v = (uint32_t)((u + 1) & 1) * TILE16;
+        const uint32_t dso = (uint32_t)(u & 1) * DS16;
+        const uint32_t acc0 = u > 0 ? 1u : 0u;
+        const bool more = u + 1 < nit;
+        // S^T of the next tile, once the P/dS warps have read this one
+        if (more) {
+          if (!(ok = warp_wait(bar(B_QF0 + qs_v), qph_v, p.ctl, abort, 64))) break;
+          if (!(ok = warp_wait(bar(B_STF), u & 1, p.ctl, abort, 65))) break;
+          tc_fence_after();
+          issue_st(qo_v);
+        }
+        // dV += P^T dO_u   (A = P^T bf16 in TMEM, B = dO_u query-major)
+        if (!(ok = warp_wait(bar(B_P), u & 1, p.ctl, abort, 66))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::BQ / 16; ++k)
+          mma_ts_e(lead, tDV, tPT + k * 8, doMN + dof_u + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
+        mma_commit_e(lead, bar(B_PV));                   // P^T columns free
+        mma_commit_e(lead, bar(B_DOE0 + (u & 1)));       // dO_u slot free
+        // dP^T of the next tile, once the P/dS warps have read this one
+        if (more) {
+          if (!(ok = warp_wait(bar(B_DOF0 + ((u + 1) & 1)), ((u + 1) >> 1) & 1, p.ctl, abort, 67))) break;
+          if (!(ok = warp_wait(bar(B_DPTF), u & 1, p.ctl, abort, 68))) break;
+          tc_fence_after();
+          issue_dpt(dof_v);
+        }
+        // dK += dS^T Q_u   (A = dS key rows, K-major in shared memory; B = Q_u query-major)
+        if (!(ok = warp_wait(bar(B_DS0 + (u & 1)), (u >> 1) & 1, p.ctl, abort, 69))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::BQ / 16; ++k)
+          mma_ss_e(lead, tDK, dsK + dso + (k >> 2) * 1024 + (k & 3) * 2, HI, qMN + qo_u + 128 * k, HI, kIdG,
+                   k > 0 ? 1u : acc0);
+        mma_commit_e(lead, bar(B_QE0 + (int)(qo_u / TILE16)));  // Q_u slot free
+        // dQ_u = dS K   (A = the same dS buffer read query-major, B = K key-major)
+        if (u > 0 && !(ok = warp_wait(bar(B_DQE), (u - 1) & 1, p.ctl, abort, 70))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::BK / 16; ++k)
+          mma_ss_e(lead, tDQ, dsMN + dso + 128 * k, HI, kMN + 128 * k, HI, kIdQ, k > 0);
+        mma_commit_e(lead, bar(B_DQF));
+        mma_commit_e(lead, bar(B_DSF0 + (u & 1)));       // dS buffer free
+        qo_u = qo_v;
+        if (++qs_v == C::QSLOTS) {
+          qs_v = 0;
+          qph_v ^= 1u;
+        }
+      }
+      if (ok) mma_commit_e(lead, bar(B_FIN));
+      mma_commit_e(lead, bar(B_DRAIN));
+      mbar_wait_quiet(bar(B_DRAIN), 0, 200000000ull);
+    }
+  } else if (warp < 8) {
+    // --------------------------------------------- P / dS warpgroups (x2)
+    const int h = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int cb = 64 * h;                          // first query column of this thread
+    const uint32_t tST = tmem + lane_off + C::COL_ST + cb, tDPT = tmem + lane_off + C::COL_DPT + cb,
+                   tPT = tmem + lane_off + C::COL_PT + cb / 2;
+    const uint64_t sc2 = f2_pack(p.scale2, p.scale2);
+    const size_t rowbase = (size_t)bh * p.N;
+    if (h == 0) {
+      const int q = i0 * C::BQ + r;
+      lse_sh[r] = q < p.N ? -p.lse[rowbase + q] * kLog2e : -INFINITY;
+      d_sh[r] = q < p.N ? -p.D[rowbase + q] : 0.f;
+    }
+    mbar_arrive(bar(B_WG));
+    bool ok = warp_wait(bar(B_WG), 0, p.ctl, abort, 80);
+    const uint32_t sw = (uint32_t)(r & 7);
+    for (int u = 0; u < nit && ok; ++u) {
+      const int qt = i0 + u;
+      const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
+      const float* d_u = d_sh + (u & 1) * C::BQ + cb;
+      float nl = -INFINITY, nd = 0.f;
+      if (h == 0 && u + 1 < nit) {
+        const int q = (qt + 1) * C::BQ + r;
+        if (q < p.N) {
+          nl = -p.lse[rowbase + q] * kLog2e;
+          nd = -p.D[rowbase + q];
+        }
+      }
+      // ---- P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query < key
+      if (!(ok = warp_wait(bar(B_ST), u & 1, p.ctl, abort, 81))) break;
+      tc_fence_after();
+      uint32_t pk[32];
+      {
+        float pr[64];
+        tmem_ld32(tST, *reinterpret_cast<uint32_t(*)[32]>(pr));
+        tmem_ld32(tST + 32, *reinterpret_cast<uint32_t(*)[32]>(pr + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_STF));    // S^T columns may be overwritten
+        const bool diag = CAUSAL && qt == kt;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int q = 2 * i;
+          const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(lse_u + q);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(pr[q], pr[q + 1]), sc2, nl2), x0, x1);
+          float p0 = ex2(x0), p1 = ex2(x1);
+          if (diag && cb + q < r) p0 = 0.f;
+          if (diag && cb + q + 1 < r) p1 = 0.f;
+          pk[i] = pack_bf16(p0, p1);
+        }
+      }
+      // the P^T columns are the A operand of dV(u-1): wait until it is done
+      if (u > 0 && !(ok = warp_wait(bar(B_PV), (u - 1) & 1, p.ctl, abort, 82))) break;
+      tc_fence_after();
+      tmem_st16(tPT, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+      tmem_st16(tPT + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_P));
+      // ---- dS = P o (dP - D), with P the bf16 values dV multiplied
+      if (!(ok = warp_wait(bar(B_DPT), u & 1, p.ctl, abort, 83))) break;
+      tc_fence_after();
+      uint32_t dp[64];
+      tmem_ld32(tDPT, *reinterpret_cast<uint32_t(*)[32]>(dp));
+      tmem_ld32(tDPT + 32, *reinterpret_cast<uint32_t(*)[32]>(dp + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DPTF));     // dP^T columns may be overwritten
+      // dS buffer u&1 was last read by dK(u-2) and dQ(u-2)
+      if (u >= 2 && !(ok = warp_wait(bar(B_DSF0 + (u & 1)), ((u >> 1) - 1) & 1, p.ctl, abort, 84))) break;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(d_u + 2 * i);
+        const uint32_t w = pk[i];
+        const uint64_t pv = f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+        float a, b;
+        f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), nd2), pv), a, b);
+        pk[i] = pack_bf16(a, b);
+      }
+      // key row r of the dS buffer: 64 queries of half h, 128-byte swizzled
+      const uint32_t srow = sDS + (uint32_t)(u & 1) * C::DS_BYTES + (uint32_t)h * 16384u + (uint32_t)r * 128u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + (((uint32_t)c ^ sw) << 4)),
+                     "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                     : "memory");
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DS0 + (u & 1)));
+      if (h == 0) {
+        lse_sh[((u + 1) & 1) * C::BQ + r] = nl;
+        d_sh[((u + 1) & 1) * C::BQ + r] = nd;
+      }
+      mbar_arrive(bar(B_WG));
+      if (!(ok = warp_wait(bar(B_WG), (u + 1) & 1, p.ctl, abort, 85))) break;
+    }
+    // epilogue: dV rows of this key tile, columns [32h, 32h + 32)
+    if (ok && warp_wait(bar(B_FIN), 0, p.ctl, abort, 86)) {
+      tc_fence_after();
+      const int key = kt * C::BK + r;
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_off + C::COL_DV + 32 * h, v);
+      tmem_wait_ld();
+      uint32_t pkv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pkv[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      if (key < p.N) {
+        uint4* d4 = reinterpret_cast<uint4*>(p.dv + (rowbase + key) * C::HD + 32 * h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pkv[4 * i], pkv[4 * i + 1], pkv[4 * i + 2], pkv[4 * i + 3]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- dQ drain
+    // dQ_u (128 query rows x 64, fp32) leaves TMEM once per tile and is added
+    // into dQacc by TMA bulk reductions of two 32-row x 32-column boxes per
+    // warp, staged (128-byte swizzled) in this warp's 8 KB of the staging area.
+    const int sp = warp & 3;
+    const int r = sp * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
+    const size_t rowbase = (size_t)bh * p.N;
+    const uint32_t sw = (uint32_t)(lane & 7);
+    const uint32_t stage = s0 + C::OFF_STAGE + (uint32_t)sp * 8192u;
+    bool ok = true;
+    for (int u = 0; u < nit; ++u) {
+      if (!(ok = warp_wait(bar(B_DQF), u & 1, p.ctl, abort, 90))) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld32(tmem + lane_off + C::COL_DQ, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld32(tmem + lane_off + C::COL_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_DQE));                   // dQ's TMEM columns are free again
+        bulk_wait_group_read<0>();                 // the previous boxes have left the staging area
+      }
+      __syncwarp();
+      const int y = (i0 + u) * C::BQ + sp * 32;
+#pragma unroll
+      for (int bb = 0; bb < 2; ++bb) {
+        const uint32_t row = stage + (uint32_t)bb * 4096u + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int col = bb * 32 + c * 4;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((uint32_t)c ^ sw) << 4)),
+                       "r"(v[col]), "r"(v[col + 1]), "r"(v[col + 2]), "r"(v[col + 3])
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&tdq, stage, 0, y, bh);
+        tma_reduce_add_3d(&tdq, stage + 4096u, 32, y, bh);
+        bulk_commit_group();
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+    // epilogue: dK rows of this key tile (scaled)
+    if (ok && warp_wait(bar(B_FIN), 0, p.ctl, abort, 91)) {
+      tc_fence_after();
+      const int key = kt * C::BK + r;
+      const float scale = p.scale;
+#pragma unroll 1
+      for (int c0 = 0; c0 < C::HD; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + C::COL_DK + c0, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
+        if (key < p.N) {
+          uint4* d4 = reinterpret_cast<uint4*>(p.dk + (rowbase + key) * C::HD + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::W_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <bool CAUSAL>
+cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
+  using C = Cfg64;
+  auto kern = fa_bwd_d64_kernel<CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  BwdParams64 p;
+  p.lse = a.lse;
+  p.D = a.D;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.N = a.N;
+  p.nq = (a.N + C::BQ - 1) / C::BQ;
+  p.nkv = (a.N + C::BK - 1) / C::BK;
+  p.BH = a.BH;
+  p.group = head_group(a.BH, p.nkv, a.num_sms);
+  p.scale = a.scale;
+  p.scale2 = a.scale * kLog2e;
+  p.ctl = a.ctl;
+  dim3 grid((unsigned)((long)p.nkv * a.BH));
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main_d64(const BwdLaunch& a, cudaStream_t stream) {
+  return a.causal ? launch_t<true>(a, stream) : launch_t<false>(a, stream);
+}
+
+}  // namespace fa

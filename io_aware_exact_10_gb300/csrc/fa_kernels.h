@@ -68,5 +68,7 @@ __host__ __device__ inline GridPos decode_grid(int L, int BH, int tiles, int gro
 // Each returns cudaSuccess or the launch error; nothing is synchronised.
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream);
+// main backward kernel for d = 64 (the D preprocess and dQ convert stay in launch_bwd)
+cudaError_t launch_bwd_main_d64(const BwdLaunch& a, cudaStream_t stream);
 
 }  // namespace fa
