@@ -251,56 +251,66 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (warp == C::W_MMA) {
     // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
+    // The whole warp runs the issue loop (control flow and descriptors stay
+    // warp-uniform); one elected lane issues.
+    {
+      const uint32_t lead = elect_one();
       constexpr uint32_t kIdS = idesc_bf16(128, C::BQ, false, false);  // S^T, dP^T
       constexpr uint32_t kIdG = idesc_bf16(128, HD, false, true);      // dV, dK (A in TMEM)
       constexpr uint32_t kIdQ = idesc_bf16(128, HD, true, true);       // dQ = dS K
       const uint32_t tST = tmem + C::COL_ST, tDPT = tmem + C::COL_DPT, tDV = tmem + C::COL_DV,
                      tDK = tmem + C::COL_DK;
-      bool ok = mbar_wait(bar(B_KV), 0, p.ctl, abort, 20);
+      // descriptor halves (sdesc_lo / sdesc_hi): K-major operands with lbo
+      // 16, M/N-major ones with lbo 16384; ring slot 0 of Q and dO
+      constexpr uint32_t HI = sdesc_hi(1024);
+      constexpr uint32_t TILE16 = C::TILE >> 4;
+      const uint32_t kK = sdesc_lo(sK, 16), kMN = sdesc_lo(sK, 16384), vK = sdesc_lo(sV, 16);
+      const uint32_t qK = sdesc_lo(sQ, 16), qMN = sdesc_lo(sQ, 16384);
+      const uint32_t doK = sdesc_lo(sDO, 16), doMN = sdesc_lo(sDO, 16384), dsMN = sdesc_lo(sDS, 16384);
+      bool ok = warp_wait_b(bar(B_KV), 0, p.ctl, abort, 20);
       for (int u = 0; u < nit && ok; ++u) {
         const int st = u & 1, par = (u >> 1) & 1;
-        const uint32_t q0 = sQ + st * C::TILE, do0 = sDO + st * C::TILE;
-        if (!(ok = mbar_wait(bar(B_QF0 + st), par, p.ctl, abort, 21))) break;
+        const uint32_t so = (uint32_t)st * TILE16;
+        const uint32_t acc0 = u > 0 ? 1u : 0u;
+        if (!(ok = warp_wait_b(bar(B_QF0 + st), par, p.ctl, abort, 21))) break;
         tc_fence_after();
         // S^T = K Q_i^T   (M = keys, N = queries, K = d; both K-major)
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          mma_ss(tST, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q0 + off, 16, 1024), kIdS, k > 0);
+          const uint32_t off = (uint32_t)(k / 4) * 1024 + (uint32_t)(k % 4) * 2;
+          mma_ss_e(lead, tST, kK + off, HI, qK + so + off, HI, kIdS, k > 0);
         }
-        mma_commit(bar(B_ST));
-        if (!(ok = mbar_wait(bar(B_DOF0 + st), par, p.ctl, abort, 22))) break;
-        if (u > 0 && !(ok = mbar_wait(bar(B_DQE), (u - 1) & 1, p.ctl, abort, 23))) break;
+        mma_commit_e(lead, bar(B_ST));
+        if (!(ok = warp_wait_b(bar(B_DOF0 + st), par, p.ctl, abort, 22))) break;
+        if (u > 0 && !(ok = warp_wait_b(bar(B_DQE), (u - 1) & 1, p.ctl, abort, 23))) break;
         tc_fence_after();
         // dP^T = V dO_i^T
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          mma_ss(tDPT, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(do0 + off, 16, 1024), kIdS, k > 0);
+          const uint32_t off = (uint32_t)(k / 4) * 1024 + (uint32_t)(k % 4) * 2;
+          mma_ss_e(lead, tDPT, vK + off, HI, doK + so + off, HI, kIdS, k > 0);
         }
-        mma_commit(bar(B_DPT));
+        mma_commit_e(lead, bar(B_DPT));
         // dV += P^T dO_i   (A = P^T bf16 in TMEM, B = dO_i query-major)
-        if (!(ok = mbar_wait(bar(B_P), u & 1, p.ctl, abort, 24))) break;
+        if (!(ok = warp_wait_b(bar(B_P), u & 1, p.ctl, abort, 24))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
-          mma_ts(tDV, tST + pcol(k), sdesc_sw128(do0 + k * 2048, 16384, 1024), kIdG, u > 0 || k > 0);
+          mma_ts_e(lead, tDV, tST + pcol(k), doMN + so + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
         // dK += dS^T Q_i   (A = dS^T bf16 in TMEM)
-        if (!(ok = mbar_wait(bar(B_DS), u & 1, p.ctl, abort, 25))) break;
+        if (!(ok = warp_wait_b(bar(B_DS), u & 1, p.ctl, abort, 25))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
-          mma_ts(tDK, tDPT + pcol(k), sdesc_sw128(q0 + k * 2048, 16384, 1024), kIdG, u > 0 || k > 0);
+          mma_ts_e(lead, tDK, tDPT + pcol(k), qMN + so + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
         // dQ_i = dS K   (M = queries, N = d, K = keys; A = dS smem query-major, B = K key-major)
 #pragma unroll
         for (int k = 0; k < C::BK / 16; ++k)
-          mma_ss(tDPT, sdesc_sw128(sDS + k * 2048, 16384, 1024),
-                 sdesc_sw128(sK + k * 2048, 16384, 1024), kIdQ, k > 0);
-        mma_commit(bar(B_DQF));
+          mma_ss_e(lead, tDPT, dsMN + 128 * k, HI, kMN + 128 * k, HI, kIdQ, k > 0);
+        mma_commit_e(lead, bar(B_DQF));
       }
-      if (ok) mma_commit(bar(B_FIN));
-      mma_commit(bar(B_DRAIN));
+      if (ok) mma_commit_e(lead, bar(B_FIN));
+      mma_commit_e(lead, bar(B_DRAIN));
       mbar_wait_quiet(bar(B_DRAIN), 0, 200000000ull);
     }
   } else if (warp < 8) {

@@ -181,47 +181,53 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     }
   } else if (warp == C::W_MMA) {
     // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
+    // The whole warp runs the issue loop (control flow and descriptors stay
+    // warp-uniform); one elected lane issues.
+    {
+      const uint32_t lead = elect_one();
       constexpr uint32_t kIdS = idesc_bf16(128, C::BN, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, HD, false, true);
+      // descriptor halves (sdesc_lo / sdesc_hi) of Q tile 0 and ring slot 0
+      constexpr uint32_t HI = sdesc_hi(1024);
+      constexpr uint32_t QT16 = C::QTILE >> 4, KV16 = C::KVTILE >> 4, BLK16 = (C::BM * 128) >> 4;
+      const uint32_t qK = sdesc_lo(sQ, 16), rK = sdesc_lo(sRing, 16), rMN = sdesc_lo(sRing, C::BN * 128);
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
-        if (valid[t]) ok = mbar_wait(smem_u32(&bar_q[t]), 0, p.ctl, abort, 20);
+        if (valid[t]) ok = warp_wait(smem_u32(&bar_q[t]), 0, p.ctl, abort, 20);
 
       // S_t = Q_t K^T for the K tile in ring slot `slot`.
       auto issue_s = [&](int t, int slot) {
-        const uint32_t a0 = sQ + t * C::QTILE, b0 = sRing + slot * C::KVTILE;
+        const uint32_t a0 = qK + (uint32_t)t * QT16, b0 = rK + (uint32_t)slot * KV16;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (k / 4) * (C::BM * 128) + (k % 4) * 32;
-          mma_ss(tmem + t * 128, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
-                 kIdS, k > 0);
+          const uint32_t off = (uint32_t)(k / 4) * BLK16 + (uint32_t)(k % 4) * 2;
+          mma_ss_e(lead, tmem + t * 128, a0 + off, HI, b0 + off, HI, kIdS, k > 0);
         }
-        mma_commit(smem_u32(&bar_s[t]));
+        mma_commit_e(lead, smem_u32(&bar_s[t]));
       };
       // O_t (+)= P_t V for the V tile in ring slot `slot`.
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t b0 = sRing + slot * C::KVTILE;
+        const uint32_t b0 = rMN + (uint32_t)slot * KV16;
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts(tmem + 256 + t * HD, tmem + t * 128 + p_col<NH>(k),
-                 sdesc_sw128(b0 + k * 2048, C::BN * 128, 1024), kIdPV, acc || k > 0);
+          mma_ts_e(lead, tmem + 256 + t * HD, tmem + t * 128 + p_col<NH>(k), b0 + 128 * k, HI, kIdPV,
+                   (acc || k > 0) ? 1u : 0u);
       };
 
       int it = 0;
       if (ok) {
-        ok = mbar_wait(smem_u32(&bar_full[0]), 0, p.ctl, abort, 21);
+        ok = warp_wait(smem_u32(&bar_full[0]), 0, p.ctl, abort, 21);
         if (ok) {
           tc_fence_after();
           for (int t = 0; t < 2; ++t)
             if (valid[t]) issue_s(t, 0);
-          mma_commit(smem_u32(&bar_empty[0]));
+          mma_commit_e(lead, smem_u32(&bar_empty[0]));
           it = 1;
         }
       }
       for (int j = 1; j <= nmax && ok; ++j) {
         const int vslot = it % C::STAGES;
-        ok = mbar_wait(smem_u32(&bar_full[vslot]), (it / C::STAGES) & 1, p.ctl, abort, 22);
+        ok = warp_wait(smem_u32(&bar_full[vslot]), (it / C::STAGES) & 1, p.ctl, abort, 22);
         ++it;
         if (!ok) break;
         tc_fence_after();
@@ -231,14 +237,14 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         bool k_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (!valid[t] || j - 1 >= nkv_t[t]) continue;
-          ok = mbar_wait(smem_u32(&bar_p[t]), (j - 1) & 1, p.ctl, abort, 23);
+          ok = warp_wait(smem_u32(&bar_p[t]), (j - 1) & 1, p.ctl, abort, 23);
           if (!ok) break;
           tc_fence_after();
           issue_pv(t, vslot, j - 1 > 0);
-          if (j - 1 == nkv_t[t] - 1) mma_commit(smem_u32(&bar_o[t]));
+          if (j - 1 == nkv_t[t] - 1) mma_commit_e(lead, smem_u32(&bar_o[t]));
           if (j < nkv_t[t]) {
             if (!k_ready) {
-              ok = mbar_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 24);
+              ok = warp_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 24);
               if (!ok) break;
               tc_fence_after();
               k_ready = true;
@@ -247,17 +253,17 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&bar_empty[vslot]));
+        mma_commit_e(lead, smem_u32(&bar_empty[vslot]));
         if (have_k) {
           if (!k_ready) {
-            ok = mbar_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 25);
+            ok = warp_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 25);
             if (!ok) break;
           }
-          mma_commit(smem_u32(&bar_empty[kslot]));
+          mma_commit_e(lead, smem_u32(&bar_empty[kslot]));
         }
       }
       // Drain: every MMA issued above completes before TMEM is released.
-      mma_commit(smem_u32(&bar_drain));
+      mma_commit_e(lead, smem_u32(&bar_drain));
       mbar_wait_quiet(smem_u32(&bar_drain), 0, 200000000ull);
     }
   } else if (warp < C::WS) {
