@@ -340,14 +340,19 @@ __global__ void __launch_bounds__(448, 1)
       const int qt = i0 + u;
       const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
       const float* d_u = d_sh + (u & 1) * C::BQ + cb;
-      // prefetch the next tile's statistics
-      float nl = -INFINITY, nd = 0.f;
-      if (h == 0 && u + 1 < nit) {
-        const int q = (qt + 1) * C::BQ + r;
-        if (q < p.N) {
-          nl = -p.lse[rowbase + q] * kLog2e;
-          nd = -p.D[rowbase + q];
-        }
+      // next tile's statistics: copied asynchronously (zero past N) and
+      // converted after the wait at the end of the iteration, so that no
+      // warp stalls on the global loads
+      const int qn = (qt + 1) * C::BQ + r;
+      float* lse_n = lse_sh + ((u + 1) & 1) * C::BQ + r;
+      float* d_n = d_sh + ((u + 1) & 1) * C::BQ + r;
+      const bool fetch = h == 0 && u + 1 < nit;
+      if (fetch) {
+        const size_t src = rowbase + (qn < p.N ? qn : 0);
+        const uint32_t sz = qn < p.N ? 4u : 0u;
+        cp_async_4(smem_u32(lse_n), p.lse + src, sz);
+        cp_async_4(smem_u32(d_n), p.D + src, sz);
+        cp_async_commit();
       }
       if (!(ok = warp_wait_b(bar(B_ST), u & 1, p.ctl, abort, 30))) break;
       tc_fence_after();
@@ -419,14 +424,16 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS));
-      // publish the next tile's statistics
-      if (h == 0) {
-        lse_sh[((u + 1) & 1) * C::BQ + r] = nl;
-        d_sh[((u + 1) & 1) * C::BQ + r] = nd;
+      // publish the next tile's statistics (-LSE log2 e, -D; -inf past N)
+      if (fetch) {
+        cp_async_wait_all();
+        *lse_n = qn < p.N ? -*lse_n * kLog2e : -INFINITY;
+        *d_n = -*d_n;
       }
       mbar_arrive(bar(B_WG));
       if (!(ok = warp_wait_b(bar(B_WG), (u + 1) & 1, p.ctl, abort, 35))) break;
     }
+    cp_async_wait_all();  // none in flight when a wait above gave up
     // epilogue: dV rows of this key tile, columns [h*HD/2, (h+1)*HD/2)
     if (ok && warp_wait_b(bar(B_FIN), 0, p.ctl, abort, 33)) {
       tc_fence_after();

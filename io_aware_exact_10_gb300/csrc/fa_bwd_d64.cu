@@ -300,13 +300,19 @@ __global__ void __launch_bounds__(448, 1)
       const int qt = i0 + u;
       const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
       const float* d_u = d_sh + (u & 1) * C::BQ + cb;
-      float nl = -INFINITY, nd = 0.f;
-      if (h == 0 && u + 1 < nit) {
-        const int q = (qt + 1) * C::BQ + r;
-        if (q < p.N) {
-          nl = -p.lse[rowbase + q] * kLog2e;
-          nd = -p.D[rowbase + q];
-        }
+      // next tile's statistics: copied asynchronously (zero past N) and
+      // converted after the wait at the end of the iteration, so that no
+      // warp stalls on the global loads
+      const int qn = (qt + 1) * C::BQ + r;
+      float* lse_n = lse_sh + ((u + 1) & 1) * C::BQ + r;
+      float* d_n = d_sh + ((u + 1) & 1) * C::BQ + r;
+      const bool fetch = h == 0 && u + 1 < nit;
+      if (fetch) {
+        const size_t src = rowbase + (qn < p.N ? qn : 0);
+        const uint32_t sz = qn < p.N ? 4u : 0u;
+        cp_async_4(smem_u32(lse_n), p.lse + src, sz);
+        cp_async_4(smem_u32(d_n), p.D + src, sz);
+        cp_async_commit();
       }
       // ---- P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query < key
       if (!(ok = warp_wait(bar(B_ST), u & 1, p.ctl, abort, 81))) break;
@@ -373,13 +379,16 @@ __global__ void __launch_bounds__(448, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS0 + (u & 1)));
-      if (h == 0) {
-        lse_sh[((u + 1) & 1) * C::BQ + r] = nl;
-        d_sh[((u + 1) & 1) * C::BQ + r] = nd;
+      // publish the next tile's statistics (-LSE log2 e, -D; -inf past N)
+      if (fetch) {
+        cp_async_wait_all();
+        *lse_n = qn < p.N ? -*lse_n * kLog2e : -INFINITY;
+        *d_n = -*d_n;
       }
       mbar_arrive(bar(B_WG));
       if (!(ok = warp_wait(bar(B_WG), (u + 1) & 1, p.ctl, abort, 85))) break;
     }
+    cp_async_wait_all();  // none in flight when a wait above gave up
     // epilogue: dV rows of this key tile, columns [32h, 32h + 32)
     if (ok && warp_wait(bar(B_FIN), 0, p.ctl, abort, 86)) {
       tc_fence_after();
