@@ -10,16 +10,21 @@
 //
 // At d = 64 the operands are small enough to software-pipeline the loop:
 // tensor memory holds S^T, dP^T, P^T (bf16), dV, dK and dQ in separate
-// columns, so S^T of the next query tile is computed while the P/dS warps
-// work on the current one, and dP^T of the next tile as soon as the current
-// dP^T has been read.  The tensor pipe then runs
-//   ... S^T(u+1), dV(u), dP^T(u+1), dK(u), dQ(u), S^T(u+2) ...
-// while the P/dS warps run P(u), dS(u), P(u+1), ... back to back.  dK takes
-// dS from shared memory (key rows, query-contiguous: a K-major operand) and
-// dQ takes the same buffer as an M-major operand, so dS^T is never written to
-// tensor memory.  dS is double-buffered in shared memory, Q goes through a
-// 3-slot ring (its next tile is needed early), dO through a 2-slot ring, and
-// the dQ drain stages its reductions in a buffer of its own.
+// columns.  Per query tile u the MMA warp issues
+//   [P(u) ready]   dV(u), S^T(u+1)
+//   [dS(u) ready]  dP^T(u+1), dK(u), dQ(u)
+// so the next tile's S^T and dP^T are computed while the P/dS warps work on
+// the current one, and the P/dS warps run P(u), dS(u), P(u+1), ... with two
+// waits per tile.  The hand-offs rely on a tcgen05.commit tracking every
+// MMA issued before it: "S^T(u+1) done" also says that dV(u) has read the
+// P^T columns, and "dP^T(u) done" that dK(u-2) and dQ(u-2) have read the dS
+// buffer the P/dS warps are about to overwrite.  dK takes dS from shared
+// memory (key rows, query-contiguous: a K-major operand) and dQ takes the
+// same buffer as an M-major operand, so dS^T is never written to tensor
+// memory.  dS is double-buffered in shared memory, Q goes through a 3-slot
+// ring, dO through a 2-slot ring, and the dQ drain stages its reductions in
+// a buffer of its own.  Each P/dS warp fetches the LSE and D values of its
+// own 64 queries with cp.async, one tile ahead.
 //
 // Roles (448 threads):
 //   warps 0-7   P / dS: thread = key row = TMEM lane; warps 0-3 take query
@@ -50,9 +55,10 @@ struct Cfg64 {
   static constexpr int OFF_DO = OFF_Q + QSLOTS * TILE;
   static constexpr int OFF_DS = OFF_DO + DOSLOTS * TILE;     // 2 buffers
   static constexpr int OFF_STAGE = OFF_DS + 2 * DS_BYTES;    // dQ boxes, 8 KB per drain warp
-  static constexpr int OFF_LSE = OFF_STAGE + BQ * HD * 4;    // 2 x 128 floats (-LSE * log2 e)
-  static constexpr int OFF_D = OFF_LSE + 2 * BQ * 4;         // 2 x 128 floats (-D)
-  static constexpr int OFF_BAR = OFF_D + 2 * BQ * 4;
+  // per P/dS warp, two buffers of [64 x -LSE log2 e, 64 x -D]
+  static constexpr int OFF_STATS = OFF_STAGE + BQ * HD * 4;
+  static constexpr int STATS_WARP = 2 * 128 * 4;
+  static constexpr int OFF_BAR = OFF_STATS + 8 * STATS_WARP;
   static constexpr int NBAR = 32;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static constexpr int THREADS = 448;
@@ -67,17 +73,14 @@ static_assert(Cfg64::QSLOTS >= 2 && Cfg64::QSLOTS <= 3 && Cfg64::DOSLOTS == 2, "
 // barrier indices
 enum : int {
   B_K = 0, B_V, B_QF0, B_QF1, B_QF2, B_QE0, B_QE1, B_QE2, B_DOF0, B_DOF1, B_DOE0, B_DOE1,
-  B_ST, B_STF, B_P, B_PV, B_DPT, B_DPTF, B_DS0, B_DS1, B_DSF0, B_DSF1, B_DQF, B_DQE,
-  B_FIN, B_DRAIN, B_WG, B_COUNT
+  B_ST, B_P, B_DPT, B_DS, B_DQF, B_DQE, B_FIN, B_DRAIN, B_COUNT
 };
 static_assert(B_COUNT <= Cfg64::NBAR, "barrier area");
-// arrival counts: TMA and tcgen05.commit barriers take one arrival; the
-// P/dS hand-offs (STF, P, DPTF, DS*) one per P/dS warp; DQE one per drain
-// warp; WG every P/dS thread.
+// arrival counts: TMA and tcgen05.commit barriers take one arrival; P and DS
+// one per P/dS warp; DQE one per drain warp.
 __device__ __constant__ const uint32_t kBarCount64[B_COUNT] = {
     1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1,   // K, V, QF*, QE*, DOF*, DOE*
-    1, 8, 8, 1, 1, 8, 8, 8, 1, 1, 1, 4,   // ST, STF, P, PV, DPT, DPTF, DS*, DSF*, DQF, DQE
-    1, 1, 256};                           // FIN, DRAIN, WG
+    1, 8, 1, 8, 1, 4, 1, 1};              // ST, P, DPT, DS, DQF, DQE, FIN, DRAIN
 
 struct BwdParams64 {
   const float* lse;
@@ -121,8 +124,6 @@ __global__ void __launch_bounds__(448, 1)
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
                  sDO = s0 + C::OFF_DO, sDS = s0 + C::OFF_DS;
-  float* lse_sh = reinterpret_cast<float*>(smem + C::OFF_LSE);
-  float* d_sh = reinterpret_cast<float*>(smem + C::OFF_D);
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -230,31 +231,29 @@ __global__ void __launch_bounds__(448, 1)
         const uint32_t dso = (uint32_t)(u & 1) * DS16;
         const uint32_t acc0 = u > 0 ? 1u : 0u;
         const bool more = u + 1 < nit;
-        // S^T of the next tile, once the P/dS warps have read this one
-        if (more) {
-          if (!(ok = warp_wait(bar(B_QF0 + qs_v), qph_v, p.ctl, abort, 64))) break;
-          if (!(ok = warp_wait(bar(B_STF), u & 1, p.ctl, abort, 65))) break;
-          tc_fence_after();
-          issue_st(qo_v);
-        }
         // dV += P^T dO_u   (A = P^T bf16 in TMEM, B = dO_u query-major)
         if (!(ok = warp_wait(bar(B_P), u & 1, p.ctl, abort, 66))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
           mma_ts_e(lead, tDV, tPT + k * 8, doMN + dof_u + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
-        mma_commit_e(lead, bar(B_PV));                   // P^T columns free
         mma_commit_e(lead, bar(B_DOE0 + (u & 1)));       // dO_u slot free
-        // dP^T of the next tile, once the P/dS warps have read this one
+        // S^T of the next tile: its completion also covers dV(u), so the
+        // P/dS warps may then overwrite the P^T columns
+        if (more) {
+          if (!(ok = warp_wait(bar(B_QF0 + qs_v), qph_v, p.ctl, abort, 64))) break;
+          tc_fence_after();
+          issue_st(qo_v);
+        }
+        // dS(u) is in shared memory and dP^T(u) has been read
+        if (!(ok = warp_wait(bar(B_DS), u & 1, p.ctl, abort, 69))) break;
+        tc_fence_after();
         if (more) {
           if (!(ok = warp_wait(bar(B_DOF0 + ((u + 1) & 1)), ((u + 1) >> 1) & 1, p.ctl, abort, 67))) break;
-          if (!(ok = warp_wait(bar(B_DPTF), u & 1, p.ctl, abort, 68))) break;
           tc_fence_after();
           issue_dpt(dof_v);
         }
         // dK += dS^T Q_u   (A = dS key rows, K-major in shared memory; B = Q_u query-major)
-        if (!(ok = warp_wait(bar(B_DS0 + (u & 1)), (u >> 1) & 1, p.ctl, abort, 69))) break;
-        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
           mma_ss_e(lead, tDK, dsK + dso + (k >> 2) * 1024 + (k & 3) * 2, HI, qMN + qo_u + 128 * k, HI, kIdG,
@@ -267,7 +266,6 @@ __global__ void __launch_bounds__(448, 1)
         for (int k = 0; k < C::BK / 16; ++k)
           mma_ss_e(lead, tDQ, dsMN + dso + 128 * k, HI, kMN + 128 * k, HI, kIdQ, k > 0);
         mma_commit_e(lead, bar(B_DQF));
-        mma_commit_e(lead, bar(B_DSF0 + (u & 1)));       // dS buffer free
         qo_u = qo_v;
         if (++qs_v == C::QSLOTS) {
           qs_v = 0;
@@ -288,33 +286,45 @@ __global__ void __launch_bounds__(448, 1)
                    tPT = tmem + lane_off + C::COL_PT + cb / 2;
     const uint64_t sc2 = f2_pack(p.scale2, p.scale2);
     const size_t rowbase = (size_t)bh * p.N;
-    if (h == 0) {
-      const int q = i0 * C::BQ + r;
-      lse_sh[r] = q < p.N ? -p.lse[rowbase + q] * kLog2e : -INFINITY;
-      d_sh[r] = q < p.N ? -p.D[rowbase + q] : 0.f;
-    }
-    mbar_arrive(bar(B_WG));
-    bool ok = warp_wait(bar(B_WG), 0, p.ctl, abort, 80);
+    // This warp's statistics: buffer b holds -LSE log2 e (64 floats) then -D
+    // (64 floats) of queries [cb, cb + 64) of a tile; lane l fetches and
+    // converts entries l and l + 32.
+    float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS + warp * C::STATS_WARP);
+    auto fetch = [&](int tile, int b) {
+      float* st = stats + b * 128;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int q = tile * C::BQ + cb + lane + 32 * j;
+        const size_t src = rowbase + (q < p.N ? q : 0);
+        const uint32_t sz = q < p.N ? 4u : 0u;
+        cp_async_4(smem_u32(st + lane + 32 * j), p.lse + src, sz);
+        cp_async_4(smem_u32(st + 64 + lane + 32 * j), p.D + src, sz);
+      }
+      cp_async_commit();
+    };
+    auto convert = [&](int tile, int b) {
+      cp_async_wait_all();
+      float* st = stats + b * 128;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int q = tile * C::BQ + cb + lane + 32 * j;
+        float* l = st + lane + 32 * j;
+        *l = q < p.N ? -*l * kLog2e : -INFINITY;
+        st[64 + lane + 32 * j] = -st[64 + lane + 32 * j];
+      }
+      __syncwarp();
+    };
+    fetch(i0, 0);
+    convert(i0, 0);
+    bool ok = true;
     const uint32_t sw = (uint32_t)(r & 7);
     for (int u = 0; u < nit && ok; ++u) {
       const int qt = i0 + u;
-      const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
-      const float* d_u = d_sh + (u & 1) * C::BQ + cb;
-      // next tile's statistics: copied asynchronously (zero past N) and
-      // converted after the wait at the end of the iteration, so that no
-      // warp stalls on the global loads
-      const int qn = (qt + 1) * C::BQ + r;
-      float* lse_n = lse_sh + ((u + 1) & 1) * C::BQ + r;
-      float* d_n = d_sh + ((u + 1) & 1) * C::BQ + r;
-      const bool fetch = h == 0 && u + 1 < nit;
-      if (fetch) {
-        const size_t src = rowbase + (qn < p.N ? qn : 0);
-        const uint32_t sz = qn < p.N ? 4u : 0u;
-        cp_async_4(smem_u32(lse_n), p.lse + src, sz);
-        cp_async_4(smem_u32(d_n), p.D + src, sz);
-        cp_async_commit();
-      }
+      const float* lse_u = stats + (u & 1) * 128;
+      const float* d_u = lse_u + 64;
+      if (u + 1 < nit) fetch(qt + 1, (u + 1) & 1);
       // ---- P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query < key
+      // (S^T(u) done also means dV(u-1) has read the P^T columns)
       if (!(ok = warp_wait(bar(B_ST), u & 1, p.ctl, abort, 81))) break;
       tc_fence_after();
       uint32_t pk[32];
@@ -323,9 +333,6 @@ __global__ void __launch_bounds__(448, 1)
         tmem_ld32(tST, *reinterpret_cast<uint32_t(*)[32]>(pr));
         tmem_ld32(tST + 32, *reinterpret_cast<uint32_t(*)[32]>(pr + 32));
         tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_STF));    // S^T columns may be overwritten
         const bool diag = CAUSAL && qt == kt;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -339,9 +346,6 @@ __global__ void __launch_bounds__(448, 1)
           pk[i] = pack_bf16(p0, p1);
         }
       }
-      // the P^T columns are the A operand of dV(u-1): wait until it is done
-      if (u > 0 && !(ok = warp_wait(bar(B_PV), (u - 1) & 1, p.ctl, abort, 82))) break;
-      tc_fence_after();
       tmem_st16(tPT, *reinterpret_cast<const uint32_t(*)[16]>(pk));
       tmem_st16(tPT + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
       tmem_wait_st();
@@ -349,17 +353,13 @@ __global__ void __launch_bounds__(448, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P));
       // ---- dS = P o (dP - D), with P the bf16 values dV multiplied
+      // (dP^T(u) done also means dK(u-2) and dQ(u-2) have read dS buffer u&1)
       if (!(ok = warp_wait(bar(B_DPT), u & 1, p.ctl, abort, 83))) break;
       tc_fence_after();
       uint32_t dp[64];
       tmem_ld32(tDPT, *reinterpret_cast<uint32_t(*)[32]>(dp));
       tmem_ld32(tDPT + 32, *reinterpret_cast<uint32_t(*)[32]>(dp + 32));
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DPTF));     // dP^T columns may be overwritten
-      // dS buffer u&1 was last read by dK(u-2) and dQ(u-2)
-      if (u >= 2 && !(ok = warp_wait(bar(B_DSF0 + (u & 1)), ((u >> 1) - 1) & 1, p.ctl, abort, 84))) break;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(d_u + 2 * i);
@@ -377,16 +377,10 @@ __global__ void __launch_bounds__(448, 1)
                      "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                      : "memory");
       fence_proxy_async_smem();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DS0 + (u & 1)));
-      // publish the next tile's statistics (-LSE log2 e, -D; -inf past N)
-      if (fetch) {
-        cp_async_wait_all();
-        *lse_n = qn < p.N ? -*lse_n * kLog2e : -INFINITY;
-        *d_n = -*d_n;
-      }
-      mbar_arrive(bar(B_WG));
-      if (!(ok = warp_wait(bar(B_WG), (u + 1) & 1, p.ctl, abort, 85))) break;
+      if (lane == 0) mbar_arrive(bar(B_DS));         // also: dP^T(u) has been read
+      if (u + 1 < nit) convert(qt + 1, (u + 1) & 1);
     }
     cp_async_wait_all();  // none in flight when a wait above gave up
     // epilogue: dV rows of this key tile, columns [32h, 32h + 32)
