@@ -21,6 +21,8 @@
  *     pointer to fp32 [B][H][N].  Every pointer must be 16-byte aligned.
  *   - d must be 64 or 128.  N >= 1 is any length (the last tile is masked).
  *     B, H >= 1.  B == 0, H == 0 or N == 0 is an empty problem: FA_OK, no work.
+ *     B * H * ceil(N / 128) must be at most 2^27 - 1 (grid limits); larger
+ *     problems return FA_ERR_INVALID_ARG.
  *   - scale multiplies Q K^T before the softmax; it must be finite and > 0
  *     (usually 1/sqrt(d)).
  *   - causal = 1: key j is visible to query i iff j <= i (N_q = N_k = N).
@@ -70,9 +72,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int N, int d, float scale, int causal, struct CUstream_st* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: fp32 D = rowsum(dO * o) of shape
- * [B][H][N] followed by an fp32 dQ accumulator of shape [B][H][N][d], each
- * region rounded up to 256 bytes.  0 for an empty problem or invalid sizes.
+ * Bytes of device workspace fa_bwd needs: fp32 row statistics, two per row
+ * (-lse log2 e and -D with D = rowsum(dO * o)) with each head padded to whole
+ * 128-row tiles, i.e. B*H*ceil(N/128)*256 floats, followed by an fp32 dQ
+ * accumulator of shape [B][H][N][d]; each region rounded up to 256 bytes.
+ * 0 for an empty problem or invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -103,20 +107,21 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * cudaMalloc (it may synchronise the device and takes unbounded time).
  *
  * Same arguments, semantics and outputs as fa_bwd minus the workspace: the
- * scratch (D and the fp32 dQ accumulator) lives in a 64 MiB array that the
- * library holds on every device that loads it, until the process exits.
+ * scratch (the row statistics and the fp32 dQ accumulator) lives in a 64 MiB
+ * array that the library holds on every device that loads it, until the
+ * process exits.
  *   - Capacity: fa_bwd_workspace_size(B, H, N, d) must be <= 64 MiB
- *     (67108864 bytes): up to about 130,000 rows (B*H*N) at d=128 and
- *     258,000 at d=64; larger problems return FA_ERR_INVALID_ARG before
- *     anything is launched.
+ *     (67108864 bytes): up to about 129,000 rows (B*H*N) at d=128 and
+ *     254,000 at d=64 (N a multiple of 128); larger problems return
+ *     FA_ERR_INVALID_ARG before anything is launched.
  *   - The first call on a device looks up the array's device address (a
  *     one-time runtime query, with that device current); make that first
  *     call before any stream capture.
- *   - Every call on a device shares the one array.  Each call rewrites D and
- *     re-zeroes the accumulator before use, so earlier contents never leak
- *     into a result, but calls that overlap on the GPU (on different streams
- *     without ordering between them) race on the array and give wrong
- *     gradients.
+ *   - Every call on a device shares the one array.  Each call rewrites the
+ *     statistics and re-zeroes the accumulator before use, so earlier
+ *     contents never leak into a result, but calls that overlap on the GPU
+ *     (on different streams without ordering between them) race on the array
+ *     and give wrong gradients.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.
  */
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,

@@ -123,13 +123,17 @@ fa_status check_common(int B, int H, int N, int d, float scale, int causal, bool
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   *empty = (B == 0 || H == 0 || N == 0);
   if (*empty) return FA_OK;
-  // one-dimensional grids of (query-tile pairs or key tiles) x heads
+  // one-dimensional grids of (query-tile pairs or key tiles) x heads, and
+  // the backward preprocess's 16 blocks per 128-row tile
   const long long BH = (long long)B * H;
-  if (BH * ((N + 127) / 128) > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
+  if (BH * ((N + 127) / 128) * 16 > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+// floats of the backward's row statistics: two per row, each head padded to
+// whole 128-row tiles
+size_t stats_floats(int BH, int N) { return (size_t)BH * (size_t)((N + 127) / 128) * 256; }
 
 }  // namespace
 
@@ -171,7 +175,7 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   bool empty = false;
   if (check_common(B, H, N, d, 1.0f, 0, &empty) != FA_OK || empty) return 0;
   const size_t rows = (size_t)B * H * N;
-  return round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
+  return round256(stats_floats(B * H, N) * sizeof(float)) + round256(rows * d * sizeof(float));
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -195,12 +199,12 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (!encode_bf16_3d(&a.tq, q, BH, N, d) || !encode_bf16_3d(&a.tk, k, BH, N, d) ||
       !encode_bf16_3d(&a.tv, v, BH, N, d) || !encode_bf16_3d(&a.tdo, dO, BH, N, d))
     return FA_ERR_INVALID_ARG;
-  const size_t rows = (size_t)BH * N;
   a.o = o;
   a.dO = dO;
   a.lse = lse;
-  a.D = static_cast<float*>(workspace);
-  a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * sizeof(float)));
+  a.stats = static_cast<float*>(workspace);
+  a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                      round256(stats_floats(BH, N) * sizeof(float)));
   if (!encode_f32_3d(&a.tdq, a.dq_acc, BH, N, d)) return FA_ERR_INVALID_ARG;
   a.dq = dq;
   a.dk = dk;

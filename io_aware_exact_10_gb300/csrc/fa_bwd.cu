@@ -44,41 +44,55 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
-// preprocess: D = rowsum(dO * O), dQacc = 0.  One warp per row.
+// preprocess: for every row q of every head, D = rowsum(dO * O) and the
+// row's statistics for the main kernels, -LSE log2 e and -D (-inf and 0 for
+// the pad rows q >= N of a head's last tile); and dQacc = 0.  Statistics
+// layout: per head and 128-query tile, 128 values of -LSE log2 e then 128 of
+// -D.  A thread takes 8 elements (16 bytes) of a row, a group of HD / 8
+// lanes one row; blockIdx.x = head * (blocks per tile * nq) + block.
 // ---------------------------------------------------------------------------
 template <int HD>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dO,
-                                                         float* __restrict__ D,
-                                                         float* __restrict__ dq_acc, long rows) {
-  constexpr int PER = HD / 32;  // bf16 elements per lane (2 or 4)
-  const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const size_t base = (size_t)row * HD + lane * PER;
+                                                         const float* __restrict__ lse,
+                                                         float* __restrict__ stats,
+                                                         float* __restrict__ dq_acc, int N, int nq) {
+  constexpr int TPR = HD / 8;                  // threads per row
+  constexpr int ROWS = 256 / TPR;              // rows per block
+  constexpr int BLOCKS_PER_TILE = 128 / ROWS;
+  const unsigned blocks_per_head = (unsigned)nq * BLOCKS_PER_TILE;
+  const unsigned hb = blockIdx.x / blocks_per_head;
+  const int qp = (int)((blockIdx.x - hb * blocks_per_head) * ROWS + threadIdx.x / TPR);  // padded row
+  const int part = threadIdx.x % TPR;
+  float* st = stats + ((size_t)hb * nq + (qp >> 7)) * 256 + (qp & 127);
+  // pad rows take no loads but stay in the warp for the shuffles below
+  const bool valid = qp < N;
+  const size_t row = (size_t)hb * N + (valid ? qp : 0);
+  const float l = valid && part == 0 ? lse[row] : 0.f;
+  const size_t base = row * HD + part * 8;
+  uint4 a = make_uint4(0u, 0u, 0u, 0u), b = make_uint4(0u, 0u, 0u, 0u);
+  if (valid) {
+    a = *reinterpret_cast<const uint4*>(o + base);
+    b = *reinterpret_cast<const uint4*>(dO + base);
+    float4* z = reinterpret_cast<float4*>(dq_acc + base);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
   float acc = 0.f;
-  if constexpr (PER == 4) {
-    const uint2 a = *reinterpret_cast<const uint2*>(o + base);
-    const uint2 b = *reinterpret_cast<const uint2*>(dO + base);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float2 fa2 = __bfloat1622float2(a2[i]), fb2 = __bfloat1622float2(b2[i]);
-      acc = fmaf(fa2.x, fb2.x, acc);
-      acc = fmaf(fa2.y, fb2.y, acc);
-    }
-    *reinterpret_cast<float4*>(dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
-  } else {
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dO + base);
-    const float2 fa2 = __bfloat1622float2(a), fb2 = __bfloat1622float2(b);
-    acc = fmaf(fa2.x, fb2.x, fmaf(fa2.y, fb2.y, 0.f));
-    *reinterpret_cast<float2*>(dq_acc + base) = make_float2(0.f, 0.f);
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa2 = __bfloat1622float2(a2[i]), fb2 = __bfloat1622float2(b2[i]);
+    acc = fmaf(fa2.x, fb2.x, acc);
+    acc = fmaf(fa2.y, fb2.y, acc);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) D[row] = acc;
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (part == 0) {
+    st[0] = valid ? -l * kLog2e : -INFINITY;
+    st[128] = valid ? -acc : 0.f;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -139,8 +153,7 @@ __device__ __constant__ const uint32_t kBarCount[B_COUNT] = {1, 1, 1, 1, 1, 4, 4
                                                              1, 4, 1, 1, 256};
 
 struct BwdParams {
-  const float* lse;
-  const float* D;
+  const float* stats;  // per tile: -LSE log2 e (128), -D (128)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int N, nq, nkv, BH, group;
@@ -328,9 +341,9 @@ __global__ void __launch_bounds__(448, 1)
     // warpgroup 0 stages the negated log2-scaled LSE and negated D of the
     // first query tile
     if (h == 0) {
-      const int q = i0 * C::BQ + r;
-      lse_sh[r] = q < p.N ? -p.lse[rowbase + q] * kLog2e : -INFINITY;
-      d_sh[r] = q < p.N ? -p.D[rowbase + q] : 0.f;
+      const float* st = p.stats + ((size_t)bh * p.nq + i0) * 256;
+      lse_sh[r] = st[r];
+      d_sh[r] = st[128 + r];
     }
     // Both warpgroups synchronise on an mbarrier (256 arrivals per phase) so
     // that the wait stays bounded if another warp gives up.
@@ -340,18 +353,15 @@ __global__ void __launch_bounds__(448, 1)
       const int qt = i0 + u;
       const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
       const float* d_u = d_sh + (u & 1) * C::BQ + cb;
-      // next tile's statistics: copied asynchronously (zero past N) and
-      // converted after the wait at the end of the iteration, so that no
-      // warp stalls on the global loads
-      const int qn = (qt + 1) * C::BQ + r;
+      // next tile's statistics, copied asynchronously so that no warp
+      // stalls on the global loads; waited for at the end of the iteration
       float* lse_n = lse_sh + ((u + 1) & 1) * C::BQ + r;
       float* d_n = d_sh + ((u + 1) & 1) * C::BQ + r;
       const bool fetch = h == 0 && u + 1 < nit;
       if (fetch) {
-        const size_t src = rowbase + (qn < p.N ? qn : 0);
-        const uint32_t sz = qn < p.N ? 4u : 0u;
-        cp_async_4(smem_u32(lse_n), p.lse + src, sz);
-        cp_async_4(smem_u32(d_n), p.D + src, sz);
+        const float* st = p.stats + ((size_t)bh * p.nq + qt + 1) * 256;
+        cp_async_4(smem_u32(lse_n), st + r, 4u);
+        cp_async_4(smem_u32(d_n), st + 128 + r, 4u);
         cp_async_commit();
       }
       if (!(ok = warp_wait_b(bar(B_ST), u & 1, p.ctl, abort, 30))) break;
@@ -424,12 +434,8 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS));
-      // publish the next tile's statistics (-LSE log2 e, -D; -inf past N)
-      if (fetch) {
-        cp_async_wait_all();
-        *lse_n = qn < p.N ? -*lse_n * kLog2e : -INFINITY;
-        *d_n = -*d_n;
-      }
+      // publish the next tile's statistics
+      if (fetch) cp_async_wait_all();
       mbar_arrive(bar(B_WG));
       if (!(ok = warp_wait_b(bar(B_WG), (u + 1) & 1, p.ctl, abort, 35))) break;
     }
@@ -564,8 +570,7 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   BwdParams p;
-  p.lse = a.lse;
-  p.D = a.D;
+  p.stats = a.stats;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.N = a.N;
@@ -584,9 +589,10 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
 template <int HD>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
   const long rows = (long)a.BH * a.N;
-  fa_bwd_pre_kernel<HD><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.D,
-      a.dq_acc, rows);
+  const int nq = (a.N + 127) / 128;
+  fa_bwd_pre_kernel<HD><<<(unsigned)((long)a.BH * nq * (128 / (256 / (HD / 8)))), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.stats,
+      a.dq_acc, a.N, nq);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if constexpr (HD == 64)

@@ -23,15 +23,16 @@
 // same buffer as an M-major operand, so dS^T is never written to tensor
 // memory.  dS is double-buffered in shared memory, Q goes through a 3-slot
 // ring, dO through a 2-slot ring, and the dQ drain stages its reductions in
-// a buffer of its own.  Each P/dS warp fetches the LSE and D values of its
-// own 64 queries with cp.async, one tile ahead.
+// a buffer of its own.  The row statistics of each query tile (-LSE log2 e
+// and -D, written by the preprocess kernel) come with its Q tile.
 //
-// Roles (448 threads):
-//   warps 0-7   P / dS: thread = key row = TMEM lane; warps 0-3 take query
-//               columns 0-63 of the tile, warps 4-7 columns 64-127
-//   warps 8-11  dQ drain (thread = query row), then the dK epilogue
-//   warp  12    TMA producer
-//   warp  13    tcgen05 MMA issuer and TMEM owner
+// Roles (704 threads):
+//   warps 0-15  P / dS: thread = key row = TMEM lane (warp w takes lanes
+//               32 (w % 4) ...); warp w takes query columns [32 g, 32 g + 32)
+//               of the tile, g = w / 4, so each scheduler runs four of them
+//   warps 16-19 dQ drain (thread = query row), then the dK epilogue
+//   warp  20    TMA producer
+//   warp  21    tcgen05 MMA issuer and TMEM owner
 #include <cuda_bf16.h>
 
 #include "fa_kernels.h"
@@ -55,20 +56,26 @@ struct Cfg64 {
   static constexpr int OFF_DO = OFF_Q + QSLOTS * TILE;
   static constexpr int OFF_DS = OFF_DO + DOSLOTS * TILE;     // 2 buffers
   static constexpr int OFF_STAGE = OFF_DS + 2 * DS_BYTES;    // dQ boxes, 8 KB per drain warp
-  // per P/dS warp, two buffers of [64 x -LSE log2 e, 64 x -D]
+  // P/dS warps: NG column groups per TMEM lane quarter, CW query columns each
+  static constexpr int NG = 2;
+  static constexpr int NPW = 4 * NG;
+  static constexpr int CW = BQ / NG;
+  // row statistics of the tile in each Q slot: 128 x -LSE log2 e, 128 x -D
   static constexpr int OFF_STATS = OFF_STAGE + BQ * HD * 4;
-  static constexpr int STATS_WARP = 2 * 128 * 4;
-  static constexpr int OFF_BAR = OFF_STATS + 8 * STATS_WARP;
+  static constexpr int STATS_SLOT = 2 * BQ * 4;
+  static constexpr int OFF_BAR = OFF_STATS + QSLOTS * STATS_SLOT;
   static constexpr int NBAR = 32;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
-  static constexpr int THREADS = 448;
-  static constexpr int W_LOAD = 12, W_MMA = 13;
+  // roles: P/dS warps, 4 dQ drain warps, the TMA warp, the MMA warp
+  static constexpr int W_LOAD = NPW + 4, W_MMA = NPW + 5;  // drain: warps NPW ... NPW + 3
+  static constexpr int THREADS = (NPW + 6) * 32;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_PT = 256, COL_DV = 320, COL_DK = 384,
                             COL_DQ = 448;
 };
 static_assert(Cfg64::SMEM <= 232448, "shared memory budget");
 static_assert(Cfg64::QSLOTS >= 2 && Cfg64::QSLOTS <= 3 && Cfg64::DOSLOTS == 2, "ring sizes");
+static_assert(Cfg64::NG == 2 || Cfg64::NG == 4, "32 or 64 query columns per P/dS warp");
 
 // barrier indices
 enum : int {
@@ -79,12 +86,11 @@ static_assert(B_COUNT <= Cfg64::NBAR, "barrier area");
 // arrival counts: TMA and tcgen05.commit barriers take one arrival; P and DS
 // one per P/dS warp; DQE one per drain warp.
 __device__ __constant__ const uint32_t kBarCount64[B_COUNT] = {
-    1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1,   // K, V, QF*, QE*, DOF*, DOE*
-    1, 8, 1, 8, 1, 4, 1, 1};              // ST, P, DPT, DS, DQF, DQE, FIN, DRAIN
+    1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1,           // K, V, QF*, QE*, DOF*, DOE*
+    1, Cfg64::NPW, 1, Cfg64::NPW, 1, 4, 1, 1};    // ST, P, DPT, DS, DQF, DQE, FIN, DRAIN
 
 struct BwdParams64 {
-  const float* lse;
-  const float* D;
+  const float* stats;  // per tile: -LSE log2 e (128), -D (128)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int N, nq, nkv, BH, group;
@@ -99,7 +105,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const K
 }
 
 template <bool CAUSAL>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(Cfg64::THREADS, 1)
     fa_bwd_d64_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                       const __grid_constant__ CUtensorMap tdq, const BwdParams64 p) {
@@ -156,8 +162,10 @@ __global__ void __launch_bounds__(448, 1)
         const int qt = i0 + u;
         const int qs = u % C::QSLOTS, qn = u / C::QSLOTS;
         if (qn > 0 && !(ok = mbar_wait(bar(B_QE0 + qs), (qn - 1) & 1, p.ctl, abort, 50))) break;
-        mbar_arrive_expect_tx(bar(B_QF0 + qs), C::TILE);
+        mbar_arrive_expect_tx(bar(B_QF0 + qs), C::TILE + C::STATS_SLOT);
         tma_load_3d(sQ + qs * C::TILE, &tq, bar(B_QF0 + qs), 0, qt * C::BQ, bh);
+        bulk_load(s0 + C::OFF_STATS + qs * C::STATS_SLOT, p.stats + ((size_t)bh * p.nq + qt) * 256,
+                  C::STATS_SLOT, bar(B_QF0 + qs));
         ++nq_issued;
         if (u == 0) {
           mbar_arrive_expect_tx(bar(B_V), C::TILE);
@@ -276,66 +284,50 @@ __global__ void __launch_bounds__(448, 1)
       mma_commit_e(lead, bar(B_DRAIN));
       mbar_wait_quiet(bar(B_DRAIN), 0, 200000000ull);
     }
-  } else if (warp < 8) {
-    // --------------------------------------------- P / dS warpgroups (x2)
-    const int h = warp >> 2;
+  } else if (warp < C::NPW) {
+    // ------------------------------------------------------------- P / dS
+    constexpr int CW = C::CW;                       // query columns of this warp
+    const int g = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int cb = 64 * h;                          // first query column of this thread
+    const int cb = CW * g;                          // first query column of this thread
     const uint32_t tST = tmem + lane_off + C::COL_ST + cb, tDPT = tmem + lane_off + C::COL_DPT + cb,
                    tPT = tmem + lane_off + C::COL_PT + cb / 2;
     const uint64_t sc2 = f2_pack(p.scale2, p.scale2);
     const size_t rowbase = (size_t)bh * p.N;
-    // This warp's statistics: buffer b holds -LSE log2 e (64 floats) then -D
-    // (64 floats) of queries [cb, cb + 64) of a tile; lane l fetches and
-    // converts entries l and l + 32.
-    float* stats = reinterpret_cast<float*>(smem + C::OFF_STATS + warp * C::STATS_WARP);
-    auto fetch = [&](int tile, int b) {
-      float* st = stats + b * 128;
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int q = tile * C::BQ + cb + lane + 32 * j;
-        const size_t src = rowbase + (q < p.N ? q : 0);
-        const uint32_t sz = q < p.N ? 4u : 0u;
-        cp_async_4(smem_u32(st + lane + 32 * j), p.lse + src, sz);
-        cp_async_4(smem_u32(st + 64 + lane + 32 * j), p.D + src, sz);
-      }
-      cp_async_commit();
-    };
-    auto convert = [&](int tile, int b) {
-      cp_async_wait_all();
-      float* st = stats + b * 128;
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int q = tile * C::BQ + cb + lane + 32 * j;
-        float* l = st + lane + 32 * j;
-        *l = q < p.N ? -*l * kLog2e : -INFINITY;
-        st[64 + lane + 32 * j] = -st[64 + lane + 32 * j];
-      }
-      __syncwarp();
-    };
-    fetch(i0, 0);
-    convert(i0, 0);
+    // statistics of the tile in Q slot s: 128 x -LSE log2 e, 128 x -D,
+    // loaded with the Q tile (same barrier)
+    const float* stats = reinterpret_cast<const float*>(smem + C::OFF_STATS);
+    int qs_u = 0;
+    uint32_t qph_u = 0;
     bool ok = true;
     const uint32_t sw = (uint32_t)(r & 7);
+    // this thread's 16-byte chunks of a dS key row: 64-query block cb / 64,
+    // chunks (cb % 64) / 8 ... of 8 queries each
+    const uint32_t ds_row = (uint32_t)(cb >> 6) * 16384u + (uint32_t)r * 128u;
+    const uint32_t ds_c0 = (uint32_t)((cb & 63) >> 3);
     for (int u = 0; u < nit && ok; ++u) {
       const int qt = i0 + u;
-      const float* lse_u = stats + (u & 1) * 128;
-      const float* d_u = lse_u + 64;
-      if (u + 1 < nit) fetch(qt + 1, (u + 1) & 1);
+      const float* lse_u = stats + qs_u * 256 + cb;
+      const float* d_u = lse_u + 128;
+      if (!(ok = warp_wait(bar(B_QF0 + qs_u), qph_u, p.ctl, abort, 80))) break;
+      if (++qs_u == C::QSLOTS) {
+        qs_u = 0;
+        qph_u ^= 1u;
+      }
       // ---- P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query < key
       // (S^T(u) done also means dV(u-1) has read the P^T columns)
       if (!(ok = warp_wait(bar(B_ST), u & 1, p.ctl, abort, 81))) break;
       tc_fence_after();
-      uint32_t pk[32];
+      uint32_t pk[CW / 2];
       {
-        float pr[64];
-        tmem_ld32(tST, *reinterpret_cast<uint32_t(*)[32]>(pr));
-        tmem_ld32(tST + 32, *reinterpret_cast<uint32_t(*)[32]>(pr + 32));
+        float pr[CW];
+#pragma unroll
+        for (int c = 0; c < CW; c += 32) tmem_ld32(tST + c, *reinterpret_cast<uint32_t(*)[32]>(pr + c));
         tmem_wait_ld();
         const bool diag = CAUSAL && qt == kt;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < CW / 2; ++i) {
           const int q = 2 * i;
           const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(lse_u + q);
           float x0, x1;
@@ -346,8 +338,8 @@ __global__ void __launch_bounds__(448, 1)
           pk[i] = pack_bf16(p0, p1);
         }
       }
-      tmem_st16(tPT, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-      tmem_st16(tPT + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+#pragma unroll
+      for (int c = 0; c < CW / 2; c += 16) tmem_st16(tPT + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -356,12 +348,12 @@ __global__ void __launch_bounds__(448, 1)
       // (dP^T(u) done also means dK(u-2) and dQ(u-2) have read dS buffer u&1)
       if (!(ok = warp_wait(bar(B_DPT), u & 1, p.ctl, abort, 83))) break;
       tc_fence_after();
-      uint32_t dp[64];
-      tmem_ld32(tDPT, *reinterpret_cast<uint32_t(*)[32]>(dp));
-      tmem_ld32(tDPT + 32, *reinterpret_cast<uint32_t(*)[32]>(dp + 32));
+      uint32_t dp[CW];
+#pragma unroll
+      for (int c = 0; c < CW; c += 32) tmem_ld32(tDPT + c, *reinterpret_cast<uint32_t(*)[32]>(dp + c));
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < CW / 2; ++i) {
         const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(d_u + 2 * i);
         const uint32_t w = pk[i];
         const uint64_t pv = f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
@@ -369,34 +361,37 @@ __global__ void __launch_bounds__(448, 1)
         f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), nd2), pv), a, b);
         pk[i] = pack_bf16(a, b);
       }
-      // key row r of the dS buffer: 64 queries of half h, 128-byte swizzled
-      const uint32_t srow = sDS + (uint32_t)(u & 1) * C::DS_BYTES + (uint32_t)h * 16384u + (uint32_t)r * 128u;
+      // key row r of dS buffer u&1, 128-byte swizzled
+      const uint32_t srow = sDS + (uint32_t)(u & 1) * C::DS_BYTES + ds_row;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + (((uint32_t)c ^ sw) << 4)),
+      for (int c = 0; c < CW / 8; ++c)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + (((ds_c0 + (uint32_t)c) ^ sw) << 4)),
                      "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                      : "memory");
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS));         // also: dP^T(u) has been read
-      if (u + 1 < nit) convert(qt + 1, (u + 1) & 1);
     }
-    cp_async_wait_all();  // none in flight when a wait above gave up
-    // epilogue: dV rows of this key tile, columns [32h, 32h + 32)
+    // epilogue: dV rows of this key tile, columns [DVC g, DVC g + DVC)
+    constexpr int DVC = C::HD / C::NG;
     if (ok && warp_wait(bar(B_FIN), 0, p.ctl, abort, 86)) {
       tc_fence_after();
       const int key = kt * C::BK + r;
       uint32_t v[32];
-      tmem_ld32(tmem + lane_off + C::COL_DV + 32 * h, v);
+      if constexpr (DVC == 32) {
+        tmem_ld32(tmem + lane_off + C::COL_DV + DVC * g, v);
+      } else {
+        tmem_ld16(tmem + lane_off + C::COL_DV + DVC * g, *reinterpret_cast<uint32_t(*)[16]>(v));
+      }
       tmem_wait_ld();
-      uint32_t pkv[16];
+      uint32_t pkv[DVC / 2];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) pkv[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      for (int i = 0; i < DVC / 2; ++i) pkv[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
       if (key < p.N) {
-        uint4* d4 = reinterpret_cast<uint4*>(p.dv + (rowbase + key) * C::HD + 32 * h);
+        uint4* d4 = reinterpret_cast<uint4*>(p.dv + (rowbase + key) * C::HD + DVC * g);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pkv[4 * i], pkv[4 * i + 1], pkv[4 * i + 2], pkv[4 * i + 3]);
+        for (int i = 0; i < DVC / 8; ++i) d4[i] = make_uint4(pkv[4 * i], pkv[4 * i + 1], pkv[4 * i + 2], pkv[4 * i + 3]);
       }
     }
   } else {
@@ -414,28 +409,26 @@ __global__ void __launch_bounds__(448, 1)
     for (int u = 0; u < nit; ++u) {
       if (!(ok = warp_wait(bar(B_DQF), u & 1, p.ctl, abort, 90))) break;
       tc_fence_after();
-      uint32_t v[64];
-      tmem_ld32(tmem + lane_off + C::COL_DQ, *reinterpret_cast<uint32_t(*)[32]>(v));
-      tmem_ld32(tmem + lane_off + C::COL_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(B_DQE));                   // dQ's TMEM columns are free again
-        bulk_wait_group_read<0>();                 // the previous boxes have left the staging area
-      }
+      if (lane == 0) bulk_wait_group_read<0>();  // the previous boxes have left the staging area
       __syncwarp();
       const int y = (i0 + u) * C::BQ + sp * 32;
+      // columns [32 bb, 32 bb + 32) -> box bb
 #pragma unroll
       for (int bb = 0; bb < 2; ++bb) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + C::COL_DQ + 32 * bb, v);
+        tmem_wait_ld();
+        if (bb == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_DQE));  // dQ's TMEM columns are free again
+        }
         const uint32_t row = stage + (uint32_t)bb * 4096u + (uint32_t)lane * 128u;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int col = bb * 32 + c * 4;
+        for (int c = 0; c < 8; ++c)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((uint32_t)c ^ sw) << 4)),
-                       "r"(v[col]), "r"(v[col + 1]), "r"(v[col + 2]), "r"(v[col + 3])
+                       "r"(v[4 * c]), "r"(v[4 * c + 1]), "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
                        : "memory");
-        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -486,8 +479,7 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   BwdParams64 p;
-  p.lse = a.lse;
-  p.D = a.D;
+  p.stats = a.stats;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.N = a.N;

@@ -29,7 +29,8 @@ struct BwdLaunch {
   const void* o;                // bf16 [BH][N][d]
   const void* dO;               // bf16 [BH][N][d]
   const float* lse;             // fp32 [BH][N]
-  float* D;                     // fp32 [BH][N] workspace
+  float* stats;                 // fp32 [BH][nq][2][128] workspace: per 128-query tile,
+                                // -LSE log2 e then -D of its rows (-inf, 0 past N)
   float* dq_acc;                // fp32 [BH][N][d] workspace
   void* dq;                     // bf16 [BH][N][d]
   void* dk;                     // bf16 [BH][N][d]

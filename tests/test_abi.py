@@ -47,9 +47,10 @@ def test_strerror_and_version(L):
 def test_workspace_size(L):
     import io_aware_exact_10_gb300 as fa
     r256 = lambda x: (x + 255) // 256 * 256
-    for B, H, N, d in ((1, 1, 128, 64), (2, 3, 200, 128), (64, 16, 1024, 64)):
+    for B, H, N, d in ((1, 1, 128, 64), (2, 3, 200, 128), (64, 16, 1024, 64), (1, 1, 1, 64)):
         rows = B * H * N
-        assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(rows * 4) + r256(rows * d * 4)
+        stats = B * H * ((N + 127) // 128) * 256  # two floats per row, heads padded to 128 rows
+        assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(stats * 4) + r256(rows * d * 4)
     assert fa.fa_bwd_workspace_size(0, 1, 128, 64) == 0
     assert fa.fa_bwd_workspace_size(1, 1, 128, 96) == 0
     assert fa.fa_bwd_workspace_size(-1, 1, 128, 64) == 0
