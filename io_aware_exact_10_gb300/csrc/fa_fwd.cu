@@ -12,11 +12,15 @@
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer (Q tiles once, then K_0, V_0, K_1, V_1, ...)
 //   warp  9    tcgen05 MMA issuer (one thread) and TMEM owner
-// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1.  The softmax writes P as
-// bf16 pairs into the first 64 columns of its S region and the MMA reads it
-// from there as the A operand of O += P V.  The two query tiles alternate on
-// the tensor core: while one tile's softmax runs, the other tile's
-// O += P V and S = Q K^T run.
+// Tensor memory (512 columns) at d = 128: S_0 | S_1 | O_0 | O_1.  The softmax
+// writes P as bf16 pairs into the first 64 columns of its S region and the
+// MMA reads it from there as the A operand of O += P V.  The two query tiles
+// alternate on the tensor core: while one tile's softmax runs, the other
+// tile's O += P V and S = Q K^T run.
+// At d = 64: S_0 | S_1 | P_0 | P_1 | O_0 | O_1.  With P in columns of its own,
+// the softmax takes its whole S row into registers and releases S at once,
+// so S_t(j+1) is computed while the softmax of step j runs; "P_t free"
+// (PV_t(j-1) complete) guards the P store and the rare rescale of O.
 //
 // Online softmax in base 2 with the scale folded into one FMA: the running
 // max m and normaliser l of each row follow the recurrence of Flash Attention,
@@ -54,6 +58,11 @@ struct FwdCfg {
   static constexpr int CPT = 128 / NH;            // key columns per softmax thread
   static constexpr int OCPT = HD / NH;            // O columns per softmax thread
   static constexpr uint32_t TMEM_COLS = 512;
+  // P in columns of its own (d = 64 only: S, P and O of two tiles fill the 512)
+  static constexpr bool SEPP = HD == 64 && NH == 1;
+  static constexpr uint32_t colS(int t) { return (uint32_t)t * 128; }
+  static constexpr uint32_t colP(int t) { return SEPP ? 256 + (uint32_t)t * 64 : (uint32_t)t * 128; }
+  static constexpr uint32_t colO(int t) { return SEPP ? 384 + (uint32_t)t * 64 : 256 + (uint32_t)t * HD; }
 };
 
 struct FwdParams {
@@ -93,6 +102,8 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   __shared__ __align__(8) uint64_t bar_s[2];
   __shared__ __align__(8) uint64_t bar_p[2];
   __shared__ __align__(8) uint64_t bar_o[2];
+  __shared__ __align__(8) uint64_t bar_sf[2];  // S_t read by its softmax (P in own columns)
+  __shared__ __align__(8) uint64_t bar_pf[2];  // PV_t complete (P in own columns)
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ __align__(8) uint64_t bar_x[2][4];  // partner-warp exchange (NH == 2)
   __shared__ float xch[2][2][2][128];             // [tile][parity][half][row]
@@ -126,6 +137,8 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       mbar_init(smem_u32(&bar_p[t]), 4 * NH);
       for (int sp = 0; sp < 4; ++sp) mbar_init(smem_u32(&bar_x[t][sp]), 64);
       mbar_init(smem_u32(&bar_o[t]), 1);
+      mbar_init(smem_u32(&bar_sf[t]), 4 * NH);
+      mbar_init(smem_u32(&bar_pf[t]), 1);
     }
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
@@ -201,7 +214,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint32_t off = (uint32_t)(k / 4) * BLK16 + (uint32_t)(k % 4) * 2;
-          mma_ss_e(lead, tmem + t * 128, a0 + off, HI, b0 + off, HI, kIdS, k > 0);
+          mma_ss_e(lead, tmem + C::colS(t), a0 + off, HI, b0 + off, HI, kIdS, k > 0);
         }
         mma_commit_e(lead, smem_u32(&bar_s[t]));
       };
@@ -210,10 +223,49 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         const uint32_t b0 = rMN + (uint32_t)slot * KV16;
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts_e(lead, tmem + 256 + t * HD, tmem + t * 128 + p_col<NH>(k), b0 + 128 * k, HI, kIdPV,
+          mma_ts_e(lead, tmem + C::colO(t), tmem + C::colP(t) + p_col<NH>(k), b0 + 128 * k, HI, kIdPV,
                    (acc || k > 0) ? 1u : 0u);
       };
 
+      if constexpr (C::SEPP) {
+        // Ring index of K_j is 2j, of V_j 2j + 1.  Per step j:
+        //   [S_t(j) read] S_t(j+1);  [P_t(j) ready] O_t += P_t(j) V_j
+        if (ok) {
+          ok = warp_wait(smem_u32(&bar_full[0]), 0, p.ctl, abort, 21);
+          if (ok) {
+            tc_fence_after();
+            for (int t = 0; t < 2; ++t)
+              if (valid[t]) issue_s(t, 0);
+            mma_commit_e(lead, smem_u32(&bar_empty[0]));
+          }
+        }
+        for (int j = 0; j < nmax && ok; ++j) {
+          if (j + 1 < nmax) {
+            const int ik = 2 * (j + 1), ks = ik % C::STAGES;
+            if (!(ok = warp_wait(smem_u32(&bar_full[ks]), (ik / C::STAGES) & 1, p.ctl, abort, 24))) break;
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (!valid[t] || j + 1 >= nkv_t[t]) continue;
+              if (!(ok = warp_wait(smem_u32(&bar_sf[t]), j & 1, p.ctl, abort, 26))) break;
+              tc_fence_after();
+              issue_s(t, ks);
+            }
+            if (!ok) break;
+            mma_commit_e(lead, smem_u32(&bar_empty[ks]));
+          }
+          const int iv = 2 * j + 1, vs = iv % C::STAGES;
+          if (!(ok = warp_wait(smem_u32(&bar_full[vs]), (iv / C::STAGES) & 1, p.ctl, abort, 22))) break;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (!valid[t] || j >= nkv_t[t]) continue;
+            if (!(ok = warp_wait(smem_u32(&bar_p[t]), j & 1, p.ctl, abort, 23))) break;
+            tc_fence_after();
+            issue_pv(t, vs, j > 0);
+            mma_commit_e(lead, smem_u32(&bar_pf[t]));
+            if (j == nkv_t[t] - 1) mma_commit_e(lead, smem_u32(&bar_o[t]));
+          }
+          if (!ok) break;
+          mma_commit_e(lead, smem_u32(&bar_empty[vs]));
+        }
+      } else {
       int it = 0;
       if (ok) {
         ok = warp_wait(smem_u32(&bar_full[0]), 0, p.ctl, abort, 21);
@@ -262,6 +314,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           mma_commit_e(lead, smem_u32(&bar_empty[kslot]));
         }
       }
+      }
       // Drain: every MMA issued above completes before TMEM is released.
       mma_commit_e(lead, smem_u32(&bar_drain));
       mbar_wait_quiet(smem_u32(&bar_drain), 0, 200000000ull);
@@ -281,8 +334,8 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       const int qt = qt0 + t;
       const int row = qt * C::BM + r;
       const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
-      const uint32_t tS = tmem + lane_off + t * 128;
-      const uint32_t tO = tmem + lane_off + 256 + t * HD;
+      const uint32_t tS = tmem + lane_off + C::colS(t);
+      const uint32_t tO = tmem + lane_off + C::colO(t);
       const float scale2 = p.scale2;
       const bool tail = (p.N % C::BN) != 0;
       const uint32_t xbar = smem_u32(&bar_x[t][sp]);
@@ -306,6 +359,93 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       // combined once at the end.
       float m = -INFINITY, l = 0.f, lr = 0.f;
       bool ok = true;
+      if constexpr (C::SEPP) {
+        const uint32_t tP = tmem + lane_off + C::colP(t);
+        for (int j = 0; j < nkv_t[t]; ++j) {
+          if (!warp_wait(smem_u32(&bar_s[t]), j & 1, p.ctl, abort, 30)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          int lim = 128;
+          if (CAUSAL && j == qt) lim = r + 1;
+          if (!CAUSAL && tail && j == p.nkv - 1) lim = p.N - j * C::BN;
+          // The whole row of S into registers; S_t may then be overwritten.
+          float sv[128];
+#pragma unroll
+          for (int c = 0; c < 128; c += 32) tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(sv + c));
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_sf[t]));
+          if (lim < 128) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim) sv[c] = -INFINITY;
+          }
+          float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mc[e] = fmax3(mc[e], sv[c + 2 * e], sv[c + 2 * e + 1]);
+          }
+          const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+          const float m_new = fmaxf(m, mx * scale2);
+          const bool need = m_new > m + kTau;
+          // P_t and O_t: PV_t(j-1) must have completed
+          if (j > 0 && !warp_wait(smem_u32(&bar_pf[t]), (j - 1) & 1, p.ctl, abort, 33)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2(m - m_new) : 1.0f;
+            if (need) m = m_new;
+            l *= alpha;
+            lr *= alpha;
+            if (j > 0) {
+#pragma unroll 1
+              for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t ov[32];
+                tmem_ld32(tO + c0, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                tmem_st32(tO + c0, ov);
+              }
+            }
+          }
+          {
+            const float pmax = ex2(fmaf(mx, scale2, -m));
+            lr += __uint_as_float(pack_bf16(pmax, 0.f) << 16) - pmax;
+          }
+          const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-m, -m);
+          uint64_t l2 = f2_pack(0.f, 0.f);
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(sv[c0 + 2 * i], sv[c0 + 2 * i + 1]), sc2, nm2), x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              pk[i] = pack_bf16(p0, p1);
+              l2 = f2_add(l2, f2_pack(p0, p1));
+            }
+            tmem_st16(tP + c0 / 2, pk);
+          }
+          {
+            float a0, a1;
+            f2_unpack(l2, a0, a1);
+            l += a0 + a1;
+            lr += a0 + a1;
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_p[t]));
+        }
+      } else {
       for (int j = 0; j < nkv_t[t]; ++j) {
         if (!warp_wait(smem_u32(&bar_s[t]), j & 1, p.ctl, abort, 30)) {
           ok = false;
@@ -414,6 +554,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_p[t]));
+      }
       }
       // Epilogue: O / lr -> bf16, and LSE = ln 2 * (m + log2 l).
       if (ok && NH == 2) {
