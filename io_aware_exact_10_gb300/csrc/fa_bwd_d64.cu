@@ -70,8 +70,13 @@ struct Cfg64 {
   static constexpr int W_LOAD = NPW + 4, W_MMA = NPW + 5;  // drain: warps NPW ... NPW + 3
   static constexpr int THREADS = (NPW + 6) * 32;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_PT = 256, COL_DV = 320, COL_DK = 384,
-                            COL_DQ = 448;
+  // S^T (then P^T bf16 pairs) | dP^T (then dS^T pairs) | dV | dK | dQ | K | V
+  static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384,
+                            COL_KT = 448, COL_VT = 480;
+  // Column, relative to S^T (or dP^T), of the bf16 pairs of P^T (or dS^T) for
+  // MMA K-step k (16 queries): each P/dS warp packs its CW queries into the
+  // first CW/2 of its own, already read, columns.
+  static constexpr uint32_t pcol(int k) { return (uint32_t)((k / (CW / 16)) * CW + (k % (CW / 16)) * 8); }
 };
 static_assert(Cfg64::SMEM <= 232448, "shared memory budget");
 static_assert(Cfg64::QSLOTS >= 2 && Cfg64::QSLOTS <= 3 && Cfg64::DOSLOTS == 2, "ring sizes");
@@ -80,14 +85,15 @@ static_assert(Cfg64::NG == 2 || Cfg64::NG == 4, "32 or 64 query columns per P/dS
 // barrier indices
 enum : int {
   B_K = 0, B_V, B_QF0, B_QF1, B_QF2, B_QE0, B_QE1, B_QE2, B_DOF0, B_DOF1, B_DOE0, B_DOE1,
-  B_ST, B_P, B_DPT, B_DS, B_DQF, B_DQE, B_FIN, B_DRAIN, B_COUNT
+  B_ST, B_P, B_DPT, B_DS, B_DQF, B_DQE, B_FIN, B_DRAIN, B_KVT, B_COUNT
 };
 static_assert(B_COUNT <= Cfg64::NBAR, "barrier area");
 // arrival counts: TMA and tcgen05.commit barriers take one arrival; P and DS
-// one per P/dS warp; DQE one per drain warp.
+// one per P/dS warp; DQE and KVT one per drain warp.
 __device__ __constant__ const uint32_t kBarCount64[B_COUNT] = {
     1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1,           // K, V, QF*, QE*, DOF*, DOE*
-    1, Cfg64::NPW, 1, Cfg64::NPW, 1, 4, 1, 1};    // ST, P, DPT, DS, DQF, DQE, FIN, DRAIN
+    1, Cfg64::NPW, 1, Cfg64::NPW, 1, 4, 1, 1,     // ST, P, DPT, DS, DQF, DQE, FIN, DRAIN
+    4};                                           // KVT (K, V copied to tensor memory)
 
 struct BwdParams64 {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
@@ -195,32 +201,47 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       constexpr uint32_t kIdS = idesc_bf16(128, C::BQ, false, false);  // S^T, dP^T
       constexpr uint32_t kIdG = idesc_bf16(128, C::HD, false, true);   // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16(128, C::HD, true, true);    // dQ = dS K
-      const uint32_t tST = tmem + C::COL_ST, tDPT = tmem + C::COL_DPT, tPT = tmem + C::COL_PT,
-                     tDV = tmem + C::COL_DV, tDK = tmem + C::COL_DK, tDQ = tmem + C::COL_DQ;
+      const uint32_t tST = tmem + C::COL_ST, tDPT = tmem + C::COL_DPT, tDV = tmem + C::COL_DV,
+                     tDK = tmem + C::COL_DK, tDQ = tmem + C::COL_DQ, tKT = tmem + C::COL_KT,
+                     tVT = tmem + C::COL_VT;
       // Descriptor low halves of every operand tile (sdesc_lo): K-major
       // operands with lbo 16, M/N-major ones with lbo 16384 (the distance
       // between 64-element blocks); the high half is the same for all.
       constexpr uint32_t HI = sdesc_hi(1024);
       constexpr uint32_t TILE16 = C::TILE >> 4, DS16 = C::DS_BYTES >> 4;
-      const uint32_t kK = sdesc_lo(sK, 16), kMN = sdesc_lo(sK, 16384), vK = sdesc_lo(sV, 16);
+      const uint32_t kMN = sdesc_lo(sK, 16384);
       const uint32_t qK = sdesc_lo(sQ, 16), qMN = sdesc_lo(sQ, 16384);
       const uint32_t doK = sdesc_lo(sDO, 16), doMN = sdesc_lo(sDO, 16384);
-      const uint32_t dsK = sdesc_lo(sDS, 16), dsMN = sdesc_lo(sDS, 16384);
-      // S^T = K Q_v^T   (M = keys, N = queries, K = d; both K-major)
+      const uint32_t dsMN = sdesc_lo(sDS, 16384);
+      // S^T = K Q_v^T   (M = keys, N = queries, K = d; A = K in tensor memory)
       auto issue_st = [&](uint32_t qo) {
 #pragma unroll
         for (int k = 0; k < C::HD / 16; ++k)
-          mma_ss_e(lead, tST, kK + 2 * k, HI, qK + qo + 2 * k, HI, kIdS, k > 0);
+          mma_ts_e(lead, tST, tKT + 8 * k, qK + qo + 2 * k, HI, kIdS, k > 0);
         mma_commit_e(lead, bar(B_ST));
       };
-      // dP^T = V dO_v^T
+      // dP^T = V dO_v^T   (A = V in tensor memory)
       auto issue_dpt = [&](uint32_t dof) {
 #pragma unroll
         for (int k = 0; k < C::HD / 16; ++k)
-          mma_ss_e(lead, tDPT, vK + 2 * k, HI, doK + dof + 2 * k, HI, kIdS, k > 0);
+          mma_ts_e(lead, tDPT, tVT + 8 * k, doK + dof + 2 * k, HI, kIdS, k > 0);
         mma_commit_e(lead, bar(B_DPT));
       };
-      bool ok = warp_wait(bar(B_K), 0, p.ctl, abort, 60) && warp_wait(bar(B_QF0), 0, p.ctl, abort, 61);
+      // dQ_w = dS K   (A = dS buffer w&1 read query-major, B = K key-major),
+      // once the drain has taken dQ_{w-1} out of tensor memory; issued after
+      // dP^T(w+1), whose completion then covers dQ(w-1)
+      auto issue_dq = [&](int w) -> bool {
+        if (w > 0 && !warp_wait(bar(B_DQE), (w - 1) & 1, p.ctl, abort, 70)) return false;
+        tc_fence_after();
+        const uint32_t dsw = (uint32_t)(w & 1) * DS16;
+#pragma unroll
+        for (int k = 0; k < C::BK / 16; ++k)
+          mma_ss_e(lead, tDQ, dsMN + dsw + 128 * k, HI, kMN + 128 * k, HI, kIdQ, k > 0);
+        mma_commit_e(lead, bar(B_DQF));
+        return true;
+      };
+      bool ok = warp_wait(bar(B_K), 0, p.ctl, abort, 60) && warp_wait(bar(B_KVT), 0, p.ctl, abort, 59) &&
+                warp_wait(bar(B_QF0), 0, p.ctl, abort, 61);
       if (ok) {
         tc_fence_after();
         issue_st(0);
@@ -236,7 +257,6 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       for (int u = 0; u < nit && ok; ++u) {
         const uint32_t qo_v = (uint32_t)qs_v * TILE16;
         const uint32_t dof_u = (uint32_t)(u & 1) * TILE16, dof_v = (uint32_t)((u + 1) & 1) * TILE16;
-        const uint32_t dso = (uint32_t)(u & 1) * DS16;
         const uint32_t acc0 = u > 0 ? 1u : 0u;
         const bool more = u + 1 < nit;
         // dV += P^T dO_u   (A = P^T bf16 in TMEM, B = dO_u query-major)
@@ -244,36 +264,32 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
-          mma_ts_e(lead, tDV, tPT + k * 8, doMN + dof_u + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
+          mma_ts_e(lead, tDV, tST + C::pcol(k), doMN + dof_u + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
         mma_commit_e(lead, bar(B_DOE0 + (u & 1)));       // dO_u slot free
-        // S^T of the next tile: its completion also covers dV(u), so the
-        // P/dS warps may then overwrite the P^T columns
+        // S^T of the next tile overwrites the P^T pairs only after dV(u) has
+        // read them (tcgen05.mma runs in issue order)
         if (more) {
           if (!(ok = warp_wait(bar(B_QF0 + qs_v), qph_v, p.ctl, abort, 64))) break;
           tc_fence_after();
           issue_st(qo_v);
         }
-        // dS(u) is in shared memory and dP^T(u) has been read
+        // dS(u) is in shared memory, its transpose in the dP^T columns
         if (!(ok = warp_wait(bar(B_DS), u & 1, p.ctl, abort, 69))) break;
         tc_fence_after();
+        // dK += dS^T Q_u   (A = dS^T bf16 pairs in TMEM, B = Q_u query-major)
+#pragma unroll
+        for (int k = 0; k < C::BQ / 16; ++k)
+          mma_ts_e(lead, tDK, tDPT + C::pcol(k), qMN + qo_u + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
+        mma_commit_e(lead, bar(B_QE0 + (int)(qo_u / TILE16)));  // Q_u slot free
+        // dP^T of the next tile overwrites the dS^T pairs only after dK(u)
+        // has read them; its completion covers dK(u), dQ(u-1) and every
+        // earlier MMA
         if (more) {
           if (!(ok = warp_wait(bar(B_DOF0 + ((u + 1) & 1)), ((u + 1) >> 1) & 1, p.ctl, abort, 67))) break;
           tc_fence_after();
           issue_dpt(dof_v);
         }
-        // dK += dS^T Q_u   (A = dS key rows, K-major in shared memory; B = Q_u query-major)
-#pragma unroll
-        for (int k = 0; k < C::BQ / 16; ++k)
-          mma_ss_e(lead, tDK, dsK + dso + (k >> 2) * 1024 + (k & 3) * 2, HI, qMN + qo_u + 128 * k, HI, kIdG,
-                   k > 0 ? 1u : acc0);
-        mma_commit_e(lead, bar(B_QE0 + (int)(qo_u / TILE16)));  // Q_u slot free
-        // dQ_u = dS K   (A = the same dS buffer read query-major, B = K key-major)
-        if (u > 0 && !(ok = warp_wait(bar(B_DQE), (u - 1) & 1, p.ctl, abort, 70))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < C::BK / 16; ++k)
-          mma_ss_e(lead, tDQ, dsMN + dso + 128 * k, HI, kMN + 128 * k, HI, kIdQ, k > 0);
-        mma_commit_e(lead, bar(B_DQF));
+        if (!(ok = issue_dq(u))) break;
         qo_u = qo_v;
         if (++qs_v == C::QSLOTS) {
           qs_v = 0;
@@ -291,8 +307,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int cb = CW * g;                          // first query column of this thread
-    const uint32_t tST = tmem + lane_off + C::COL_ST + cb, tDPT = tmem + lane_off + C::COL_DPT + cb,
-                   tPT = tmem + lane_off + C::COL_PT + cb / 2;
+    const uint32_t tST = tmem + lane_off + C::COL_ST + cb, tDPT = tmem + lane_off + C::COL_DPT + cb;
     const uint64_t sc2 = f2_pack(p.scale2, p.scale2);
     const size_t rowbase = (size_t)bh * p.N;
     // statistics of the tile in Q slot s: 128 x -LSE log2 e, 128 x -D,
@@ -316,7 +331,9 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         qph_u ^= 1u;
       }
       // ---- P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query < key
-      // (S^T(u) done also means dV(u-1) has read the P^T columns)
+      // (S^T(u) was issued after dV(u-1): the P^T pairs of the last tile are
+      // consumed.  This thread's pairs go into the first CW/2 of its own
+      // S^T columns once it has read them.)
       if (!(ok = warp_wait(bar(B_ST), u & 1, p.ctl, abort, 81))) break;
       tc_fence_after();
       uint32_t pk[CW / 2];
@@ -339,13 +356,14 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         }
       }
 #pragma unroll
-      for (int c = 0; c < CW / 2; c += 16) tmem_st16(tPT + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
+      for (int c = 0; c < CW / 2; c += 16) tmem_st16(tST + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P));
       // ---- dS = P o (dP - D), with P the bf16 values dV multiplied
-      // (dP^T(u) done also means dK(u-2) and dQ(u-2) have read dS buffer u&1)
+      // (dP^T(u) was issued after dK(u-1) and dQ(u-2): the dS^T pairs of the
+      // last tile and dS buffer u&1 are consumed.)
       if (!(ok = warp_wait(bar(B_DPT), u & 1, p.ctl, abort, 83))) break;
       tc_fence_after();
       uint32_t dp[CW];
@@ -361,7 +379,10 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), nd2), pv), a, b);
         pk[i] = pack_bf16(a, b);
       }
-      // key row r of dS buffer u&1, 128-byte swizzled
+      // dS^T pairs for dK into the first CW/2 of this thread's dP^T columns
+#pragma unroll
+      for (int c = 0; c < CW / 2; c += 16) tmem_st16(tDPT + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
+      // key row r of dS buffer u&1, 128-byte swizzled (A operand of dQ)
       const uint32_t srow = sDS + (uint32_t)(u & 1) * C::DS_BYTES + ds_row;
 #pragma unroll
       for (int c = 0; c < CW / 8; ++c)
@@ -369,6 +390,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
                      "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                      : "memory");
       fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS));         // also: dP^T(u) has been read
@@ -405,29 +427,52 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const size_t rowbase = (size_t)bh * p.N;
     const uint32_t sw = (uint32_t)(lane & 7);
     const uint32_t stage = s0 + C::OFF_STAGE + (uint32_t)sp * 8192u;
-    bool ok = true;
-    for (int u = 0; u < nit; ++u) {
+    // First, K and V rows of this warp's key rows into tensor memory (the A
+    // operands of S^T and dP^T): 128 bytes of a 128-byte-swizzled row are 32
+    // words, element 2c in the low half of word c.
+    bool ok = warp_wait(bar(B_K), 0, p.ctl, abort, 92) && warp_wait(bar(B_V), 0, p.ctl, abort, 93);
+    if (ok) {
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint32_t src = (m == 0 ? sK : sV) + (uint32_t)r * 128u;
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]), "=r"(w[4 * c + 3])
+                       : "r"(src + (((uint32_t)c ^ sw) << 4))
+                       : "memory");
+        tmem_st32(tmem + lane_off + (m == 0 ? C::COL_KT : C::COL_VT), w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_KVT));
+    }
+    for (int u = 0; u < nit && ok; ++u) {
       if (!(ok = warp_wait(bar(B_DQF), u & 1, p.ctl, abort, 90))) break;
       tc_fence_after();
-      if (lane == 0) bulk_wait_group_read<0>();  // the previous boxes have left the staging area
+      uint32_t v[64];
+      tmem_ld32(tmem + lane_off + C::COL_DQ, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld32(tmem + lane_off + C::COL_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_DQE));                   // dQ's TMEM columns are free again
+        bulk_wait_group_read<0>();                 // the previous boxes have left the staging area
+      }
       __syncwarp();
       const int y = (i0 + u) * C::BQ + sp * 32;
       // columns [32 bb, 32 bb + 32) -> box bb
 #pragma unroll
       for (int bb = 0; bb < 2; ++bb) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + C::COL_DQ + 32 * bb, v);
-        tmem_wait_ld();
-        if (bb == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_DQE));  // dQ's TMEM columns are free again
-        }
         const uint32_t row = stage + (uint32_t)bb * 4096u + (uint32_t)lane * 128u;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((uint32_t)c ^ sw) << 4)),
-                       "r"(v[4 * c]), "r"(v[4 * c + 1]), "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
+                       "r"(v[32 * bb + 4 * c]), "r"(v[32 * bb + 4 * c + 1]), "r"(v[32 * bb + 4 * c + 2]),
+                       "r"(v[32 * bb + 4 * c + 3])
                        : "memory");
       }
       fence_proxy_async_smem();
