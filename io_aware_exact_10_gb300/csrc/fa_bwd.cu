@@ -375,11 +375,19 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t pk[16];
+        // statistics four at a time (one 16-byte broadcast load per two pairs)
+        uint64_t nlp[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(lse_u + c0 + 4 * i);
+          nlp[2 * i] = v.x;
+          nlp[2 * i + 1] = v.y;
+        }
         // two queries per paired FMA: scale2 * s - LSE2 (the shared copy holds -LSE2)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int q = c0 + 2 * i;
-          const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(lse_u + q);
+          const uint64_t nl2 = nlp[i];
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(pr[q], pr[q + 1]), sc2, nl2), x0, x1);
           float p0 = ex2(x0), p1 = ex2(x1);
@@ -408,11 +416,18 @@ __global__ void __launch_bounds__(448, 1)
         tmem_ld16(tST + cb + c0 / 2, pp);
         tmem_wait_ld();
         uint32_t pk[16];
+        uint64_t ndp[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(d_u + c0 + 4 * i);
+          ndp[2 * i] = v.x;
+          ndp[2 * i + 1] = v.y;
+        }
         // two queries per paired add and multiply: (dP - D) * P (the shared
         // copy holds -D)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(d_u + c0 + 2 * i);
+          const uint64_t nd2 = ndp[i];
           const uint32_t w = pp[i];
           const uint64_t pv = f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
           float a, b;

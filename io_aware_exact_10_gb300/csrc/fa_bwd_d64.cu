@@ -343,10 +343,18 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         for (int c = 0; c < CW; c += 32) tmem_ld32(tST + c, *reinterpret_cast<uint32_t(*)[32]>(pr + c));
         tmem_wait_ld();
         const bool diag = CAUSAL && qt == kt;
+        // statistics four at a time (one 16-byte broadcast load per two pairs)
+        uint64_t nlp[CW / 2];
+#pragma unroll
+        for (int i = 0; i < CW / 4; ++i) {
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(lse_u + 4 * i);
+          nlp[2 * i] = v.x;
+          nlp[2 * i + 1] = v.y;
+        }
 #pragma unroll
         for (int i = 0; i < CW / 2; ++i) {
           const int q = 2 * i;
-          const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(lse_u + q);
+          const uint64_t nl2 = nlp[i];
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(pr[q], pr[q + 1]), sc2, nl2), x0, x1);
           float p0 = ex2(x0), p1 = ex2(x1);
@@ -370,9 +378,16 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < CW; c += 32) tmem_ld32(tDPT + c, *reinterpret_cast<uint32_t(*)[32]>(dp + c));
       tmem_wait_ld();
+      uint64_t ndp[CW / 2];
+#pragma unroll
+      for (int i = 0; i < CW / 4; ++i) {
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(d_u + 4 * i);
+        ndp[2 * i] = v.x;
+        ndp[2 * i + 1] = v.y;
+      }
 #pragma unroll
       for (int i = 0; i < CW / 2; ++i) {
-        const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(d_u + 2 * i);
+        const uint64_t nd2 = ndp[i];
         const uint32_t w = pk[i];
         const uint64_t pv = f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
         float a, b;
