@@ -44,9 +44,9 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # over its three launches, from one ncu capture (profiles/
 # launches_gpt2_medium_fwd_bwd.md), and the commit of the kernels it measured.
 # The bench line reports it only while the kernel sources are unchanged.
-NCU_TRAFFIC_BYTES = 2148.0e6
-NCU_TRAFFIC_COMMIT = "6955ff5"
-NCU_TRAFFIC_SOURCES_SHA256 = None
+NCU_TRAFFIC_BYTES = 2145.5e6
+NCU_TRAFFIC_COMMIT = "10c1d3f"
+NCU_TRAFFIC_SOURCES_SHA256 = "2f3876eea2cc85023c7578b3f6d77e5af5e5fc3ee52ce93749ae6324b2869e0a"
 
 
 def kernel_sources_sha256() -> str:
