@@ -208,10 +208,34 @@ __global__ void __launch_bounds__(448, 1)
   float* lse_sh = reinterpret_cast<float*>(smem + C::OFF_LSE);
   float* d_sh = reinterpret_cast<float*>(smem + C::OFF_D);
 
-  if (threadIdx.x == 0) {
+  // The TMA thread initialises the barriers and issues the copies that need
+  // no wait (K, V, and Q and dO of the first two query tiles) before the
+  // CTA-wide sync, so their latency overlaps the rest of the set-up.
+  auto issue_qdo = [&](int u) {
+    const int st = u & 1, qt = i0 + u;
+    mbar_arrive_expect_tx(bar(B_QF0 + st), C::TILE);
+    for (int b = 0; b < C::KB; ++b)
+      tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, bh);
+    mbar_arrive_expect_tx(bar(B_DOF0 + st), C::TILE);
+    for (int b = 0; b < C::KB; ++b)
+      tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, bh);
+  };
+  const int pre = nit < 2 ? nit : 2;  // query tiles issued before the sync
+  if (warp == C::W_LOAD && lane == 0) {
     *abort = 0;
     for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), kBarCount[i]);
     fence_barrier_init();
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+    tma_prefetch_desc(&tdq);
+    mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
+    for (int b = 0; b < C::KB; ++b) {
+      tma_load_3d(sK + b * 16384, &tk, bar(B_KV), b * 64, kt * C::BK, bh);
+      tma_load_3d(sV + b * 16384, &tv, bar(B_KV), b * 64, kt * C::BK, bh);
+    }
+    for (int u = 0; u < pre; ++u) issue_qdo(u);
   }
   if (warp == C::W_MMA) {
     tmem_alloc(smem_u32(tmem_base_sh), C::TMEM_COLS);
@@ -225,18 +249,8 @@ __global__ void __launch_bounds__(448, 1)
   if (warp == C::W_LOAD) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      tma_prefetch_desc(&tdo);
-      tma_prefetch_desc(&tdq);
-      mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
-      for (int b = 0; b < C::KB; ++b) {
-        tma_load_3d(sK + b * 16384, &tk, bar(B_KV), b * 64, kt * C::BK, bh);
-        tma_load_3d(sV + b * 16384, &tv, bar(B_KV), b * 64, kt * C::BK, bh);
-      }
       bool ok = true;
-      int u = 0;
+      int u = pre;
       for (; u < nit && ok; ++u) {
         const int st = u & 1, use = u >> 1, qt = i0 + u;
         if (use > 0 && !mbar_wait(bar(B_QE0 + st), (use - 1) & 1, p.ctl, abort, 10)) { ok = false; break; }

@@ -137,10 +137,45 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
                  sDO = s0 + C::OFF_DO, sDS = s0 + C::OFF_DS;
 
-  if (threadIdx.x == 0) {
+  // The TMA thread initialises the barriers and issues the copies that need
+  // no wait (K, V, and Q with its statistics and dO of the first two query
+  // tiles) before the CTA-wide sync, so their latency overlaps the set-up.
+  int nq_issued = 0, ndo_issued = 0;
+  auto issue_q = [&](int u) {
+    const int qs = u % C::QSLOTS;
+    mbar_arrive_expect_tx(bar(B_QF0 + qs), C::TILE + C::STATS_SLOT);
+    tma_load_3d(sQ + qs * C::TILE, &tq, bar(B_QF0 + qs), 0, (i0 + u) * C::BQ, bh);
+    bulk_load(s0 + C::OFF_STATS + qs * C::STATS_SLOT, p.stats + ((size_t)bh * p.nq + i0 + u) * 256,
+              C::STATS_SLOT, bar(B_QF0 + qs));
+    ++nq_issued;
+  };
+  auto issue_do = [&](int u) {
+    const int ds = u % C::DOSLOTS;
+    mbar_arrive_expect_tx(bar(B_DOF0 + ds), C::TILE);
+    tma_load_3d(sDO + ds * C::TILE, &tdo, bar(B_DOF0 + ds), 0, (i0 + u) * C::BQ, bh);
+    ++ndo_issued;
+  };
+  const int pre = nit < C::DOSLOTS ? nit : C::DOSLOTS;   // tiles issued before the sync
+  if (warp == C::W_LOAD && lane == 0) {
     *abort = 0;
     for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), kBarCount64[i]);
     fence_barrier_init();
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+    tma_prefetch_desc(&tdq);
+    // K and Q_0 first: S^T of the first tile needs only those two
+    mbar_arrive_expect_tx(bar(B_K), C::TILE);
+    tma_load_3d(sK, &tk, bar(B_K), 0, kt * C::BK, bh);
+    for (int u = 0; u < pre; ++u) {
+      issue_q(u);
+      if (u == 0) {
+        mbar_arrive_expect_tx(bar(B_V), C::TILE);
+        tma_load_3d(sV, &tv, bar(B_V), 0, kt * C::BK, bh);
+      }
+      issue_do(u);
+    }
   }
   if (warp == C::W_MMA) {
     tmem_alloc(smem_u32(tmem_base_sh), C::TMEM_COLS);
@@ -154,34 +189,14 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   if (warp == C::W_LOAD) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      tma_prefetch_desc(&tdo);
-      tma_prefetch_desc(&tdq);
-      // K and Q_0 first: S^T of the first tile needs only those two
-      mbar_arrive_expect_tx(bar(B_K), C::TILE);
-      tma_load_3d(sK, &tk, bar(B_K), 0, kt * C::BK, bh);
       bool ok = true;
-      int nq_issued = 0, ndo_issued = 0;
-      for (int u = 0; u < nit; ++u) {
-        const int qt = i0 + u;
+      for (int u = pre; u < nit; ++u) {
         const int qs = u % C::QSLOTS, qn = u / C::QSLOTS;
         if (qn > 0 && !(ok = mbar_wait(bar(B_QE0 + qs), (qn - 1) & 1, p.ctl, abort, 50))) break;
-        mbar_arrive_expect_tx(bar(B_QF0 + qs), C::TILE + C::STATS_SLOT);
-        tma_load_3d(sQ + qs * C::TILE, &tq, bar(B_QF0 + qs), 0, qt * C::BQ, bh);
-        bulk_load(s0 + C::OFF_STATS + qs * C::STATS_SLOT, p.stats + ((size_t)bh * p.nq + qt) * 256,
-                  C::STATS_SLOT, bar(B_QF0 + qs));
-        ++nq_issued;
-        if (u == 0) {
-          mbar_arrive_expect_tx(bar(B_V), C::TILE);
-          tma_load_3d(sV, &tv, bar(B_V), 0, kt * C::BK, bh);
-        }
+        issue_q(u);
         const int ds = u % C::DOSLOTS, dn = u / C::DOSLOTS;
         if (dn > 0 && !(ok = mbar_wait(bar(B_DOE0 + ds), (dn - 1) & 1, p.ctl, abort, 51))) break;
-        mbar_arrive_expect_tx(bar(B_DOF0 + ds), C::TILE);
-        tma_load_3d(sDO + ds * C::TILE, &tdo, bar(B_DOF0 + ds), 0, qt * C::BQ, bh);
-        ++ndo_issued;
+        issue_do(u);
       }
       if (!ok) {
         // Abort: let every copy already issued land before the CTA exits.

@@ -129,7 +129,21 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sRing = sQ + 2 * C::QTILE;
 
-  if (threadIdx.x == 0) {
+  // The TMA thread initialises the barriers and issues the copies that need
+  // no wait (the Q tiles and the first ring slots) before the CTA-wide sync,
+  // so their latency overlaps the rest of the set-up.  Ring index it holds
+  // K_{it/2} (it even) or V_{it/2} (it odd).
+  auto issue_kv = [&](int it) {
+    const int slot = it % C::STAGES, j = it >> 1;
+    const uint32_t bar = smem_u32(&bar_full[slot]);
+    mbar_arrive_expect_tx(bar, C::KVTILE);
+    const uint32_t dst = sRing + slot * C::KVTILE;
+    for (int b = 0; b < C::KB; ++b)
+      tma_load_3d(dst + b * C::BN * 128, (it & 1) ? &tv : &tk, bar, b * 64, j * C::BN, bh);
+  };
+  const int n_it = 2 * nmax;                                 // ring uses: K_j, V_j for j < nmax
+  const int pre_it = n_it < C::STAGES ? n_it : C::STAGES;    // issued before the sync
+  if (warp == C::W_LOAD && lane == 0) {
     abort_sh = 0;
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bar_q[t]), 1);
@@ -146,6 +160,17 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     }
     mbar_init(smem_u32(&bar_drain), 1);
     fence_barrier_init();
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    for (int t = 0; t < 2; ++t) {
+      if (!valid[t]) continue;
+      const uint32_t bar = smem_u32(&bar_q[t]);
+      mbar_arrive_expect_tx(bar, C::QTILE);
+      for (int b = 0; b < C::KB; ++b)
+        tma_load_3d(sQ + t * C::QTILE + b * C::BM * 128, &tq, bar, b * 64, (qt0 + t) * C::BM, bh);
+    }
+    for (int it = 0; it < pre_it; ++it) issue_kv(it);
   }
   if (warp == C::W_MMA) {
     tmem_alloc(smem_u32(&tmem_base_sh), C::TMEM_COLS);
@@ -158,31 +183,15 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   if (warp == C::W_LOAD) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      for (int t = 0; t < 2; ++t) {
-        if (!valid[t]) continue;
-        const uint32_t bar = smem_u32(&bar_q[t]);
-        mbar_arrive_expect_tx(bar, C::QTILE);
-        for (int b = 0; b < C::KB; ++b)
-          tma_load_3d(sQ + t * C::QTILE + b * C::BM * 128, &tq, bar, b * 64, (qt0 + t) * C::BM, bh);
-      }
-      int it = 0;
+      int it = pre_it;
       bool ok = true;
-      for (int j = 0; j < nmax && ok; ++j) {
-        for (int w = 0; w < 2; ++w, ++it) {
-          const int slot = it % C::STAGES, use = it / C::STAGES;
-          if (use > 0 && !mbar_wait(smem_u32(&bar_empty[slot]), (use - 1) & 1, p.ctl, abort, 10)) {
-            ok = false;
-            break;
-          }
-          const uint32_t bar = smem_u32(&bar_full[slot]);
-          mbar_arrive_expect_tx(bar, C::KVTILE);
-          const uint32_t dst = sRing + slot * C::KVTILE;
-          for (int b = 0; b < C::KB; ++b)
-            tma_load_3d(dst + b * C::BN * 128, w ? &tv : &tk, bar, b * 64, j * C::BN, bh);
+      for (; it < n_it; ++it) {
+        const int slot = it % C::STAGES, use = it / C::STAGES;
+        if (use > 0 && !mbar_wait(smem_u32(&bar_empty[slot]), (use - 1) & 1, p.ctl, abort, 10)) {
+          ok = false;
+          break;
         }
+        issue_kv(it);
       }
       if (!ok) {
         // Abort: let the copies already issued land before the CTA exits.
