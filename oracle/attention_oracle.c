@@ -38,8 +38,18 @@
  *   dq_ic = scale * sum_j ds_ij k_jc
  *   dk_jc = scale * sum_i ds_ij q_ic
  *
- * Layout: every tensor is a dense fp64 array [BH][N][d] (d innermost); lse
- * and the per-row statistics are [BH][N].  BH = B*H independent heads.
+ * Grouped key/value heads (GQA; MQA when there is one key/value head): the
+ * pages note that FlashAttention 2 and 3 support multi-query and
+ * grouped-query attention (Flash Attention, "Evolution: Flash Attention 2 &
+ * 3") without defining the grouping.  Reading taken: with BH query heads and
+ * BH / G key/value heads, query head h attends with key/value head h / G
+ * (integer division; G consecutive query heads share one K, V).  By the
+ * chain rule through the shared K and V, dk and dv of key/value head hk sum
+ * the per-head terms above over its query heads hk*G ... hk*G + G - 1.
+ *
+ * Layout: every tensor is a dense fp64 array [heads][N][d] (d innermost);
+ * q, o, dO, dq have BH heads, k, v, dk, dv BH / G; lse and the per-row
+ * statistics are [BH][N].  BH = B*H independent query heads.
  * Parallelism: OpenMP over (head, row) for the row-wise passes and over
  * (head, key) for the key-wise pass.  No blocking, no online softmax, no
  * reordering beyond the loops of the definition.
@@ -91,17 +101,17 @@ static void row_stats(const double *q, const double *k, long i, int N, int d,
 }
 
 /*
- * Forward: o = softmax(scale Q K^T [masked]) V and lse, per head.
- * q, k, v, o: [BH][N][d]; lse: [BH][N].
+ * Forward: o = softmax(scale Q K^T [masked]) V and lse, per query head.
+ * q, o: [BH][N][d]; k, v: [BH/G][N][d]; lse: [BH][N].  G = group >= 1.
  */
 void oracle_attn_fwd(const double *q, const double *k, const double *v,
                      double *o, double *lse, int BH, int N, int d,
-                     double scale, int causal) {
+                     double scale, int causal, int group) {
     const long hs = (long)N * d;
 #pragma omp parallel for collapse(2) schedule(dynamic, 4)
     for (int h = 0; h < BH; ++h) {
         for (int i = 0; i < N; ++i) {
-            const double *qh = q + h * hs, *kh = k + h * hs, *vh = v + h * hs;
+            const double *qh = q + h * hs, *kh = k + (h / group) * hs, *vh = v + (h / group) * hs;
             double m, l;
             row_stats(qh, kh, i, N, d, scale, causal, &m, &l);
             double *oi = o + h * hs + (long)i * d;
@@ -118,15 +128,15 @@ void oracle_attn_fwd(const double *q, const double *k, const double *v,
 }
 
 /*
- * Backward: dq, dk, dv of L with dL/dO = dO, per head.
- * All tensor arguments [BH][N][d].  Forward quantities are recomputed here
- * from q, k, v (the oracle takes nothing produced by the GPU path).
- * D_out (may be NULL): [BH][N], receives D_i = sum_j p_ij dp_ij.
+ * Backward: dq, dk, dv of L with dL/dO = dO.
+ * q, dO, dq: [BH][N][d]; k, v, dk, dv: [BH/G][N][d].  Forward quantities are
+ * recomputed here from q, k, v (the oracle takes nothing produced by the GPU
+ * path).  D_out (may be NULL): [BH][N], receives D_i = sum_j p_ij dp_ij.
  */
 void oracle_attn_bwd(const double *q, const double *k, const double *v,
                      const double *dO, double *dq, double *dk, double *dv,
                      double *D_out, int BH, int N, int d, double scale,
-                     int causal) {
+                     int causal, int group) {
     const long hs = (long)N * d;
     double *m = (double *)malloc(sizeof(double) * (size_t)BH * N);
     double *l = (double *)malloc(sizeof(double) * (size_t)BH * N);
@@ -136,7 +146,7 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
 #pragma omp parallel for collapse(2) schedule(dynamic, 4)
     for (int h = 0; h < BH; ++h) {
         for (int i = 0; i < N; ++i) {
-            const double *qh = q + h * hs, *kh = k + h * hs, *vh = v + h * hs;
+            const double *qh = q + h * hs, *kh = k + (h / group) * hs, *vh = v + (h / group) * hs;
             const double *dOi = dO + h * hs + (long)i * d;
             const long r = (long)h * N + i;
             row_stats(qh, kh, i, N, d, scale, causal, &m[r], &l[r]);
@@ -164,25 +174,31 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
         }
     }
 
-    /* Pass over keys: dv_j = sum_i p_ij dO_i, dk_j = scale * sum_i ds_ij q_i. */
+    /* Pass over keys of each key/value head hk:
+     * dv_j = sum over its query heads h and rows i of p_ij dO_i,
+     * dk_j = scale * sum over the same of ds_ij q_i. */
+    const int BHkv = BH / group;
 #pragma omp parallel for collapse(2) schedule(dynamic, 4)
-    for (int h = 0; h < BH; ++h) {
+    for (int hk = 0; hk < BHkv; ++hk) {
         for (int j = 0; j < N; ++j) {
-            const double *qh = q + h * hs, *kh = k + h * hs, *vh = v + h * hs;
-            const double *dOh = dO + h * hs;
-            double *dvj = dv + h * hs + (long)j * d;
-            double *dkj = dk + h * hs + (long)j * d;
+            const double *kh = k + hk * hs, *vh = v + hk * hs;
+            double *dvj = dv + hk * hs + (long)j * d;
+            double *dkj = dk + hk * hs + (long)j * d;
             for (int c = 0; c < d; ++c) { dvj[c] = 0.0; dkj[c] = 0.0; }
-            for (long i = 0; i < N; ++i) {
-                if (!visible(causal, i, j)) continue;
-                const long r = (long)h * N + i;
-                double p = exp(score(qh + i * d, kh + (long)j * d, d, scale) - m[r]) / l[r];
-                double dp = 0.0;
-                for (int c = 0; c < d; ++c) dp += dOh[i * d + c] * vh[(long)j * d + c];
-                double ds = p * (dp - D[r]);
-                for (int c = 0; c < d; ++c) {
-                    dvj[c] += p * dOh[i * d + c];
-                    dkj[c] += scale * ds * qh[i * d + c];
+            for (int g = 0; g < group; ++g) {
+                const int h = hk * group + g;
+                const double *qh = q + h * hs, *dOh = dO + h * hs;
+                for (long i = 0; i < N; ++i) {
+                    if (!visible(causal, i, j)) continue;
+                    const long r = (long)h * N + i;
+                    double p = exp(score(qh + i * d, kh + (long)j * d, d, scale) - m[r]) / l[r];
+                    double dp = 0.0;
+                    for (int c = 0; c < d; ++c) dp += dOh[i * d + c] * vh[(long)j * d + c];
+                    double ds = p * (dp - D[r]);
+                    for (int c = 0; c < d; ++c) {
+                        dvj[c] += p * dOh[i * d + c];
+                        dkj[c] += scale * ds * qh[i * d + c];
+                    }
                 }
             }
         }

@@ -52,6 +52,13 @@ def _heads(a: np.ndarray):
     return a.reshape(-1, N, d), N, d
 
 
+def _group(BH: int, BHk: int, BHv: int) -> int:
+    """Query heads per key/value head (1 for standard multi-head)."""
+    if BHk != BHv or BHk < 1 or BH % BHk != 0:
+        raise ValueError(f"k, v heads ({BHk}, {BHv}) must be equal and divide q heads ({BH})")
+    return BH // BHk
+
+
 class OracleLib:
     """The oracle's entry points, bound to one compiled shared object."""
 
@@ -60,10 +67,10 @@ class OracleLib:
         dp = ctypes.POINTER(ctypes.c_double)
         ip = ctypes.POINTER(ctypes.c_int)
         ci, cd = ctypes.c_int, ctypes.c_double
-        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, cd, ci]
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, cd, ci, ci]
         lib.oracle_attn_fwd.restype = None
         lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
-                                        ci, ci, ci, cd, ci]
+                                        ci, ci, ci, cd, ci, ci]
         lib.oracle_attn_bwd.restype = None
         lib.oracle_attn_fwd_rows.argtypes = [dp, dp, dp, ip, ci, dp, dp,
                                              ci, ci, cd, ci]
@@ -78,7 +85,10 @@ class OracleLib:
     def attn_fwd(self, q, k, v, scale: float, causal: bool):
         """o = softmax(scale * q k^T [causal]) v and lse (natural log), fp64.
 
-        q, k, v: [..., N, d].  Returns (o shaped like q, lse shaped [..., N]).
+        q: [..., N, d]; k, v: [..., N, d] with the same or a dividing number
+        of heads (grouped key/value heads: query head h uses key/value head
+        h // G over the flattened head axis).  Returns (o shaped like q, lse
+        shaped [..., N] like q's heads).
         """
         q, k, v = _f64(q), _f64(k), _f64(v)
         lead = q.shape[:-2]
@@ -86,11 +96,12 @@ class OracleLib:
         kh, _, _ = _heads(k)
         vh, _, _ = _heads(v)
         BH = qh.shape[0]
+        group = _group(BH, kh.shape[0], vh.shape[0])
         o = np.empty_like(qh)
         lse = np.empty((BH, N), dtype=np.float64)
         self._lib.oracle_attn_fwd(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(o),
                                   _ptr(lse), BH, N, d, float(scale),
-                                  int(bool(causal)))
+                                  int(bool(causal)), group)
         return o.reshape(*lead, N, d), lse.reshape(*lead, N)
 
     def attn_bwd(self, q, k, v, dO, scale: float, causal: bool,
@@ -98,23 +109,27 @@ class OracleLib:
         """Gradients (dq, dk, dv) of L with dL/dO = dO, fp64.
 
         With ``return_D`` also returns D = rowsum(P * dP) shaped [..., N].
+        k, v may have fewer heads than q (see attn_fwd); dk, dv are shaped
+        like k and sum over each key/value head's query heads.
         """
         q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
         lead = q.shape[:-2]
+        lead_kv = k.shape[:-2]
         qh, N, d = _heads(q)
         kh, _, _ = _heads(k)
         vh, _, _ = _heads(v)
         dOh, _, _ = _heads(dO)
         BH = qh.shape[0]
+        group = _group(BH, kh.shape[0], vh.shape[0])
         dq = np.empty_like(qh)
-        dk = np.empty_like(qh)
-        dv = np.empty_like(qh)
+        dk = np.empty_like(kh)
+        dv = np.empty_like(kh)
         D = np.empty((BH, N), dtype=np.float64)
         self._lib.oracle_attn_bwd(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(dOh),
                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(D),
-                                  BH, N, d, float(scale), int(bool(causal)))
-        out = (dq.reshape(*lead, N, d), dk.reshape(*lead, N, d),
-               dv.reshape(*lead, N, d))
+                                  BH, N, d, float(scale), int(bool(causal)), group)
+        out = (dq.reshape(*lead, N, d), dk.reshape(*lead_kv, N, d),
+               dv.reshape(*lead_kv, N, d))
         if return_D:
             return out + (D.reshape(*lead, N),)
         return out

@@ -319,9 +319,66 @@ def check_torch_autograd(orc):
         assert np.allclose(dv, tv.grad.numpy(), atol=1e-11, rtol=0)
 
 
+# ----------------------------------------------------------------------------
+# grouped key/value heads (GQA / MQA)
+# ----------------------------------------------------------------------------
+
+def check_gqa_torch(orc):
+    """Grouped key/value heads against torch in fp64: K, V repeated over each
+    group with repeat_interleave (query head h takes key/value head h // G),
+    scaled_dot_product_attention forward, and autograd back through the
+    repeat, which sums dk, dv over each group.  Covers MQA (one key/value
+    head) and a batch of two."""
+    import torch
+    import torch.nn.functional as F
+    r = _rng(14)
+    for causal in (False, True):
+        for B, H, Hkv in ((2, 4, 2), (1, 6, 1), (1, 3, 3)):
+            N, d, G = 23, 8, H // Hkv
+            q, dO = (r.normal(size=(B, H, N, d)) for _ in range(2))
+            k, v = (r.normal(size=(B, Hkv, N, d)) for _ in range(2))
+            tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (q, k, v))
+            out = F.scaled_dot_product_attention(
+                tq, torch.repeat_interleave(tk, G, dim=1), torch.repeat_interleave(tv, G, dim=1),
+                is_causal=causal, scale=0.4)
+            out.backward(torch.from_numpy(dO))
+            o, _ = orc.attn_fwd(q, k, v, 0.4, causal)
+            dq, dk, dv = orc.attn_bwd(q, k, v, dO, 0.4, causal)
+            assert dk.shape == k.shape and dv.shape == v.shape
+            assert np.allclose(o, out.detach().numpy(), atol=1e-12, rtol=0)
+            assert np.allclose(dq, tq.grad.numpy(), atol=1e-11, rtol=0)
+            assert np.allclose(dk, tk.grad.numpy(), atol=1e-11, rtol=0)
+            assert np.allclose(dv, tv.grad.numpy(), atol=1e-11, rtol=0)
+
+
+def check_gqa_finite_differences(orc):
+    """Central differences of L = sum(dO * O) w.r.t. every entry of the shared
+    K and V (two query heads per key/value head) agree with dk, dv."""
+    r = _rng(15)
+    h = 1e-6
+    for causal in (False, True):
+        N, d = 5, 2
+        q, dO = (r.normal(size=(1, 2, N, d)) for _ in range(2))
+        k, v = (r.normal(size=(1, 1, N, d)) for _ in range(2))
+        _, dk, dv = orc.attn_bwd(q, k, v, dO, 0.8, causal)
+        for which, (x, g) in enumerate(((k, dk), (v, dv))):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                kp, vp = (xp, v) if which == 0 else (k, xp)
+                km, vm = (xm, v) if which == 0 else (k, xm)
+                num[idx] = (_loss(orc, q, kp, vp, dO, 0.8, causal)
+                            - _loss(orc, q, km, vm, dO, 0.8, causal)) / (2 * h)
+            err = np.abs(num - g).max()
+            assert err / max(np.abs(num).max(), 1e-3) < 1e-6, (causal, which, err)
+
+
 FWD_CHECKS = (check_four_scores, check_rows_sum_to_one, check_softmax_of_scores,
               check_identical_keys, check_causal_row0, check_zero_queries,
               check_dominant_key, check_blocked_online_softmax,
               check_multi_head_independent, check_rows_entry, check_torch_sdpa_fwd)
 BWD_CHECKS = (check_finite_differences, check_gradient_invariants, check_torch_autograd)
-ALL_CHECKS = FWD_CHECKS + BWD_CHECKS
+GQA_CHECKS = (check_gqa_torch, check_gqa_finite_differences)
+ALL_CHECKS = FWD_CHECKS + BWD_CHECKS + GQA_CHECKS

@@ -34,6 +34,12 @@ MUTANTS = {
         "dp += dOh[i * d + c] * vh[(long)j * d + c];",
         "dp += dOh[(long)j * d + c] * vh[i * d + c];"),
     "key_pass_D_dropped": ("double ds = p * (dp - D[r]);", "double ds = p * dp;"),
+    # grouped key/value heads
+    "gqa_kv_head_modulo": ("*kh = k + (h / group) * hs, *vh = v + (h / group) * hs;",
+                           "*kh = k + (h % group) * hs, *vh = v + (h % group) * hs;"),
+    "gqa_group_sum_first_head_only": ("for (int g = 0; g < group; ++g) {",
+                                      "for (int g = 0; g < 1; ++g) {"),
+    "gqa_interleaved_grouping": ("const int h = hk * group + g;", "const int h = g * BHkv + hk;"),
 }
 
 
