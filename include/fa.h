@@ -72,6 +72,19 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int N, int d, float scale, int causal, struct CUstream_st* stream);
 
 /*
+ * Grouped key/value heads (GQA; MQA when H_kv = 1).  Same as fa_fwd, except
+ * that k and v have H_kv heads: bf16 [B][H_kv][N][d], H_kv >= 1 dividing H.
+ * Query head h attends with key/value head h / (H / H_kv) (consecutive query
+ * heads share one K, V).  fa_fwd is this with H_kv = H.  H_kv outside
+ * 1 ... H or not dividing H => FA_ERR_INVALID_ARG.  Source: Flash Attention,
+ * "Evolution: Flash Attention 2 & 3" (multi-query and grouped-query support;
+ * the grouping itself is the library's reading).
+ */
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int H_kv, int N, int d, float scale, int causal,
+                     struct CUstream_st* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: fp32 row statistics, two per row
  * (-lse log2 e and -D with D = rowsum(dO * o)) with each head padded to whole
  * 128-row tiles, i.e. B*H*ceil(N/128)*256 floats, followed by an fp32 dQ
@@ -98,6 +111,18 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                  float scale, int causal, void* workspace, size_t workspace_bytes,
                  struct CUstream_st* stream);
+
+/*
+ * Backward for grouped key/value heads: the counterpart of fa_fwd_gqa.  k, v,
+ * dk, dv are bf16 [B][H_kv][N][d]; dk and dv of a key/value head are the sums
+ * of the gradients through it of its H / H_kv query heads (chain rule through
+ * the shared K, V).  The workspace is fa_bwd_workspace_size(B, H, N, d)
+ * (query heads).  fa_bwd is this with H_kv = H.
+ */
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk, void* dv, int B, int H,
+                     int H_kv, int N, int d, float scale, int causal, void* workspace,
+                     size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
  * Backward with no workspace argument and no allocation.  The paper has no

@@ -44,10 +44,15 @@ def lib() -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd.restype = i
+        L.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_fwd_gqa.restype = i
         L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_size.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
         L.fa_bwd.restype = i
+        L.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz,
+                                 vp]
+        L.fa_bwd_gqa.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd_noalloc.restype = i
         L.fa_last_device_error.argtypes = [vp]
@@ -104,6 +109,17 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream=None, check=True) 
     return s
 
 
+def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, stream=None,
+               check=True) -> int:
+    """fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, stream) -> status:
+    k, v have H_kv heads; query head h uses key/value head h // (H // H_kv)."""
+    s = lib().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                         int(H_kv), int(N), int(d), float(scale), int(causal), _stream(stream))
+    if check:
+        _check(s, "fa_fwd_gqa")
+    return s
+
+
 def fa_bwd_workspace_size(B, H, N, d) -> int:
     return int(lib().fa_bwd_workspace_size(int(B), int(H), int(N), int(d)))
 
@@ -117,6 +133,20 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace
                      int(causal), _ptr(workspace), int(workspace_bytes), _stream(stream))
     if check:
         _check(s, "fa_bwd")
+    return s
+
+
+def fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N, d, scale, causal, workspace,
+               workspace_bytes, stream=None, check=True) -> int:
+    """fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N, d, scale, causal,
+    workspace, workspace_bytes, stream) -> status: dk, dv (H_kv heads) sum
+    over each key/value head's query heads."""
+    s = lib().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                         _ptr(dk), _ptr(dv), int(B), int(H), int(H_kv), int(N), int(d),
+                         float(scale), int(causal), _ptr(workspace), int(workspace_bytes),
+                         _stream(stream))
+    if check:
+        _check(s, "fa_bwd_gqa")
     return s
 
 

@@ -141,22 +141,31 @@ extern "C" {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, struct CUstream_st* stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, scale, causal, stream);
+}
+
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int H_kv, int N, int d, float scale, int causal,
+                     struct CUstream_st* stream) {
   bool empty = false;
   fa_status s = check_common(B, H, N, d, scale, causal, &empty);
-  if (s != FA_OK || empty) return s;
+  if (s != FA_OK) return s;
+  if (!empty && (H_kv < 1 || H_kv > H || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
+  if (empty) return s;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
   DeviceState* dev = nullptr;
   if ((s = current_device(&dev)) != FA_OK) return s;
   if (!get_encoder()) return FA_ERR_LAUNCH;
   fa::FwdLaunch a;
-  const int BH = B * H;
-  if (!encode_bf16_3d(&a.tq, q, BH, N, d) || !encode_bf16_3d(&a.tk, k, BH, N, d) ||
-      !encode_bf16_3d(&a.tv, v, BH, N, d))
+  const int BH = B * H, BHkv = B * H_kv;
+  if (!encode_bf16_3d(&a.tq, q, BH, N, d) || !encode_bf16_3d(&a.tk, k, BHkv, N, d) ||
+      !encode_bf16_3d(&a.tv, v, BHkv, N, d))
     return FA_ERR_INVALID_ARG;
   a.o = o;
   a.lse = lse;
   a.BH = BH;
+  a.group = H / H_kv;
   a.N = N;
   a.d = d;
   a.scale = scale;
@@ -182,9 +191,19 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                  float scale, int causal, void* workspace, size_t workspace_bytes,
                  struct CUstream_st* stream) {
+  return fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, scale, causal, workspace,
+                    workspace_bytes, stream);
+}
+
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk, void* dv, int B, int H,
+                     int H_kv, int N, int d, float scale, int causal, void* workspace,
+                     size_t workspace_bytes, struct CUstream_st* stream) {
   bool empty = false;
   fa_status s = check_common(B, H, N, d, scale, causal, &empty);
-  if (s != FA_OK || empty) return s;
+  if (s != FA_OK) return s;
+  if (!empty && (H_kv < 1 || H_kv > H || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
+  if (empty) return s;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
@@ -195,9 +214,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if ((s = current_device(&dev)) != FA_OK) return s;
   if (!get_encoder()) return FA_ERR_LAUNCH;
   fa::BwdLaunch a;
-  const int BH = B * H;
-  if (!encode_bf16_3d(&a.tq, q, BH, N, d) || !encode_bf16_3d(&a.tk, k, BH, N, d) ||
-      !encode_bf16_3d(&a.tv, v, BH, N, d) || !encode_bf16_3d(&a.tdo, dO, BH, N, d))
+  const int BH = B * H, BHkv = B * H_kv;
+  if (!encode_bf16_3d(&a.tq, q, BH, N, d) || !encode_bf16_3d(&a.tk, k, BHkv, N, d) ||
+      !encode_bf16_3d(&a.tv, v, BHkv, N, d) || !encode_bf16_3d(&a.tdo, dO, BH, N, d))
     return FA_ERR_INVALID_ARG;
   a.o = o;
   a.dO = dO;
@@ -210,6 +229,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.dk = dk;
   a.dv = dv;
   a.BH = BH;
+  a.group = H / H_kv;
   a.N = N;
   a.d = d;
   a.scale = scale;

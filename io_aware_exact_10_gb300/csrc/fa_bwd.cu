@@ -156,7 +156,8 @@ struct BwdParams {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int N, nq, nkv, BH, group;
+  int N, nq, nkv, BHkv, group;
+  int kv_group;  // query heads per key/value head (1: multi-head)
   float scale, scale2;
   KernelCtl ctl;
 };
@@ -196,11 +197,16 @@ __global__ void __launch_bounds__(448, 1)
   // group's heads run together, share their Q, dO in L2 and add into the same
   // dQ rows (which then stay in L2).  Key tile 0 (the most work when causal)
   // of every head in the group comes first.
-  const GridPos gp = decode_grid((int)blockIdx.x, p.BH, p.nkv, p.group);
-  const int bh = gp.bh;
+  // One CTA per (key/value head, key tile).  It loops over the query tiles
+  // i0 ... nq-1 of each of the kv_group query heads that share the key/value
+  // head, in that order; each role follows the (tile, head) pair of its own
+  // position in the loop with a TileWalk.
+  const GridPos gp = decode_grid((int)blockIdx.x, p.BHkv, p.nkv, p.group);
+  const int bk = gp.bh;
   const int kt = gp.rank;
   const int i0 = CAUSAL ? kt : 0;                  // first query tile that sees this key tile
-  const int nit = p.nq - i0;                       // query tiles to process
+  const int nit = (p.nq - i0) * p.kv_group;        // query tiles to process
+  const TileWalk walk0{i0, bk * p.kv_group};
 
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
@@ -211,14 +217,16 @@ __global__ void __launch_bounds__(448, 1)
   // The TMA thread initialises the barriers and issues the copies that need
   // no wait (K, V, and Q and dO of the first two query tiles) before the
   // CTA-wide sync, so their latency overlaps the rest of the set-up.
-  auto issue_qdo = [&](int u) {
-    const int st = u & 1, qt = i0 + u;
+  TileWalk lw = walk0;  // the TMA thread's position
+  auto issue_qdo = [&](int u) {  // moves to the next tile
+    const int st = u & 1, qt = lw.qt, zq = lw.qh;
+    lw.next(i0, p.nq);
     mbar_arrive_expect_tx(bar(B_QF0 + st), C::TILE);
     for (int b = 0; b < C::KB; ++b)
-      tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, bh);
+      tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, zq);
     mbar_arrive_expect_tx(bar(B_DOF0 + st), C::TILE);
     for (int b = 0; b < C::KB; ++b)
-      tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, bh);
+      tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, zq);
   };
   const int pre = nit < 2 ? nit : 2;  // query tiles issued before the sync
   if (warp == C::W_LOAD && lane == 0) {
@@ -232,8 +240,8 @@ __global__ void __launch_bounds__(448, 1)
     tma_prefetch_desc(&tdq);
     mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
     for (int b = 0; b < C::KB; ++b) {
-      tma_load_3d(sK + b * 16384, &tk, bar(B_KV), b * 64, kt * C::BK, bh);
-      tma_load_3d(sV + b * 16384, &tv, bar(B_KV), b * 64, kt * C::BK, bh);
+      tma_load_3d(sK + b * 16384, &tk, bar(B_KV), b * 64, kt * C::BK, bk);
+      tma_load_3d(sV + b * 16384, &tv, bar(B_KV), b * 64, kt * C::BK, bk);
     }
     for (int u = 0; u < pre; ++u) issue_qdo(u);
   }
@@ -252,11 +260,11 @@ __global__ void __launch_bounds__(448, 1)
       bool ok = true;
       int u = pre;
       for (; u < nit && ok; ++u) {
-        const int st = u & 1, use = u >> 1, qt = i0 + u;
+        const int st = u & 1, use = u >> 1, qt = lw.qt, zq = lw.qh;
         if (use > 0 && !mbar_wait(bar(B_QE0 + st), (use - 1) & 1, p.ctl, abort, 10)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(B_QF0 + st), C::TILE);
         for (int b = 0; b < C::KB; ++b)
-          tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, bh);
+          tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, zq);
         if (use > 0 && !mbar_wait(bar(B_DOE0 + st), (use - 1) & 1, p.ctl, abort, 11)) {
           ok = false;
           // the Q load above is in flight; wait for it below
@@ -265,7 +273,8 @@ __global__ void __launch_bounds__(448, 1)
         }
         mbar_arrive_expect_tx(bar(B_DOF0 + st), C::TILE);
         for (int b = 0; b < C::KB; ++b)
-          tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, bh);
+          tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, zq);
+        lw.next(i0, p.nq);
       }
       if (!ok) {
         // Abort: let every copy already issued land before the CTA exits.
@@ -351,11 +360,11 @@ __global__ void __launch_bounds__(448, 1)
     const int cb = 64 * h;                          // first query column of this thread
     const float scale2 = p.scale2;
     const uint64_t sc2 = f2_pack(scale2, scale2);
-    const size_t rowbase = (size_t)bh * p.N;
+    const size_t rowbase = (size_t)bk * p.N;         // key rows (dK, dV)
     // warpgroup 0 stages the negated log2-scaled LSE and negated D of the
     // first query tile
     if (h == 0) {
-      const float* st = p.stats + ((size_t)bh * p.nq + i0) * 256;
+      const float* st = p.stats + ((size_t)walk0.qh * p.nq + walk0.qt) * 256;
       lse_sh[r] = st[r];
       d_sh[r] = st[128 + r];
     }
@@ -363,8 +372,10 @@ __global__ void __launch_bounds__(448, 1)
     // that the wait stays bounded if another warp gives up.
     mbar_arrive(bar(B_WG));
     bool ok = warp_wait_b(bar(B_WG), 0, p.ctl, abort, 34);
+    TileWalk w = walk0;
     for (int u = 0; u < nit && ok; ++u) {
-      const int qt = i0 + u;
+      const int qt = w.qt;
+      w.next(i0, p.nq);  // w now names tile u + 1
       const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
       const float* d_u = d_sh + (u & 1) * C::BQ + cb;
       // next tile's statistics, copied asynchronously so that no warp
@@ -373,7 +384,7 @@ __global__ void __launch_bounds__(448, 1)
       float* d_n = d_sh + ((u + 1) & 1) * C::BQ + r;
       const bool fetch = h == 0 && u + 1 < nit;
       if (fetch) {
-        const float* st = p.stats + ((size_t)bh * p.nq + qt + 1) * 256;
+        const float* st = p.stats + ((size_t)w.qh * p.nq + w.qt) * 256;
         cp_async_4(smem_u32(lse_n), st + r, 4u);
         cp_async_4(smem_u32(d_n), st + 128 + r, 4u);
         cp_async_commit();
@@ -500,17 +511,18 @@ __global__ void __launch_bounds__(448, 1)
     const int sp = warp & 3;
     const int r = sp * 32 + lane;  // query row within the tile (dQ) / key row (dK)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
-    const size_t rowbase = (size_t)bh * p.N;
+    const size_t rowbase = (size_t)bk * p.N;         // key rows (dK, dV)
     const uint32_t sw = (uint32_t)(lane & 7);
     constexpr int BOXES_PER_SLOT = HD / 64;          // 4 KB boxes in a warp's quarter
     bool ok = true;
-    for (int u = 0; u < nit; ++u) {
+    TileWalk w = walk0;
+    for (int u = 0; u < nit; ++u, w.next(i0, p.nq)) {
       if (!(ok = warp_wait_b(bar(B_DQF), u & 1, p.ctl, abort, 40))) break;
       tc_fence_after();
       const int st = u & 1;
       const uint32_t quarter = (uint32_t)sp * (uint32_t)(C::TILE / 4);
       const uint32_t stage_do = sDO + st * C::TILE + quarter, stage_q = sQ + st * C::TILE + quarter;
-      const int y = (i0 + u) * C::BQ + sp * 32;
+      const int y = w.qt * C::BQ + sp * 32, zq = w.qh;
 #pragma unroll
       for (int hh = 0; hh < HD / 64; ++hh) {
         uint32_t v[64];
@@ -544,7 +556,7 @@ __global__ void __launch_bounds__(448, 1)
             const int box = 2 * hh + bb;
             const uint32_t base = (box < BOXES_PER_SLOT ? stage_do : stage_q) +
                                   (uint32_t)(box % BOXES_PER_SLOT) * 4096u;
-            tma_reduce_add_3d(&tdq, base, box * 32, y, bh);
+            tma_reduce_add_3d(&tdq, base, box * 32, y, zq);
           }
           bulk_commit_group();
         }
@@ -605,12 +617,13 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   p.N = a.N;
   p.nq = (a.N + C::BQ - 1) / C::BQ;
   p.nkv = (a.N + C::BK - 1) / C::BK;
-  p.BH = a.BH;
-  p.group = head_group(a.BH, p.nkv, a.num_sms);
+  p.BHkv = a.BH / a.group;
+  p.kv_group = a.group;
+  p.group = head_group(p.BHkv, p.nkv, a.num_sms);
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
-  dim3 grid((unsigned)((long)p.nkv * a.BH));
+  dim3 grid((unsigned)((long)p.nkv * p.BHkv));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();
 }

@@ -99,7 +99,8 @@ struct BwdParams64 {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int N, nq, nkv, BH, group;
+  int N, nq, nkv, BHkv, group;
+  int kv_group;  // query heads per key/value head (1: multi-head)
   float scale, scale2;
   KernelCtl ctl;
 };
@@ -127,11 +128,16 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const GridPos gp = decode_grid((int)blockIdx.x, p.BH, p.nkv, p.group);
-  const int bh = gp.bh;
+  // One CTA per (key/value head, key tile).  It loops over the query tiles
+  // i0 ... nq-1 of each of the kv_group query heads that share the key/value
+  // head, in that order; each role follows the (tile, head) pair of its own
+  // position in the loop with a TileWalk.
+  const GridPos gp = decode_grid((int)blockIdx.x, p.BHkv, p.nkv, p.group);
+  const int bk = gp.bh;
   const int kt = gp.rank;
   const int i0 = CAUSAL ? kt : 0;                  // first query tile that sees this key tile
-  const int nit = p.nq - i0;                       // query tiles to process
+  const int nit = (p.nq - i0) * p.kv_group;        // query tiles to process
+  const TileWalk walk0{i0, bk * p.kv_group};
 
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
@@ -141,19 +147,21 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   // no wait (K, V, and Q with its statistics and dO of the first two query
   // tiles) before the CTA-wide sync, so their latency overlaps the set-up.
   int nq_issued = 0, ndo_issued = 0;
+  TileWalk lw = walk0;  // the TMA thread's position
   auto issue_q = [&](int u) {
     const int qs = u % C::QSLOTS;
     mbar_arrive_expect_tx(bar(B_QF0 + qs), C::TILE + C::STATS_SLOT);
-    tma_load_3d(sQ + qs * C::TILE, &tq, bar(B_QF0 + qs), 0, (i0 + u) * C::BQ, bh);
-    bulk_load(s0 + C::OFF_STATS + qs * C::STATS_SLOT, p.stats + ((size_t)bh * p.nq + i0 + u) * 256,
+    tma_load_3d(sQ + qs * C::TILE, &tq, bar(B_QF0 + qs), 0, lw.qt * C::BQ, lw.qh);
+    bulk_load(s0 + C::OFF_STATS + qs * C::STATS_SLOT, p.stats + ((size_t)lw.qh * p.nq + lw.qt) * 256,
               C::STATS_SLOT, bar(B_QF0 + qs));
     ++nq_issued;
   };
-  auto issue_do = [&](int u) {
+  auto issue_do = [&](int u) {  // after issue_q(u); moves to the next tile
     const int ds = u % C::DOSLOTS;
     mbar_arrive_expect_tx(bar(B_DOF0 + ds), C::TILE);
-    tma_load_3d(sDO + ds * C::TILE, &tdo, bar(B_DOF0 + ds), 0, (i0 + u) * C::BQ, bh);
+    tma_load_3d(sDO + ds * C::TILE, &tdo, bar(B_DOF0 + ds), 0, lw.qt * C::BQ, lw.qh);
     ++ndo_issued;
+    lw.next(i0, p.nq);
   };
   const int pre = nit < C::DOSLOTS ? nit : C::DOSLOTS;   // tiles issued before the sync
   if (warp == C::W_LOAD && lane == 0) {
@@ -167,12 +175,12 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     tma_prefetch_desc(&tdq);
     // K and Q_0 first: S^T of the first tile needs only those two
     mbar_arrive_expect_tx(bar(B_K), C::TILE);
-    tma_load_3d(sK, &tk, bar(B_K), 0, kt * C::BK, bh);
+    tma_load_3d(sK, &tk, bar(B_K), 0, kt * C::BK, bk);
     for (int u = 0; u < pre; ++u) {
       issue_q(u);
       if (u == 0) {
         mbar_arrive_expect_tx(bar(B_V), C::TILE);
-        tma_load_3d(sV, &tv, bar(B_V), 0, kt * C::BK, bh);
+        tma_load_3d(sV, &tv, bar(B_V), 0, kt * C::BK, bk);
       }
       issue_do(u);
     }
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int cb = CW * g;                          // first query column of this thread
     const uint32_t tST = tmem + lane_off + C::COL_ST + cb, tDPT = tmem + lane_off + C::COL_DPT + cb;
     const uint64_t sc2 = f2_pack(p.scale2, p.scale2);
-    const size_t rowbase = (size_t)bh * p.N;
+    const size_t rowbase = (size_t)bk * p.N;         // key rows (dK, dV)
     // statistics of the tile in Q slot s: 128 x -LSE log2 e, 128 x -D,
     // loaded with the Q tile (same barrier)
     const float* stats = reinterpret_cast<const float*>(smem + C::OFF_STATS);
@@ -336,8 +344,9 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     // chunks (cb % 64) / 8 ... of 8 queries each
     const uint32_t ds_row = (uint32_t)(cb >> 6) * 16384u + (uint32_t)r * 128u;
     const uint32_t ds_c0 = (uint32_t)((cb & 63) >> 3);
-    for (int u = 0; u < nit && ok; ++u) {
-      const int qt = i0 + u;
+    TileWalk w = walk0;
+    for (int u = 0; u < nit && ok; ++u, w.next(i0, p.nq)) {
+      const int qt = w.qt;
       const float* lse_u = stats + qs_u * 256 + cb;
       const float* d_u = lse_u + 128;
       if (!(ok = warp_wait(bar(B_QF0 + qs_u), qph_u, p.ctl, abort, 80))) break;
@@ -454,7 +463,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int sp = warp & 3;
     const int r = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
-    const size_t rowbase = (size_t)bh * p.N;
+    const size_t rowbase = (size_t)bk * p.N;         // key rows (dK, dV)
     const uint32_t sw = (uint32_t)(lane & 7);
     const uint32_t stage = s0 + C::OFF_STAGE + (uint32_t)sp * 8192u;
     // First, K and V rows of this warp's key rows into tensor memory (the A
@@ -479,7 +488,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_KVT));
     }
-    for (int u = 0; u < nit && ok; ++u) {
+    TileWalk w = walk0;
+    for (int u = 0; u < nit && ok; ++u, w.next(i0, p.nq)) {
       if (!(ok = warp_wait(bar(B_DQF), u & 1, p.ctl, abort, 90))) break;
       tc_fence_after();
       uint32_t v[64];
@@ -493,7 +503,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         bulk_wait_group_read<0>();                 // the previous boxes have left the staging area
       }
       __syncwarp();
-      const int y = (i0 + u) * C::BQ + sp * 32;
+      const int y = w.qt * C::BQ + sp * 32, zq = w.qh;
       // columns [32 bb, 32 bb + 32) -> box bb
 #pragma unroll
       for (int bb = 0; bb < 2; ++bb) {
@@ -508,8 +518,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_reduce_add_3d(&tdq, stage, 0, y, bh);
-        tma_reduce_add_3d(&tdq, stage + 4096u, 32, y, bh);
+        tma_reduce_add_3d(&tdq, stage, 0, y, zq);
+        tma_reduce_add_3d(&tdq, stage + 4096u, 32, y, zq);
         bulk_commit_group();
       }
     }
@@ -560,12 +570,13 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   p.N = a.N;
   p.nq = (a.N + C::BQ - 1) / C::BQ;
   p.nkv = (a.N + C::BK - 1) / C::BK;
-  p.BH = a.BH;
-  p.group = head_group(a.BH, p.nkv, a.num_sms);
+  p.BHkv = a.BH / a.group;
+  p.kv_group = a.group;
+  p.group = head_group(p.BHkv, p.nkv, a.num_sms);
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
-  dim3 grid((unsigned)((long)p.nkv * a.BH));
+  dim3 grid((unsigned)((long)p.nkv * p.BHkv));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();
 }

@@ -69,6 +69,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int N, nq, nkv, npairs, BH, group;
+  int kv_group;  // query heads per key/value head (1: multi-head)
   float scale2;  // scale * log2(e)
   KernelCtl ctl;
 };
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   // group the heaviest (causal) query-tile pairs launch first.
   const GridPos gp = decode_grid((int)blockIdx.x, p.BH, p.npairs, p.group);
   const int bh = gp.bh;
+  const int bhkv = bh / p.kv_group;  // key/value head of this query head
   const int qt0 = 2 * (p.npairs - 1 - gp.rank);
   bool valid[2];
   int nkv_t[2];
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     mbar_arrive_expect_tx(bar, C::KVTILE);
     const uint32_t dst = sRing + slot * C::KVTILE;
     for (int b = 0; b < C::KB; ++b)
-      tma_load_3d(dst + b * C::BN * 128, (it & 1) ? &tv : &tk, bar, b * 64, j * C::BN, bh);
+      tma_load_3d(dst + b * C::BN * 128, (it & 1) ? &tv : &tk, bar, b * 64, j * C::BN, bhkv);
   };
   const int n_it = 2 * nmax;                                 // ring uses: K_j, V_j for j < nmax
   const int pre_it = n_it < C::STAGES ? n_it : C::STAGES;    // issued before the sync
@@ -624,6 +626,7 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   p.npairs = (p.nq + 1) / 2;
   p.BH = a.BH;
   p.group = head_group(a.BH, p.npairs, a.num_sms);
+  p.kv_group = a.group;
   p.scale2 = a.scale * 1.4426950408889634f;
   p.ctl = a.ctl;
   dim3 grid((unsigned)((long)p.npairs * a.BH));

@@ -12,10 +12,12 @@ namespace fa {
 
 // Everything a forward launch needs; tensor maps are encoded by the caller.
 struct FwdLaunch {
-  CUtensorMap tq, tk, tv;       // bf16 [BH][N][d], box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tq;               // bf16 [BH][N][d], box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tk, tv;           // bf16 [BH / group][N][d], same box
   void* o;                      // bf16 [BH][N][d]
   float* lse;                   // fp32 [BH][N]
   int BH, N, d;
+  int group;                    // query heads per key/value head (1: multi-head)
   int num_sms;                  // multiprocessors of the device (grid ordering)
   float scale;
   int causal;
@@ -24,7 +26,8 @@ struct FwdLaunch {
 
 // Everything a backward launch needs.
 struct BwdLaunch {
-  CUtensorMap tq, tk, tv, tdo;  // bf16 [BH][N][d], box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tq, tdo;          // bf16 [BH][N][d], box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tk, tv;           // bf16 [BH / group][N][d], same box
   CUtensorMap tdq;              // fp32 dQacc [BH][N][d], box {32, 32, 1}, 128-byte swizzle
   const void* o;                // bf16 [BH][N][d]
   const void* dO;               // bf16 [BH][N][d]
@@ -33,13 +36,26 @@ struct BwdLaunch {
                                 // -LSE log2 e then -D of its rows (-inf, 0 past N)
   float* dq_acc;                // fp32 [BH][N][d] workspace
   void* dq;                     // bf16 [BH][N][d]
-  void* dk;                     // bf16 [BH][N][d]
-  void* dv;                     // bf16 [BH][N][d]
+  void* dk;                     // bf16 [BH / group][N][d]
+  void* dv;                     // bf16 [BH / group][N][d]
   int BH, N, d;
+  int group;                    // query heads per key/value head (1: multi-head)
   int num_sms;                  // multiprocessors of the device (grid ordering)
   float scale;
   int causal;
   KernelCtl ctl;
+};
+
+// Position in a backward CTA's loop over (query head, query tile): tiles
+// first .. nq-1 of one query head, then of the next head of the group.
+struct TileWalk {
+  int qt, qh;
+  __host__ __device__ void next(int first, int nq) {
+    if (++qt == nq) {
+      qt = first;
+      ++qh;
+    }
+  }
 };
 
 // Heads per scheduling group: enough tiles for about two waves of CTAs, so a

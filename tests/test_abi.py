@@ -26,8 +26,8 @@ def declared_functions():
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    for required in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_last_device_error",
-                     "fa_strerror"):
+    for required in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_workspace_size",
+                     "fa_last_device_error", "fa_strerror"):
         assert required in names
 
 
@@ -99,3 +99,22 @@ def test_bwd_argument_errors(L):
     assert bwd(L, scale=-1.0) == INV
     assert bwd(L, d=32) == fa.FA_ERR_UNSUPPORTED
     assert bwd(L, N=0) == fa.FA_OK
+
+
+def test_gqa_argument_errors(L):
+    """Grouped key/value heads: H_kv must lie in 1 ... H and divide H."""
+    import io_aware_exact_10_gb300 as fa
+    INV = fa.FA_ERR_INVALID_ARG
+    f = lambda H, Hkv, B=1: L.fa_fwd_gqa(A, A, A, A, A, B, H, Hkv, 128, 64, ctypes.c_float(0.125),
+                                         0, None)
+    b = lambda H, Hkv: L.fa_bwd_gqa(A, A, A, A, A, A, A, A, A, 1, H, Hkv, 128, 64,
+                                    ctypes.c_float(0.125), 0, A, 1 << 30, None)
+    for H, Hkv in ((4, 0), (4, 3), (4, 5), (4, -2), (6, 4)):
+        assert f(H, Hkv) == INV, (H, Hkv)
+        assert b(H, Hkv) == INV, (H, Hkv)
+    # valid groupings pass validation (and stop later, at the device)
+    for H, Hkv in ((4, 4), (4, 2), (4, 1), (6, 3)):
+        assert f(H, Hkv) != INV, (H, Hkv)
+        assert b(H, Hkv) != INV, (H, Hkv)
+    # an empty problem succeeds whatever H_kv is
+    assert f(4, 0, B=0) == fa.FA_OK

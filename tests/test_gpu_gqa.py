@@ -1,0 +1,110 @@
+"""Grouped key/value heads (GQA, MQA): GPU path against the fp64 oracle.
+
+k and v have H_kv heads; query head h attends with key/value head
+h // (H // H_kv), and dk, dv of a key/value head sum over its query heads.
+Tolerances as in parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import io_aware_exact_10_gb300 as fa
+import oracle
+from parity import TOL_GRAD, TOL_LSE, TOL_O, f64, rel_fro, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def gqa_inputs(B, H, H_kv, N, d, seed):
+    """Seeded fp32 N(0,1) draws rounded to bf16: q, k, v, dO in that order
+    (k, v with H_kv heads)."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, H, N, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, H_kv, N, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H_kv, N, d), generator=g).to(torch.bfloat16)
+    dO = torch.randn((B, H, N, d), generator=g).to(torch.bfloat16)
+    return q, k, v, dO
+
+
+def check_groups(q, k, v, dO, out, scale, causal, kv_heads):
+    """Every query head of each listed key/value head (b, hk), and dk, dv of
+    that head, against the oracle run on the group."""
+    H, H_kv = q.shape[1], k.shape[1]
+    G = H // H_kv
+    for b, hk in kv_heads:
+        hs = slice(hk * G, hk * G + G)
+        qg, dOg = f64(q[b, hs]), f64(dO[b, hs])
+        kg, vg = f64(k[b, hk:hk + 1]), f64(v[b, hk:hk + 1])
+        o_ref, lse_ref = oracle.attn_fwd(qg, kg, vg, scale, causal)
+        eo = float(np.abs(f64(out["o"][b, hs]) - o_ref).max())
+        el = float(np.abs(f64(out["lse"][b, hs]) - lse_ref).max())
+        assert eo <= TOL_O, f"O max-abs {eo} at key/value head {(b, hk)}"
+        assert el <= TOL_LSE, f"LSE max-abs {el} at key/value head {(b, hk)}"
+        dq_ref, dk_ref, dv_ref = oracle.attn_bwd(qg, kg, vg, dOg, scale, causal)
+        for g in range(G):
+            e = rel_fro(f64(out["dq"][b, hk * G + g]), dq_ref[g])
+            assert e <= TOL_GRAD, f"dq rel-Frobenius {e} at query head {(b, hk * G + g)}"
+        for name, r in (("dk", dk_ref[0]), ("dv", dv_ref[0])):
+            e = rel_fro(f64(out[name][b, hk]), r)
+            assert e <= TOL_GRAD, f"{name} rel-Frobenius {e} at key/value head {(b, hk)}"
+
+
+GQA_SHAPES = [
+    # B, H, H_kv, N, d, causal
+    (1, 4, 2, 256, 64, False), (1, 4, 1, 200, 128, True),      # GQA; MQA with a ragged tail
+    (2, 6, 2, 384, 64, True), (1, 8, 2, 1000, 128, False),     # several tiles + tail
+    (1, 2, 2, 128, 64, True), (2, 4, 4, 129, 128, True),       # one query head per group
+    (1, 16, 1, 64, 64, True), (1, 4, 2, 1, 64, False),         # MQA short; a single row
+]
+
+
+@pytest.mark.parametrize("B,H,H_kv,N,d,causal", GQA_SHAPES)
+def test_gqa_shapes(B, H, H_kv, N, d, causal):
+    q, k, v, dO = gqa_inputs(B, H, H_kv, N, d, seed=N + d + H_kv)
+    scale = d ** -0.5
+    out = run_gpu(q, k, v, dO, scale, causal)
+    assert out["dk"].shape == k.shape and out["dv"].shape == v.shape
+    check_groups(q, k, v, dO, out, scale, causal, [(b, hk) for b in range(B) for hk in range(H_kv)])
+
+
+def test_gqa_with_all_heads_equals_multi_head():
+    """H_kv = H through fa_fwd_gqa / fa_bwd_gqa gives exactly fa_fwd / fa_bwd."""
+    B, H, N, d = 1, 3, 384, 64
+    q, k, v, dO = gqa_inputs(B, H, H, N, d, seed=5)
+    dev = "cuda"
+    qd, kd, vd, dOd = (t.to(dev) for t in (q, k, v, dO))
+    scale = d ** -0.5
+    res = []
+    for gqa in (False, True):
+        o, lse = torch.empty_like(qd), torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+        if gqa:
+            fa.fa_fwd_gqa(qd, kd, vd, o, lse, B, H, H, N, d, scale, 1)
+            fa.fa_bwd_gqa(qd, kd, vd, o, lse, dOd, dq, dk, dv, B, H, H, N, d, scale, 1, ws, ws.numel())
+        else:
+            fa.fa_fwd(qd, kd, vd, o, lse, B, H, N, d, scale, 1)
+            fa.fa_bwd(qd, kd, vd, o, lse, dOd, dq, dk, dv, B, H, N, d, scale, 1, ws, ws.numel())
+        torch.cuda.synchronize()
+        res.append([t.cpu() for t in (o, lse, dq, dk, dv)])
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+
+
+def test_gqa_long_causal_sampled():
+    """A grouped-query shape of current decoder models (32 query heads on 8
+    key/value heads, d=128, N=4096, causal): two key/value groups in full, and
+    the group identities of the gradients on every head (sum_j dk_j = 0;
+    sum_j dv_j = the sum of dO over the group's query rows)."""
+    B, H, H_kv, N, d = 1, 32, 8, 4096, 128
+    q, k, v, dO = gqa_inputs(B, H, H_kv, N, d, seed=77)
+    scale = d ** -0.5
+    out = run_gpu(q, k, v, dO, scale, True)
+    check_groups(q, k, v, dO, out, scale, True, [(0, 0), (0, 5)])
+    G = H // H_kv
+    dk, dv = out["dk"].double(), out["dv"].double()
+    sdo = dO.double().sum(dim=2).reshape(B, H_kv, G, d).sum(dim=2)
+    fro = lambda t: t.pow(2).sum(dim=(-1, -2)).sqrt().clamp_min(1e-12)
+    err_v = ((dv.sum(dim=2) - sdo).norm(dim=-1) / fro(dv)).max().item()
+    err_k = (dk.sum(dim=2).norm(dim=-1) / fro(dk)).max().item()
+    assert err_v <= 3e-2 and err_k <= 3e-2, (err_v, err_k)
