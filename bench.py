@@ -131,9 +131,13 @@ def cpu_oracle_sample(w, cpu_inputs, n_heads: int):
     import oracle
     from io_aware_exact_10_gb300 import workloads as W
     oracle.build()
+    G = w.H // w.kv_heads  # query heads per key/value head
+    n_heads = max(G, n_heads // G * G)  # whole groups
     sub = W.Workload(w.name, 1, n_heads, w.N, w.d, causal=w.causal, seed=w.seed)
-    flat = lambda t: t.reshape(w.B * w.H, w.N, w.d)[:n_heads].double().numpy()
-    qs, ks, vs, dOs = (flat(t) for t in cpu_inputs)
+    flat = lambda t, n: t.reshape(-1, w.N, w.d)[:n].double().numpy()
+    q, k, v, dO = cpu_inputs
+    qs, dOs = flat(q, n_heads), flat(dO, n_heads)
+    ks, vs = flat(k, n_heads // G), flat(v, n_heads // G)
     t0 = time.perf_counter()
     oracle.attn_fwd(qs, ks, vs, w.scale, w.causal)
     oracle.attn_bwd(qs, ks, vs, dOs, w.scale, w.causal)
@@ -158,16 +162,18 @@ def run_reference(args, w):
     from io_aware_exact_10_gb300 import workloads as W
     oracle.build()
     q, k, v, dO = W.make_inputs(w)
-    flat = lambda t: t.reshape(w.B * w.H, w.N, w.d).double().numpy()
+    G = w.H // w.kv_heads  # query heads per key/value head
+    heads_per_step = max(G, heads_per_step // G * G)  # whole groups
+    flat = lambda t: t.reshape(-1, w.N, w.d).double().numpy()
     qs, ks, vs, dOs = flat(q), flat(k), flat(v), flat(dO)
     sub = W.Workload(w.name, 1, heads_per_step, w.N, w.d, causal=w.causal)
     flops_step = sub.fwd_flops() + sub.bwd_flops()
 
     def step(i):
         lo = (i * heads_per_step) % (w.B * w.H)
-        sl = slice(lo, lo + heads_per_step)
-        oracle.attn_fwd(qs[sl], ks[sl], vs[sl], w.scale, w.causal)
-        oracle.attn_bwd(qs[sl], ks[sl], vs[sl], dOs[sl], w.scale, w.causal)
+        sl, sk = slice(lo, lo + heads_per_step), slice(lo // G, (lo + heads_per_step) // G)
+        oracle.attn_fwd(qs[sl], ks[sk], vs[sk], w.scale, w.causal)
+        oracle.attn_bwd(qs[sl], ks[sk], vs[sk], dOs[sl], w.scale, w.causal)
 
     for i in range(args.warmup):
         step(i)
@@ -194,10 +200,16 @@ def run_reference(args, w):
 
 
 def config_of(w):
-    return {"workload": f"{w.name}, forward+backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-            "causal": w.causal, "scale": w.scale,
-            "l2": "inputs larger than L2 (4 x %.0f MB bf16), no flush" % (w.B * w.H * w.N * w.d * 2 / 1e6),
-            "flops": "fwd 4*B*H*N^2*d (x1/2 causal); bwd 2.5x fwd"}
+    c = {"workload": f"{w.name}, forward+backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+         "causal": w.causal, "scale": w.scale,
+         "l2": "inputs larger than L2 (4 x %.0f MB bf16), no flush" % (w.B * w.H * w.N * w.d * 2 / 1e6),
+         "flops": "fwd 4*B*H*N^2*d (x1/2 causal); bwd 2.5x fwd"}
+    if w.kv_heads != w.H:
+        c["H_kv"] = w.kv_heads
+        qb, kb = (w.B * h * w.N * w.d * 2 / 1e6 for h in (w.H, w.kv_heads))
+        c["l2"] = ("inputs larger than L2 together (Q, dO %.0f MB, K, V %.0f MB bf16 each: "
+                   "%.0f MB), no flush" % (qb, kb, 2 * qb + 2 * kb))
+    return c
 
 
 def run_ours(args, w):
@@ -217,22 +229,23 @@ def run_ours(args, w):
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
 
-    B, H, N, d = w.B, w.H, w.N, w.d
+    B, H, Hkv, N, d = w.B, w.H, w.kv_heads, w.N, w.d
     cpu_inputs = W.make_inputs(w)
     q, k, v, dO = (t.to(dev) for t in cpu_inputs)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     causal = int(w.causal)
 
+    # fa_fwd_gqa / fa_bwd_gqa with H_kv = H are fa_fwd / fa_bwd
     def fwd():
-        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, w.scale, causal, stream)
+        fa.fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, w.scale, causal, stream)
 
     def bwd():
-        fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, w.scale, causal, ws, ws_bytes,
-                  stream)
+        fa.fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, w.scale, causal, ws,
+                      ws_bytes, stream)
 
     def barrier():
         if world > 1:
@@ -291,7 +304,8 @@ def run_ours(args, w):
     hq, hk, hv, hdO = (t.cpu().pin_memory() for t in (q, k, v, dO))
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3))
+    hdq = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hdk, hdv = (torch.empty(k.shape, dtype=k.dtype).pin_memory() for _ in range(2))
 
     def e2e_step():
         for h, dd in ((hq, q), (hk, k), (hv, v), (hdO, dO)):

@@ -6,7 +6,8 @@ value produced by the GPU.
 
 Recipe (the same for every workload): one CPU ``torch.Generator`` seeded with
 ``seed`` draws Q, K, V and dO, in that order, as fp32 N(0, 1) tensors of shape
-[B, H, N, d]; Q and K are multiplied by ``qk_std``; when ``boost_every`` is set,
+[B, H, N, d] (K and V with ``H_kv`` heads when the workload groups key/value
+heads); Q and K are multiplied by ``qk_std``; when ``boost_every`` is set,
 key rows j with (j + 1) % boost_every == 0 (the 97th, 194th, ... row of each
 head, counting from one) are multiplied by ``boost``; then every tensor is
 rounded to bf16 (round to nearest even).  The default scale is 1/sqrt(d).
@@ -31,6 +32,11 @@ class Workload:
     boost_every: int = 0
     boost: float = 1.0
     seed: int = 0
+    H_kv: int = 0  # key/value heads (0: one per query head)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
 
     @property
     def scale(self) -> float:
@@ -56,6 +62,9 @@ STRESS_CAUSAL = Workload("stress_B8_H16_N4096_d128_causal", 8, 16, 4096, 128, ca
                          qk_std=4.0, boost_every=97, boost=8.0)
 STRESS = Workload("stress_B8_H16_N4096_d128", 8, 16, 4096, 128, causal=False,
                   qk_std=4.0, boost_every=97, boost=8.0)
+# grouped-query attention of current decoder models: 32 query heads on 8
+# key/value heads
+GQA_CAUSAL = Workload("gqa_B2_H32_Hkv8_N4096_d128_causal", 2, 32, 4096, 128, causal=True, H_kv=8)
 
 SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384, 32768)
 SWEEP_D = (64, 128)
@@ -71,11 +80,11 @@ def make_inputs(w: Workload, device: str = "cpu", with_grad: bool = True):
     """Draw (q, k, v, dO) as bf16 [B, H, N, d] tensors following the recipe."""
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed)
-    shape = (w.B, w.H, w.N, w.d)
     out = []
     names = ("q", "k", "v", "dO") if with_grad else ("q", "k", "v")
     for name in names:
-        t = torch.randn(shape, generator=g, dtype=torch.float32)
+        heads = w.kv_heads if name in ("k", "v") else w.H
+        t = torch.randn((w.B, heads, w.N, w.d), generator=g, dtype=torch.float32)
         if name in ("q", "k") and w.qk_std != 1.0:
             t.mul_(w.qk_std)
         if name == "k" and w.boost_every:
@@ -87,12 +96,12 @@ def make_inputs(w: Workload, device: str = "cpu", with_grad: bool = True):
 
 
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD, GPT2_MEDIUM, GPT2_MEDIUM_CAUSAL, LONG_CAUSAL,
-                                  STRESS_CAUSAL, STRESS)}
+                                  STRESS_CAUSAL, STRESS, GQA_CAUSAL)}
 WORKLOADS.update({sweep(N, d).name: sweep(N, d) for N in SWEEP_N for d in SWEEP_D})
 # short aliases
 WORKLOADS.update({"gpt2_medium": GPT2_MEDIUM, "gpt2_medium_causal": GPT2_MEDIUM_CAUSAL,
                   "long_causal": LONG_CAUSAL, "stress": STRESS, "stress_causal": STRESS_CAUSAL,
-                  "single_head": SINGLE_HEAD})
+                  "single_head": SINGLE_HEAD, "gqa_causal": GQA_CAUSAL})
 
 
 def make_inputs_on_device(w: Workload, device, with_grad: bool = True):
@@ -101,10 +110,10 @@ def make_inputs_on_device(w: Workload, device, with_grad: bool = True):
     host-side draw of a large workload would dominate)."""
     g = torch.Generator(device=device)
     g.manual_seed(w.seed)
-    shape = (w.B, w.H, w.N, w.d)
     out = []
     for name in (("q", "k", "v", "dO") if with_grad else ("q", "k", "v")):
-        t = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
+        heads = w.kv_heads if name in ("k", "v") else w.H
+        t = torch.randn((w.B, heads, w.N, w.d), generator=g, dtype=torch.float32, device=device)
         if name in ("q", "k") and w.qk_std != 1.0:
             t.mul_(w.qk_std)
         if name == "k" and w.boost_every:
