@@ -47,9 +47,17 @@
  * chain rule through the shared K and V, dk and dv of key/value head hk sum
  * the per-head terms above over its query heads hk*G ... hk*G + G - 1.
  *
- * Layout: every tensor is a dense fp64 array [heads][N][d] (d innermost);
- * q, o, dO, dq have BH heads, k, v, dk, dv BH / G; lse and the per-row
- * statistics are [BH][N].  BH = B*H independent query heads.
+ * Query and key lengths may differ (Nq query rows, Nk keys; the pages list
+ * variable sequence lengths among FlashAttention 2's changes, Flash
+ * Attention, "Evolution: Flash Attention 2 & 3").  Causal masking then
+ * aligns the last query with the last key (the library's reading): key j is
+ * visible to query i iff j <= i + (Nk - Nq), which is j <= i when the
+ * lengths are equal; it requires Nk >= Nq so that every row sees a key.
+ *
+ * Layout: every tensor is a dense fp64 array [heads][rows][d] (d innermost);
+ * q, o, dO, dq have BH heads of Nq rows, k, v, dk, dv BH / G heads of Nk
+ * rows; lse and the per-row statistics are [BH][Nq].  BH = B*H independent
+ * query heads.
  * Parallelism: OpenMP over (head, row) for the row-wise passes and over
  * (head, key) for the key-wise pass.  No blocking, no online softmax, no
  * reordering beyond the loops of the definition.
@@ -71,8 +79,9 @@ int oracle_num_threads(void) {
 #endif
 }
 
-/* key j is visible to query i: everything when not causal, j <= i when causal */
-static int visible(int causal, long i, long j) { return !causal || j <= i; }
+/* key j is visible to query i: everything when not causal, j <= i + off when
+ * causal (off = Nk - Nq >= 0) */
+static int visible(int causal, long off, long i, long j) { return !causal || j <= i + off; }
 
 /* s_ij = scale * q_i . k_j (no masking here; callers skip invisible keys) */
 static double score(const double *qi, const double *kj, int d, double scale) {
@@ -82,18 +91,18 @@ static double score(const double *qi, const double *kj, int d, double scale) {
 }
 
 /* Row statistics of the safe softmax of row i: m_i and l_i. */
-static void row_stats(const double *q, const double *k, long i, int N, int d,
+static void row_stats(const double *q, const double *k, long i, int Nk, long off, int d,
                       double scale, int causal, double *m_out, double *l_out) {
     const double *qi = q + i * (long)d;
     double m = -INFINITY;
-    for (long j = 0; j < N; ++j) {
-        if (!visible(causal, i, j)) continue;
+    for (long j = 0; j < Nk; ++j) {
+        if (!visible(causal, off, i, j)) continue;
         double s = score(qi, k + j * (long)d, d, scale);
         if (s > m) m = s;
     }
     double l = 0.0;
-    for (long j = 0; j < N; ++j) {
-        if (!visible(causal, i, j)) continue;
+    for (long j = 0; j < Nk; ++j) {
+        if (!visible(causal, off, i, j)) continue;
         l += exp(score(qi, k + j * (long)d, d, scale) - m);
     }
     *m_out = m;
@@ -102,58 +111,58 @@ static void row_stats(const double *q, const double *k, long i, int N, int d,
 
 /*
  * Forward: o = softmax(scale Q K^T [masked]) V and lse, per query head.
- * q, o: [BH][N][d]; k, v: [BH/G][N][d]; lse: [BH][N].  G = group >= 1.
+ * q, o: [BH][Nq][d]; k, v: [BH/G][Nk][d]; lse: [BH][Nq].  G = group >= 1.
  */
 void oracle_attn_fwd(const double *q, const double *k, const double *v,
-                     double *o, double *lse, int BH, int N, int d,
+                     double *o, double *lse, int BH, int Nq, int Nk, int d,
                      double scale, int causal, int group) {
-    const long hs = (long)N * d;
+    const long hq = (long)Nq * d, hk = (long)Nk * d, off = (long)Nk - Nq;
 #pragma omp parallel for collapse(2) schedule(dynamic, 4)
     for (int h = 0; h < BH; ++h) {
-        for (int i = 0; i < N; ++i) {
-            const double *qh = q + h * hs, *kh = k + (h / group) * hs, *vh = v + (h / group) * hs;
+        for (int i = 0; i < Nq; ++i) {
+            const double *qh = q + h * hq, *kh = k + (h / group) * hk, *vh = v + (h / group) * hk;
             double m, l;
-            row_stats(qh, kh, i, N, d, scale, causal, &m, &l);
-            double *oi = o + h * hs + (long)i * d;
+            row_stats(qh, kh, i, Nk, off, d, scale, causal, &m, &l);
+            double *oi = o + h * hq + (long)i * d;
             for (int c = 0; c < d; ++c) oi[c] = 0.0;
-            for (long j = 0; j < N; ++j) {
-                if (!visible(causal, i, j)) continue;
+            for (long j = 0; j < Nk; ++j) {
+                if (!visible(causal, off, i, j)) continue;
                 double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m) / l;
                 const double *vj = vh + j * d;
                 for (int c = 0; c < d; ++c) oi[c] += p * vj[c];
             }
-            lse[(long)h * N + i] = m + log(l);
+            lse[(long)h * Nq + i] = m + log(l);
         }
     }
 }
 
 /*
  * Backward: dq, dk, dv of L with dL/dO = dO.
- * q, dO, dq: [BH][N][d]; k, v, dk, dv: [BH/G][N][d].  Forward quantities are
- * recomputed here from q, k, v (the oracle takes nothing produced by the GPU
- * path).  D_out (may be NULL): [BH][N], receives D_i = sum_j p_ij dp_ij.
+ * q, dO, dq: [BH][Nq][d]; k, v, dk, dv: [BH/G][Nk][d].  Forward quantities
+ * are recomputed here from q, k, v (the oracle takes nothing produced by the
+ * GPU path).  D_out (may be NULL): [BH][Nq], receives D_i = sum_j p_ij dp_ij.
  */
 void oracle_attn_bwd(const double *q, const double *k, const double *v,
                      const double *dO, double *dq, double *dk, double *dv,
-                     double *D_out, int BH, int N, int d, double scale,
+                     double *D_out, int BH, int Nq, int Nk, int d, double scale,
                      int causal, int group) {
-    const long hs = (long)N * d;
-    double *m = (double *)malloc(sizeof(double) * (size_t)BH * N);
-    double *l = (double *)malloc(sizeof(double) * (size_t)BH * N);
-    double *D = (double *)malloc(sizeof(double) * (size_t)BH * N);
+    const long hq = (long)Nq * d, hk = (long)Nk * d, off = (long)Nk - Nq;
+    double *m = (double *)malloc(sizeof(double) * (size_t)BH * Nq);
+    double *l = (double *)malloc(sizeof(double) * (size_t)BH * Nq);
+    double *D = (double *)malloc(sizeof(double) * (size_t)BH * Nq);
 
     /* Pass over query rows: row statistics, D_i, and dq_i. */
 #pragma omp parallel for collapse(2) schedule(dynamic, 4)
     for (int h = 0; h < BH; ++h) {
-        for (int i = 0; i < N; ++i) {
-            const double *qh = q + h * hs, *kh = k + (h / group) * hs, *vh = v + (h / group) * hs;
-            const double *dOi = dO + h * hs + (long)i * d;
-            const long r = (long)h * N + i;
-            row_stats(qh, kh, i, N, d, scale, causal, &m[r], &l[r]);
+        for (int i = 0; i < Nq; ++i) {
+            const double *qh = q + h * hq, *kh = k + (h / group) * hk, *vh = v + (h / group) * hk;
+            const double *dOi = dO + h * hq + (long)i * d;
+            const long r = (long)h * Nq + i;
+            row_stats(qh, kh, i, Nk, off, d, scale, causal, &m[r], &l[r]);
             /* D_i = sum_j p_ij dp_ij */
             double Di = 0.0;
-            for (long j = 0; j < N; ++j) {
-                if (!visible(causal, i, j)) continue;
+            for (long j = 0; j < Nk; ++j) {
+                if (!visible(causal, off, i, j)) continue;
                 double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m[r]) / l[r];
                 double dp = 0.0;
                 for (int c = 0; c < d; ++c) dp += dOi[c] * vh[j * d + c];
@@ -161,10 +170,10 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
             }
             D[r] = Di;
             /* dq_i = scale * sum_j ds_ij k_j */
-            double *dqi = dq + h * hs + (long)i * d;
+            double *dqi = dq + h * hq + (long)i * d;
             for (int c = 0; c < d; ++c) dqi[c] = 0.0;
-            for (long j = 0; j < N; ++j) {
-                if (!visible(causal, i, j)) continue;
+            for (long j = 0; j < Nk; ++j) {
+                if (!visible(causal, off, i, j)) continue;
                 double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m[r]) / l[r];
                 double dp = 0.0;
                 for (int c = 0; c < d; ++c) dp += dOi[c] * vh[j * d + c];
@@ -179,18 +188,18 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
      * dk_j = scale * sum over the same of ds_ij q_i. */
     const int BHkv = BH / group;
 #pragma omp parallel for collapse(2) schedule(dynamic, 4)
-    for (int hk = 0; hk < BHkv; ++hk) {
-        for (int j = 0; j < N; ++j) {
-            const double *kh = k + hk * hs, *vh = v + hk * hs;
-            double *dvj = dv + hk * hs + (long)j * d;
-            double *dkj = dk + hk * hs + (long)j * d;
+    for (int kv = 0; kv < BHkv; ++kv) {
+        for (int j = 0; j < Nk; ++j) {
+            const double *kh = k + kv * hk, *vh = v + kv * hk;
+            double *dvj = dv + kv * hk + (long)j * d;
+            double *dkj = dk + kv * hk + (long)j * d;
             for (int c = 0; c < d; ++c) { dvj[c] = 0.0; dkj[c] = 0.0; }
             for (int g = 0; g < group; ++g) {
-                const int h = hk * group + g;
-                const double *qh = q + h * hs, *dOh = dO + h * hs;
-                for (long i = 0; i < N; ++i) {
-                    if (!visible(causal, i, j)) continue;
-                    const long r = (long)h * N + i;
+                const int h = kv * group + g;
+                const double *qh = q + h * hq, *dOh = dO + h * hq;
+                for (long i = 0; i < Nq; ++i) {
+                    if (!visible(causal, off, i, j)) continue;
+                    const long r = (long)h * Nq + i;
                     double p = exp(score(qh + i * d, kh + (long)j * d, d, scale) - m[r]) / l[r];
                     double dp = 0.0;
                     for (int c = 0; c < d; ++c) dp += dOh[i * d + c] * vh[(long)j * d + c];
@@ -205,7 +214,7 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
     }
 
     if (D_out) {
-        for (long r = 0; r < (long)BH * N; ++r) D_out[r] = D[r];
+        for (long r = 0; r < (long)BH * Nq; ++r) D_out[r] = D[r];
     }
     free(m);
     free(l);
@@ -215,20 +224,21 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
 /*
  * Forward for a chosen subset of query rows of one head (for sampled checks
  * at sizes where the full oracle would take too long).  rows: [R] indices.
- * q, k, v: [N][d] of that head; o: [R][d]; lse: [R].
+ * q: [Nq][d], k, v: [Nk][d] of that head; o: [R][d]; lse: [R].
  */
 void oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
                           const int *rows, int R, double *o, double *lse,
-                          int N, int d, double scale, int causal) {
+                          int Nq, int Nk, int d, double scale, int causal) {
+    const long off = (long)Nk - Nq;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int t = 0; t < R; ++t) {
         const long i = rows[t];
         double m, l;
-        row_stats(q, k, i, N, d, scale, causal, &m, &l);
+        row_stats(q, k, i, Nk, off, d, scale, causal, &m, &l);
         double *oi = o + (long)t * d;
         for (int c = 0; c < d; ++c) oi[c] = 0.0;
-        for (long j = 0; j < N; ++j) {
-            if (!visible(causal, i, j)) continue;
+        for (long j = 0; j < Nk; ++j) {
+            if (!visible(causal, off, i, j)) continue;
             double p = exp(score(q + i * d, k + j * d, d, scale) - m) / l;
             for (int c = 0; c < d; ++c) oi[c] += p * v[j * d + c];
         }

@@ -1,7 +1,10 @@
 """ctypes wrapper around the fp64 C oracle (``attention_oracle.c``).
 
 Test infrastructure only: see the package docstring.  Arrays are numpy fp64,
-shaped [..., N, d] (flattened to BH heads); lse is [..., N].
+shaped [..., rows, d] (flattened to heads): q, o, dO, dq have Nq rows, k, v,
+dk, dv Nk rows; lse is [..., Nq].  With causal masking and Nq != Nk the last
+query row is aligned with the last key (key j visible to query i iff
+j <= i + Nk - Nq), which needs Nk >= Nq.
 """
 from __future__ import annotations
 
@@ -52,6 +55,16 @@ def _heads(a: np.ndarray):
     return a.reshape(-1, N, d), N, d
 
 
+def _kv_rows(Nq: int, kh: np.ndarray, vh: np.ndarray, d: int, causal: bool) -> int:
+    """Key count Nk of k, v (equal shapes, same d as q; Nk >= Nq when causal)."""
+    if kh.shape != vh.shape or kh.shape[-1] != d:
+        raise ValueError(f"k {kh.shape} and v {vh.shape} must match and have d={d}")
+    Nk = kh.shape[1]
+    if causal and Nk < Nq:
+        raise ValueError(f"causal attention needs Nk >= Nq (Nq={Nq}, Nk={Nk})")
+    return Nk
+
+
 def _group(BH: int, BHk: int, BHv: int) -> int:
     """Query heads per key/value head (1 for standard multi-head)."""
     if BHk != BHv or BHk < 1 or BH % BHk != 0:
@@ -67,13 +80,13 @@ class OracleLib:
         dp = ctypes.POINTER(ctypes.c_double)
         ip = ctypes.POINTER(ctypes.c_int)
         ci, cd = ctypes.c_int, ctypes.c_double
-        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, cd, ci, ci]
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, ci, cd, ci, ci]
         lib.oracle_attn_fwd.restype = None
         lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
-                                        ci, ci, ci, cd, ci, ci]
+                                        ci, ci, ci, ci, cd, ci, ci]
         lib.oracle_attn_bwd.restype = None
         lib.oracle_attn_fwd_rows.argtypes = [dp, dp, dp, ip, ci, dp, dp,
-                                             ci, ci, cd, ci]
+                                             ci, ci, ci, cd, ci]
         lib.oracle_attn_fwd_rows.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ci
@@ -85,22 +98,23 @@ class OracleLib:
     def attn_fwd(self, q, k, v, scale: float, causal: bool):
         """o = softmax(scale * q k^T [causal]) v and lse (natural log), fp64.
 
-        q: [..., N, d]; k, v: [..., N, d] with the same or a dividing number
-        of heads (grouped key/value heads: query head h uses key/value head
-        h // G over the flattened head axis).  Returns (o shaped like q, lse
-        shaped [..., N] like q's heads).
+        q: [..., Nq, d]; k, v: [..., Nk, d] with the same or a dividing
+        number of heads (grouped key/value heads: query head h uses key/value
+        head h // G over the flattened head axis).  Returns (o shaped like q,
+        lse shaped [..., Nq] like q's heads).
         """
         q, k, v = _f64(q), _f64(k), _f64(v)
         lead = q.shape[:-2]
         qh, N, d = _heads(q)
         kh, _, _ = _heads(k)
         vh, _, _ = _heads(v)
+        Nk = _kv_rows(N, kh, vh, d, causal)
         BH = qh.shape[0]
         group = _group(BH, kh.shape[0], vh.shape[0])
         o = np.empty_like(qh)
         lse = np.empty((BH, N), dtype=np.float64)
         self._lib.oracle_attn_fwd(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(o),
-                                  _ptr(lse), BH, N, d, float(scale),
+                                  _ptr(lse), BH, N, Nk, d, float(scale),
                                   int(bool(causal)), group)
         return o.reshape(*lead, N, d), lse.reshape(*lead, N)
 
@@ -108,17 +122,21 @@ class OracleLib:
                  return_D: bool = False):
         """Gradients (dq, dk, dv) of L with dL/dO = dO, fp64.
 
-        With ``return_D`` also returns D = rowsum(P * dP) shaped [..., N].
-        k, v may have fewer heads than q (see attn_fwd); dk, dv are shaped
-        like k and sum over each key/value head's query heads.
+        With ``return_D`` also returns D = rowsum(P * dP) shaped [..., Nq].
+        k, v may have fewer heads and another length than q (see attn_fwd);
+        dk, dv are shaped like k and sum over each key/value head's query
+        heads.
         """
         q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+        if dO.shape != q.shape:
+            raise ValueError(f"dO {dO.shape} must be shaped like q {q.shape}")
         lead = q.shape[:-2]
         lead_kv = k.shape[:-2]
         qh, N, d = _heads(q)
         kh, _, _ = _heads(k)
         vh, _, _ = _heads(v)
         dOh, _, _ = _heads(dO)
+        Nk = _kv_rows(N, kh, vh, d, causal)
         BH = qh.shape[0]
         group = _group(BH, kh.shape[0], vh.shape[0])
         dq = np.empty_like(qh)
@@ -127,20 +145,22 @@ class OracleLib:
         D = np.empty((BH, N), dtype=np.float64)
         self._lib.oracle_attn_bwd(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(dOh),
                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(D),
-                                  BH, N, d, float(scale), int(bool(causal)), group)
-        out = (dq.reshape(*lead, N, d), dk.reshape(*lead_kv, N, d),
-               dv.reshape(*lead_kv, N, d))
+                                  BH, N, Nk, d, float(scale), int(bool(causal)), group)
+        out = (dq.reshape(*lead, N, d), dk.reshape(*lead_kv, Nk, d),
+               dv.reshape(*lead_kv, Nk, d))
         if return_D:
             return out + (D.reshape(*lead, N),)
         return out
 
     def attn_fwd_rows(self, q, k, v, rows, scale: float, causal: bool):
-        """Forward for selected query rows of ONE head: q, k, v are [N, d].
+        """Forward for selected query rows of ONE head: q is [Nq, d], k, v
+        are [Nk, d].
 
         Returns (o [R, d], lse [R]) for the rows listed in ``rows``.
         """
         q, k, v = _f64(q), _f64(k), _f64(v)
         N, d = q.shape
+        Nk = _kv_rows(N, k[None], v[None], d, causal)
         rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
         R = rows.shape[0]
         o = np.empty((R, d), dtype=np.float64)
@@ -148,7 +168,7 @@ class OracleLib:
         self._lib.oracle_attn_fwd_rows(
             _ptr(q), _ptr(k), _ptr(v),
             rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), R,
-            _ptr(o), _ptr(lse), N, d, float(scale), int(bool(causal)))
+            _ptr(o), _ptr(lse), N, Nk, d, float(scale), int(bool(causal)))
         return o, lse
 
 

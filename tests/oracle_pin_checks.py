@@ -375,10 +375,104 @@ def check_gqa_finite_differences(orc):
             assert err / max(np.abs(num).max(), 1e-3) < 1e-6, (causal, which, err)
 
 
+# ----------------------------------------------------------------------------
+# query and key lengths that differ (Nq != Nk)
+# ----------------------------------------------------------------------------
+
+def _bottom_right_mask(Nq, Nk):
+    """Boolean [Nq, Nk]: query i may see key j iff j <= i + Nk - Nq."""
+    import torch
+    return torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=Nk - Nq)
+
+
+def check_cross_torch(orc):
+    """Nq != Nk against torch in fp64: scaled_dot_product_attention with no
+    mask, or with an explicit bottom-right causal mask built by tril, forward
+    and autograd; grouped key/value heads and several heads so that a head
+    stride taken from the wrong length shows.  The first case has Nq < Nk."""
+    import torch
+    import torch.nn.functional as F
+    r = _rng(16)
+    for Nq, Nk, causal in ((7, 19, True), (7, 19, False), (19, 7, False), (1, 9, True),
+                           (13, 13, True), (5, 130, True), (130, 5, False)):
+        B, H, Hkv, d = 1, 4, 2, 8
+        G = H // Hkv
+        q, dO = (r.normal(size=(B, H, Nq, d)) for _ in range(2))
+        k, v = (r.normal(size=(B, Hkv, Nk, d)) for _ in range(2))
+        tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (q, k, v))
+        mask = _bottom_right_mask(Nq, Nk) if causal else None
+        out = F.scaled_dot_product_attention(
+            tq, torch.repeat_interleave(tk, G, dim=1), torch.repeat_interleave(tv, G, dim=1),
+            attn_mask=mask, scale=0.45)
+        out.backward(torch.from_numpy(dO))
+        o, lse = orc.attn_fwd(q, k, v, 0.45, causal)
+        assert o.shape == q.shape and lse.shape == q.shape[:-1]
+        assert np.allclose(o, out.detach().numpy(), atol=1e-12, rtol=0), (Nq, Nk, causal)
+        dq, dk, dv = orc.attn_bwd(q, k, v, dO, 0.45, causal)
+        assert dk.shape == k.shape and dv.shape == v.shape
+        assert np.allclose(dq, tq.grad.numpy(), atol=1e-11, rtol=0), (Nq, Nk, causal)
+        assert np.allclose(dk, tk.grad.numpy(), atol=1e-11, rtol=0), (Nq, Nk, causal)
+        assert np.allclose(dv, tv.grad.numpy(), atol=1e-11, rtol=0), (Nq, Nk, causal)
+        rows = np.array([0, Nq - 1, Nq // 2], dtype=np.int32)
+        o_r, l_r = orc.attn_fwd_rows(q[0, 1], k[0, 0], v[0, 0], rows, 0.45, causal)
+        assert np.allclose(o_r, o[0, 1, rows], atol=1e-13, rtol=0)
+        assert np.allclose(l_r, lse[0, 1, rows], atol=1e-13, rtol=0)
+
+
+def check_cross_causal_is_suffix(orc):
+    """Causal attention of Nq queries on Nk >= Nq keys is the last Nq rows of
+    square causal attention over Nk queries whose last Nq rows are those
+    queries (a chunk of queries appended after Nk - Nq earlier positions).
+    dq is the suffix of the square problem's dq, and dk, dv equal the square
+    problem's with dO zero on the first Nk - Nq rows."""
+    r = _rng(17)
+    for Nq, Nk in ((3, 11), (1, 6), (8, 8), (9, 40)):
+        d = 4
+        q_full, dO_full = (r.normal(size=(2, Nk, d)) for _ in range(2))
+        k, v = (r.normal(size=(2, Nk, d)) for _ in range(2))
+        dO_full[:, :Nk - Nq] = 0.0
+        q, dO = q_full[:, Nk - Nq:], dO_full[:, Nk - Nq:]
+        o_f, lse_f = orc.attn_fwd(q_full, k, v, 0.7, True)
+        o, lse = orc.attn_fwd(q, k, v, 0.7, True)
+        assert np.allclose(o, o_f[:, Nk - Nq:], atol=1e-13, rtol=0), (Nq, Nk)
+        assert np.allclose(lse, lse_f[:, Nk - Nq:], atol=1e-13, rtol=0), (Nq, Nk)
+        dq_f, dk_f, dv_f = orc.attn_bwd(q_full, k, v, dO_full, 0.7, True)
+        dq, dk, dv = orc.attn_bwd(q, k, v, dO, 0.7, True)
+        assert np.allclose(dq, dq_f[:, Nk - Nq:], atol=1e-12, rtol=0), (Nq, Nk)
+        assert np.allclose(dk, dk_f, atol=1e-12, rtol=0), (Nq, Nk)
+        assert np.allclose(dv, dv_f, atol=1e-12, rtol=0), (Nq, Nk)
+
+
+def check_cross_finite_differences(orc):
+    """Central differences of L = sum(dO * O) w.r.t. every entry of Q, K, V
+    with Nq != Nk (bottom-right causal and unmasked) agree with the analytic
+    gradients to 1e-6 relative."""
+    r = _rng(18)
+    h = 1e-6
+    for Nq, Nk, causal in ((2, 5, True), (2, 5, False), (4, 3, False), (1, 4, True)):
+        d = 2
+        q, dO = (r.normal(size=(Nq, d)) for _ in range(2))
+        k, v = (r.normal(size=(Nk, d)) for _ in range(2))
+        g = orc.attn_bwd(q, k, v, dO, 0.9, causal)
+        for which, x in enumerate((q, k, v)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = [q, k, v]; args_p[which] = xp
+                args_m = [q, k, v]; args_m[which] = xm
+                num[idx] = (_loss(orc, *args_p, dO, 0.9, causal)
+                            - _loss(orc, *args_m, dO, 0.9, causal)) / (2 * h)
+            err = np.abs(num - g[which]).max()
+            assert err / max(np.abs(num).max(), 1e-3) < 1e-6, (Nq, Nk, causal, which, err)
+
+
 FWD_CHECKS = (check_four_scores, check_rows_sum_to_one, check_softmax_of_scores,
               check_identical_keys, check_causal_row0, check_zero_queries,
               check_dominant_key, check_blocked_online_softmax,
               check_multi_head_independent, check_rows_entry, check_torch_sdpa_fwd)
 BWD_CHECKS = (check_finite_differences, check_gradient_invariants, check_torch_autograd)
 GQA_CHECKS = (check_gqa_torch, check_gqa_finite_differences)
-ALL_CHECKS = FWD_CHECKS + BWD_CHECKS + GQA_CHECKS
+CROSS_CHECKS = (check_cross_torch, check_cross_causal_is_suffix, check_cross_finite_differences)
+ALL_CHECKS = FWD_CHECKS + BWD_CHECKS + GQA_CHECKS + CROSS_CHECKS

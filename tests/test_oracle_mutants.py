@@ -15,11 +15,11 @@ MUTANTS = {
     # forward
     "max_wrong_direction": ("if (s > m) m = s;", "if (s < m) m = s;"),
     "scale_dropped": ("return scale * acc;", "return acc;"),
-    "lse_sign": ("lse[(long)h * N + i] = m + log(l);", "lse[(long)h * N + i] = m - log(l);"),
-    "lse_log_dropped": ("lse[(long)h * N + i] = m + log(l);", "lse[(long)h * N + i] = m + l;"),
+    "lse_sign": ("lse[(long)h * Nq + i] = m + log(l);", "lse[(long)h * Nq + i] = m - log(l);"),
+    "lse_log_dropped": ("lse[(long)h * Nq + i] = m + log(l);", "lse[(long)h * Nq + i] = m + l;"),
     "value_row_index": ("const double *vj = vh + j * d;", "const double *vj = vh + i * d;"),
-    "causal_off_by_one": ("return !causal || j <= i;", "return !causal || j < i;"),
-    "causal_transposed": ("return !causal || j <= i;", "return !causal || j >= i;"),
+    "causal_off_by_one": ("return !causal || j <= i + off;", "return !causal || j < i + off;"),
+    "causal_transposed": ("return !causal || j <= i + off;", "return !causal || j >= i + off;"),
     "normaliser_dropped": (
         "double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m) / l;",
         "double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m);"),
@@ -35,11 +35,19 @@ MUTANTS = {
         "dp += dOh[(long)j * d + c] * vh[i * d + c];"),
     "key_pass_D_dropped": ("double ds = p * (dp - D[r]);", "double ds = p * dp;"),
     # grouped key/value heads
-    "gqa_kv_head_modulo": ("*kh = k + (h / group) * hs, *vh = v + (h / group) * hs;",
-                           "*kh = k + (h % group) * hs, *vh = v + (h % group) * hs;"),
+    "gqa_kv_head_modulo": ("*kh = k + (h / group) * hk, *vh = v + (h / group) * hk;",
+                           "*kh = k + (h % group) * hk, *vh = v + (h % group) * hk;"),
     "gqa_group_sum_first_head_only": ("for (int g = 0; g < group; ++g) {",
                                       "for (int g = 0; g < 1; ++g) {"),
-    "gqa_interleaved_grouping": ("const int h = hk * group + g;", "const int h = g * BHkv + hk;"),
+    "gqa_interleaved_grouping": ("const int h = kv * group + g;", "const int h = g * BHkv + kv;"),
+    # query and key lengths that differ
+    "cross_causal_offset_dropped": ("return !causal || j <= i + off;", "return !causal || j <= i;"),
+    "cross_causal_offset_sign": ("return !causal || j <= i + off;",
+                                 "return !causal || j <= i - off;"),
+    "cross_offset_top_left": ("off = (long)Nk - Nq;", "off = 0;"),
+    "cross_key_stride_query_len": ("hk = (long)Nk * d,", "hk = (long)Nq * d,"),
+    "cross_key_loop_query_len": ("for (long j = 0; j < Nk; ++j) {\n                if (!visible(causal, off, i, j)) continue;\n                double p",
+                                 "for (long j = 0; j < Nq; ++j) {\n                if (!visible(causal, off, i, j)) continue;\n                double p"),
 }
 
 
