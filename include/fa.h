@@ -19,13 +19,14 @@
  *   - Tensors q, k, v, o, dO, dq, dk, dv are DEVICE pointers to contiguous
  *     bf16 arrays of shape [B][H][N][d] (d innermost).  lse is a device
  *     pointer to fp32 [B][H][N].  Every pointer must be 16-byte aligned.
- *   - d must be 64 or 128.  N >= 1 is any length (the last tile is masked).
- *     B, H >= 1.  B == 0, H == 0 or N == 0 is an empty problem: FA_OK, no work.
- *     B * H * ceil(N / 128) must be at most 2^27 - 1 (grid limits); larger
- *     problems return FA_ERR_INVALID_ARG.
+ *   - d must be 64 or 128.  N >= 1 is any length up to 2^30 (the last tile
+ *     is masked).  B, H >= 1.  B == 0, H == 0 or N == 0 is an empty problem:
+ *     FA_OK, no work.  B * H * ceil(N / 128) must be at most 2^27 - 1 (grid
+ *     limits); larger problems return FA_ERR_INVALID_ARG.
  *   - scale multiplies Q K^T before the softmax; it must be finite and > 0
  *     (usually 1/sqrt(d)).
- *   - causal = 1: key j is visible to query i iff j <= i (N_q = N_k = N).
+ *   - causal = 1: key j is visible to query i iff j <= i (N_q = N_k = N;
+ *     fa_fwd_ex / fa_bwd_ex below state the rule for N_q != N_k).
  *     causal = 0: every key is visible.
  *   - lse[i] = ln( sum over visible j of exp(scale * q_i . k_j) ).
  *   - The caller owns every buffer, including the backward workspace.  The
@@ -85,6 +86,25 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
                      struct CUstream_st* stream);
 
 /*
+ * General forward: grouped key/value heads and query and key lengths that
+ * differ.  q, o: bf16 [B][H][N_q][d]; k, v: bf16 [B][H_kv][N_k][d]; lse: fp32
+ * [B][H][N_q].  H_kv as in fa_fwd_gqa.  Query row i attends to keys 0 ...
+ * N_k - 1 (causal = 0), or to keys j <= i + (N_k - N_q) (causal = 1: the last
+ * query row is aligned with the last key, as for a block of new queries
+ * appended after N_k - N_q earlier positions; needs N_k >= N_q).
+ *   - N_q == 0 (or B == 0 or H == 0) is an empty problem: FA_OK, no work.
+ *   - N_k == 0 with N_q >= 1, or causal with N_k < N_q, or N_q or N_k
+ *     above 2^30 => FA_ERR_INVALID_ARG.  B * H * ceil(N_q / 128) must be
+ *     at most 2^27 - 1.
+ * fa_fwd_gqa is this with N_q = N_k = N.  Source: Flash Attention,
+ * "Evolution: Flash Attention 2 & 3" (variable sequence lengths; the causal
+ * alignment for N_q != N_k is the library's reading).
+ */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                    struct CUstream_st* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: fp32 row statistics, two per row
  * (-lse log2 e and -D with D = rowsum(dO * o)) with each head padded to whole
  * 128-row tiles, i.e. B*H*ceil(N/128)*256 floats, followed by an fp32 dQ
@@ -123,6 +143,21 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, void* dq, void* dk, void* dv, int B, int H,
                      int H_kv, int N, int d, float scale, int causal, void* workspace,
                      size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * General backward: the counterpart of fa_fwd_ex.  q, o, dO, dq: bf16
+ * [B][H][N_q][d]; k, v, dk, dv: bf16 [B][H_kv][N_k][d]; lse: fp32 [B][H][N_q]
+ * from fa_fwd_ex with the same arguments.  The workspace depends on the
+ * query side only: fa_bwd_workspace_size(B, H, N_q, d) bytes.
+ *   - N_q == 0 with B, H, N_k >= 1: dk and dv are set to zero (sums over no
+ *     query rows) with two cudaMemsetAsync on `stream`; nothing else is read.
+ *   - Other sizes and errors as for fa_fwd_ex.
+ * fa_bwd_gqa is this with N_q = N_k = N.
+ */
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N_q,
+                    int N_k, int d, float scale, int causal, void* workspace,
+                    size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
  * Backward with no workspace argument and no allocation.  The paper has no

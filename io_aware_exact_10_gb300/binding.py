@@ -46,6 +46,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd.restype = i
         L.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_fwd_gqa.restype = i
+        L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        L.fa_fwd_ex.restype = i
         L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         L.fa_bwd_workspace_size.restype = sz
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
@@ -53,6 +55,9 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz,
                                  vp]
         L.fa_bwd_gqa.restype = i
+        L.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz,
+                                vp]
+        L.fa_bwd_ex.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd_noalloc.restype = i
         L.fa_last_device_error.argtypes = [vp]
@@ -120,6 +125,18 @@ def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, stream=None,
     return s
 
 
+def fa_fwd_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, stream=None,
+              check=True) -> int:
+    """fa_fwd_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, stream) -> status:
+    q, o have N_q rows, k, v N_k; causal aligns the last query with the last key."""
+    s = lib().fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                        int(H_kv), int(N_q), int(N_k), int(d), float(scale), int(causal),
+                        _stream(stream))
+    if check:
+        _check(s, "fa_fwd_ex")
+    return s
+
+
 def fa_bwd_workspace_size(B, H, N, d) -> int:
     return int(lib().fa_bwd_workspace_size(int(B), int(H), int(N), int(d)))
 
@@ -147,6 +164,20 @@ def fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N, d, scale, causal,
                          _stream(stream))
     if check:
         _check(s, "fa_bwd_gqa")
+    return s
+
+
+def fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N_q, N_k, d, scale, causal,
+              workspace, workspace_bytes, stream=None, check=True) -> int:
+    """fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N_q, N_k, d, scale, causal,
+    workspace, workspace_bytes, stream) -> status: the counterpart of fa_fwd_ex;
+    the workspace is fa_bwd_workspace_size(B, H, N_q, d) bytes."""
+    s = lib().fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                        _ptr(dk), _ptr(dv), int(B), int(H), int(H_kv), int(N_q), int(N_k),
+                        int(d), float(scale), int(causal), _ptr(workspace),
+                        int(workspace_bytes), _stream(stream))
+    if check:
+        _check(s, "fa_bwd_ex")
     return s
 
 

@@ -115,18 +115,28 @@ bool encode_f32_3d(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Shared validation of sizes and scalars.  *empty is set for a zero-size problem.
-fa_status check_common(int B, int H, int N, int d, float scale, int causal, bool* empty) {
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+constexpr int kMaxRows = 1 << 30;  // per head, query rows and keys
+
+// Shared validation of sizes and scalars.  *empty is set for a problem with
+// no query rows (B, H or Nq zero); nothing is computed for it.
+fa_status check_common(int B, int H, int H_kv, int Nq, int Nk, int d, float scale, int causal,
+                       bool* empty) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || Nq > kMaxRows || Nk > kMaxRows)
+    return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  *empty = (B == 0 || H == 0 || N == 0);
+  *empty = (B == 0 || H == 0 || Nq == 0);
+  if (B > 0 && H > 0 && (H_kv < 1 || H_kv > H || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
   if (*empty) return FA_OK;
+  // every query row needs a key; causal masking aligns the last query with
+  // the last key, so it needs at least as many keys as queries
+  if (Nk == 0 || (causal && Nk < Nq)) return FA_ERR_INVALID_ARG;
   // one-dimensional grids of (query-tile pairs or key tiles) x heads, and
   // the backward preprocess's 16 blocks per 128-row tile
   const long long BH = (long long)B * H;
-  if (BH * ((N + 127) / 128) * 16 > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
+  if (BH * ((Nq + 127) / 128) * 16 > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
+  if (BH * ((Nk + 127) / 128) > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 
@@ -147,11 +157,15 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int H, int H_kv, int N, int d, float scale, int causal,
                      struct CUstream_st* stream) {
+  return fa_fwd_ex(q, k, v, o, lse, B, H, H_kv, N, N, d, scale, causal, stream);
+}
+
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                    struct CUstream_st* stream) {
   bool empty = false;
-  fa_status s = check_common(B, H, N, d, scale, causal, &empty);
-  if (s != FA_OK) return s;
-  if (!empty && (H_kv < 1 || H_kv > H || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
-  if (empty) return s;
+  fa_status s = check_common(B, H, H_kv, N_q, N_k, d, scale, causal, &empty);
+  if (s != FA_OK || empty) return s;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
   DeviceState* dev = nullptr;
@@ -159,14 +173,15 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
   if (!get_encoder()) return FA_ERR_LAUNCH;
   fa::FwdLaunch a;
   const int BH = B * H, BHkv = B * H_kv;
-  if (!encode_bf16_3d(&a.tq, q, BH, N, d) || !encode_bf16_3d(&a.tk, k, BHkv, N, d) ||
-      !encode_bf16_3d(&a.tv, v, BHkv, N, d))
+  if (!encode_bf16_3d(&a.tq, q, BH, N_q, d) || !encode_bf16_3d(&a.tk, k, BHkv, N_k, d) ||
+      !encode_bf16_3d(&a.tv, v, BHkv, N_k, d))
     return FA_ERR_INVALID_ARG;
   a.o = o;
   a.lse = lse;
   a.BH = BH;
   a.group = H / H_kv;
-  a.N = N;
+  a.Nq = N_q;
+  a.Nk = N_k;
   a.d = d;
   a.scale = scale;
   a.causal = causal;
@@ -182,7 +197,7 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   bool empty = false;
-  if (check_common(B, H, N, d, 1.0f, 0, &empty) != FA_OK || empty) return 0;
+  if (check_common(B, H, H, N, N, d, 1.0f, 0, &empty) != FA_OK || empty) return 0;
   const size_t rows = (size_t)B * H * N;
   return round256(stats_floats(B * H, N) * sizeof(float)) + round256(rows * d * sizeof(float));
 }
@@ -199,38 +214,59 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, void* dq, void* dk, void* dv, int B, int H,
                      int H_kv, int N, int d, float scale, int causal, void* workspace,
                      size_t workspace_bytes, struct CUstream_st* stream) {
+  return fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N, N, d, scale, causal, workspace,
+                   workspace_bytes, stream);
+}
+
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N_q,
+                    int N_k, int d, float scale, int causal, void* workspace,
+                    size_t workspace_bytes, struct CUstream_st* stream) {
   bool empty = false;
-  fa_status s = check_common(B, H, N, d, scale, causal, &empty);
+  fa_status s = check_common(B, H, H_kv, N_q, N_k, d, scale, causal, &empty);
   if (s != FA_OK) return s;
-  if (!empty && (H_kv < 1 || H_kv > H || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
-  if (empty) return s;
+  if (empty) {
+    // No query rows: dk and dv are sums over nothing, i.e. zero.
+    if (B == 0 || H == 0 || N_k == 0) return FA_OK;
+    if (!aligned16(dk) || !aligned16(dv)) return FA_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    if ((s = current_device(&dev)) != FA_OK) return s;
+    const size_t bytes = (size_t)B * H_kv * N_k * d * 2;  // bf16 +0.0 is all zero bits
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(dk, 0, bytes, st) != cudaSuccess || cudaMemsetAsync(dv, 0, bytes, st) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
+    return FA_OK;
+  }
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
-      workspace_bytes < fa_bwd_workspace_size(B, H, N, d))
+      workspace_bytes < fa_bwd_workspace_size(B, H, N_q, d))
     return FA_ERR_INVALID_ARG;
   DeviceState* dev = nullptr;
   if ((s = current_device(&dev)) != FA_OK) return s;
   if (!get_encoder()) return FA_ERR_LAUNCH;
   fa::BwdLaunch a;
   const int BH = B * H, BHkv = B * H_kv;
-  if (!encode_bf16_3d(&a.tq, q, BH, N, d) || !encode_bf16_3d(&a.tk, k, BHkv, N, d) ||
-      !encode_bf16_3d(&a.tv, v, BHkv, N, d) || !encode_bf16_3d(&a.tdo, dO, BH, N, d))
+  if (!encode_bf16_3d(&a.tq, q, BH, N_q, d) || !encode_bf16_3d(&a.tk, k, BHkv, N_k, d) ||
+      !encode_bf16_3d(&a.tv, v, BHkv, N_k, d) || !encode_bf16_3d(&a.tdo, dO, BH, N_q, d))
     return FA_ERR_INVALID_ARG;
   a.o = o;
   a.dO = dO;
   a.lse = lse;
   a.stats = static_cast<float*>(workspace);
   a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                      round256(stats_floats(BH, N) * sizeof(float)));
-  if (!encode_f32_3d(&a.tdq, a.dq_acc, BH, N, d)) return FA_ERR_INVALID_ARG;
+                                      round256(stats_floats(BH, N_q) * sizeof(float)));
+  if (!encode_f32_3d(&a.tdq, a.dq_acc, BH, N_q, d)) return FA_ERR_INVALID_ARG;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
   a.BH = BH;
   a.group = H / H_kv;
-  a.N = N;
+  a.Nq = N_q;
+  a.Nk = N_k;
   a.d = d;
   a.scale = scale;
   a.causal = causal;
@@ -336,7 +372,7 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          int H, int N, int d, float scale, int causal,
                          struct CUstream_st* stream) {
   bool empty = false;
-  fa_status s = check_common(B, H, N, d, scale, causal, &empty);
+  fa_status s = check_common(B, H, H, N, N, d, scale, causal, &empty);
   if (s != FA_OK || empty) return s;
   // Problems whose D + dQ accumulator exceed the static array are refused.
   if (fa_bwd_workspace_size(B, H, N, d) > kStaticScratchBytes) return FA_ERR_INVALID_ARG;

@@ -46,7 +46,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---------------------------------------------------------------------------
 // preprocess: for every row q of every head, D = rowsum(dO * O) and the
 // row's statistics for the main kernels, -LSE log2 e and -D (-inf and 0 for
-// the pad rows q >= N of a head's last tile); and dQacc = 0.  Statistics
+// the pad rows q >= N of a head's last tile; N = query rows); and dQacc = 0.  Statistics
 // layout: per head and 128-query tile, 128 values of -LSE log2 e then 128 of
 // -D.  A thread takes 8 elements (16 bytes) of a row, a group of HD / 8
 // lanes one row; blockIdx.x = head * (blocks per tile * nq) + block.
@@ -156,7 +156,9 @@ struct BwdParams {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int N, nq, nkv, BHkv, group;
+  int Nq, Nk;    // query rows and keys per head
+  int nq, nkv, BHkv, group;
+  int coff;      // causal offset Nk - Nq: query i sees keys j <= i + coff
   int kv_group;  // query heads per key/value head (1: multi-head)
   float scale, scale2;
   KernelCtl ctl;
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(448, 1)
   const GridPos gp = decode_grid((int)blockIdx.x, p.BHkv, p.nkv, p.group);
   const int bk = gp.bh;
   const int kt = gp.rank;
-  const int i0 = CAUSAL ? kt : 0;                  // first query tile that sees this key tile
+  const int i0 = CAUSAL ? first_query_tile(kt, p.coff) : 0;  // first query tile that sees this key tile
   const int nit = (p.nq - i0) * p.kv_group;        // query tiles to process
   const TileWalk walk0{i0, bk * p.kv_group};
 
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(448, 1)
     const int cb = 64 * h;                          // first query column of this thread
     const float scale2 = p.scale2;
     const uint64_t sc2 = f2_pack(scale2, scale2);
-    const size_t rowbase = (size_t)bk * p.N;         // key rows (dK, dV)
+    const size_t rowbase = (size_t)bk * p.Nk;        // key rows (dK, dV)
     // warpgroup 0 stages the negated log2-scaled LSE and negated D of the
     // first query tile
     if (h == 0) {
@@ -395,8 +397,12 @@ __global__ void __launch_bounds__(448, 1)
       tmem_ld32(tST + cb, *reinterpret_cast<uint32_t(*)[32]>(pr));
       tmem_ld32(tST + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(pr + 32));
       tmem_wait_ld();
-      // P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query < key
-      const bool diag = CAUSAL && qt == kt;
+      // P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query
+      // qt*128 + q does not see key kt*128 + r, i.e. q < r + (kt - qt)*128 - coff.
+      // The tile needs it when that bound is positive for the last key.
+      const int qdelta = (kt - qt) * C::BK - p.coff;
+      const bool diag = CAUSAL && qdelta > 1 - C::BK;
+      const int rlim = r + qdelta;
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t pk[16];
@@ -416,8 +422,8 @@ __global__ void __launch_bounds__(448, 1)
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(pr[q], pr[q + 1]), sc2, nl2), x0, x1);
           float p0 = ex2(x0), p1 = ex2(x1);
-          if (diag && cb + q < r) p0 = 0.f;
-          if (diag && cb + q + 1 < r) p1 = 0.f;
+          if (diag && cb + q < rlim) p0 = 0.f;
+          if (diag && cb + q + 1 < rlim) p1 = 0.f;
           pk[i] = pack_bf16(p0, p1);
         }
         tmem_st16(tST + cb + c0 / 2, pk);
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(448, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-        if (key < p.N) {
+        if (key < p.Nk) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -511,7 +517,7 @@ __global__ void __launch_bounds__(448, 1)
     const int sp = warp & 3;
     const int r = sp * 32 + lane;  // query row within the tile (dQ) / key row (dK)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
-    const size_t rowbase = (size_t)bk * p.N;         // key rows (dK, dV)
+    const size_t rowbase = (size_t)bk * p.Nk;        // key rows (dK, dV)
     const uint32_t sw = (uint32_t)(lane & 7);
     constexpr int BOXES_PER_SLOT = HD / 64;          // 4 KB boxes in a warp's quarter
     bool ok = true;
@@ -586,7 +592,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
-        if (key < p.N) {
+        if (key < p.Nk) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -614,9 +620,11 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   p.stats = a.stats;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
-  p.N = a.N;
-  p.nq = (a.N + C::BQ - 1) / C::BQ;
-  p.nkv = (a.N + C::BK - 1) / C::BK;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.coff = a.Nk - a.Nq;
+  p.nq = (a.Nq + C::BQ - 1) / C::BQ;
+  p.nkv = (a.Nk + C::BK - 1) / C::BK;
   p.BHkv = a.BH / a.group;
   p.kv_group = a.group;
   p.group = head_group(p.BHkv, p.nkv, a.num_sms);
@@ -630,11 +638,11 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
 
 template <int HD>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
-  const long rows = (long)a.BH * a.N;
-  const int nq = (a.N + 127) / 128;
+  const long rows = (long)a.BH * a.Nq;
+  const int nq = (a.Nq + 127) / 128;
   fa_bwd_pre_kernel<HD><<<(unsigned)((long)a.BH * nq * (128 / (256 / (HD / 8)))), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.stats,
-      a.dq_acc, a.N, nq);
+      a.dq_acc, a.Nq, nq);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if constexpr (HD == 64)

@@ -99,7 +99,9 @@ struct BwdParams64 {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int N, nq, nkv, BHkv, group;
+  int Nq, Nk;    // query rows and keys per head
+  int nq, nkv, BHkv, group;
+  int coff;      // causal offset Nk - Nq: query i sees keys j <= i + coff
   int kv_group;  // query heads per key/value head (1: multi-head)
   float scale, scale2;
   KernelCtl ctl;
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   const GridPos gp = decode_grid((int)blockIdx.x, p.BHkv, p.nkv, p.group);
   const int bk = gp.bh;
   const int kt = gp.rank;
-  const int i0 = CAUSAL ? kt : 0;                  // first query tile that sees this key tile
+  const int i0 = CAUSAL ? first_query_tile(kt, p.coff) : 0;  // first query tile that sees this key tile
   const int nit = (p.nq - i0) * p.kv_group;        // query tiles to process
   const TileWalk walk0{i0, bk * p.kv_group};
 
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int cb = CW * g;                          // first query column of this thread
     const uint32_t tST = tmem + lane_off + C::COL_ST + cb, tDPT = tmem + lane_off + C::COL_DPT + cb;
     const uint64_t sc2 = f2_pack(p.scale2, p.scale2);
-    const size_t rowbase = (size_t)bk * p.N;         // key rows (dK, dV)
+    const size_t rowbase = (size_t)bk * p.Nk;        // key rows (dK, dV)
     // statistics of the tile in Q slot s: 128 x -LSE log2 e, 128 x -D,
     // loaded with the Q tile (same barrier)
     const float* stats = reinterpret_cast<const float*>(smem + C::OFF_STATS);
@@ -366,7 +368,12 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < CW; c += 32) tmem_ld32(tST + c, *reinterpret_cast<uint32_t(*)[32]>(pr + c));
         tmem_wait_ld();
-        const bool diag = CAUSAL && qt == kt;
+        // causal: zero where query qt*128 + q does not see key kt*128 + r,
+        // i.e. q < r + (kt - qt)*128 - coff; the tile needs it when that
+        // bound is positive for the last key
+        const int qdelta = (kt - qt) * C::BK - p.coff;
+        const bool diag = CAUSAL && qdelta > 1 - C::BK;
+        const int rlim = r + qdelta;
         // statistics four at a time (one 16-byte broadcast load per two pairs)
         uint64_t nlp[CW / 2];
 #pragma unroll
@@ -382,8 +389,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(pr[q], pr[q + 1]), sc2, nl2), x0, x1);
           float p0 = ex2(x0), p1 = ex2(x1);
-          if (diag && cb + q < r) p0 = 0.f;
-          if (diag && cb + q + 1 < r) p1 = 0.f;
+          if (diag && cb + q < rlim) p0 = 0.f;
+          if (diag && cb + q + 1 < rlim) p1 = 0.f;
           pk[i] = pack_bf16(p0, p1);
         }
       }
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       uint32_t pkv[DVC / 2];
 #pragma unroll
       for (int i = 0; i < DVC / 2; ++i) pkv[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-      if (key < p.N) {
+      if (key < p.Nk) {
         uint4* d4 = reinterpret_cast<uint4*>(p.dv + (rowbase + key) * C::HD + DVC * g);
 #pragma unroll
         for (int i = 0; i < DVC / 8; ++i) d4[i] = make_uint4(pkv[4 * i], pkv[4 * i + 1], pkv[4 * i + 2], pkv[4 * i + 3]);
@@ -463,7 +470,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int sp = warp & 3;
     const int r = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
-    const size_t rowbase = (size_t)bk * p.N;         // key rows (dK, dV)
+    const size_t rowbase = (size_t)bk * p.Nk;        // key rows (dK, dV)
     const uint32_t sw = (uint32_t)(lane & 7);
     const uint32_t stage = s0 + C::OFF_STAGE + (uint32_t)sp * 8192u;
     // First, K and V rows of this warp's key rows into tensor memory (the A
@@ -539,7 +546,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
-        if (key < p.N) {
+        if (key < p.Nk) {
           uint4* d4 = reinterpret_cast<uint4*>(p.dk + (rowbase + key) * C::HD + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -567,9 +574,11 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   p.stats = a.stats;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
-  p.N = a.N;
-  p.nq = (a.N + C::BQ - 1) / C::BQ;
-  p.nkv = (a.N + C::BK - 1) / C::BK;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.coff = a.Nk - a.Nq;
+  p.nq = (a.Nq + C::BQ - 1) / C::BQ;
+  p.nkv = (a.Nk + C::BK - 1) / C::BK;
   p.BHkv = a.BH / a.group;
   p.kv_group = a.group;
   p.group = head_group(p.BHkv, p.nkv, a.num_sms);

@@ -1,7 +1,7 @@
 // fa_fwd.cu -- exact softmax attention forward for sm_103a.
 //
 // Computes O = softmax(scale * Q K^T [causal]) V and the per-row natural-log
-// log-sum-exp, tiled so the N x N score matrix never leaves the SM
+// log-sum-exp, tiled so the Nq x Nk score matrix never leaves the SM
 // (FlashAttention: exact attention made fast by counting memory traffic,
 // "The method"; Flash Attention (ostralyan.com), "Block-Wise Attention
 // Computation" and "Core Flash Attention Algorithm").
@@ -68,8 +68,10 @@ struct FwdCfg {
 struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
-  int N, nq, nkv, npairs, BH, group;
+  int Nq, Nk;    // query rows and keys per head
+  int nq, nkv, npairs, BH, group;
   int kv_group;  // query heads per key/value head (1: multi-head)
+  int coff;      // causal offset Nk - Nq: query i sees keys j <= i + coff
   float scale2;  // scale * log2(e)
   KernelCtl ctl;
 };
@@ -124,7 +126,10 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   int nkv_t[2];
   for (int t = 0; t < 2; ++t) {
     valid[t] = qt0 + t < p.nq;
-    nkv_t[t] = !valid[t] ? 0 : (CAUSAL ? min(qt0 + t + 1, p.nkv) : p.nkv);
+    // causal: up to the tile of the last key its last row sees
+    nkv_t[t] = !valid[t] ? 0
+                         : (CAUSAL ? min(((qt0 + t) * C::BM + C::BM - 1 + p.coff) / C::BN + 1, p.nkv)
+                                   : p.nkv);
   }
   const int nmax = max(nkv_t[0], nkv_t[1]);
 
@@ -348,7 +353,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       const uint32_t tS = tmem + lane_off + C::colS(t);
       const uint32_t tO = tmem + lane_off + C::colO(t);
       const float scale2 = p.scale2;
-      const bool tail = (p.N % C::BN) != 0;
+      const bool tail = (p.Nk % C::BN) != 0;
       const uint32_t xbar = smem_u32(&bar_x[t][sp]);
       int xph = 0;
       // Exchange one value per row with the partner warp (the other column
@@ -379,8 +384,8 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           }
           tc_fence_after();
           int lim = 128;
-          if (CAUSAL && j == qt) lim = r + 1;
-          if (!CAUSAL && tail && j == p.nkv - 1) lim = p.N - j * C::BN;
+          if (CAUSAL) lim = min(lim, row + p.coff + 1 - j * C::BN);
+          if (!CAUSAL && tail && j == p.nkv - 1) lim = p.Nk - j * C::BN;
           // The whole row of S into registers; S_t may then be overwritten.
           float sv[128];
 #pragma unroll
@@ -463,11 +468,13 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           break;
         }
         tc_fence_after();
-        // Keys c >= lim of this row are masked in this tile (causal diagonal,
-        // or the ragged last tile).
+        // Keys c >= lim of this row are masked in this tile (the causal
+        // boundary, key index <= row + coff; or the ragged last tile).  lim
+        // may be <= 0: a tile past the row's last key.  Key 0 is in every
+        // row's first tile, so the running max is finite from there on.
         int lim = 128;
-        if (CAUSAL && j == qt) lim = r + 1;
-        if (!CAUSAL && tail && j == p.nkv - 1) lim = p.N - j * C::BN;
+        if (CAUSAL) lim = min(lim, row + p.coff + 1 - j * C::BN);
+        if (!CAUSAL && tail && j == p.nkv - 1) lim = p.Nk - j * C::BN;
         // Pass 1: max over this thread's columns, 64 at a time (pass 2 reads
         // them again chunk by chunk).
         float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -579,7 +586,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       if (ok && warp_wait(smem_u32(&bar_o[t]), 0, p.ctl, abort, 31)) {
         tc_fence_after();
         const float inv_l = 1.0f / lr;
-        __nv_bfloat16* orow = p.o + ((size_t)bh * p.N + row) * HD;
+        __nv_bfloat16* orow = p.o + ((size_t)bh * p.Nq + row) * HD;
 #pragma unroll 1
         for (int c0 = 0; c0 < C::OCPT; c0 += 32) {
           uint32_t ov[32];
@@ -589,14 +596,14 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
-          if (row < p.N) {
+          if (row < p.Nq) {
             uint4* dst = reinterpret_cast<uint4*>(orow + ob + c0);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
         }
-        if (h == 0 && row < p.N) p.lse[(size_t)bh * p.N + row] = (m + __log2f(l)) * kLn2;
+        if (h == 0 && row < p.Nq) p.lse[(size_t)bh * p.Nq + row] = (m + __log2f(l)) * kLn2;
       }
     }
   }
@@ -620,9 +627,11 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   FwdParams p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
-  p.N = a.N;
-  p.nq = (a.N + C::BM - 1) / C::BM;
-  p.nkv = (a.N + C::BN - 1) / C::BN;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.coff = a.Nk - a.Nq;
+  p.nq = (a.Nq + C::BM - 1) / C::BM;
+  p.nkv = (a.Nk + C::BN - 1) / C::BN;
   p.npairs = (p.nq + 1) / 2;
   p.BH = a.BH;
   p.group = head_group(a.BH, p.npairs, a.num_sms);

@@ -12,11 +12,11 @@ namespace fa {
 
 // Everything a forward launch needs; tensor maps are encoded by the caller.
 struct FwdLaunch {
-  CUtensorMap tq;               // bf16 [BH][N][d], box {64, 128, 1}, 128-byte swizzle
-  CUtensorMap tk, tv;           // bf16 [BH / group][N][d], same box
-  void* o;                      // bf16 [BH][N][d]
-  float* lse;                   // fp32 [BH][N]
-  int BH, N, d;
+  CUtensorMap tq;               // bf16 [BH][Nq][d], box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tk, tv;           // bf16 [BH / group][Nk][d], same box
+  void* o;                      // bf16 [BH][Nq][d]
+  float* lse;                   // fp32 [BH][Nq]
+  int BH, Nq, Nk, d;            // causal requires Nk >= Nq (bottom-right aligned)
   int group;                    // query heads per key/value head (1: multi-head)
   int num_sms;                  // multiprocessors of the device (grid ordering)
   float scale;
@@ -26,25 +26,32 @@ struct FwdLaunch {
 
 // Everything a backward launch needs.
 struct BwdLaunch {
-  CUtensorMap tq, tdo;          // bf16 [BH][N][d], box {64, 128, 1}, 128-byte swizzle
-  CUtensorMap tk, tv;           // bf16 [BH / group][N][d], same box
-  CUtensorMap tdq;              // fp32 dQacc [BH][N][d], box {32, 32, 1}, 128-byte swizzle
-  const void* o;                // bf16 [BH][N][d]
-  const void* dO;               // bf16 [BH][N][d]
-  const float* lse;             // fp32 [BH][N]
+  CUtensorMap tq, tdo;          // bf16 [BH][Nq][d], box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tk, tv;           // bf16 [BH / group][Nk][d], same box
+  CUtensorMap tdq;              // fp32 dQacc [BH][Nq][d], box {32, 32, 1}, 128-byte swizzle
+  const void* o;                // bf16 [BH][Nq][d]
+  const void* dO;               // bf16 [BH][Nq][d]
+  const float* lse;             // fp32 [BH][Nq]
   float* stats;                 // fp32 [BH][nq][2][128] workspace: per 128-query tile,
-                                // -LSE log2 e then -D of its rows (-inf, 0 past N)
-  float* dq_acc;                // fp32 [BH][N][d] workspace
-  void* dq;                     // bf16 [BH][N][d]
-  void* dk;                     // bf16 [BH / group][N][d]
-  void* dv;                     // bf16 [BH / group][N][d]
-  int BH, N, d;
+                                // -LSE log2 e then -D of its rows (-inf, 0 past Nq)
+  float* dq_acc;                // fp32 [BH][Nq][d] workspace
+  void* dq;                     // bf16 [BH][Nq][d]
+  void* dk;                     // bf16 [BH / group][Nk][d]
+  void* dv;                     // bf16 [BH / group][Nk][d]
+  int BH, Nq, Nk, d;            // causal requires Nk >= Nq (bottom-right aligned)
   int group;                    // query heads per key/value head (1: multi-head)
   int num_sms;                  // multiprocessors of the device (grid ordering)
   float scale;
   int causal;
   KernelCtl ctl;
 };
+
+// First query tile whose rows see any key of key tile kt (tiles of 128):
+// query i sees key j iff j <= i + coff, so the tile holding row kt*128 - coff.
+__host__ __device__ inline int first_query_tile(int kt, int coff) {
+  const int r = kt * 128 - coff;
+  return r > 0 ? r / 128 : 0;
+}
 
 // Position in a backward CTA's loop over (query head, query tile): tiles
 // first .. nq-1 of one query head, then of the next head of the group.

@@ -97,3 +97,38 @@ def seeded_heads(B, H, n, seed=0):
     g = np.random.default_rng(seed)
     idx = g.choice(B * H, size=min(n, B * H), replace=False)
     return [(int(i) // H, int(i) % H) for i in sorted(idx)]
+
+
+def gqa_inputs(B, H, H_kv, N, d, seed, N_k=None):
+    """Seeded fp32 N(0,1) draws rounded to bf16: q, k, v, dO in that order
+    (k, v with H_kv heads and N_k rows, N_k = N unless given)."""
+    N_k = N if N_k is None else N_k
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, H, N, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, H_kv, N_k, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H_kv, N_k, d), generator=g).to(torch.bfloat16)
+    dO = torch.randn((B, H, N, d), generator=g).to(torch.bfloat16)
+    return q, k, v, dO
+
+
+def check_groups(q, k, v, dO, out, scale, causal, kv_heads):
+    """Every query head of each listed key/value head (b, hk), and dk, dv of
+    that head, against the oracle run on the group."""
+    H, H_kv = q.shape[1], k.shape[1]
+    G = H // H_kv
+    for b, hk in kv_heads:
+        hs = slice(hk * G, hk * G + G)
+        qg, dOg = f64(q[b, hs]), f64(dO[b, hs])
+        kg, vg = f64(k[b, hk:hk + 1]), f64(v[b, hk:hk + 1])
+        o_ref, lse_ref = oracle.attn_fwd(qg, kg, vg, scale, causal)
+        eo = float(np.abs(f64(out["o"][b, hs]) - o_ref).max())
+        el = float(np.abs(f64(out["lse"][b, hs]) - lse_ref).max())
+        assert eo <= TOL_O, f"O max-abs {eo} at key/value head {(b, hk)}"
+        assert el <= TOL_LSE, f"LSE max-abs {el} at key/value head {(b, hk)}"
+        dq_ref, dk_ref, dv_ref = oracle.attn_bwd(qg, kg, vg, dOg, scale, causal)
+        for g in range(G):
+            e = rel_fro(f64(out["dq"][b, hk * G + g]), dq_ref[g])
+            assert e <= TOL_GRAD, f"dq rel-Frobenius {e} at query head {(b, hk * G + g)}"
+        for name, r in (("dk", dk_ref[0]), ("dv", dv_ref[0])):
+            e = rel_fro(f64(out[name][b, hk]), r)
+            assert e <= TOL_GRAD, f"{name} rel-Frobenius {e} at key/value head {(b, hk)}"

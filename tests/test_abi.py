@@ -26,8 +26,8 @@ def declared_functions():
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    for required in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_workspace_size",
-                     "fa_last_device_error", "fa_strerror"):
+    for required in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_ex", "fa_bwd_ex",
+                     "fa_bwd_workspace_size", "fa_last_device_error", "fa_strerror"):
         assert required in names
 
 
@@ -118,3 +118,29 @@ def test_gqa_argument_errors(L):
         assert b(H, Hkv) != INV, (H, Hkv)
     # an empty problem succeeds whatever H_kv is
     assert f(4, 0, B=0) == fa.FA_OK
+
+
+def test_cross_length_argument_errors(L):
+    """Query and key lengths that differ: causal needs N_k >= N_q; N_k = 0
+    with query rows, negative or oversized lengths are refused; N_q = 0 is
+    an empty problem for the forward, while the backward still owes zero
+    dk, dv (so it goes on to the device)."""
+    import io_aware_exact_10_gb300 as fa
+    INV, OK, NODEV = fa.FA_ERR_INVALID_ARG, fa.FA_OK, fa.FA_ERR_NO_DEVICE
+    sc = ctypes.c_float(0.125)
+    f = lambda Nq, Nk, causal, B=1: L.fa_fwd_ex(A, A, A, A, A, B, 4, 2, Nq, Nk, 64, sc, causal,
+                                                None)
+    b = lambda Nq, Nk, causal, B=1: L.fa_bwd_ex(A, A, A, A, A, A, A, A, A, B, 4, 2, Nq, Nk, 64,
+                                                sc, causal, A, 1 << 30, None)
+    for Nq, Nk, causal in ((256, 128, 1), (2, 1, 1), (5, 0, 0), (5, 0, 1), (-1, 8, 0),
+                           (8, -1, 0), ((1 << 30) + 1, 8, 0), (8, (1 << 30) + 1, 0)):
+        assert f(Nq, Nk, causal) == INV, (Nq, Nk, causal)
+        assert b(Nq, Nk, causal) == INV, (Nq, Nk, causal)
+    for Nq, Nk, causal in ((128, 256, 1), (1, 4096, 1), (300, 7, 0), (7, 300, 0), (64, 64, 1)):
+        assert f(Nq, Nk, causal) == NODEV, (Nq, Nk, causal)
+        assert b(Nq, Nk, causal) == NODEV, (Nq, Nk, causal)
+    assert f(0, 100, 1) == OK and f(0, 0, 0) == OK and f(8, 8, 1, B=0) == OK
+    assert b(0, 0, 0) == OK and b(8, 8, 1, B=0) == OK
+    assert b(0, 100, 1) == NODEV  # zeroes dk, dv on the device
+    assert L.fa_bwd_ex(A, A, A, A, A, A, A, A, None, 1, 4, 2, 0, 100, 64, sc, 0, A, 0,
+                       None) == INV  # ... which must then be valid pointers

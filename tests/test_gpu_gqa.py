@@ -4,49 +4,13 @@ k and v have H_kv heads; query head h attends with key/value head
 h // (H // H_kv), and dk, dv of a key/value head sum over its query heads.
 Tolerances as in parity.py.
 """
-import numpy as np
 import pytest
 import torch
 
 import io_aware_exact_10_gb300 as fa
-import oracle
-from parity import TOL_GRAD, TOL_LSE, TOL_O, f64, rel_fro, run_gpu
+from parity import check_groups, gqa_inputs, run_gpu
 
 pytestmark = pytest.mark.gpu
-
-
-def gqa_inputs(B, H, H_kv, N, d, seed):
-    """Seeded fp32 N(0,1) draws rounded to bf16: q, k, v, dO in that order
-    (k, v with H_kv heads)."""
-    g = torch.Generator().manual_seed(seed)
-    q = torch.randn((B, H, N, d), generator=g).to(torch.bfloat16)
-    k = torch.randn((B, H_kv, N, d), generator=g).to(torch.bfloat16)
-    v = torch.randn((B, H_kv, N, d), generator=g).to(torch.bfloat16)
-    dO = torch.randn((B, H, N, d), generator=g).to(torch.bfloat16)
-    return q, k, v, dO
-
-
-def check_groups(q, k, v, dO, out, scale, causal, kv_heads):
-    """Every query head of each listed key/value head (b, hk), and dk, dv of
-    that head, against the oracle run on the group."""
-    H, H_kv = q.shape[1], k.shape[1]
-    G = H // H_kv
-    for b, hk in kv_heads:
-        hs = slice(hk * G, hk * G + G)
-        qg, dOg = f64(q[b, hs]), f64(dO[b, hs])
-        kg, vg = f64(k[b, hk:hk + 1]), f64(v[b, hk:hk + 1])
-        o_ref, lse_ref = oracle.attn_fwd(qg, kg, vg, scale, causal)
-        eo = float(np.abs(f64(out["o"][b, hs]) - o_ref).max())
-        el = float(np.abs(f64(out["lse"][b, hs]) - lse_ref).max())
-        assert eo <= TOL_O, f"O max-abs {eo} at key/value head {(b, hk)}"
-        assert el <= TOL_LSE, f"LSE max-abs {el} at key/value head {(b, hk)}"
-        dq_ref, dk_ref, dv_ref = oracle.attn_bwd(qg, kg, vg, dOg, scale, causal)
-        for g in range(G):
-            e = rel_fro(f64(out["dq"][b, hk * G + g]), dq_ref[g])
-            assert e <= TOL_GRAD, f"dq rel-Frobenius {e} at query head {(b, hk * G + g)}"
-        for name, r in (("dk", dk_ref[0]), ("dv", dv_ref[0])):
-            e = rel_fro(f64(out[name][b, hk]), r)
-            assert e <= TOL_GRAD, f"{name} rel-Frobenius {e} at key/value head {(b, hk)}"
 
 
 GQA_SHAPES = [
