@@ -133,8 +133,8 @@ def cpu_oracle_sample(w, cpu_inputs, n_heads: int):
     oracle.build()
     G = w.H // w.kv_heads  # query heads per key/value head
     n_heads = max(G, n_heads // G * G)  # whole groups
-    sub = W.Workload(w.name, 1, n_heads, w.N, w.d, causal=w.causal, seed=w.seed)
-    flat = lambda t, n: t.reshape(-1, w.N, w.d)[:n].double().numpy()
+    sub = W.Workload(w.name, 1, n_heads, w.N, w.d, causal=w.causal, seed=w.seed, N_k=w.N_k)
+    flat = lambda t, n: t.reshape(-1, t.shape[-2], w.d)[:n].double().numpy()
     q, k, v, dO = cpu_inputs
     qs, dOs = flat(q, n_heads), flat(dO, n_heads)
     ks, vs = flat(k, n_heads // G), flat(v, n_heads // G)
@@ -164,9 +164,9 @@ def run_reference(args, w):
     q, k, v, dO = W.make_inputs(w)
     G = w.H // w.kv_heads  # query heads per key/value head
     heads_per_step = max(G, heads_per_step // G * G)  # whole groups
-    flat = lambda t: t.reshape(-1, w.N, w.d).double().numpy()
+    flat = lambda t: t.reshape(-1, t.shape[-2], w.d).double().numpy()
     qs, ks, vs, dOs = flat(q), flat(k), flat(v), flat(dO)
-    sub = W.Workload(w.name, 1, heads_per_step, w.N, w.d, causal=w.causal)
+    sub = W.Workload(w.name, 1, heads_per_step, w.N, w.d, causal=w.causal, N_k=w.N_k)
     flops_step = sub.fwd_flops() + sub.bwd_flops()
 
     def step(i):
@@ -204,9 +204,15 @@ def config_of(w):
          "causal": w.causal, "scale": w.scale,
          "l2": "inputs larger than L2 (4 x %.0f MB bf16), no flush" % (w.B * w.H * w.N * w.d * 2 / 1e6),
          "flops": "fwd 4*B*H*N^2*d (x1/2 causal); bwd 2.5x fwd"}
-    if w.kv_heads != w.H:
-        c["H_kv"] = w.kv_heads
-        qb, kb = (w.B * h * w.N * w.d * 2 / 1e6 for h in (w.H, w.kv_heads))
+    if w.kv_heads != w.H or w.kv_len != w.N:
+        if w.kv_heads != w.H:
+            c["H_kv"] = w.kv_heads
+        if w.kv_len != w.N:
+            c["N_k"] = w.kv_len
+            c["flops"] = ("fwd 4*B*H*d*pairs, pairs = N*N_k (causal: N*N_k - N^2/2, the last "
+                          "query aligned with the last key); bwd 2.5x fwd")
+        qb = w.B * w.H * w.N * w.d * 2 / 1e6
+        kb = w.B * w.kv_heads * w.kv_len * w.d * 2 / 1e6
         c["l2"] = ("inputs larger than L2 together (Q, dO %.0f MB, K, V %.0f MB bf16 each: "
                    "%.0f MB), no flush" % (qb, kb, 2 * qb + 2 * kb))
     return c
@@ -229,7 +235,7 @@ def run_ours(args, w):
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
 
-    B, H, Hkv, N, d = w.B, w.H, w.kv_heads, w.N, w.d
+    B, H, Hkv, N, Nk, d = w.B, w.H, w.kv_heads, w.N, w.kv_len, w.d
     cpu_inputs = W.make_inputs(w)
     q, k, v, dO = (t.to(dev) for t in cpu_inputs)
     o = torch.empty_like(q)
@@ -239,13 +245,13 @@ def run_ours(args, w):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     causal = int(w.causal)
 
-    # fa_fwd_gqa / fa_bwd_gqa with H_kv = H are fa_fwd / fa_bwd
+    # fa_fwd_ex / fa_bwd_ex with H_kv = H and N_k = N are fa_fwd / fa_bwd
     def fwd():
-        fa.fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, w.scale, causal, stream)
+        fa.fa_fwd_ex(q, k, v, o, lse, B, H, Hkv, N, Nk, d, w.scale, causal, stream)
 
     def bwd():
-        fa.fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, w.scale, causal, ws,
-                      ws_bytes, stream)
+        fa.fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, Nk, d, w.scale, causal, ws,
+                     ws_bytes, stream)
 
     def barrier():
         if world > 1:

@@ -7,7 +7,8 @@ value produced by the GPU.
 Recipe (the same for every workload): one CPU ``torch.Generator`` seeded with
 ``seed`` draws Q, K, V and dO, in that order, as fp32 N(0, 1) tensors of shape
 [B, H, N, d] (K and V with ``H_kv`` heads when the workload groups key/value
-heads); Q and K are multiplied by ``qk_std``; when ``boost_every`` is set,
+heads, and ``N_k`` rows when the keys outnumber or undercount the queries);
+Q and K are multiplied by ``qk_std``; when ``boost_every`` is set,
 key rows j with (j + 1) % boost_every == 0 (the 97th, 194th, ... row of each
 head, counting from one) are multiplied by ``boost``; then every tensor is
 rounded to bf16 (round to nearest even).  The default scale is 1/sqrt(d).
@@ -33,19 +34,25 @@ class Workload:
     boost: float = 1.0
     seed: int = 0
     H_kv: int = 0  # key/value heads (0: one per query head)
+    N_k: int = 0   # keys per head (0: N, as many as query rows)
 
     @property
     def kv_heads(self) -> int:
         return self.H_kv or self.H
 
     @property
+    def kv_len(self) -> int:
+        return self.N_k or self.N
+
+    @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.d)
 
     def fwd_flops(self) -> float:
-        """4*B*H*N^2*d, halved when causal (two N^2 d contractions, 2 flop/MAC)."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.d
-        return f / 2 if self.causal else f
+        """Two contractions over the (query, key) pairs, 2 flop/MAC: 4*B*H*N*N_k*d,
+        with N*N_k - N^2/2 pairs when causal (N^2/2 for N_k = N)."""
+        pairs = self.N * self.kv_len - (self.N * self.N / 2 if self.causal else 0)
+        return 4.0 * self.B * self.H * pairs * self.d
 
     def bwd_flops(self) -> float:
         """Five N^2 d contractions in the backward: 2.5x the forward."""
@@ -65,6 +72,10 @@ STRESS = Workload("stress_B8_H16_N4096_d128", 8, 16, 4096, 128, causal=False,
 # grouped-query attention of current decoder models: 32 query heads on 8
 # key/value heads
 GQA_CAUSAL = Workload("gqa_B2_H32_Hkv8_N4096_d128_causal", 2, 32, 4096, 128, causal=True, H_kv=8)
+# a prefill chunk: 1024 new queries after 7168 earlier positions (8192 keys),
+# grouped heads as above
+PREFILL_CHUNK = Workload("prefill_B4_H32_Hkv8_Nq1024_Nk8192_d128_causal", 4, 32, 1024, 128,
+                         causal=True, H_kv=8, N_k=8192)
 
 SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384, 32768)
 SWEEP_D = (64, 128)
@@ -77,18 +88,19 @@ def sweep(N: int, d: int, causal: bool = True) -> Workload:
 
 
 def make_inputs(w: Workload, device: str = "cpu", with_grad: bool = True):
-    """Draw (q, k, v, dO) as bf16 [B, H, N, d] tensors following the recipe."""
+    """Draw (q, k, v, dO) as bf16 [B, H, N, d] tensors following the recipe
+    (k, v: [B, H_kv, N_k, d])."""
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed)
     out = []
     names = ("q", "k", "v", "dO") if with_grad else ("q", "k", "v")
     for name in names:
-        heads = w.kv_heads if name in ("k", "v") else w.H
-        t = torch.randn((w.B, heads, w.N, w.d), generator=g, dtype=torch.float32)
+        heads, rows_n = (w.kv_heads, w.kv_len) if name in ("k", "v") else (w.H, w.N)
+        t = torch.randn((w.B, heads, rows_n, w.d), generator=g, dtype=torch.float32)
         if name in ("q", "k") and w.qk_std != 1.0:
             t.mul_(w.qk_std)
         if name == "k" and w.boost_every:
-            rows = torch.arange(w.N)
+            rows = torch.arange(rows_n)
             sel = ((rows + 1) % w.boost_every) == 0
             t[:, :, sel, :] *= w.boost
         out.append(t.to(torch.bfloat16).to(device))
@@ -96,12 +108,13 @@ def make_inputs(w: Workload, device: str = "cpu", with_grad: bool = True):
 
 
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD, GPT2_MEDIUM, GPT2_MEDIUM_CAUSAL, LONG_CAUSAL,
-                                  STRESS_CAUSAL, STRESS, GQA_CAUSAL)}
+                                  STRESS_CAUSAL, STRESS, GQA_CAUSAL, PREFILL_CHUNK)}
 WORKLOADS.update({sweep(N, d).name: sweep(N, d) for N in SWEEP_N for d in SWEEP_D})
 # short aliases
 WORKLOADS.update({"gpt2_medium": GPT2_MEDIUM, "gpt2_medium_causal": GPT2_MEDIUM_CAUSAL,
                   "long_causal": LONG_CAUSAL, "stress": STRESS, "stress_causal": STRESS_CAUSAL,
-                  "single_head": SINGLE_HEAD, "gqa_causal": GQA_CAUSAL})
+                  "single_head": SINGLE_HEAD, "gqa_causal": GQA_CAUSAL,
+                  "prefill_chunk": PREFILL_CHUNK})
 
 
 def make_inputs_on_device(w: Workload, device, with_grad: bool = True):
@@ -112,12 +125,13 @@ def make_inputs_on_device(w: Workload, device, with_grad: bool = True):
     g.manual_seed(w.seed)
     out = []
     for name in (("q", "k", "v", "dO") if with_grad else ("q", "k", "v")):
-        heads = w.kv_heads if name in ("k", "v") else w.H
-        t = torch.randn((w.B, heads, w.N, w.d), generator=g, dtype=torch.float32, device=device)
+        heads, rows_n = (w.kv_heads, w.kv_len) if name in ("k", "v") else (w.H, w.N)
+        t = torch.randn((w.B, heads, rows_n, w.d), generator=g, dtype=torch.float32,
+                        device=device)
         if name in ("q", "k") and w.qk_std != 1.0:
             t.mul_(w.qk_std)
         if name == "k" and w.boost_every:
-            rows = torch.arange(w.N, device=device)
+            rows = torch.arange(rows_n, device=device)
             t[:, :, ((rows + 1) % w.boost_every) == 0, :] *= w.boost
         out.append(t.to(torch.bfloat16))
     return tuple(out)
