@@ -54,6 +54,17 @@
  * visible to query i iff j <= i + (Nk - Nq), which is j <= i when the
  * lengths are equal; it requires Nk >= Nq so that every row sees a key.
  *
+ * Block-sparse attention: the pages name a block-sparse extension of the
+ * method (FlashAttention: exact attention made fast by counting memory
+ * traffic, "The method", Sec 3.3) and list predefined block-sparse patterns
+ * among the sparse variants (Flash Attention, "Sparse Flash Attention"),
+ * without giving their form.  Reading taken: an optional block mask
+ * bm[ceil(Nq/bq)][ceil(Nk/bk)] (row-major, shared by every head) marks which
+ * bq x bk blocks of (query rows, keys) are kept; key j is visible to query i
+ * only if bm[i/bq][j/bk] != 0, on top of the causal rule.  A row that sees
+ * no key at all has an empty sum: l_i = 0, so lse_i = -inf, o_i = 0, and it
+ * contributes nothing to any gradient (dq_i = 0, D_i = 0).
+ *
  * Layout: every tensor is a dense fp64 array [heads][rows][d] (d innermost);
  * q, o, dO, dq have BH heads of Nq rows, k, v, dk, dv BH / G heads of Nk
  * rows; lse and the per-row statistics are [BH][Nq].  BH = B*H independent
@@ -79,9 +90,20 @@ int oracle_num_threads(void) {
 #endif
 }
 
-/* key j is visible to query i: everything when not causal, j <= i + off when
- * causal (off = Nk - Nq >= 0) */
-static int visible(int causal, long off, long i, long j) { return !causal || j <= i + off; }
+/* Which keys a query sees: the causal rule (off = Nk - Nq >= 0) and the
+ * optional block mask (bm == NULL: every block kept). */
+typedef struct {
+    int causal;
+    long off;
+    const unsigned char *bm;
+    int bq, bk, nbk; /* block sizes; blocks per mask row */
+} Mask;
+
+/* key j is visible to query i: j <= i + off when causal, and its block kept */
+static int visible(const Mask *mk, long i, long j) {
+    if (mk->causal && j > i + mk->off) return 0;
+    return !mk->bm || mk->bm[(i / mk->bq) * (long)mk->nbk + j / mk->bk] != 0;
+}
 
 /* s_ij = scale * q_i . k_j (no masking here; callers skip invisible keys) */
 static double score(const double *qi, const double *kj, int d, double scale) {
@@ -91,42 +113,50 @@ static double score(const double *qi, const double *kj, int d, double scale) {
 }
 
 /* Row statistics of the safe softmax of row i: m_i and l_i. */
-static void row_stats(const double *q, const double *k, long i, int Nk, long off, int d,
-                      double scale, int causal, double *m_out, double *l_out) {
+static void row_stats(const double *q, const double *k, long i, int Nk, const Mask *mk, int d,
+                      double scale, double *m_out, double *l_out) {
     const double *qi = q + i * (long)d;
     double m = -INFINITY;
     for (long j = 0; j < Nk; ++j) {
-        if (!visible(causal, off, i, j)) continue;
+        if (!visible(mk, i, j)) continue;
         double s = score(qi, k + j * (long)d, d, scale);
         if (s > m) m = s;
     }
     double l = 0.0;
     for (long j = 0; j < Nk; ++j) {
-        if (!visible(causal, off, i, j)) continue;
+        if (!visible(mk, i, j)) continue;
         l += exp(score(qi, k + j * (long)d, d, scale) - m);
     }
     *m_out = m;
     *l_out = l;
 }
 
+static Mask make_mask(int causal, int Nq, int Nk, const unsigned char *bm, int bq, int bk) {
+    Mask mk = {causal, (long)Nk - Nq, bm, bq, bk, bm ? (Nk + bk - 1) / bk : 0};
+    return mk;
+}
+
 /*
  * Forward: o = softmax(scale Q K^T [masked]) V and lse, per query head.
  * q, o: [BH][Nq][d]; k, v: [BH/G][Nk][d]; lse: [BH][Nq].  G = group >= 1.
+ * bm: block mask [ceil(Nq/bq)][ceil(Nk/bk)] or NULL.
  */
 void oracle_attn_fwd(const double *q, const double *k, const double *v,
                      double *o, double *lse, int BH, int Nq, int Nk, int d,
-                     double scale, int causal, int group) {
-    const long hq = (long)Nq * d, hk = (long)Nk * d, off = (long)Nk - Nq;
+                     double scale, int causal, int group,
+                     const unsigned char *bm, int bq, int bk) {
+    const long hq = (long)Nq * d, hk = (long)Nk * d;
+    const Mask mkv = make_mask(causal, Nq, Nk, bm, bq, bk), *mk = &mkv;
 #pragma omp parallel for collapse(2) schedule(dynamic, 4)
     for (int h = 0; h < BH; ++h) {
         for (int i = 0; i < Nq; ++i) {
             const double *qh = q + h * hq, *kh = k + (h / group) * hk, *vh = v + (h / group) * hk;
             double m, l;
-            row_stats(qh, kh, i, Nk, off, d, scale, causal, &m, &l);
+            row_stats(qh, kh, i, Nk, mk, d, scale, &m, &l);
             double *oi = o + h * hq + (long)i * d;
             for (int c = 0; c < d; ++c) oi[c] = 0.0;
             for (long j = 0; j < Nk; ++j) {
-                if (!visible(causal, off, i, j)) continue;
+                if (!visible(mk, i, j)) continue;
                 double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m) / l;
                 const double *vj = vh + j * d;
                 for (int c = 0; c < d; ++c) oi[c] += p * vj[c];
@@ -141,12 +171,14 @@ void oracle_attn_fwd(const double *q, const double *k, const double *v,
  * q, dO, dq: [BH][Nq][d]; k, v, dk, dv: [BH/G][Nk][d].  Forward quantities
  * are recomputed here from q, k, v (the oracle takes nothing produced by the
  * GPU path).  D_out (may be NULL): [BH][Nq], receives D_i = sum_j p_ij dp_ij.
+ * bm: block mask as for the forward, or NULL.
  */
 void oracle_attn_bwd(const double *q, const double *k, const double *v,
                      const double *dO, double *dq, double *dk, double *dv,
                      double *D_out, int BH, int Nq, int Nk, int d, double scale,
-                     int causal, int group) {
-    const long hq = (long)Nq * d, hk = (long)Nk * d, off = (long)Nk - Nq;
+                     int causal, int group, const unsigned char *bm, int bq, int bk) {
+    const long hq = (long)Nq * d, hk = (long)Nk * d;
+    const Mask mkv = make_mask(causal, Nq, Nk, bm, bq, bk), *mk = &mkv;
     double *m = (double *)malloc(sizeof(double) * (size_t)BH * Nq);
     double *l = (double *)malloc(sizeof(double) * (size_t)BH * Nq);
     double *D = (double *)malloc(sizeof(double) * (size_t)BH * Nq);
@@ -158,11 +190,11 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
             const double *qh = q + h * hq, *kh = k + (h / group) * hk, *vh = v + (h / group) * hk;
             const double *dOi = dO + h * hq + (long)i * d;
             const long r = (long)h * Nq + i;
-            row_stats(qh, kh, i, Nk, off, d, scale, causal, &m[r], &l[r]);
+            row_stats(qh, kh, i, Nk, mk, d, scale, &m[r], &l[r]);
             /* D_i = sum_j p_ij dp_ij */
             double Di = 0.0;
             for (long j = 0; j < Nk; ++j) {
-                if (!visible(causal, off, i, j)) continue;
+                if (!visible(mk, i, j)) continue;
                 double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m[r]) / l[r];
                 double dp = 0.0;
                 for (int c = 0; c < d; ++c) dp += dOi[c] * vh[j * d + c];
@@ -173,7 +205,7 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
             double *dqi = dq + h * hq + (long)i * d;
             for (int c = 0; c < d; ++c) dqi[c] = 0.0;
             for (long j = 0; j < Nk; ++j) {
-                if (!visible(causal, off, i, j)) continue;
+                if (!visible(mk, i, j)) continue;
                 double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m[r]) / l[r];
                 double dp = 0.0;
                 for (int c = 0; c < d; ++c) dp += dOi[c] * vh[j * d + c];
@@ -198,7 +230,7 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
                 const int h = kv * group + g;
                 const double *qh = q + h * hq, *dOh = dO + h * hq;
                 for (long i = 0; i < Nq; ++i) {
-                    if (!visible(causal, off, i, j)) continue;
+                    if (!visible(mk, i, j)) continue;
                     const long r = (long)h * Nq + i;
                     double p = exp(score(qh + i * d, kh + (long)j * d, d, scale) - m[r]) / l[r];
                     double dp = 0.0;
@@ -229,16 +261,16 @@ void oracle_attn_bwd(const double *q, const double *k, const double *v,
 void oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
                           const int *rows, int R, double *o, double *lse,
                           int Nq, int Nk, int d, double scale, int causal) {
-    const long off = (long)Nk - Nq;
+    const Mask mkv = make_mask(causal, Nq, Nk, NULL, 1, 1), *mk = &mkv;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int t = 0; t < R; ++t) {
         const long i = rows[t];
         double m, l;
-        row_stats(q, k, i, Nk, off, d, scale, causal, &m, &l);
+        row_stats(q, k, i, Nk, mk, d, scale, &m, &l);
         double *oi = o + (long)t * d;
         for (int c = 0; c < d; ++c) oi[c] = 0.0;
         for (long j = 0; j < Nk; ++j) {
-            if (!visible(causal, off, i, j)) continue;
+            if (!visible(mk, i, j)) continue;
             double p = exp(score(q + i * d, k + j * d, d, scale) - m) / l;
             for (int c = 0; c < d; ++c) oi[c] += p * v[j * d + c];
         }

@@ -4,7 +4,9 @@ Test infrastructure only: see the package docstring.  Arrays are numpy fp64,
 shaped [..., rows, d] (flattened to heads): q, o, dO, dq have Nq rows, k, v,
 dk, dv Nk rows; lse is [..., Nq].  With causal masking and Nq != Nk the last
 query row is aligned with the last key (key j visible to query i iff
-j <= i + Nk - Nq), which needs Nk >= Nq.
+j <= i + Nk - Nq), which needs Nk >= Nq.  An optional block mask
+[ceil(Nq/bq), ceil(Nk/bk)] (nonzero = kept, shared by every head) hides the
+keys of the blocks it zeroes; a row left with no key gets o = 0, lse = -inf.
 """
 from __future__ import annotations
 
@@ -65,6 +67,20 @@ def _kv_rows(Nq: int, kh: np.ndarray, vh: np.ndarray, d: int, causal: bool) -> i
     return Nk
 
 
+def _block_mask(block_mask, block, Nq: int, Nk: int):
+    """(pointer, bq, bk, keep-alive array) for the C call; NULL when no mask."""
+    if block_mask is None:
+        return None, 1, 1, None
+    bq, bk = (int(x) for x in block)
+    if bq < 1 or bk < 1:
+        raise ValueError(f"block sizes must be >= 1, got {block}")
+    m = np.ascontiguousarray(np.asarray(block_mask) != 0, dtype=np.uint8)
+    want = (-(-Nq // bq), -(-Nk // bk))
+    if m.shape != want:
+        raise ValueError(f"block mask shape {m.shape} != {want} for Nq={Nq}, Nk={Nk}, block={block}")
+    return m.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)), bq, bk, m
+
+
 def _group(BH: int, BHk: int, BHv: int) -> int:
     """Query heads per key/value head (1 for standard multi-head)."""
     if BHk != BHv or BHk < 1 or BH % BHk != 0:
@@ -80,10 +96,11 @@ class OracleLib:
         dp = ctypes.POINTER(ctypes.c_double)
         ip = ctypes.POINTER(ctypes.c_int)
         ci, cd = ctypes.c_int, ctypes.c_double
-        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, ci, cd, ci, ci]
+        bp = ctypes.POINTER(ctypes.c_ubyte)
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, ci, cd, ci, ci, bp, ci, ci]
         lib.oracle_attn_fwd.restype = None
         lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
-                                        ci, ci, ci, ci, cd, ci, ci]
+                                        ci, ci, ci, ci, cd, ci, ci, bp, ci, ci]
         lib.oracle_attn_bwd.restype = None
         lib.oracle_attn_fwd_rows.argtypes = [dp, dp, dp, ip, ci, dp, dp,
                                              ci, ci, ci, cd, ci]
@@ -95,13 +112,14 @@ class OracleLib:
     def num_threads(self) -> int:
         return int(self._lib.oracle_num_threads())
 
-    def attn_fwd(self, q, k, v, scale: float, causal: bool):
+    def attn_fwd(self, q, k, v, scale: float, causal: bool, block_mask=None, block=(128, 128)):
         """o = softmax(scale * q k^T [causal]) v and lse (natural log), fp64.
 
         q: [..., Nq, d]; k, v: [..., Nk, d] with the same or a dividing
         number of heads (grouped key/value heads: query head h uses key/value
-        head h // G over the flattened head axis).  Returns (o shaped like q,
-        lse shaped [..., Nq] like q's heads).
+        head h // G over the flattened head axis).  block_mask: optional
+        [ceil(Nq/bq), ceil(Nk/bk)] array, block = (bq, bk).  Returns (o
+        shaped like q, lse shaped [..., Nq] like q's heads).
         """
         q, k, v = _f64(q), _f64(k), _f64(v)
         lead = q.shape[:-2]
@@ -111,21 +129,22 @@ class OracleLib:
         Nk = _kv_rows(N, kh, vh, d, causal)
         BH = qh.shape[0]
         group = _group(BH, kh.shape[0], vh.shape[0])
+        bm, bq, bk, _keep = _block_mask(block_mask, block, N, Nk)
         o = np.empty_like(qh)
         lse = np.empty((BH, N), dtype=np.float64)
         self._lib.oracle_attn_fwd(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(o),
                                   _ptr(lse), BH, N, Nk, d, float(scale),
-                                  int(bool(causal)), group)
+                                  int(bool(causal)), group, bm, bq, bk)
         return o.reshape(*lead, N, d), lse.reshape(*lead, N)
 
     def attn_bwd(self, q, k, v, dO, scale: float, causal: bool,
-                 return_D: bool = False):
+                 return_D: bool = False, block_mask=None, block=(128, 128)):
         """Gradients (dq, dk, dv) of L with dL/dO = dO, fp64.
 
         With ``return_D`` also returns D = rowsum(P * dP) shaped [..., Nq].
         k, v may have fewer heads and another length than q (see attn_fwd);
         dk, dv are shaped like k and sum over each key/value head's query
-        heads.
+        heads.  block_mask, block: as for attn_fwd.
         """
         q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
         if dO.shape != q.shape:
@@ -143,9 +162,11 @@ class OracleLib:
         dk = np.empty_like(kh)
         dv = np.empty_like(kh)
         D = np.empty((BH, N), dtype=np.float64)
+        bm, bq, bk, _keep = _block_mask(block_mask, block, N, Nk)
         self._lib.oracle_attn_bwd(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(dOh),
                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(D),
-                                  BH, N, Nk, d, float(scale), int(bool(causal)), group)
+                                  BH, N, Nk, d, float(scale), int(bool(causal)), group,
+                                  bm, bq, bk)
         out = (dq.reshape(*lead, N, d), dk.reshape(*lead_kv, Nk, d),
                dv.reshape(*lead_kv, Nk, d))
         if return_D:
@@ -186,12 +207,12 @@ def num_threads() -> int:
     return default().num_threads()
 
 
-def attn_fwd(q, k, v, scale, causal):
-    return default().attn_fwd(q, k, v, scale, causal)
+def attn_fwd(q, k, v, scale, causal, block_mask=None, block=(128, 128)):
+    return default().attn_fwd(q, k, v, scale, causal, block_mask, block)
 
 
-def attn_bwd(q, k, v, dO, scale, causal, return_D=False):
-    return default().attn_bwd(q, k, v, dO, scale, causal, return_D)
+def attn_bwd(q, k, v, dO, scale, causal, return_D=False, block_mask=None, block=(128, 128)):
+    return default().attn_bwd(q, k, v, dO, scale, causal, return_D, block_mask, block)
 
 
 def attn_fwd_rows(q, k, v, rows, scale, causal):

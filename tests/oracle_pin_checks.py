@@ -468,6 +468,131 @@ def check_cross_finite_differences(orc):
             assert err / max(np.abs(num).max(), 1e-3) < 1e-6, (Nq, Nk, causal, which, err)
 
 
+# ----------------------------------------------------------------------------
+# block-sparse attention (a block mask over (query, key) blocks)
+# ----------------------------------------------------------------------------
+
+def _element_mask(block_mask, bq, bk, Nq, Nk, causal):
+    """Boolean [Nq, Nk] element mask: the block mask expanded by kron with
+    ones(bq, bk), cut to Nq x Nk, and the bottom-right causal rule."""
+    import torch
+    m = torch.from_numpy(np.kron(np.asarray(block_mask, dtype=np.uint8),
+                                 np.ones((bq, bk), dtype=np.uint8))[:Nq, :Nk] != 0)
+    if causal:
+        m &= torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=Nk - Nq)
+    return m
+
+
+def check_block_sparse_torch(orc):
+    """Random block masks against torch in fp64: SDPA with the element mask
+    (kron expansion of the block mask, and the causal rule), forward and
+    autograd, grouped heads, ragged last blocks, blocks taller or wider than
+    they are long.  Every row keeps a key (block column 0 stays on), so the
+    masked softmax is defined everywhere.  The first case has fewer query
+    blocks than key blocks and bq < bk."""
+    import torch
+    import torch.nn.functional as F
+    r = _rng(19)
+    for Nq, Nk, bq, bk, causal in ((10, 29, 4, 8, False), (10, 29, 4, 8, True),
+                                   (21, 21, 8, 4, True), (17, 9, 5, 3, False),
+                                   (1, 40, 1, 7, True), (33, 64, 16, 16, True)):
+        B, H, Hkv, d = 1, 4, 2, 8
+        G = H // Hkv
+        nbq, nbk = -(-Nq // bq), -(-Nk // bk)
+        bm = (r.random((nbq, nbk)) < 0.5).astype(np.uint8)
+        bm[:, 0] = 1
+        q, dO = (r.normal(size=(B, H, Nq, d)) for _ in range(2))
+        k, v = (r.normal(size=(B, Hkv, Nk, d)) for _ in range(2))
+        tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (q, k, v))
+        out = F.scaled_dot_product_attention(
+            tq, torch.repeat_interleave(tk, G, dim=1), torch.repeat_interleave(tv, G, dim=1),
+            attn_mask=_element_mask(bm, bq, bk, Nq, Nk, causal), scale=0.5)
+        out.backward(torch.from_numpy(dO))
+        case = (Nq, Nk, bq, bk, causal)
+        o, _ = orc.attn_fwd(q, k, v, 0.5, causal, block_mask=bm, block=(bq, bk))
+        assert np.allclose(o, out.detach().numpy(), atol=1e-12, rtol=0), case
+        dq, dk, dv = orc.attn_bwd(q, k, v, dO, 0.5, causal, block_mask=bm, block=(bq, bk))
+        assert np.allclose(dq, tq.grad.numpy(), atol=1e-11, rtol=0), case
+        assert np.allclose(dk, tk.grad.numpy(), atol=1e-11, rtol=0), case
+        assert np.allclose(dv, tv.grad.numpy(), atol=1e-11, rtol=0), case
+
+
+def check_block_sparse_empty_rows(orc):
+    """A row that sees no key: o = 0, lse = -inf, dq = 0, D = 0, and dk, dv
+    are those of the same problem without that row.  Unmasked: block row 1
+    of three is all zero (rows 4..7 of 12).  Causal: block (0, 0) off leaves
+    the rows of block row 0 whose visible keys all lie in it empty."""
+    r = _rng(20)
+    Nq, Nk, b, d = 12, 12, 4, 3
+    q, k, v, dO = (r.normal(size=(Nq if i in (0, 3) else Nk, d)) for i in range(4))
+    bm = np.ones((3, 3), dtype=np.uint8)
+    bm[1] = 0
+    o, lse = orc.attn_fwd(q, k, v, 0.6, False, block_mask=bm, block=(b, b))
+    dq, dk, dv, D = orc.attn_bwd(q, k, v, dO, 0.6, False, return_D=True, block_mask=bm,
+                                 block=(b, b))
+    assert np.all(o[4:8] == 0) and np.all(np.isneginf(lse[4:8])) and np.all(np.isfinite(lse[:4]))
+    assert np.all(dq[4:8] == 0) and np.all(D[4:8] == 0)
+    keep = np.r_[0:4, 8:12]
+    o2, lse2 = orc.attn_fwd(q[keep], k, v, 0.6, False)
+    _, dk2, dv2 = orc.attn_bwd(q[keep], k, v, dO[keep], 0.6, False)
+    assert np.allclose(o[keep], o2, atol=1e-14, rtol=0) and np.allclose(lse[keep], lse2, atol=1e-14)
+    assert np.allclose(dk, dk2, atol=1e-13, rtol=0) and np.allclose(dv, dv2, atol=1e-13, rtol=0)
+    # causal, square: rows 0..3 see only keys <= i, all in block (0, 0)
+    bm = np.ones((3, 3), dtype=np.uint8)
+    bm[0, 0] = 0
+    o, lse = orc.attn_fwd(q, k, v, 0.6, True, block_mask=bm, block=(b, b))
+    dq, dk, dv = orc.attn_bwd(q, k, v, dO, 0.6, True, block_mask=bm, block=(b, b))
+    assert np.all(o[:4] == 0) and np.all(np.isneginf(lse[:4])) and np.all(dq[:4] == 0)
+    assert np.all(np.isfinite(lse[4:])) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+
+
+def check_block_diagonal_is_independent(orc):
+    """A block-diagonal mask splits attention into independent problems:
+    query block i attends only to key block i, so every output equals the
+    unmasked oracle run on that pair of blocks alone."""
+    r = _rng(21)
+    for causal in (False, True):
+        b, nb, d = 5, 3, 4
+        N = b * nb
+        q, k, v, dO = (r.normal(size=(2, N, d)) for _ in range(4))
+        bm = np.eye(nb, dtype=np.uint8)
+        o, lse = orc.attn_fwd(q, k, v, 0.8, causal, block_mask=bm, block=(b, b))
+        dq, dk, dv = orc.attn_bwd(q, k, v, dO, 0.8, causal, block_mask=bm, block=(b, b))
+        for i in range(nb):
+            s = slice(i * b, i * b + b)
+            ob, lb = orc.attn_fwd(q[:, s], k[:, s], v[:, s], 0.8, causal)
+            gb = orc.attn_bwd(q[:, s], k[:, s], v[:, s], dO[:, s], 0.8, causal)
+            assert np.allclose(o[:, s], ob, atol=1e-14, rtol=0) and np.allclose(lse[:, s], lb, atol=1e-14)
+            for g, ref in zip((dq, dk, dv), gb):
+                assert np.allclose(g[:, s], ref, atol=1e-13, rtol=0), (causal, i)
+
+
+def check_block_sparse_finite_differences(orc):
+    """Central differences of L = sum(dO * O) w.r.t. every entry of Q, K, V
+    under a block mask agree with the analytic gradients to 1e-6 relative."""
+    r = _rng(22)
+    h = 1e-6
+    for causal in (False, True):
+        Nq, Nk, bq, bk, d = 4, 6, 2, 3, 2
+        bm = np.array([[1, 0], [1, 1]], dtype=np.uint8)
+        q, dO = (r.normal(size=(Nq, d)) for _ in range(2))
+        k, v = (r.normal(size=(Nk, d)) for _ in range(2))
+        g = orc.attn_bwd(q, k, v, dO, 0.9, causal, block_mask=bm, block=(bq, bk))
+        loss = lambda *a: float((orc.attn_fwd(*a, 0.9, causal, block_mask=bm,
+                                               block=(bq, bk))[0] * dO).sum())
+        for which, x in enumerate((q, k, v)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = [q, k, v]; args_p[which] = xp
+                args_m = [q, k, v]; args_m[which] = xm
+                num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            err = np.abs(num - g[which]).max()
+            assert err / max(np.abs(num).max(), 1e-3) < 1e-6, (causal, which, err)
+
+
 FWD_CHECKS = (check_four_scores, check_rows_sum_to_one, check_softmax_of_scores,
               check_identical_keys, check_causal_row0, check_zero_queries,
               check_dominant_key, check_blocked_online_softmax,
@@ -475,4 +600,6 @@ FWD_CHECKS = (check_four_scores, check_rows_sum_to_one, check_softmax_of_scores,
 BWD_CHECKS = (check_finite_differences, check_gradient_invariants, check_torch_autograd)
 GQA_CHECKS = (check_gqa_torch, check_gqa_finite_differences)
 CROSS_CHECKS = (check_cross_torch, check_cross_causal_is_suffix, check_cross_finite_differences)
-ALL_CHECKS = FWD_CHECKS + BWD_CHECKS + GQA_CHECKS + CROSS_CHECKS
+SPARSE_CHECKS = (check_block_sparse_torch, check_block_sparse_empty_rows,
+                 check_block_diagonal_is_independent, check_block_sparse_finite_differences)
+ALL_CHECKS = FWD_CHECKS + BWD_CHECKS + GQA_CHECKS + CROSS_CHECKS + SPARSE_CHECKS

@@ -18,8 +18,10 @@ MUTANTS = {
     "lse_sign": ("lse[(long)h * Nq + i] = m + log(l);", "lse[(long)h * Nq + i] = m - log(l);"),
     "lse_log_dropped": ("lse[(long)h * Nq + i] = m + log(l);", "lse[(long)h * Nq + i] = m + l;"),
     "value_row_index": ("const double *vj = vh + j * d;", "const double *vj = vh + i * d;"),
-    "causal_off_by_one": ("return !causal || j <= i + off;", "return !causal || j < i + off;"),
-    "causal_transposed": ("return !causal || j <= i + off;", "return !causal || j >= i + off;"),
+    "causal_off_by_one": ("if (mk->causal && j > i + mk->off) return 0;",
+                          "if (mk->causal && j >= i + mk->off) return 0;"),
+    "causal_transposed": ("if (mk->causal && j > i + mk->off) return 0;",
+                          "if (mk->causal && j < i + mk->off) return 0;"),
     "normaliser_dropped": (
         "double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m) / l;",
         "double p = exp(score(qh + (long)i * d, kh + j * d, d, scale) - m);"),
@@ -41,13 +43,23 @@ MUTANTS = {
                                       "for (int g = 0; g < 1; ++g) {"),
     "gqa_interleaved_grouping": ("const int h = kv * group + g;", "const int h = g * BHkv + kv;"),
     # query and key lengths that differ
-    "cross_causal_offset_dropped": ("return !causal || j <= i + off;", "return !causal || j <= i;"),
-    "cross_causal_offset_sign": ("return !causal || j <= i + off;",
-                                 "return !causal || j <= i - off;"),
-    "cross_offset_top_left": ("off = (long)Nk - Nq;", "off = 0;"),
-    "cross_key_stride_query_len": ("hk = (long)Nk * d,", "hk = (long)Nq * d,"),
-    "cross_key_loop_query_len": ("for (long j = 0; j < Nk; ++j) {\n                if (!visible(causal, off, i, j)) continue;\n                double p",
-                                 "for (long j = 0; j < Nq; ++j) {\n                if (!visible(causal, off, i, j)) continue;\n                double p"),
+    "cross_causal_offset_dropped": ("if (mk->causal && j > i + mk->off) return 0;",
+                                    "if (mk->causal && j > i) return 0;"),
+    "cross_causal_offset_sign": ("if (mk->causal && j > i + mk->off) return 0;",
+                                 "if (mk->causal && j > i - mk->off) return 0;"),
+    "cross_offset_top_left": ("Mask mk = {causal, (long)Nk - Nq,", "Mask mk = {causal, 0,"),
+    "cross_key_stride_query_len": ("hk = (long)Nk * d;", "hk = (long)Nq * d;"),
+    "cross_key_loop_query_len": ("for (long j = 0; j < Nk; ++j) {\n                if (!visible(mk, i, j)) continue;\n                double p",
+                                 "for (long j = 0; j < Nq; ++j) {\n                if (!visible(mk, i, j)) continue;\n                double p"),
+    # block-sparse masks (the first block-sparse pin keeps these in bounds)
+    "sparse_mask_inverted": ("mk->bm[(i / mk->bq) * (long)mk->nbk + j / mk->bk] != 0;",
+                             "mk->bm[(i / mk->bq) * (long)mk->nbk + j / mk->bk] == 0;"),
+    "sparse_mask_ignored_when_causal": ("return !mk->bm ||", "return mk->causal || !mk->bm ||"),
+    "sparse_row_block_from_key_size": ("mk->bm[(i / mk->bq) *", "mk->bm[(i / mk->bk) *"),
+    "sparse_row_stride_from_queries": ("bm ? (Nk + bk - 1) / bk : 0", "bm ? (Nq + bq - 1) / bq : 0"),
+    "sparse_key_pass_ignores_mask": (
+        "                    if (!visible(mk, i, j)) continue;",
+        "                    if (mk->causal && j > i + mk->off) continue;"),
 }
 
 
