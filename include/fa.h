@@ -160,6 +160,33 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                     size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
+ * Block-sparse attention: fa_fwd_ex and fa_bwd_ex restricted by a block
+ * mask.  block_mask is a DEVICE pointer to ceil(N_q/128) x ceil(N_k/128)
+ * bytes, row-major (row = 128-row block of queries, column = 128-key block),
+ * shared by every batch and head; a nonzero byte keeps the block, zero drops
+ * it: key j is visible to query i only if byte [i/128][j/128] is nonzero,
+ * and, when causal, j <= i + N_k - N_q.  Dropped blocks are neither loaded
+ * nor computed.  A query row that sees no key gets o = 0 and lse = -inf and
+ * contributes nothing to dq, dk or dv; a key that no row sees gets dk = dv = 0.
+ * block_mask == NULL is the dense computation of fa_fwd_ex / fa_bwd_ex.
+ * Both sides of the mask are limited to 4096 blocks (N_q, N_k <= 524288);
+ * larger => FA_ERR_INVALID_ARG.  fa_bwd_sparse needs the o and lse of
+ * fa_fwd_sparse with the same mask, and the workspace of fa_bwd_ex.  Source:
+ * FlashAttention: exact attention made fast by counting memory traffic, "The
+ * method" (the block-sparse extension, Sec 3.3); Flash Attention, "Sparse
+ * Flash Attention" (predefined block-sparse patterns).  The mask's form and
+ * the empty-row convention are the library's reading.
+ */
+fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                        const unsigned char* block_mask, struct CUstream_st* stream);
+fa_status fa_bwd_sparse(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                        int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                        const unsigned char* block_mask, void* workspace,
+                        size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
  * Backward with no workspace argument and no allocation.  The paper has no
  * counterpart; this entry point exists for callers that cannot allocate
  * device memory: plugins inside a host framework that owns all device memory

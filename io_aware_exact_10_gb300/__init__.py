@@ -28,11 +28,13 @@ from .binding import (  # noqa: F401
     fa_bwd_ex,
     fa_bwd_gqa,
     fa_bwd_noalloc,
+    fa_bwd_sparse,
     fa_bwd_workspace_size,
     fa_device_error_word,
     fa_fwd,
     fa_fwd_ex,
     fa_fwd_gqa,
+    fa_fwd_sparse,
     fa_last_device_error,
     fa_set_wait_timeout_ns,
     fa_strerror,
@@ -47,22 +49,38 @@ def _shape(q):
     return tuple(int(x) for x in q.shape)
 
 
-def forward(q, k, v, scale=None, causal=False, stream=None):
+def _mask_arg(block_mask, N_q, N_k, device):
+    """A contiguous device uint8 [ceil(N_q/128), ceil(N_k/128)] copy of block_mask."""
+    import torch
+    want = ((N_q + 127) // 128, (N_k + 127) // 128)
+    if tuple(block_mask.shape) != want:
+        raise ValueError(f"block mask shape {tuple(block_mask.shape)} != {want}")
+    return (block_mask != 0).to(device=device, dtype=torch.uint8).contiguous()
+
+
+def forward(q, k, v, scale=None, causal=False, stream=None, block_mask=None):
     """O, LSE for bf16 [B, H, N_q, d] q and [B, H_kv, N_k, d] k, v CUDA tensors
     (outputs allocated with torch).  H_kv < H: grouped key/value heads;
-    N_k != N_q: causal aligns the last query with the last key."""
+    N_k != N_q: causal aligns the last query with the last key; block_mask:
+    [ceil(N_q/128), ceil(N_k/128)] tensor, nonzero keeps a 128 x 128 block."""
     import torch
     B, H, N, d = _shape(q)
     _, H_kv, N_k, _ = _shape(k)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fwd_ex(q, k, v, o, lse, B, H, H_kv, N, N_k, d, scale, causal, stream)
+    if block_mask is None:
+        fa_fwd_ex(q, k, v, o, lse, B, H, H_kv, N, N_k, d, scale, causal, stream)
+    else:
+        m = _mask_arg(block_mask, N, N_k, q.device)
+        fa_fwd_sparse(q, k, v, o, lse, B, H, H_kv, N, N_k, d, scale, causal, m, stream)
     return o, lse
 
 
-def backward(q, k, v, o, lse, dO, scale=None, causal=False, stream=None, workspace=None):
-    """dQ, dK, dV for the forward that produced (o, lse)."""
+def backward(q, k, v, o, lse, dO, scale=None, causal=False, stream=None, workspace=None,
+             block_mask=None):
+    """dQ, dK, dV for the forward that produced (o, lse) (with the same
+    block_mask, if any)."""
     import torch
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -71,6 +89,12 @@ def backward(q, k, v, o, lse, dO, scale=None, causal=False, stream=None, workspa
     ws_bytes = fa_bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
-    fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N, N_k, d, scale, causal, workspace,
-              workspace.numel() * workspace.element_size(), stream)
+    wsb = workspace.numel() * workspace.element_size()
+    if block_mask is None:
+        fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N, N_k, d, scale, causal, workspace,
+                  wsb, stream)
+    else:
+        m = _mask_arg(block_mask, N, N_k, q.device)
+        fa_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N, N_k, d, scale, causal, m,
+                      workspace, wsb, stream)
     return dq, dk, dv

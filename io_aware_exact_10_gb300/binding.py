@@ -58,6 +58,11 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz,
                                 vp]
         L.fa_bwd_ex.restype = i
+        L.fa_fwd_sparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp]
+        L.fa_fwd_sparse.restype = i
+        L.fa_bwd_sparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i,
+                                    vp, vp, sz, vp]
+        L.fa_bwd_sparse.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd_noalloc.restype = i
         L.fa_last_device_error.argtypes = [vp]
@@ -178,6 +183,31 @@ def fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N_q, N_k, d, scale, c
                         int(workspace_bytes), _stream(stream))
     if check:
         _check(s, "fa_bwd_ex")
+    return s
+
+
+def fa_fwd_sparse(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, block_mask,
+                  stream=None, check=True) -> int:
+    """fa_fwd_sparse(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, block_mask,
+    stream) -> status: block_mask is a device uint8 [ceil(N_q/128), ceil(N_k/128)]."""
+    s = lib().fa_fwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                            int(H_kv), int(N_q), int(N_k), int(d), float(scale), int(causal),
+                            _ptr(block_mask), _stream(stream))
+    if check:
+        _check(s, "fa_fwd_sparse")
+    return s
+
+
+def fa_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N_q, N_k, d, scale, causal,
+                  block_mask, workspace, workspace_bytes, stream=None, check=True) -> int:
+    """fa_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N_q, N_k, d, scale, causal,
+    block_mask, workspace, workspace_bytes, stream) -> status."""
+    s = lib().fa_bwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                            _ptr(dk), _ptr(dv), int(B), int(H), int(H_kv), int(N_q), int(N_k),
+                            int(d), float(scale), int(causal), _ptr(block_mask),
+                            _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if check:
+        _check(s, "fa_bwd_sparse")
     return s
 
 

@@ -141,6 +141,11 @@ fa_status check_common(int B, int H, int H_kv, int Nq, int Nk, int d, float scal
 }
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+// a block mask has at most kMaskMaxTiles tiles per side (the kernels keep a
+// row or column of it as a bitset in shared memory)
+bool mask_fits(int Nq, int Nk) {
+  return (Nq + 127) / 128 <= fa::kMaskMaxTiles && (Nk + 127) / 128 <= fa::kMaskMaxTiles;
+}
 // floats of the backward's row statistics: two per row, each head padded to
 // whole 128-row tiles
 size_t stats_floats(int BH, int N) { return (size_t)BH * (size_t)((N + 127) / 128) * 256; }
@@ -163,9 +168,16 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                     int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
                     struct CUstream_st* stream) {
+  return fa_fwd_sparse(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, nullptr, stream);
+}
+
+fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                        const unsigned char* block_mask, struct CUstream_st* stream) {
   bool empty = false;
   fa_status s = check_common(B, H, H_kv, N_q, N_k, d, scale, causal, &empty);
   if (s != FA_OK || empty) return s;
+  if (block_mask && !mask_fits(N_q, N_k)) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
   DeviceState* dev = nullptr;
@@ -185,6 +197,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
   a.d = d;
   a.scale = scale;
   a.causal = causal;
+  a.bmask = block_mask;
   a.num_sms = dev->num_sms;
   a.ctl.err = dev->err;
   a.ctl.timeout_ns = timeout_ns();
@@ -222,9 +235,19 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                     const void* dO, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N_q,
                     int N_k, int d, float scale, int causal, void* workspace,
                     size_t workspace_bytes, struct CUstream_st* stream) {
+  return fa_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, N_q, N_k, d, scale, causal,
+                       nullptr, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_sparse(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                        int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                        const unsigned char* block_mask, void* workspace,
+                        size_t workspace_bytes, struct CUstream_st* stream) {
   bool empty = false;
   fa_status s = check_common(B, H, H_kv, N_q, N_k, d, scale, causal, &empty);
   if (s != FA_OK) return s;
+  if (!empty && block_mask && !mask_fits(N_q, N_k)) return FA_ERR_INVALID_ARG;
   if (empty) {
     // No query rows: dk and dv are sums over nothing, i.e. zero.
     if (B == 0 || H == 0 || N_k == 0) return FA_OK;
@@ -270,6 +293,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   a.d = d;
   a.scale = scale;
   a.causal = causal;
+  a.bmask = block_mask;
   a.num_sms = dev->num_sms;
   a.ctl.err = dev->err;
   a.ctl.timeout_ns = timeout_ns();

@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (part == 0) {
-    st[0] = valid ? -l * kLog2e : -INFINITY;
+    // -inf also for a row that sees no key (lse = -inf under a block mask)
+    st[0] = valid && l != -INFINITY ? -l * kLog2e : -INFINITY;
     st[128] = valid ? -acc : 0.f;
   }
 }
@@ -139,6 +140,8 @@ struct BwdCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + HD;
 };
+static_assert(BwdCfg<128>::SMEM % 16 == 0 && BwdCfg<128>::SMEM + kMaskWords * 4 + 16 <= 232448,
+              "shared memory budget with a block-mask column");
 
 // barrier indices
 enum : int {
@@ -160,6 +163,7 @@ struct BwdParams {
   int nq, nkv, BHkv, group;
   int coff;      // causal offset Nk - Nq: query i sees keys j <= i + coff
   int kv_group;  // query heads per key/value head (1: multi-head)
+  const uint8_t* bmask;  // block mask [nq][nkv] (block-sparse kernels only)
   float scale, scale2;
   KernelCtl ctl;
 };
@@ -176,7 +180,7 @@ __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, const
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(448, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -207,8 +211,30 @@ __global__ void __launch_bounds__(448, 1)
   const int bk = gp.bh;
   const int kt = gp.rank;
   const int i0 = CAUSAL ? first_query_tile(kt, p.coff) : 0;  // first query tile that sees this key tile
-  const int nit = (p.nq - i0) * p.kv_group;        // query tiles to process
-  const TileWalk walk0{i0, bk * p.kv_group};
+  // Block-sparse: the TMA warp turns this key tile's mask column (query
+  // tiles i0 .. nq-1) into a bitset after the barrier area; with no kept
+  // tile the CTA only zeroes its dK, dV rows.
+  QuerySeq<SPARSE> qseq{reinterpret_cast<const uint32_t*>(smem + C::SMEM), (p.nq + 31) >> 5, i0, p.nq};
+  int nqt = p.nq - i0;  // query tiles per query head
+  if constexpr (SPARSE) {
+    uint32_t* qbits = reinterpret_cast<uint32_t*>(smem + C::SMEM);
+    int* qcount = reinterpret_cast<int*>(smem + C::SMEM + kMaskWords * 4);
+    if (warp == C::W_LOAD) {
+      mask_bits_warp(p.bmask + kt, p.nkv, i0, p.nq, qseq.nw, qbits, lane);
+      __syncwarp();
+      const int n = mask_popc_warp(qbits, qseq.nw, lane);
+      if (lane == 0) *qcount = n;
+    }
+    __syncthreads();
+    nqt = *qcount;
+    if (nqt == 0) {
+      zero_key_tile<HD>(p.dk, p.dv, bk, kt, p.Nk);
+      return;
+    }
+    qseq.first = next_bit(qbits, qseq.nw, -1);
+  }
+  const int nit = nqt * p.kv_group;                // query tiles to process
+  const TileWalk walk0{qseq.first, bk * p.kv_group};
 
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
@@ -222,7 +248,7 @@ __global__ void __launch_bounds__(448, 1)
   TileWalk lw = walk0;  // the TMA thread's position
   auto issue_qdo = [&](int u) {  // moves to the next tile
     const int st = u & 1, qt = lw.qt, zq = lw.qh;
-    lw.next(i0, p.nq);
+    qseq.next(lw);
     mbar_arrive_expect_tx(bar(B_QF0 + st), C::TILE);
     for (int b = 0; b < C::KB; ++b)
       tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, zq);
@@ -276,7 +302,7 @@ __global__ void __launch_bounds__(448, 1)
         mbar_arrive_expect_tx(bar(B_DOF0 + st), C::TILE);
         for (int b = 0; b < C::KB; ++b)
           tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, zq);
-        lw.next(i0, p.nq);
+        qseq.next(lw);
       }
       if (!ok) {
         // Abort: let every copy already issued land before the CTA exits.
@@ -377,7 +403,7 @@ __global__ void __launch_bounds__(448, 1)
     TileWalk w = walk0;
     for (int u = 0; u < nit && ok; ++u) {
       const int qt = w.qt;
-      w.next(i0, p.nq);  // w now names tile u + 1
+      qseq.next(w);  // w now names tile u + 1
       const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
       const float* d_u = d_sh + (u & 1) * C::BQ + cb;
       // next tile's statistics, copied asynchronously so that no warp
@@ -522,7 +548,7 @@ __global__ void __launch_bounds__(448, 1)
     constexpr int BOXES_PER_SLOT = HD / 64;          // 4 KB boxes in a warp's quarter
     bool ok = true;
     TileWalk w = walk0;
-    for (int u = 0; u < nit; ++u, w.next(i0, p.nq)) {
+    for (int u = 0; u < nit; ++u, qseq.next(w)) {
       if (!(ok = warp_wait_b(bar(B_DQF), u & 1, p.ctl, abort, 40))) break;
       tc_fence_after();
       const int st = u & 1;
@@ -610,11 +636,13 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool SPARSE>
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   using C = BwdCfg<HD>;
-  auto kern = fa_bwd_kernel<HD, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  auto kern = fa_bwd_kernel<HD, CAUSAL, SPARSE>;
+  // block-sparse: the mask column's bitset and its count follow the layout
+  const int smem_bytes = C::SMEM + (SPARSE ? kMaskWords * 4 + 16 : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   BwdParams p;
   p.stats = a.stats;
@@ -627,12 +655,13 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   p.nkv = (a.Nk + C::BK - 1) / C::BK;
   p.BHkv = a.BH / a.group;
   p.kv_group = a.group;
+  p.bmask = a.bmask;
   p.group = head_group(p.BHkv, p.nkv, a.num_sms);
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
   dim3 grid((unsigned)((long)p.nkv * p.BHkv));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
+  kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();
 }
 
@@ -648,7 +677,10 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
   if constexpr (HD == 64)
     e = launch_bwd_main_d64(a, stream);
   else
-    e = a.causal ? launch_bwd_main<HD, true>(a, stream) : launch_bwd_main<HD, false>(a, stream);
+    e = a.bmask ? (a.causal ? launch_bwd_main<HD, true, true>(a, stream)
+                            : launch_bwd_main<HD, false, true>(a, stream))
+                : (a.causal ? launch_bwd_main<HD, true, false>(a, stream)
+                            : launch_bwd_main<HD, false, false>(a, stream));
   if (e != cudaSuccess) return e;
   const long n8 = rows * HD / 8;
   fa_bwd_dq_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(

@@ -79,6 +79,8 @@ struct Cfg64 {
   static constexpr uint32_t pcol(int k) { return (uint32_t)((k / (CW / 16)) * CW + (k % (CW / 16)) * 8); }
 };
 static_assert(Cfg64::SMEM <= 232448, "shared memory budget");
+static_assert(Cfg64::SMEM % 16 == 0 && Cfg64::SMEM + kMaskWords * 4 + 16 <= 232448,
+              "shared memory budget with a block-mask column");
 static_assert(Cfg64::QSLOTS >= 2 && Cfg64::QSLOTS <= 3 && Cfg64::DOSLOTS == 2, "ring sizes");
 static_assert(Cfg64::NG == 2 || Cfg64::NG == 4, "32 or 64 query columns per P/dS warp");
 
@@ -103,6 +105,7 @@ struct BwdParams64 {
   int nq, nkv, BHkv, group;
   int coff;      // causal offset Nk - Nq: query i sees keys j <= i + coff
   int kv_group;  // query heads per key/value head (1: multi-head)
+  const uint8_t* bmask;  // block mask [nq][nkv] (block-sparse kernels only)
   float scale, scale2;
   KernelCtl ctl;
 };
@@ -113,7 +116,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const K
   return __all_sync(0xffffffffu, ok);
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     fa_bwd_d64_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -138,8 +141,30 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   const int bk = gp.bh;
   const int kt = gp.rank;
   const int i0 = CAUSAL ? first_query_tile(kt, p.coff) : 0;  // first query tile that sees this key tile
-  const int nit = (p.nq - i0) * p.kv_group;        // query tiles to process
-  const TileWalk walk0{i0, bk * p.kv_group};
+  // Block-sparse: the TMA warp turns this key tile's mask column (query
+  // tiles i0 .. nq-1) into a bitset after the statistics; with no kept tile
+  // the CTA only zeroes its dK, dV rows.
+  QuerySeq<SPARSE> qseq{reinterpret_cast<const uint32_t*>(smem + C::SMEM), (p.nq + 31) >> 5, i0, p.nq};
+  int nqt = p.nq - i0;  // query tiles per query head
+  if constexpr (SPARSE) {
+    uint32_t* qbits = reinterpret_cast<uint32_t*>(smem + C::SMEM);
+    int* qcount = reinterpret_cast<int*>(smem + C::SMEM + kMaskWords * 4);
+    if (warp == C::W_LOAD) {
+      mask_bits_warp(p.bmask + kt, p.nkv, i0, p.nq, qseq.nw, qbits, lane);
+      __syncwarp();
+      const int n = mask_popc_warp(qbits, qseq.nw, lane);
+      if (lane == 0) *qcount = n;
+    }
+    __syncthreads();
+    nqt = *qcount;
+    if (nqt == 0) {
+      zero_key_tile<C::HD>(p.dk, p.dv, bk, kt, p.Nk);
+      return;
+    }
+    qseq.first = next_bit(qbits, qseq.nw, -1);
+  }
+  const int nit = nqt * p.kv_group;                // query tiles to process
+  const TileWalk walk0{qseq.first, bk * p.kv_group};
 
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
@@ -163,7 +188,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     mbar_arrive_expect_tx(bar(B_DOF0 + ds), C::TILE);
     tma_load_3d(sDO + ds * C::TILE, &tdo, bar(B_DOF0 + ds), 0, lw.qt * C::BQ, lw.qh);
     ++ndo_issued;
-    lw.next(i0, p.nq);
+    qseq.next(lw);
   };
   const int pre = nit < C::DOSLOTS ? nit : C::DOSLOTS;   // tiles issued before the sync
   if (warp == C::W_LOAD && lane == 0) {
@@ -347,7 +372,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const uint32_t ds_row = (uint32_t)(cb >> 6) * 16384u + (uint32_t)r * 128u;
     const uint32_t ds_c0 = (uint32_t)((cb & 63) >> 3);
     TileWalk w = walk0;
-    for (int u = 0; u < nit && ok; ++u, w.next(i0, p.nq)) {
+    for (int u = 0; u < nit && ok; ++u, qseq.next(w)) {
       const int qt = w.qt;
       const float* lse_u = stats + qs_u * 256 + cb;
       const float* d_u = lse_u + 128;
@@ -496,7 +521,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       if (lane == 0) mbar_arrive(bar(B_KVT));
     }
     TileWalk w = walk0;
-    for (int u = 0; u < nit && ok; ++u, w.next(i0, p.nq)) {
+    for (int u = 0; u < nit && ok; ++u, qseq.next(w)) {
       if (!(ok = warp_wait(bar(B_DQF), u & 1, p.ctl, abort, 90))) break;
       tc_fence_after();
       uint32_t v[64];
@@ -564,11 +589,13 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   }
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool SPARSE>
 cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   using C = Cfg64;
-  auto kern = fa_bwd_d64_kernel<CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  auto kern = fa_bwd_d64_kernel<CAUSAL, SPARSE>;
+  // block-sparse: the mask column's bitset and its count follow the layout
+  const int smem_bytes = C::SMEM + (SPARSE ? kMaskWords * 4 + 16 : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   BwdParams64 p;
   p.stats = a.stats;
@@ -581,19 +608,21 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   p.nkv = (a.Nk + C::BK - 1) / C::BK;
   p.BHkv = a.BH / a.group;
   p.kv_group = a.group;
+  p.bmask = a.bmask;
   p.group = head_group(p.BHkv, p.nkv, a.num_sms);
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
   dim3 grid((unsigned)((long)p.nkv * p.BHkv));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
+  kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_main_d64(const BwdLaunch& a, cudaStream_t stream) {
-  return a.causal ? launch_t<true>(a, stream) : launch_t<false>(a, stream);
+  if (a.bmask) return a.causal ? launch_t<true, true>(a, stream) : launch_t<false, true>(a, stream);
+  return a.causal ? launch_t<true, false>(a, stream) : launch_t<false, false>(a, stream);
 }
 
 }  // namespace fa

@@ -72,6 +72,7 @@ struct FwdParams {
   int nq, nkv, npairs, BH, group;
   int kv_group;  // query heads per key/value head (1: multi-head)
   int coff;      // causal offset Nk - Nq: query i sees keys j <= i + coff
+  const uint8_t* bmask;  // block mask [nq][nkv] (block-sparse kernels only)
   float scale2;  // scale * log2(e)
   KernelCtl ctl;
 };
@@ -91,7 +92,7 @@ __device__ __forceinline__ uint32_t p_col(int k) {
   return NH == 1 ? (uint32_t)(k * 8) : (uint32_t)(k * 8 + (k >= 4 ? 32 : 0));
 }
 
-template <int HD, bool CAUSAL, int NH>
+template <int HD, bool CAUSAL, int NH, bool SPARSE>
 __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -113,6 +114,10 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   volatile int* abort = &abort_sh;
+  // block-sparse: the key tiles query tile 0 keeps, tile 1 keeps, and their
+  // union (the tiles the pair streams); mcount holds their sizes
+  __shared__ uint32_t mbits[SPARSE ? 3 * kMaskWords : 1];
+  __shared__ int mcount[3];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // One-dimensional grid over (head group, pair rank, head): the CTAs that
@@ -131,7 +136,33 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
                          : (CAUSAL ? min(((qt0 + t) * C::BM + C::BM - 1 + p.coff) / C::BN + 1, p.nkv)
                                    : p.nkv);
   }
-  const int nmax = max(nkv_t[0], nkv_t[1]);
+  // Key tiles each query tile visits (ntile) and the tiles the pair streams
+  // (nu): dense, tiles 0 .. nkv_t-1 and 0 .. max(nkv_t)-1; block-sparse, the
+  // tiles the mask keeps within those bounds, in ascending order.  The TMA
+  // warp builds the bitsets; every other warp reads the counts after the
+  // CTA-wide sync.
+  int ntile[2] = {nkv_t[0], nkv_t[1]};
+  int nu = max(nkv_t[0], nkv_t[1]);
+  const int nw = (p.nkv + 31) >> 5;
+  uint32_t* const ubits = mbits + (SPARSE ? 2 * kMaskWords : 0);
+  if constexpr (SPARSE) {
+    if (warp == C::W_LOAD) {
+      for (int t = 0; t < 2; ++t)
+        mask_bits_warp(p.bmask + (valid[t] ? (size_t)(qt0 + t) * p.nkv : 0), 1, 0,
+                       valid[t] ? nkv_t[t] : 0, nw, mbits + t * kMaskWords, lane);
+      __syncwarp();
+      for (int w = lane; w < nw; w += 32) ubits[w] = mbits[w] | mbits[kMaskWords + w];
+      __syncwarp();
+      ntile[0] = mask_popc_warp(mbits, nw, lane);
+      ntile[1] = mask_popc_warp(mbits + kMaskWords, nw, lane);
+      nu = mask_popc_warp(ubits, nw, lane);
+      if (lane == 0) {
+        mcount[0] = ntile[0];
+        mcount[1] = ntile[1];
+        mcount[2] = nu;
+      }
+    }
+  }
 
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sRing = sQ + 2 * C::QTILE;
@@ -139,17 +170,18 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   // The TMA thread initialises the barriers and issues the copies that need
   // no wait (the Q tiles and the first ring slots) before the CTA-wide sync,
   // so their latency overlaps the rest of the set-up.  Ring index it holds
-  // K_{it/2} (it even) or V_{it/2} (it odd).
-  auto issue_kv = [&](int it) {
-    const int slot = it % C::STAGES, j = it >> 1;
+  // K_j (it even) or V_j (it odd) of the pair's (it/2)-th key tile j.
+  auto issue_kv = [&](int it, int j) {
+    const int slot = it % C::STAGES;
     const uint32_t bar = smem_u32(&bar_full[slot]);
     mbar_arrive_expect_tx(bar, C::KVTILE);
     const uint32_t dst = sRing + slot * C::KVTILE;
     for (int b = 0; b < C::KB; ++b)
       tma_load_3d(dst + b * C::BN * 128, (it & 1) ? &tv : &tk, bar, b * 64, j * C::BN, bhkv);
   };
-  const int n_it = 2 * nmax;                                 // ring uses: K_j, V_j for j < nmax
+  const int n_it = 2 * nu;                                   // ring uses: K, V of each tile
   const int pre_it = n_it < C::STAGES ? n_it : C::STAGES;    // issued before the sync
+  int jw = 0;  // the TMA thread's key tile (of ring index it)
   if (warp == C::W_LOAD && lane == 0) {
     abort_sh = 0;
     for (int t = 0; t < 2; ++t) {
@@ -171,13 +203,17 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
     for (int t = 0; t < 2; ++t) {
-      if (!valid[t]) continue;
+      if (!valid[t] || ntile[t] == 0) continue;
       const uint32_t bar = smem_u32(&bar_q[t]);
       mbar_arrive_expect_tx(bar, C::QTILE);
       for (int b = 0; b < C::KB; ++b)
         tma_load_3d(sQ + t * C::QTILE + b * C::BM * 128, &tq, bar, b * 64, (qt0 + t) * C::BM, bh);
     }
-    for (int it = 0; it < pre_it; ++it) issue_kv(it);
+    if constexpr (SPARSE) jw = next_bit(ubits, nw, -1);
+    for (int it = 0; it < pre_it; ++it) {
+      issue_kv(it, jw);
+      if (it & 1) jw = SPARSE ? next_bit(ubits, nw, jw) : jw + 1;
+    }
   }
   if (warp == C::W_MMA) {
     tmem_alloc(smem_u32(&tmem_base_sh), C::TMEM_COLS);
@@ -187,6 +223,11 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  if constexpr (SPARSE) {
+    ntile[0] = mcount[0];
+    ntile[1] = mcount[1];
+    nu = mcount[2];
+  }
   if (warp == C::W_LOAD) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
@@ -198,14 +239,15 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           ok = false;
           break;
         }
-        issue_kv(it);
+        issue_kv(it, jw);
+        if (it & 1) jw = SPARSE ? next_bit(ubits, nw, jw) : jw + 1;
       }
       if (!ok) {
         // Abort: let the copies already issued land before the CTA exits.
         for (int s = 0; s < C::STAGES && s < it; ++s)
           mbar_wait_quiet(smem_u32(&bar_full[s]), ((it - 1 - s) / C::STAGES) & 1, 200000000ull);
         for (int t = 0; t < 2; ++t)
-          if (valid[t]) mbar_wait_quiet(smem_u32(&bar_q[t]), 0, 200000000ull);
+          if (valid[t] && ntile[t] > 0) mbar_wait_quiet(smem_u32(&bar_q[t]), 0, 200000000ull);
       }
     }
   } else if (warp == C::W_MMA) {
@@ -222,7 +264,22 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       const uint32_t qK = sdesc_lo(sQ, 16), rK = sdesc_lo(sRing, 16), rMN = sdesc_lo(sRing, C::BN * 128);
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
-        if (valid[t]) ok = warp_wait(smem_u32(&bar_q[t]), 0, p.ctl, abort, 20);
+        if (valid[t] && ntile[t] > 0) ok = warp_wait(smem_u32(&bar_q[t]), 0, p.ctl, abort, 20);
+      // Does query tile t use key tile j?  The next key tile of the pair.
+      auto active = [&](int t, int j) -> bool {
+        if constexpr (SPARSE)
+          return ((mbits[t * kMaskWords + (j >> 5)] >> (j & 31)) & 1u) != 0;
+        else
+          return valid[t] && j < nkv_t[t];
+      };
+      auto next_j = [&](int j) -> int {
+        if constexpr (SPARSE)
+          return next_bit(ubits, nw, j);
+        else
+          return j + 1;
+      };
+      // per query tile: S issued, O += P V issued (barrier phases follow them)
+      int cs[2] = {0, 0}, cp[2] = {0, 0};
 
       // S_t = Q_t K^T for the K tile in ring slot `slot`.
       auto issue_s = [&](int t, int slot) {
@@ -244,73 +301,94 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       };
 
       if constexpr (C::SEPP) {
-        // Ring index of K_j is 2j, of V_j 2j + 1.  Per step j:
-        //   [S_t(j) read] S_t(j+1);  [P_t(j) ready] O_t += P_t(j) V_j
-        if (ok) {
+        // The pair's q-th key tile u_q has K at ring index 2q, V at 2q + 1.
+        // Per q, with j = u_q and jn = u_{q+1}:
+        //   [S_t read] S_t(jn);  [P_t ready] O_t += P_t V_j
+        int j = SPARSE ? next_bit(ubits, nw, -1) : 0;
+        if (ok && nu > 0) {
           ok = warp_wait(smem_u32(&bar_full[0]), 0, p.ctl, abort, 21);
           if (ok) {
             tc_fence_after();
             for (int t = 0; t < 2; ++t)
-              if (valid[t]) issue_s(t, 0);
+              if (active(t, j)) {
+                issue_s(t, 0);
+                ++cs[t];
+              }
             mma_commit_e(lead, smem_u32(&bar_empty[0]));
           }
         }
-        for (int j = 0; j < nmax && ok; ++j) {
-          if (j + 1 < nmax) {
-            const int ik = 2 * (j + 1), ks = ik % C::STAGES;
+        for (int q = 0; q < nu && ok; ++q) {
+          const int jn = q + 1 < nu ? next_j(j) : -1;
+          if (q + 1 < nu) {
+            const int ik = 2 * (q + 1), ks = ik % C::STAGES;
             if (!(ok = warp_wait(smem_u32(&bar_full[ks]), (ik / C::STAGES) & 1, p.ctl, abort, 24))) break;
             for (int t = 0; t < 2 && ok; ++t) {
-              if (!valid[t] || j + 1 >= nkv_t[t]) continue;
-              if (!(ok = warp_wait(smem_u32(&bar_sf[t]), j & 1, p.ctl, abort, 26))) break;
+              if (!active(t, jn)) continue;
+              if (cs[t] > 0 && !(ok = warp_wait(smem_u32(&bar_sf[t]), (cs[t] - 1) & 1, p.ctl, abort, 26)))
+                break;
               tc_fence_after();
               issue_s(t, ks);
+              ++cs[t];
             }
             if (!ok) break;
             mma_commit_e(lead, smem_u32(&bar_empty[ks]));
           }
-          const int iv = 2 * j + 1, vs = iv % C::STAGES;
+          const int iv = 2 * q + 1, vs = iv % C::STAGES;
           if (!(ok = warp_wait(smem_u32(&bar_full[vs]), (iv / C::STAGES) & 1, p.ctl, abort, 22))) break;
           for (int t = 0; t < 2 && ok; ++t) {
-            if (!valid[t] || j >= nkv_t[t]) continue;
-            if (!(ok = warp_wait(smem_u32(&bar_p[t]), j & 1, p.ctl, abort, 23))) break;
+            if (!active(t, j)) continue;
+            if (!(ok = warp_wait(smem_u32(&bar_p[t]), cp[t] & 1, p.ctl, abort, 23))) break;
             tc_fence_after();
-            issue_pv(t, vs, j > 0);
+            issue_pv(t, vs, cp[t] > 0);
             mma_commit_e(lead, smem_u32(&bar_pf[t]));
-            if (j == nkv_t[t] - 1) mma_commit_e(lead, smem_u32(&bar_o[t]));
+            if (cp[t] == ntile[t] - 1) mma_commit_e(lead, smem_u32(&bar_o[t]));
+            ++cp[t];
           }
           if (!ok) break;
           mma_commit_e(lead, smem_u32(&bar_empty[vs]));
+          j = jn;
         }
       } else {
+      // Iteration q takes V of the pair's key tile j = u_{q-1}, then K of
+      // jn = u_q.  S_t(jn) overwrites the columns that O_t += P_t V read, so
+      // it is issued after tile t's last O += P V, which comes earlier in
+      // the same iteration or in an earlier one.
       int it = 0;
-      if (ok) {
+      int j = SPARSE ? next_bit(ubits, nw, -1) : 0;
+      if (ok && nu > 0) {
         ok = warp_wait(smem_u32(&bar_full[0]), 0, p.ctl, abort, 21);
         if (ok) {
           tc_fence_after();
           for (int t = 0; t < 2; ++t)
-            if (valid[t]) issue_s(t, 0);
+            if (active(t, j)) {
+              issue_s(t, 0);
+              ++cs[t];
+            }
           mma_commit_e(lead, smem_u32(&bar_empty[0]));
           it = 1;
         }
       }
-      for (int j = 1; j <= nmax && ok; ++j) {
+      for (int q = 1; q <= nu && ok; ++q) {
         const int vslot = it % C::STAGES;
         ok = warp_wait(smem_u32(&bar_full[vslot]), (it / C::STAGES) & 1, p.ctl, abort, 22);
         ++it;
         if (!ok) break;
         tc_fence_after();
-        const bool have_k = j < nmax;
+        const bool have_k = q < nu;
+        const int jn = have_k ? next_j(j) : -1;
         const int kslot = it % C::STAGES, kpar = (it / C::STAGES) & 1;
         if (have_k) ++it;
         bool k_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
-          if (!valid[t] || j - 1 >= nkv_t[t]) continue;
-          ok = warp_wait(smem_u32(&bar_p[t]), (j - 1) & 1, p.ctl, abort, 23);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, vslot, j - 1 > 0);
-          if (j - 1 == nkv_t[t] - 1) mma_commit_e(lead, smem_u32(&bar_o[t]));
-          if (j < nkv_t[t]) {
+          if (active(t, j)) {
+            ok = warp_wait(smem_u32(&bar_p[t]), cp[t] & 1, p.ctl, abort, 23);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, vslot, cp[t] > 0);
+            if (cp[t] == ntile[t] - 1) mma_commit_e(lead, smem_u32(&bar_o[t]));
+            ++cp[t];
+          }
+          if (have_k && active(t, jn)) {
             if (!k_ready) {
               ok = warp_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 24);
               if (!ok) break;
@@ -318,6 +396,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
               k_ready = true;
             }
             issue_s(t, kslot);
+            ++cs[t];
           }
         }
         if (!ok) break;
@@ -329,11 +408,14 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           }
           mma_commit_e(lead, smem_u32(&bar_empty[kslot]));
         }
+        j = jn;
       }
       }
       // Drain: every MMA issued above completes before TMEM is released.
-      mma_commit_e(lead, smem_u32(&bar_drain));
-      mbar_wait_quiet(smem_u32(&bar_drain), 0, 200000000ull);
+      if (nu > 0) {
+        mma_commit_e(lead, smem_u32(&bar_drain));
+        mbar_wait_quiet(smem_u32(&bar_drain), 0, 200000000ull);
+      }
     }
   } else if (warp < C::WS) {
     // -------------------------------------------------------------- softmax
@@ -375,10 +457,17 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       // combined once at the end.
       float m = -INFINITY, l = 0.f, lr = 0.f;
       bool ok = true;
+      // Step `step` of this tile handles key tile j: j = step when dense,
+      // the step-th kept tile when block-sparse.  Under a block mask a row may have
+      // seen no key yet (m = -inf); its exponentials then use 0 in place of
+      // m, which gives P = 0 for masked keys instead of -inf - -inf.
+      const uint32_t* tbits = mbits + t * (SPARSE ? kMaskWords : 0);
+      auto m_ref = [](float mv) { return (SPARSE && mv == -INFINITY) ? 0.f : mv; };
       if constexpr (C::SEPP) {
         const uint32_t tP = tmem + lane_off + C::colP(t);
-        for (int j = 0; j < nkv_t[t]; ++j) {
-          if (!warp_wait(smem_u32(&bar_s[t]), j & 1, p.ctl, abort, 30)) {
+        int j = SPARSE ? next_bit(tbits, nw, -1) : 0;
+        for (int step = 0; step < ntile[t]; ++step) {
+          if (!warp_wait(smem_u32(&bar_s[t]), step & 1, p.ctl, abort, 30)) {
             ok = false;
             break;
           }
@@ -408,8 +497,8 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
           const float m_new = fmaxf(m, mx * scale2);
           const bool need = m_new > m + kTau;
-          // P_t and O_t: PV_t(j-1) must have completed
-          if (j > 0 && !warp_wait(smem_u32(&bar_pf[t]), (j - 1) & 1, p.ctl, abort, 33)) {
+          // P_t and O_t: the previous O_t += P_t V must have completed
+          if (step > 0 && !warp_wait(smem_u32(&bar_pf[t]), (step - 1) & 1, p.ctl, abort, 33)) {
             ok = false;
             break;
           }
@@ -419,7 +508,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
             if (need) m = m_new;
             l *= alpha;
             lr *= alpha;
-            if (j > 0) {
+            if (step > 0) {
 #pragma unroll 1
               for (int c0 = 0; c0 < HD; c0 += 32) {
                 uint32_t ov[32];
@@ -431,11 +520,12 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
               }
             }
           }
+          const float mr = m_ref(m);
           {
-            const float pmax = ex2(fmaf(mx, scale2, -m));
+            const float pmax = ex2(fmaf(mx, scale2, -mr));
             lr += __uint_as_float(pack_bf16(pmax, 0.f) << 16) - pmax;
           }
-          const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-m, -m);
+          const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-mr, -mr);
           uint64_t l2 = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -460,18 +550,24 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bar_p[t]));
+          if constexpr (SPARSE)
+            j = next_bit(tbits, nw, j);
+          else
+            j = step + 1;
         }
       } else {
-      for (int j = 0; j < nkv_t[t]; ++j) {
-        if (!warp_wait(smem_u32(&bar_s[t]), j & 1, p.ctl, abort, 30)) {
+      int j = SPARSE ? next_bit(tbits, nw, -1) : 0;
+      for (int step = 0; step < ntile[t]; ++step) {
+        if (!warp_wait(smem_u32(&bar_s[t]), step & 1, p.ctl, abort, 30)) {
           ok = false;
           break;
         }
         tc_fence_after();
         // Keys c >= lim of this row are masked in this tile (the causal
         // boundary, key index <= row + coff; or the ragged last tile).  lim
-        // may be <= 0: a tile past the row's last key.  Key 0 is in every
-        // row's first tile, so the running max is finite from there on.
+        // may be <= 0: a tile past the row's last key.  Without a block mask
+        // key 0 is in every row's first tile, so the running max is finite
+        // from there on.
         int lim = 128;
         if (CAUSAL) lim = min(lim, row + p.coff + 1 - j * C::BN);
         if (!CAUSAL && tail && j == p.nkv - 1) lim = p.Nk - j * C::BN;
@@ -511,9 +607,10 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           if (need) m = m_new;
           l *= alpha;
           lr *= alpha;
-          if (j > 0) {
-            // O_t is complete here: S_t(j) was issued after PV_t(j-1) and its
-            // commit covers every earlier MMA of the issuing thread.
+          if (step > 0) {
+            // O_t is complete here: S_t of this step was issued after the
+            // previous O_t += P_t V and its commit covers every earlier MMA
+            // of the issuing thread.
 #pragma unroll 1
             for (int c0 = 0; c0 < C::OCPT; c0 += 32) {
               uint32_t ov[32];
@@ -527,15 +624,16 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         }
         // Rounding error of this tile's largest P (mx is the max over this
         // thread's columns, which holds the row's maximum in one half).
+        const float mr = m_ref(m);
         {
-          const float pmax = ex2(fmaf(mxh, scale2, -m));
+          const float pmax = ex2(fmaf(mxh, scale2, -mr));
           lr += __uint_as_float(pack_bf16(pmax, 0.f) << 16) - pmax;
         }
         // Pass 2: P = exp2(scale2 * s - m), two elements per paired FMA and
         // add, 32 columns at a time with the next chunk's load in flight.  P
         // of chunk c lands in columns [cb + c/2, cb + c/2 + 16), all already
         // read by this thread.
-        const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-m, -m);
+        const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-mr, -mr);
         uint64_t l2 = f2_pack(0.f, 0.f);
         float sbuf[2][32];
         tmem_ld32(tS + cb, *reinterpret_cast<uint32_t(*)[32]>(sbuf[0]));
@@ -572,6 +670,10 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_p[t]));
+        if constexpr (SPARSE)
+          j = next_bit(tbits, nw, j);
+        else
+          j = step + 1;
       }
       }
       // Epilogue: O / lr -> bf16, and LSE = ln 2 * (m + log2 l).
@@ -583,9 +685,18 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         l += lo;
         lr += lro;
       }
-      if (ok && warp_wait(smem_u32(&bar_o[t]), 0, p.ctl, abort, 31)) {
+      if (SPARSE && ntile[t] == 0) {
+        // no kept block: every row of the tile sees no key (o = 0, lse = -inf)
+        if (row < p.Nq) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.Nq + row) * HD + ob);
+#pragma unroll
+          for (int i = 0; i < C::OCPT / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (h == 0) p.lse[(size_t)bh * p.Nq + row] = -INFINITY;
+        }
+      } else if (ok && warp_wait(smem_u32(&bar_o[t]), 0, p.ctl, abort, 31)) {
         tc_fence_after();
-        const float inv_l = 1.0f / lr;
+        // a row that saw no key (block-sparse only) has lr = 0 and o = 0
+        const float inv_l = (SPARSE && !(lr > 0.f)) ? 0.f : 1.0f / lr;
         __nv_bfloat16* orow = p.o + ((size_t)bh * p.Nq + row) * HD;
 #pragma unroll 1
         for (int c0 = 0; c0 < C::OCPT; c0 += 32) {
@@ -617,11 +728,11 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   }
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool SPARSE>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   constexpr int NH = kSplit;
   using C = FwdCfg<HD, NH>;
-  auto kern = fa_fwd_kernel<HD, CAUSAL, NH>;
+  auto kern = fa_fwd_kernel<HD, CAUSAL, NH, SPARSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   FwdParams p;
@@ -636,6 +747,7 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   p.BH = a.BH;
   p.group = head_group(a.BH, p.npairs, a.num_sms);
   p.kv_group = a.group;
+  p.bmask = a.bmask;
   p.scale2 = a.scale * 1.4426950408889634f;
   p.ctl = a.ctl;
   dim3 grid((unsigned)((long)p.npairs * a.BH));
@@ -646,8 +758,14 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
-  if (a.d == 128) return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
-  return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+  if (a.bmask) {
+    if (a.d == 128)
+      return a.causal ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, false, true>(a, stream);
+    return a.causal ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);
+  }
+  if (a.d == 128)
+    return a.causal ? launch_fwd_t<128, true, false>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
+  return a.causal ? launch_fwd_t<64, true, false>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
 }
 
 }  // namespace fa

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 
 #include "sm103_ptx.cuh"
 
@@ -21,6 +22,7 @@ struct FwdLaunch {
   int num_sms;                  // multiprocessors of the device (grid ordering)
   float scale;
   int causal;
+  const uint8_t* bmask;         // block mask [ceil(Nq/128)][ceil(Nk/128)], or null (dense)
   KernelCtl ctl;
 };
 
@@ -43,6 +45,7 @@ struct BwdLaunch {
   int num_sms;                  // multiprocessors of the device (grid ordering)
   float scale;
   int causal;
+  const uint8_t* bmask;         // block mask as for the forward, or null (dense)
   KernelCtl ctl;
 };
 
@@ -51,6 +54,55 @@ struct BwdLaunch {
 __host__ __device__ inline int first_query_tile(int kt, int coff) {
   const int r = kt * 128 - coff;
   return r > 0 ? r / 128 : 0;
+}
+
+// Block-sparse attention: a block mask holds one byte per 128 x 128 block of
+// (query rows, keys), row-major [ceil(Nq/128)][ceil(Nk/128)], shared by all
+// heads; nonzero keeps the block.  A CTA turns the rows (forward) or the
+// column (backward) it needs into bitsets in shared memory.
+constexpr int kMaskMaxTiles = 4096;  // tiles per side a block mask may have
+constexpr int kMaskWords = kMaskMaxTiles / 32;
+
+// One warp: bit i of words[i / 32] = (base[i * stride] != 0) for i in
+// [lo, hi), 0 elsewhere, for words 0 .. nw-1.  Eight loads per lane are in
+// flight before the first ballot.
+__device__ __forceinline__ void mask_bits_warp(const uint8_t* __restrict__ base, long stride,
+                                               int lo, int hi, int nw, uint32_t* words, int lane) {
+  for (int w0 = 0; w0 < nw; w0 += 8) {
+    bool b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = (w0 + i) * 32 + lane;
+      b[i] = w0 + i < nw && j >= lo && j < hi && base[(long)j * stride] != 0;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t bits = __ballot_sync(0xffffffffu, b[i]);
+      if (lane == 0 && w0 + i < nw) words[w0 + i] = bits;
+    }
+  }
+}
+
+// One warp: number of set bits in words 0 .. nw-1 (every lane gets it).
+__device__ __forceinline__ int mask_popc_warp(const uint32_t* words, int nw, int lane) {
+  int c = 0;
+  for (int w = lane; w < nw; w += 32) c += __popc(words[w]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  return c;
+}
+
+// Smallest set bit index greater than `after` in words 0 .. nw-1, or -1.
+__device__ __forceinline__ int next_bit(const uint32_t* words, int nw, int after) {
+  const int j = after + 1;
+  int w = j >> 5;
+  if (w >= nw) return -1;
+  uint32_t x = words[w] & (0xffffffffu << (j & 31));
+  while (x == 0) {
+    if (++w >= nw) return -1;
+    x = words[w];
+  }
+  return (w << 5) + __ffs(x) - 1;
 }
 
 // Position in a backward CTA's loop over (query head, query tile): tiles
@@ -64,6 +116,43 @@ struct TileWalk {
     }
   }
 };
+
+// The query tiles a backward CTA visits for its key tile, per query head of
+// the group: first .. nq-1 (dense), or the tiles whose bit is set in the
+// CTA's bitset of its block-mask column (block-sparse; `first` is the lowest).
+template <bool SPARSE>
+struct QuerySeq {
+  const uint32_t* bits;
+  int nw, first, nq;
+  __device__ __forceinline__ void next(TileWalk& w) const {
+    if constexpr (SPARSE) {
+      const int n = next_bit(bits, nw, w.qt);
+      if (n < 0) {
+        w.qt = first;
+        ++w.qh;
+      } else {
+        w.qt = n;
+      }
+    } else {
+      w.next(first, nq);
+    }
+  }
+};
+
+// Zero dK and dV of key rows [kt*128, kt*128 + 128) of key/value head bk
+// (cut at Nk): a key tile that no kept block reaches has zero gradients.
+template <int HD>
+__device__ __forceinline__ void zero_key_tile(__nv_bfloat16* dk, __nv_bfloat16* dv, int bk, int kt,
+                                              int Nk) {
+  const int rows = min(128, Nk - kt * 128);
+  const size_t base = ((size_t)bk * Nk + (size_t)kt * 128) * HD;
+  uint4* zk = reinterpret_cast<uint4*>(dk + base);
+  uint4* zv = reinterpret_cast<uint4*>(dv + base);
+  for (int i = threadIdx.x; i < rows * (HD / 8); i += blockDim.x) {
+    zk[i] = make_uint4(0u, 0u, 0u, 0u);
+    zv[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
 
 // Heads per scheduling group: enough tiles for about two waves of CTAs, so a
 // group's heads stay resident in L2 while its heaviest tiles start first.

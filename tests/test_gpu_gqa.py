@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import io_aware_exact_10_gb300 as fa
-from parity import check_groups, gqa_inputs, run_gpu
+from parity import check_groups, f64, gqa_inputs, rel_fro, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +32,9 @@ def test_gqa_shapes(B, H, H_kv, N, d, causal):
 
 
 def test_gqa_with_all_heads_equals_multi_head():
-    """H_kv = H through fa_fwd_gqa / fa_bwd_gqa gives exactly fa_fwd / fa_bwd."""
+    """H_kv = H through fa_fwd_gqa / fa_bwd_gqa gives fa_fwd / fa_bwd: O, LSE,
+    dK, dV bit for bit; dQ (fp32 reduce-adds from several key-tile CTAs, in
+    run-dependent order) to rounding."""
     B, H, N, d = 1, 3, 384, 64
     q, k, v, dO = gqa_inputs(B, H, H, N, d, seed=5)
     dev = "cuda"
@@ -51,8 +53,11 @@ def test_gqa_with_all_heads_equals_multi_head():
             fa.fa_bwd(qd, kd, vd, o, lse, dOd, dq, dk, dv, B, H, N, d, scale, 1, ws, ws.numel())
         torch.cuda.synchronize()
         res.append([t.cpu() for t in (o, lse, dq, dk, dv)])
-    for a, b in zip(*res):
-        assert torch.equal(a, b)
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), *res):
+        if name == "dq":
+            assert rel_fro(f64(a), f64(b)) <= 1e-3, name
+        else:
+            assert torch.equal(a, b), name
 
 
 def test_gqa_long_causal_sampled():
