@@ -133,14 +133,16 @@ def cpu_oracle_sample(w, cpu_inputs, n_heads: int):
     oracle.build()
     G = w.H // w.kv_heads  # query heads per key/value head
     n_heads = max(G, n_heads // G * G)  # whole groups
-    sub = W.Workload(w.name, 1, n_heads, w.N, w.d, causal=w.causal, seed=w.seed, N_k=w.N_k)
+    sub = W.Workload(w.name, 1, n_heads, w.N, w.d, causal=w.causal, seed=w.seed, N_k=w.N_k,
+                     block_pattern=w.block_pattern)
     flat = lambda t, n: t.reshape(-1, t.shape[-2], w.d)[:n].double().numpy()
     q, k, v, dO = cpu_inputs
     qs, dOs = flat(q, n_heads), flat(dO, n_heads)
     ks, vs = flat(k, n_heads // G), flat(v, n_heads // G)
+    bm = W.block_mask(w) if w.block_pattern else None
     t0 = time.perf_counter()
-    oracle.attn_fwd(qs, ks, vs, w.scale, w.causal)
-    oracle.attn_bwd(qs, ks, vs, dOs, w.scale, w.causal)
+    oracle.attn_fwd(qs, ks, vs, w.scale, w.causal, block_mask=bm)
+    oracle.attn_bwd(qs, ks, vs, dOs, w.scale, w.causal, block_mask=bm)
     dt = time.perf_counter() - t0
     return dt, sub.fwd_flops() + sub.bwd_flops(), oracle.num_threads()
 
@@ -166,14 +168,16 @@ def run_reference(args, w):
     heads_per_step = max(G, heads_per_step // G * G)  # whole groups
     flat = lambda t: t.reshape(-1, t.shape[-2], w.d).double().numpy()
     qs, ks, vs, dOs = flat(q), flat(k), flat(v), flat(dO)
-    sub = W.Workload(w.name, 1, heads_per_step, w.N, w.d, causal=w.causal, N_k=w.N_k)
+    sub = W.Workload(w.name, 1, heads_per_step, w.N, w.d, causal=w.causal, N_k=w.N_k,
+                     seed=w.seed, block_pattern=w.block_pattern)
     flops_step = sub.fwd_flops() + sub.bwd_flops()
+    bm = W.block_mask(w) if w.block_pattern else None
 
     def step(i):
         lo = (i * heads_per_step) % (w.B * w.H)
         sl, sk = slice(lo, lo + heads_per_step), slice(lo // G, (lo + heads_per_step) // G)
-        oracle.attn_fwd(qs[sl], ks[sk], vs[sk], w.scale, w.causal)
-        oracle.attn_bwd(qs[sl], ks[sk], vs[sk], dOs[sl], w.scale, w.causal)
+        oracle.attn_fwd(qs[sl], ks[sk], vs[sk], w.scale, w.causal, block_mask=bm)
+        oracle.attn_bwd(qs[sl], ks[sk], vs[sk], dOs[sl], w.scale, w.causal, block_mask=bm)
 
     for i in range(args.warmup):
         step(i)
@@ -199,11 +203,22 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def block_mask_of(w):
+    from io_aware_exact_10_gb300 import workloads as W
+    return W.block_mask(w)
+
+
 def config_of(w):
     c = {"workload": f"{w.name}, forward+backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
          "causal": w.causal, "scale": w.scale,
          "l2": "inputs larger than L2 (4 x %.0f MB bf16), no flush" % (w.B * w.H * w.N * w.d * 2 / 1e6),
          "flops": "fwd 4*B*H*N^2*d (x1/2 causal); bwd 2.5x fwd"}
+    if w.block_pattern:
+        bm = block_mask_of(w)
+        c["block_pattern"] = w.block_pattern
+        c["blocks_kept"] = round(float(bm.mean()), 4)
+        c["flops"] = ("fwd 4*B*H*d*pairs, pairs = (query, key) pairs inside the kept 128x128 "
+                      "blocks (and the causal rule); bwd 2.5x fwd")
     if w.kv_heads != w.H or w.kv_len != w.N:
         if w.kv_heads != w.H:
             c["H_kv"] = w.kv_heads
@@ -245,13 +260,24 @@ def run_ours(args, w):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     causal = int(w.causal)
 
-    # fa_fwd_ex / fa_bwd_ex with H_kv = H and N_k = N are fa_fwd / fa_bwd
+    # fa_fwd_ex / fa_bwd_ex with H_kv = H and N_k = N are fa_fwd / fa_bwd; a
+    # block-sparse workload goes through fa_fwd_sparse / fa_bwd_sparse with its
+    # mask resident on the device (a fixed part of the configuration)
+    bmask = (torch.from_numpy(W.block_mask(w)).to(dev) if w.block_pattern else None)
+
     def fwd():
-        fa.fa_fwd_ex(q, k, v, o, lse, B, H, Hkv, N, Nk, d, w.scale, causal, stream)
+        if bmask is None:
+            fa.fa_fwd_ex(q, k, v, o, lse, B, H, Hkv, N, Nk, d, w.scale, causal, stream)
+        else:
+            fa.fa_fwd_sparse(q, k, v, o, lse, B, H, Hkv, N, Nk, d, w.scale, causal, bmask, stream)
 
     def bwd():
-        fa.fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, Nk, d, w.scale, causal, ws,
-                     ws_bytes, stream)
+        if bmask is None:
+            fa.fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, Nk, d, w.scale, causal, ws,
+                         ws_bytes, stream)
+        else:
+            fa.fa_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, Nk, d, w.scale, causal,
+                             bmask, ws, ws_bytes, stream)
 
     def barrier():
         if world > 1:

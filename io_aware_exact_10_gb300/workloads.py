@@ -12,13 +12,23 @@ Q and K are multiplied by ``qk_std``; when ``boost_every`` is set,
 key rows j with (j + 1) % boost_every == 0 (the 97th, 194th, ... row of each
 head, counting from one) are multiplied by ``boost``; then every tensor is
 rounded to bf16 (round to nearest even).  The default scale is 1/sqrt(d).
+
+Block-sparse workloads add a block mask over 128 x 128 (query, key) blocks,
+built by ``block_mask`` from the pattern string "localW_globalG_randomP":
+block (i, j) is kept when |i - j| <= W (a local band), or i < G or j < G
+(global blocks that see and are seen by all), or a uniform draw from a
+numpy generator seeded with ``seed`` falls below P (random blocks).
 """
 from __future__ import annotations
 
 import math
+import re
 from dataclasses import dataclass
 
+import numpy as np
 import torch
+
+BLOCK = 128  # rows and keys per block of a block mask
 
 
 @dataclass(frozen=True)
@@ -35,6 +45,7 @@ class Workload:
     seed: int = 0
     H_kv: int = 0  # key/value heads (0: one per query head)
     N_k: int = 0   # keys per head (0: N, as many as query rows)
+    block_pattern: str = ""  # block-sparse pattern (see the module docstring); "" = dense
 
     @property
     def kv_heads(self) -> int:
@@ -50,8 +61,12 @@ class Workload:
 
     def fwd_flops(self) -> float:
         """Two contractions over the (query, key) pairs, 2 flop/MAC: 4*B*H*N*N_k*d,
-        with N*N_k - N^2/2 pairs when causal (N^2/2 for N_k = N)."""
-        pairs = self.N * self.kv_len - (self.N * self.N / 2 if self.causal else 0)
+        with N*N_k - N^2/2 pairs when causal (N^2/2 for N_k = N).  Block-sparse:
+        the exact number of visible pairs in the kept blocks."""
+        if self.block_pattern:
+            pairs = visible_pairs(block_mask(self), self.N, self.kv_len, self.causal)
+        else:
+            pairs = self.N * self.kv_len - (self.N * self.N / 2 if self.causal else 0)
         return 4.0 * self.B * self.H * pairs * self.d
 
     def bwd_flops(self) -> float:
@@ -77,6 +92,11 @@ GQA_CAUSAL = Workload("gqa_B2_H32_Hkv8_N4096_d128_causal", 2, 32, 4096, 128, cau
 PREFILL_CHUNK = Workload("prefill_B4_H32_Hkv8_Nq1024_Nk8192_d128_causal", 4, 32, 1024, 128,
                          causal=True, H_kv=8, N_k=8192)
 
+# block-sparse: local band of 3 blocks each side, one global block row and
+# column, 5 % random blocks (BigBird-like; about 12 % of the blocks kept)
+SPARSE_LOCAL_GLOBAL = Workload("sparse_B4_H16_N16384_d128_local3_global1_random5pct", 4, 16, 16384,
+                               128, causal=False, block_pattern="local3_global1_random0.05")
+
 SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384, 32768)
 SWEEP_D = (64, 128)
 
@@ -85,6 +105,35 @@ def sweep(N: int, d: int, causal: bool = True) -> Workload:
     """Sequence-length sweep point: H=16, B*N = 65536 tokens."""
     return Workload(f"sweep_N{N}_d{d}" + ("_causal" if causal else ""),
                     65536 // N, 16, N, d, causal=causal)
+
+
+def block_mask(w: Workload) -> np.ndarray:
+    """uint8 [ceil(N/128), ceil(N_k/128)] block mask of a block-sparse workload."""
+    m = re.fullmatch(r"local(\d+)_global(\d+)_random([0-9.]+)", w.block_pattern)
+    if not m:
+        raise ValueError(f"unknown block pattern {w.block_pattern!r}")
+    W, G, P = int(m.group(1)), int(m.group(2)), float(m.group(3))
+    nbq, nbk = -(-w.N // BLOCK), -(-w.kv_len // BLOCK)
+    i, j = np.meshgrid(np.arange(nbq), np.arange(nbk), indexing="ij")
+    keep = (np.abs(i - j) <= W) | (i < G) | (j < G)
+    keep |= np.random.default_rng(w.seed).random((nbq, nbk)) < P
+    return keep.astype(np.uint8)
+
+
+def visible_pairs(bm: np.ndarray, Nq: int, Nk: int, causal: bool) -> int:
+    """Number of (query, key) pairs a query sees under the block mask bm and,
+    when causal, the rule key <= query + Nk - Nq."""
+    total = 0
+    off = Nk - Nq
+    for bi, bj in zip(*np.nonzero(bm)):
+        r0, r1 = bi * BLOCK, min((bi + 1) * BLOCK, Nq)
+        c0, c1 = bj * BLOCK, min((bj + 1) * BLOCK, Nk)
+        if not causal:
+            total += (r1 - r0) * (c1 - c0)
+        else:
+            rows = np.arange(r0, r1)
+            total += int(np.clip(rows + off + 1 - c0, 0, c1 - c0).sum())
+    return int(total)
 
 
 def make_inputs(w: Workload, device: str = "cpu", with_grad: bool = True):
@@ -108,13 +157,14 @@ def make_inputs(w: Workload, device: str = "cpu", with_grad: bool = True):
 
 
 WORKLOADS = {w.name: w for w in (SINGLE_HEAD, GPT2_MEDIUM, GPT2_MEDIUM_CAUSAL, LONG_CAUSAL,
-                                  STRESS_CAUSAL, STRESS, GQA_CAUSAL, PREFILL_CHUNK)}
+                                  STRESS_CAUSAL, STRESS, GQA_CAUSAL, PREFILL_CHUNK,
+                                  SPARSE_LOCAL_GLOBAL)}
 WORKLOADS.update({sweep(N, d).name: sweep(N, d) for N in SWEEP_N for d in SWEEP_D})
 # short aliases
 WORKLOADS.update({"gpt2_medium": GPT2_MEDIUM, "gpt2_medium_causal": GPT2_MEDIUM_CAUSAL,
                   "long_causal": LONG_CAUSAL, "stress": STRESS, "stress_causal": STRESS_CAUSAL,
                   "single_head": SINGLE_HEAD, "gqa_causal": GQA_CAUSAL,
-                  "prefill_chunk": PREFILL_CHUNK})
+                  "prefill_chunk": PREFILL_CHUNK, "sparse_local_global": SPARSE_LOCAL_GLOBAL})
 
 
 def make_inputs_on_device(w: Workload, device, with_grad: bool = True):

@@ -1,4 +1,5 @@
 """Host-side checks of the seeded workloads and their FLOP accounting (CPU)."""
+import numpy as np
 import pytest
 import torch
 
@@ -41,3 +42,29 @@ def test_named_workloads():
     p = W.WORKLOADS["prefill_chunk"]
     assert (p.N, p.kv_len, p.H, p.kv_heads, p.d, p.causal) == (1024, 8192, 32, 8, 128, True)
     assert W.WORKLOADS["gqa_causal"].kv_len == 4096
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(300, 300, False), (300, 300, True), (130, 700, True),
+                                          (700, 130, False)])
+def test_visible_pairs_brute_force(Nq, Nk, causal):
+    """The block-sparse pair count equals a count over the expanded element mask."""
+    g = torch.Generator().manual_seed(Nq + Nk)
+    bm = (torch.rand(((Nq + 127) // 128, (Nk + 127) // 128), generator=g) < 0.5).to(torch.uint8)
+    elem = torch.kron(bm, torch.ones(128, 128, dtype=torch.uint8))[:Nq, :Nk].bool()
+    if causal:
+        elem &= torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=Nk - Nq)
+    assert W.visible_pairs(bm.numpy(), Nq, Nk, causal) == int(elem.sum())
+
+
+def test_block_pattern():
+    w = W.Workload("t", 1, 1, 128 * 40 + 5, 64, causal=False, block_pattern="local2_global1_random0.1",
+                   seed=3)
+    m = W.block_mask(w)
+    assert m.shape == (41, 41) and m.dtype.name == "uint8"
+    i, j = np.meshgrid(np.arange(41), np.arange(41), indexing="ij")
+    assert m[np.abs(i - j) <= 2].all() and m[0].all() and m[:, 0].all()
+    off = (np.abs(i - j) > 2) & (i > 0) & (j > 0)
+    assert 0.03 < m[off].mean() < 0.2  # the random blocks
+    assert np.array_equal(m, W.block_mask(w))  # seeded
+    with pytest.raises(ValueError):
+        W.block_mask(W.Workload("t", 1, 1, 128, 64, causal=False, block_pattern="butterfly"))
