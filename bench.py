@@ -45,8 +45,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # launches_gpt2_medium_fwd_bwd.md), and the commit of the kernels it measured.
 # The bench line reports it only while the kernel sources are unchanged.
 NCU_TRAFFIC_BYTES = 2145.5e6
-NCU_TRAFFIC_COMMIT = "10c1d3f"
-NCU_TRAFFIC_SOURCES_SHA256 = "2f3876eea2cc85023c7578b3f6d77e5af5e5fc3ee52ce93749ae6324b2869e0a"
+NCU_TRAFFIC_COMMIT = "e56a2e6"
+NCU_TRAFFIC_SOURCES_SHA256 = "0bb9ee65c292f5239aa1fadeddba584141efca772a2d6cd4cd56d0a6a654139e"
 
 
 def kernel_sources_sha256() -> str:
@@ -467,6 +467,97 @@ def run_sweep(args):
                       "clocks": clk, "sweep": points}), flush=True)
 
 
+def run_compare(args, w):
+    """Standard attention against this library on one workload (the
+    comparison of the paper review's Fig. 2): a forward+backward step of
+    softmax(scale Q K^T) V computed the standard way, with S and P written to
+    and read back from device memory (torch bf16 matmul, softmax and
+    autograd: library kernels, the comparator), and the same step through
+    fa_fwd/fa_bwd.  Prints one JSON line with each side's step time, FLOP
+    rate and peak device memory.  HBM bytes come from an ncu launch list of
+    this same command (the kernels of the two sides have distinct names)."""
+    import torch
+    import io_aware_exact_10_gb300 as fa
+    from io_aware_exact_10_gb300 import workloads as W
+    import __graft_entry__
+
+    if w.kv_heads != w.H or w.kv_len != w.N or w.block_pattern:
+        raise SystemExit("--compare takes a dense multi-head workload with N_k = N")
+    torch.cuda.set_device(0)
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    B, H, N, d = w.B, w.H, w.N, w.d
+    q, k, v, dO = W.make_inputs_on_device(w, dev)
+    causal = int(w.causal)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def ours_step():
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, w.scale, causal, stream)
+        fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, w.scale, causal, ws, ws_bytes,
+                  stream)
+
+    cmask = (torch.ones(N, N, dtype=torch.bool, device=dev).triu(1) if w.causal else None)
+
+    def standard_step():
+        qq, kk, vv = (t.detach().requires_grad_(True) for t in (q, k, v))
+        s_ = torch.matmul(qq, kk.transpose(-1, -2)) * w.scale
+        if cmask is not None:
+            s_ = s_.masked_fill(cmask, float("-inf"))
+        p_ = torch.softmax(s_, dim=-1)
+        out = torch.matmul(p_, vv)
+        out.backward(dO)
+        return qq.grad, kk.grad, vv.grad
+
+    def timed(step, reps):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(reps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps, (torch.cuda.max_memory_allocated() - base) / 1e9
+
+    reps = max(1, min(args.steps, 20))
+    ours_ms, ours_peak = timed(ours_step, reps)
+    std_ms, std_mem = timed(standard_step, reps)
+    # device memory a step needs beyond its inputs: for this library the
+    # outputs and the workspace, allocated once above (plus any peak during
+    # the step); for standard attention the peak of the step, which holds S,
+    # P, their gradients and the outputs
+    ours_mem = ours_peak + sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv, ws)) / 1e9
+    if fa.fa_last_device_error(stream) != fa.FA_OK:
+        raise RuntimeError("device error in the comparison")
+    half = 0.5 if w.causal else 1.0
+    nn = B * H * N * N * d * half
+    # algorithmic FLOPs of each method: standard fwd 2 contractions, bwd 4;
+    # this library recomputes S and P in the backward (5 contractions)
+    std_flops, ours_flops = 2 * nn * 6, 2 * nn * 7
+    line = {
+        "mode": "compare", "workload": w.name, "steps": reps, "warmup": args.warmup,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), drawn on the device)",
+        "standard": {"impl": "torch bf16 matmul + softmax + matmul, autograd backward "
+                             "(S and P materialised)",
+                     "ms": std_ms, "gflop": std_flops / 1e9,
+                     "tflops": std_flops / (std_ms * 1e-3) / 1e12, "extra_mem_gb": std_mem},
+        "ours": {"impl": "fa_fwd + fa_bwd", "ms": ours_ms, "gflop": ours_flops / 1e9,
+                 "tflops": ours_flops / (ours_ms * 1e-3) / 1e12, "extra_mem_gb": ours_mem},
+        "speedup": std_ms / ours_ms,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -475,6 +566,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="gpt2_medium")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--compare", action="store_true",
+                    help="standard attention (S, P in device memory) against this library")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -483,6 +576,9 @@ def main():
         run_sweep(args)
         return
     w = W.WORKLOADS[args.workload]
+    if args.compare:
+        run_compare(args, w)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:
