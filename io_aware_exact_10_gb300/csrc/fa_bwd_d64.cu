@@ -133,17 +133,36 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One CTA per (key/value head, key tile).  It loops over the query tiles
-  // i0 ... nq-1 of each of the kv_group query heads that share the key/value
-  // head, in that order; each role follows the (tile, head) pair of its own
-  // position in the loop with a TileWalk.
-  const GridPos gp = decode_grid((int)blockIdx.x, p.BHkv, p.nkv, p.group);
-  const int bk = gp.bh;
-  const int kt = gp.rank;
-  const int i0 = CAUSAL ? first_query_tile(kt, p.coff) : 0;  // first query tile that sees this key tile
-  // Block-sparse: the TMA warp turns this key tile's mask column (query
-  // tiles i0 .. nq-1) into a bitset after the statistics; with no kept tile
-  // the CTA only zeroes its dK, dV rows.
+  // Work items are (key/value head, key tile) pairs in the grid order of
+  // decode_grid.  An item loops over the query tiles i0 ... nq-1 of each of
+  // the kv_group query heads that share the key/value head, in that order;
+  // each role follows the (tile, head) pair of its own position in the loop
+  // with a TileWalk.  A CTA takes items blockIdx.x, blockIdx.x + gridDim.x,
+  // ...: without causal masking or a block mask every item has the same work
+  // and one CTA per SM walks them, so an item's set-up overlaps the previous
+  // item's last tiles instead of costing a CTA launch; otherwise each CTA
+  // takes one item and the hardware scheduler balances them.  The ring
+  // positions and the per-tile barrier phases run on across items (global
+  // tile index U); K, V, their copy into tensor memory and FIN have one
+  // phase per item.
+  const int n_items = p.BHkv * p.nkv;
+  const int L0 = (int)blockIdx.x, LS = (int)gridDim.x;
+  struct Item {
+    int bk, kt, i0;
+  };
+  auto item_info = [&](int L) {
+    const GridPos gp = decode_grid(L, p.BHkv, p.nkv, p.group);
+    Item I;
+    I.bk = gp.bh;
+    I.kt = gp.rank;
+    I.i0 = CAUSAL ? first_query_tile(I.kt, p.coff) : 0;  // first query tile that sees this key tile
+    return I;
+  };
+  const Item I0 = item_info(L0);
+  const int bk = I0.bk, kt = I0.kt, i0 = I0.i0;
+  // Block-sparse (one item per CTA): the TMA warp turns this key tile's mask
+  // column (query tiles i0 .. nq-1) into a bitset after the statistics; with
+  // no kept tile the CTA only zeroes its dK, dV rows.
   QuerySeq<SPARSE> qseq{reinterpret_cast<const uint32_t*>(smem + C::SMEM), (p.nq + 31) >> 5, i0, p.nq};
   int nqt = p.nq - i0;  // query tiles per query head
   if constexpr (SPARSE) {
@@ -163,8 +182,16 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     }
     qseq.first = next_bit(qbits, qseq.nw, -1);
   }
-  const int nit = nqt * p.kv_group;                // query tiles to process
+  const int nit = nqt * p.kv_group;                // query tiles of the first item
   const TileWalk walk0{qseq.first, bk * p.kv_group};
+  // per item (dense items after the first): query tiles, first position,
+  // and the query-tile sequence
+  auto item_nit = [&](const Item& I) { return (p.nq - I.i0) * p.kv_group; };
+  auto item_seq = [&](const Item& I) {
+    QuerySeq<SPARSE> s = qseq;
+    if constexpr (!SPARSE) s.first = I.i0;
+    return s;
+  };
 
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
@@ -175,6 +202,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   // tiles) before the CTA-wide sync, so their latency overlaps the set-up.
   int nq_issued = 0, ndo_issued = 0;
   TileWalk lw = walk0;  // the TMA thread's position
+  QuerySeq<SPARSE> lseq = qseq;  // and its item's query-tile sequence
   auto issue_q = [&](int u) {
     const int qs = u % C::QSLOTS;
     mbar_arrive_expect_tx(bar(B_QF0 + qs), C::TILE + C::STATS_SLOT);
@@ -188,7 +216,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     mbar_arrive_expect_tx(bar(B_DOF0 + ds), C::TILE);
     tma_load_3d(sDO + ds * C::TILE, &tdo, bar(B_DOF0 + ds), 0, lw.qt * C::BQ, lw.qh);
     ++ndo_issued;
-    qseq.next(lw);
+    lseq.next(lw);
   };
   const int pre = nit < C::DOSLOTS ? nit : C::DOSLOTS;   // tiles issued before the sync
   if (warp == C::W_LOAD && lane == 0) {
@@ -225,18 +253,43 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
       bool ok = true;
-      for (int u = pre; u < nit; ++u) {
+      int nkv_issued = 1;  // items whose K, V have been issued
+      // Q_u (with its statistics) and dO_u of global tile u, once their ring
+      // slots are free
+      auto ring = [&](int u) -> bool {
         const int qs = u % C::QSLOTS, qn = u / C::QSLOTS;
-        if (qn > 0 && !(ok = mbar_wait(bar(B_QE0 + qs), (qn - 1) & 1, p.ctl, abort, 50))) break;
+        if (qn > 0 && !mbar_wait(bar(B_QE0 + qs), (qn - 1) & 1, p.ctl, abort, 50)) return false;
         issue_q(u);
         const int ds = u % C::DOSLOTS, dn = u / C::DOSLOTS;
-        if (dn > 0 && !(ok = mbar_wait(bar(B_DOE0 + ds), (dn - 1) & 1, p.ctl, abort, 51))) break;
+        if (dn > 0 && !mbar_wait(bar(B_DOE0 + ds), (dn - 1) & 1, p.ctl, abort, 51)) return false;
         issue_do(u);
+        return true;
+      };
+      int u = pre, uend = nit;  // global tile index; end of the current item
+      for (int L = L0;;) {
+        for (; u < uend && ok; ++u) ok = ring(u);
+        if (!ok) break;
+        L += LS;
+        if (L >= n_items) break;
+        // the next item: its first tiles as soon as their slots are free,
+        // then K and V once every MMA of the previous item has completed
+        const Item I = item_info(L);
+        lw = TileWalk{I.i0, I.bk * p.kv_group};
+        lseq = item_seq(I);
+        uend = u + item_nit(I);
+        const int upre = min(uend, u + C::DOSLOTS);
+        for (; u < upre && ok; ++u) ok = ring(u);
+        if (!ok || !(ok = mbar_wait(bar(B_FIN), (nkv_issued - 1) & 1, p.ctl, abort, 52))) break;
+        mbar_arrive_expect_tx(bar(B_K), C::TILE);
+        tma_load_3d(sK, &tk, bar(B_K), 0, I.kt * C::BK, I.bk);
+        mbar_arrive_expect_tx(bar(B_V), C::TILE);
+        tma_load_3d(sV, &tv, bar(B_V), 0, I.kt * C::BK, I.bk);
+        ++nkv_issued;
       }
       if (!ok) {
         // Abort: let every copy already issued land before the CTA exits.
-        mbar_wait_quiet(bar(B_K), 0, 200000000ull);
-        if (nq_issued > 0) mbar_wait_quiet(bar(B_V), 0, 200000000ull);
+        mbar_wait_quiet(bar(B_K), (nkv_issued - 1) & 1, 200000000ull);
+        mbar_wait_quiet(bar(B_V), (nkv_issued - 1) & 1, 200000000ull);
         for (int v = (nq_issued > C::QSLOTS ? nq_issued - C::QSLOTS : 0); v < nq_issued; ++v)
           mbar_wait_quiet(bar(B_QF0 + v % C::QSLOTS), (v / C::QSLOTS) & 1, 200000000ull);
         for (int v = (ndo_issued > C::DOSLOTS ? ndo_issued - C::DOSLOTS : 0); v < ndo_issued; ++v)
@@ -290,63 +343,68 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         mma_commit_e(lead, bar(B_DQF));
         return true;
       };
-      bool ok = warp_wait(bar(B_K), 0, p.ctl, abort, 60) && warp_wait(bar(B_KVT), 0, p.ctl, abort, 59) &&
-                warp_wait(bar(B_QF0), 0, p.ctl, abort, 61);
-      if (ok) {
-        tc_fence_after();
-        issue_st(0);
-        ok = warp_wait(bar(B_V), 0, p.ctl, abort, 62) && warp_wait(bar(B_DOF0), 0, p.ctl, abort, 63);
-      }
-      if (ok) {
-        tc_fence_after();
-        issue_dpt(0);
-      }
-      // ring positions: Q slot and phase of tile u + 1, Q slot offset of tile u
-      int qs_v = 1;
-      uint32_t qph_v = 0, qo_u = 0;
-      for (int u = 0; u < nit && ok; ++u) {
-        const uint32_t qo_v = (uint32_t)qs_v * TILE16;
-        const uint32_t dof_u = (uint32_t)(u & 1) * TILE16, dof_v = (uint32_t)((u + 1) & 1) * TILE16;
-        const uint32_t acc0 = u > 0 ? 1u : 0u;
-        const bool more = u + 1 < nit;
-        // dV += P^T dO_u   (A = P^T bf16 in TMEM, B = dO_u query-major)
-        if (!(ok = warp_wait(bar(B_P), u & 1, p.ctl, abort, 66))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < C::BQ / 16; ++k)
-          mma_ts_e(lead, tDV, tST + C::pcol(k), doMN + dof_u + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
-        mma_commit_e(lead, bar(B_DOE0 + (u & 1)));       // dO_u slot free
-        // S^T of the next tile overwrites the P^T pairs only after dV(u) has
-        // read them (tcgen05.mma runs in issue order)
-        if (more) {
-          if (!(ok = warp_wait(bar(B_QF0 + qs_v), qph_v, p.ctl, abort, 64))) break;
+      // Q slot offset of global tile v and the phase of its fill
+      auto q_off = [](int v) { return (uint32_t)(v % C::QSLOTS) * TILE16; };
+      auto q_ph = [](int v) { return (uint32_t)(v / C::QSLOTS) & 1u; };
+      bool ok = true;
+      int U0 = 0;  // global index of the item's first tile
+      for (int L = L0, k = 0; L < n_items && ok; L += LS, ++k) {
+        const int nit_i = L == L0 ? nit : item_nit(item_info(L));
+        const uint32_t kp = (uint32_t)k & 1u;
+        ok = warp_wait(bar(B_K), kp, p.ctl, abort, 60) && warp_wait(bar(B_KVT), kp, p.ctl, abort, 59) &&
+             warp_wait(bar(B_QF0 + U0 % C::QSLOTS), q_ph(U0), p.ctl, abort, 61);
+        if (ok) {
           tc_fence_after();
-          issue_st(qo_v);
+          issue_st(q_off(U0));
+          ok = warp_wait(bar(B_V), kp, p.ctl, abort, 62) &&
+               warp_wait(bar(B_DOF0 + (U0 & 1)), (uint32_t)(U0 >> 1) & 1u, p.ctl, abort, 63);
         }
-        // dS(u) is in shared memory, its transpose in the dP^T columns
-        if (!(ok = warp_wait(bar(B_DS), u & 1, p.ctl, abort, 69))) break;
-        tc_fence_after();
-        // dK += dS^T Q_u   (A = dS^T bf16 pairs in TMEM, B = Q_u query-major)
-#pragma unroll
-        for (int k = 0; k < C::BQ / 16; ++k)
-          mma_ts_e(lead, tDK, tDPT + C::pcol(k), qMN + qo_u + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
-        mma_commit_e(lead, bar(B_QE0 + (int)(qo_u / TILE16)));  // Q_u slot free
-        // dP^T of the next tile overwrites the dS^T pairs only after dK(u)
-        // has read them; its completion covers dK(u), dQ(u-1) and every
-        // earlier MMA
-        if (more) {
-          if (!(ok = warp_wait(bar(B_DOF0 + ((u + 1) & 1)), ((u + 1) >> 1) & 1, p.ctl, abort, 67))) break;
+        if (ok) {
           tc_fence_after();
-          issue_dpt(dof_v);
+          issue_dpt((uint32_t)(U0 & 1) * TILE16);
         }
-        if (!(ok = issue_dq(u))) break;
-        qo_u = qo_v;
-        if (++qs_v == C::QSLOTS) {
-          qs_v = 0;
-          qph_v ^= 1u;
+        for (int u = 0; u < nit_i && ok; ++u) {
+          const int U = U0 + u, Vn = U + 1;
+          const uint32_t qo_u = q_off(U), qo_v = q_off(Vn);
+          const uint32_t dof_u = (uint32_t)(U & 1) * TILE16, dof_v = (uint32_t)(Vn & 1) * TILE16;
+          const uint32_t acc0 = u > 0 ? 1u : 0u;
+          const bool more = u + 1 < nit_i;
+          // dV += P^T dO_u   (A = P^T bf16 in TMEM, B = dO_u query-major)
+          if (!(ok = warp_wait(bar(B_P), U & 1, p.ctl, abort, 66))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k2 = 0; k2 < C::BQ / 16; ++k2)
+            mma_ts_e(lead, tDV, tST + C::pcol(k2), doMN + dof_u + 128 * k2, HI, kIdG, k2 > 0 ? 1u : acc0);
+          mma_commit_e(lead, bar(B_DOE0 + (U & 1)));       // dO_u slot free
+          // S^T of the next tile overwrites the P^T pairs only after dV(u) has
+          // read them (tcgen05.mma runs in issue order)
+          if (more) {
+            if (!(ok = warp_wait(bar(B_QF0 + Vn % C::QSLOTS), q_ph(Vn), p.ctl, abort, 64))) break;
+            tc_fence_after();
+            issue_st(qo_v);
+          }
+          // dS(u) is in shared memory, its transpose in the dP^T columns
+          if (!(ok = warp_wait(bar(B_DS), U & 1, p.ctl, abort, 69))) break;
+          tc_fence_after();
+          // dK += dS^T Q_u   (A = dS^T bf16 pairs in TMEM, B = Q_u query-major)
+#pragma unroll
+          for (int k2 = 0; k2 < C::BQ / 16; ++k2)
+            mma_ts_e(lead, tDK, tDPT + C::pcol(k2), qMN + qo_u + 128 * k2, HI, kIdG, k2 > 0 ? 1u : acc0);
+          mma_commit_e(lead, bar(B_QE0 + U % C::QSLOTS));  // Q_u slot free
+          // dP^T of the next tile overwrites the dS^T pairs only after dK(u)
+          // has read them; its completion covers dK(u), dQ(u-1) and every
+          // earlier MMA
+          if (more) {
+            if (!(ok = warp_wait(bar(B_DOF0 + (Vn & 1)), (uint32_t)(Vn >> 1) & 1u, p.ctl, abort, 67))) break;
+            tc_fence_after();
+            issue_dpt(dof_v);
+          }
+          if (!(ok = issue_dq(U))) break;
         }
+        // every MMA of the item: dK, dV final, K and V free for the next item
+        if (ok) mma_commit_e(lead, bar(B_FIN));
+        U0 += nit_i;
       }
-      if (ok) mma_commit_e(lead, bar(B_FIN));
       mma_commit_e(lead, bar(B_DRAIN));
       mbar_wait_quiet(bar(B_DRAIN), 0, 200000000ull);
     }
@@ -359,7 +417,6 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int cb = CW * g;                          // first query column of this thread
     const uint32_t tST = tmem + lane_off + C::COL_ST + cb, tDPT = tmem + lane_off + C::COL_DPT + cb;
     const uint64_t sc2 = f2_pack(p.scale2, p.scale2);
-    const size_t rowbase = (size_t)bk * p.Nk;        // key rows (dK, dV)
     // statistics of the tile in Q slot s: 128 x -LSE log2 e, 128 x -D,
     // loaded with the Q tile (same barrier)
     const float* stats = reinterpret_cast<const float*>(smem + C::OFF_STATS);
@@ -371,8 +428,16 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     // chunks (cb % 64) / 8 ... of 8 queries each
     const uint32_t ds_row = (uint32_t)(cb >> 6) * 16384u + (uint32_t)r * 128u;
     const uint32_t ds_c0 = (uint32_t)((cb & 63) >> 3);
-    TileWalk w = walk0;
-    for (int u = 0; u < nit && ok; ++u, qseq.next(w)) {
+    int U0 = 0;  // global index of the item's first tile
+    for (int L = L0, k = 0; L < n_items && ok; L += LS, ++k) {
+    const Item I = L == L0 ? I0 : item_info(L);
+    const int kt = I.kt;
+    const int nit_i = L == L0 ? nit : item_nit(I);
+    const QuerySeq<SPARSE> seq = L == L0 ? qseq : item_seq(I);
+    const size_t rowbase = (size_t)I.bk * p.Nk;      // key rows (dK, dV)
+    TileWalk w = L == L0 ? walk0 : TileWalk{seq.first, I.bk * p.kv_group};
+    for (int u = 0; u < nit_i && ok; ++u, seq.next(w)) {
+      const int U = U0 + u;
       const int qt = w.qt;
       const float* lse_u = stats + qs_u * 256 + cb;
       const float* d_u = lse_u + 128;
@@ -385,7 +450,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       // (S^T(u) was issued after dV(u-1): the P^T pairs of the last tile are
       // consumed.  This thread's pairs go into the first CW/2 of its own
       // S^T columns once it has read them.)
-      if (!(ok = warp_wait(bar(B_ST), u & 1, p.ctl, abort, 81))) break;
+      if (!(ok = warp_wait(bar(B_ST), U & 1, p.ctl, abort, 81))) break;
       tc_fence_after();
       uint32_t pk[CW / 2];
       {
@@ -428,7 +493,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       // ---- dS = P o (dP - D), with P the bf16 values dV multiplied
       // (dP^T(u) was issued after dK(u-1) and dQ(u-2): the dS^T pairs of the
       // last tile and dS buffer u&1 are consumed.)
-      if (!(ok = warp_wait(bar(B_DPT), u & 1, p.ctl, abort, 83))) break;
+      if (!(ok = warp_wait(bar(B_DPT), U & 1, p.ctl, abort, 83))) break;
       tc_fence_after();
       uint32_t dp[CW];
 #pragma unroll
@@ -454,7 +519,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < CW / 2; c += 16) tmem_st16(tDPT + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
       // key row r of dS buffer u&1, 128-byte swizzled (A operand of dQ)
-      const uint32_t srow = sDS + (uint32_t)(u & 1) * C::DS_BYTES + ds_row;
+      const uint32_t srow = sDS + (uint32_t)(U & 1) * C::DS_BYTES + ds_row;
 #pragma unroll
       for (int c = 0; c < CW / 8; ++c)
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + (((ds_c0 + (uint32_t)c) ^ sw) << 4)),
@@ -466,9 +531,10 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS));         // also: dP^T(u) has been read
     }
-    // epilogue: dV rows of this key tile, columns [DVC g, DVC g + DVC)
+    // epilogue: dV rows of this key tile, columns [DVC g, DVC g + DVC); the
+    // next item's first dV (computed after this warp's next P) overwrites them
     constexpr int DVC = C::HD / C::NG;
-    if (ok && warp_wait(bar(B_FIN), 0, p.ctl, abort, 86)) {
+    if (ok && (ok = warp_wait(bar(B_FIN), (uint32_t)k & 1u, p.ctl, abort, 86))) {
       tc_fence_after();
       const int key = kt * C::BK + r;
       uint32_t v[32];
@@ -487,6 +553,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         for (int i = 0; i < DVC / 8; ++i) d4[i] = make_uint4(pkv[4 * i], pkv[4 * i + 1], pkv[4 * i + 2], pkv[4 * i + 3]);
       }
     }
+    U0 += nit_i;
+    }  // items
   } else {
     // ---------------------------------------------------------- dQ drain
     // dQ_u (128 query rows x 64, fp32) leaves TMEM once per tile and is added
@@ -495,13 +563,22 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int sp = warp & 3;
     const int r = sp * 32 + lane;
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
-    const size_t rowbase = (size_t)bk * p.Nk;        // key rows (dK, dV)
     const uint32_t sw = (uint32_t)(lane & 7);
     const uint32_t stage = s0 + C::OFF_STAGE + (uint32_t)sp * 8192u;
+    bool ok = true;
+    int U0 = 0;  // global index of the item's first tile
+    for (int L = L0, k = 0; L < n_items && ok; L += LS, ++k) {
+    const Item I = L == L0 ? I0 : item_info(L);
+    const int kt = I.kt;
+    const int nit_i = L == L0 ? nit : item_nit(I);
+    const QuerySeq<SPARSE> seq = L == L0 ? qseq : item_seq(I);
+    const size_t rowbase = (size_t)I.bk * p.Nk;      // key rows (dK, dV)
     // First, K and V rows of this warp's key rows into tensor memory (the A
     // operands of S^T and dP^T): 128 bytes of a 128-byte-swizzled row are 32
-    // words, element 2c in the low half of word c.
-    bool ok = warp_wait(bar(B_K), 0, p.ctl, abort, 92) && warp_wait(bar(B_V), 0, p.ctl, abort, 93);
+    // words, element 2c in the low half of word c.  (The previous item's
+    // MMAs are complete: this warp waited for its FIN below.)
+    ok = warp_wait(bar(B_K), (uint32_t)k & 1u, p.ctl, abort, 92) &&
+         warp_wait(bar(B_V), (uint32_t)k & 1u, p.ctl, abort, 93);
     if (ok) {
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
@@ -520,9 +597,9 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_KVT));
     }
-    TileWalk w = walk0;
-    for (int u = 0; u < nit && ok; ++u, qseq.next(w)) {
-      if (!(ok = warp_wait(bar(B_DQF), u & 1, p.ctl, abort, 90))) break;
+    TileWalk w = L == L0 ? walk0 : TileWalk{seq.first, I.bk * p.kv_group};
+    for (int u = 0; u < nit_i && ok; ++u, seq.next(w)) {
+      if (!(ok = warp_wait(bar(B_DQF), (U0 + u) & 1, p.ctl, abort, 90))) break;
       tc_fence_after();
       uint32_t v[64];
       tmem_ld32(tmem + lane_off + C::COL_DQ, *reinterpret_cast<uint32_t(*)[32]>(v));
@@ -555,10 +632,9 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         bulk_commit_group();
       }
     }
-    if (lane == 0) bulk_wait_group<0>();
-    __syncwarp();
-    // epilogue: dK rows of this key tile (scaled)
-    if (ok && warp_wait(bar(B_FIN), 0, p.ctl, abort, 91)) {
+    // epilogue: dK rows of this key tile (scaled); the next item's first dK
+    // overwrites them only after this warp's K, V copy for that item
+    if (ok && (ok = warp_wait(bar(B_FIN), (uint32_t)k & 1u, p.ctl, abort, 91))) {
       tc_fence_after();
       const int key = kt * C::BK + r;
       const float scale = p.scale;
@@ -578,6 +654,11 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         }
       }
     }
+    U0 += nit_i;
+    }  // items
+    // every reduction has landed before the CTA exits
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -613,7 +694,11 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
-  dim3 grid((unsigned)((long)p.nkv * p.BHkv));
+  // without causal masking or a block mask every item has the same work:
+  // one CTA per SM walks them; otherwise one CTA per item
+  const long n_items = (long)p.nkv * p.BHkv;
+  const long ctas = (CAUSAL || SPARSE) ? n_items : (n_items < a.num_sms ? n_items : a.num_sms);
+  dim3 grid((unsigned)ctas);
   kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();
 }
