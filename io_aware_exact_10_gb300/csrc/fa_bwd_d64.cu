@@ -87,15 +87,15 @@ static_assert(Cfg64::NG == 2 || Cfg64::NG == 4, "32 or 64 query columns per P/dS
 // barrier indices
 enum : int {
   B_K = 0, B_V, B_QF0, B_QF1, B_QF2, B_QE0, B_QE1, B_QE2, B_DOF0, B_DOF1, B_DOE0, B_DOE1,
-  B_ST, B_P, B_DPT, B_DS, B_DQF, B_DQE, B_FIN, B_DRAIN, B_KVT, B_COUNT
+  B_ST, B_P, B_DPT, B_DS, B_DQF, B_DQE, B_FIN, B_DRAIN, B_KT, B_VT, B_COUNT
 };
 static_assert(B_COUNT <= Cfg64::NBAR, "barrier area");
 // arrival counts: TMA and tcgen05.commit barriers take one arrival; P and DS
-// one per P/dS warp; DQE and KVT one per drain warp.
+// one per P/dS warp; DQE, KT and VT one per drain warp.
 __device__ __constant__ const uint32_t kBarCount64[B_COUNT] = {
     1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1,           // K, V, QF*, QE*, DOF*, DOE*
     1, Cfg64::NPW, 1, Cfg64::NPW, 1, 4, 1, 1,     // ST, P, DPT, DS, DQF, DQE, FIN, DRAIN
-    4};                                           // KVT (K, V copied to tensor memory)
+    4, 4};                                        // KT, VT (K, V copied to tensor memory)
 
 struct BwdParams64 {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
@@ -196,6 +196,12 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
                  sDO = s0 + C::OFF_DO, sDS = s0 + C::OFF_DS;
+  // K and V of item k: the two key-tile buffers swap every item.  V reaches
+  // tensor memory early in its item, after which no one reads its buffer:
+  // the next item's K is loaded there at once, and the next V goes into
+  // this item's K buffer once the last dQ (B = K) has completed.
+  auto k_buf = [&](int k) { return (k & 1) ? sV : sK; };
+  auto v_buf = [&](int k) { return (k & 1) ? sK : sV; };
 
   // The TMA thread initialises the barriers and issues the copies that need
   // no wait (K, V, and Q with its statistics and dO of the first two query
@@ -253,7 +259,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
       bool ok = true;
-      int nkv_issued = 1;  // items whose K, V have been issued
+      int nkv_issued = 1;  // items whose V has been issued (K: nk_issued)
+      int nk_issued = 1;
       // Q_u (with its statistics) and dO_u of global tile u, once their ring
       // slots are free
       auto ring = [&](int u) -> bool {
@@ -271,24 +278,28 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         if (!ok) break;
         L += LS;
         if (L >= n_items) break;
-        // the next item: its first tiles as soon as their slots are free,
-        // then K and V once every MMA of the previous item has completed
+        // the next item (index nkv_issued): its K once the previous V is in
+        // tensor memory, its first tiles as soon as their slots are free,
+        // then its V once every MMA of the previous item has completed
         const Item I = item_info(L);
+        const int kn = nkv_issued;
+        if (!(ok = mbar_wait(bar(B_VT), (kn - 1) & 1, p.ctl, abort, 53))) break;
+        mbar_arrive_expect_tx(bar(B_K), C::TILE);
+        tma_load_3d(k_buf(kn), &tk, bar(B_K), 0, I.kt * C::BK, I.bk);
+        ++nk_issued;
         lw = TileWalk{I.i0, I.bk * p.kv_group};
         lseq = item_seq(I);
         uend = u + item_nit(I);
         const int upre = min(uend, u + C::DOSLOTS);
         for (; u < upre && ok; ++u) ok = ring(u);
-        if (!ok || !(ok = mbar_wait(bar(B_FIN), (nkv_issued - 1) & 1, p.ctl, abort, 52))) break;
-        mbar_arrive_expect_tx(bar(B_K), C::TILE);
-        tma_load_3d(sK, &tk, bar(B_K), 0, I.kt * C::BK, I.bk);
+        if (!ok || !(ok = mbar_wait(bar(B_FIN), (kn - 1) & 1, p.ctl, abort, 52))) break;
         mbar_arrive_expect_tx(bar(B_V), C::TILE);
-        tma_load_3d(sV, &tv, bar(B_V), 0, I.kt * C::BK, I.bk);
+        tma_load_3d(v_buf(kn), &tv, bar(B_V), 0, I.kt * C::BK, I.bk);
         ++nkv_issued;
       }
       if (!ok) {
         // Abort: let every copy already issued land before the CTA exits.
-        mbar_wait_quiet(bar(B_K), (nkv_issued - 1) & 1, 200000000ull);
+        mbar_wait_quiet(bar(B_K), (nk_issued - 1) & 1, 200000000ull);
         mbar_wait_quiet(bar(B_V), (nkv_issued - 1) & 1, 200000000ull);
         for (int v = (nq_issued > C::QSLOTS ? nq_issued - C::QSLOTS : 0); v < nq_issued; ++v)
           mbar_wait_quiet(bar(B_QF0 + v % C::QSLOTS), (v / C::QSLOTS) & 1, 200000000ull);
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       // between 64-element blocks); the high half is the same for all.
       constexpr uint32_t HI = sdesc_hi(1024);
       constexpr uint32_t TILE16 = C::TILE >> 4, DS16 = C::DS_BYTES >> 4;
-      const uint32_t kMN = sdesc_lo(sK, 16384);
+      uint32_t kMN = sdesc_lo(sK, 16384);  // K of the current item (B of dQ)
       const uint32_t qK = sdesc_lo(sQ, 16), qMN = sdesc_lo(sQ, 16384);
       const uint32_t doK = sdesc_lo(sDO, 16), doMN = sdesc_lo(sDO, 16384);
       const uint32_t dsMN = sdesc_lo(sDS, 16384);
@@ -351,21 +362,28 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       for (int L = L0, k = 0; L < n_items && ok; L += LS, ++k) {
         const int nit_i = L == L0 ? nit : item_nit(item_info(L));
         const uint32_t kp = (uint32_t)k & 1u;
-        ok = warp_wait(bar(B_K), kp, p.ctl, abort, 60) && warp_wait(bar(B_KVT), kp, p.ctl, abort, 59) &&
+        kMN = sdesc_lo(k_buf(k), 16384);
+        // K and V in tensor memory (the drain waited for their loads)
+        ok = warp_wait(bar(B_KT), kp, p.ctl, abort, 59) &&
              warp_wait(bar(B_QF0 + U0 % C::QSLOTS), q_ph(U0), p.ctl, abort, 61);
         if (ok) {
           tc_fence_after();
           issue_st(q_off(U0));
-          ok = warp_wait(bar(B_V), kp, p.ctl, abort, 62) &&
+          ok = warp_wait(bar(B_VT), kp, p.ctl, abort, 62) &&
                warp_wait(bar(B_DOF0 + (U0 & 1)), (uint32_t)(U0 >> 1) & 1u, p.ctl, abort, 63);
         }
         if (ok) {
           tc_fence_after();
           issue_dpt((uint32_t)(U0 & 1) * TILE16);
         }
+        // Q ring of tiles u and u + 1, advanced per tile: slot offset of u,
+        // slot and fill phase of u + 1
+        uint32_t qo_u = q_off(U0);
+        int qs_v = (U0 + 1) % C::QSLOTS;
+        uint32_t qph_v = q_ph(U0 + 1);
         for (int u = 0; u < nit_i && ok; ++u) {
           const int U = U0 + u, Vn = U + 1;
-          const uint32_t qo_u = q_off(U), qo_v = q_off(Vn);
+          const uint32_t qo_v = (uint32_t)qs_v * TILE16;
           const uint32_t dof_u = (uint32_t)(U & 1) * TILE16, dof_v = (uint32_t)(Vn & 1) * TILE16;
           const uint32_t acc0 = u > 0 ? 1u : 0u;
           const bool more = u + 1 < nit_i;
@@ -379,7 +397,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
           // S^T of the next tile overwrites the P^T pairs only after dV(u) has
           // read them (tcgen05.mma runs in issue order)
           if (more) {
-            if (!(ok = warp_wait(bar(B_QF0 + Vn % C::QSLOTS), q_ph(Vn), p.ctl, abort, 64))) break;
+            if (!(ok = warp_wait(bar(B_QF0 + qs_v), qph_v, p.ctl, abort, 64))) break;
             tc_fence_after();
             issue_st(qo_v);
           }
@@ -390,7 +408,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
 #pragma unroll
           for (int k2 = 0; k2 < C::BQ / 16; ++k2)
             mma_ts_e(lead, tDK, tDPT + C::pcol(k2), qMN + qo_u + 128 * k2, HI, kIdG, k2 > 0 ? 1u : acc0);
-          mma_commit_e(lead, bar(B_QE0 + U % C::QSLOTS));  // Q_u slot free
+          mma_commit_e(lead, bar(B_QE0 + (int)(qo_u / TILE16)));  // Q_u slot free
           // dP^T of the next tile overwrites the dS^T pairs only after dK(u)
           // has read them; its completion covers dK(u), dQ(u-1) and every
           // earlier MMA
@@ -400,6 +418,11 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
             issue_dpt(dof_v);
           }
           if (!(ok = issue_dq(U))) break;
+          qo_u = qo_v;
+          if (++qs_v == C::QSLOTS) {
+            qs_v = 0;
+            qph_v ^= 1u;
+          }
         }
         // every MMA of the item: dK, dV final, K and V free for the next item
         if (ok) mma_commit_e(lead, bar(B_FIN));
@@ -565,7 +588,28 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const uint32_t sw = (uint32_t)(lane & 7);
     const uint32_t stage = s0 + C::OFF_STAGE + (uint32_t)sp * 8192u;
-    bool ok = true;
+    // This warp's 32 key rows of a K or V tile into tensor memory (the A
+    // operands of S^T and dP^T): 128 bytes of a 128-byte-swizzled row are 32
+    // words, element 2c in the low half of word c.  The K copy of an item
+    // comes right after the previous item's FIN (its MMAs are complete), the
+    // V copy after this warp's dK epilogue of the previous item.
+    auto to_tmem = [&](uint32_t buf, uint32_t col, int done) {
+      const uint32_t src = buf + (uint32_t)r * 128u;
+      uint32_t w[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]), "=r"(w[4 * c + 3])
+                     : "r"(src + (((uint32_t)c ^ sw) << 4))
+                     : "memory");
+      tmem_st32(tmem + lane_off + col, w);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(done));
+    };
+    bool ok = warp_wait(bar(B_K), 0, p.ctl, abort, 92);
+    if (ok) to_tmem(k_buf(0), C::COL_KT, B_KT);
     int U0 = 0;  // global index of the item's first tile
     for (int L = L0, k = 0; L < n_items && ok; L += LS, ++k) {
     const Item I = L == L0 ? I0 : item_info(L);
@@ -573,30 +617,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int nit_i = L == L0 ? nit : item_nit(I);
     const QuerySeq<SPARSE> seq = L == L0 ? qseq : item_seq(I);
     const size_t rowbase = (size_t)I.bk * p.Nk;      // key rows (dK, dV)
-    // First, K and V rows of this warp's key rows into tensor memory (the A
-    // operands of S^T and dP^T): 128 bytes of a 128-byte-swizzled row are 32
-    // words, element 2c in the low half of word c.  (The previous item's
-    // MMAs are complete: this warp waited for its FIN below.)
-    ok = warp_wait(bar(B_K), (uint32_t)k & 1u, p.ctl, abort, 92) &&
-         warp_wait(bar(B_V), (uint32_t)k & 1u, p.ctl, abort, 93);
-    if (ok) {
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const uint32_t src = (m == 0 ? sK : sV) + (uint32_t)r * 128u;
-        uint32_t w[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w[4 * c]), "=r"(w[4 * c + 1]), "=r"(w[4 * c + 2]), "=r"(w[4 * c + 3])
-                       : "r"(src + (((uint32_t)c ^ sw) << 4))
-                       : "memory");
-        tmem_st32(tmem + lane_off + (m == 0 ? C::COL_KT : C::COL_VT), w);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_KVT));
-    }
+    if (!(ok = warp_wait(bar(B_V), (uint32_t)k & 1u, p.ctl, abort, 93))) break;
+    to_tmem(v_buf(k), C::COL_VT, B_VT);
     TileWalk w = L == L0 ? walk0 : TileWalk{seq.first, I.bk * p.kv_group};
     for (int u = 0; u < nit_i && ok; ++u, seq.next(w)) {
       if (!(ok = warp_wait(bar(B_DQF), (U0 + u) & 1, p.ctl, abort, 90))) break;
@@ -632,10 +654,15 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         bulk_commit_group();
       }
     }
-    // epilogue: dK rows of this key tile (scaled); the next item's first dK
-    // overwrites them only after this warp's K, V copy for that item
+    // epilogue: dK rows of this key tile (scaled), after the next item's K
+    // copy (its first S^T waits for it); the next item's first dK overwrites
+    // them only after this warp's V copy for that item
     if (ok && (ok = warp_wait(bar(B_FIN), (uint32_t)k & 1u, p.ctl, abort, 91))) {
       tc_fence_after();
+      if (L + LS < n_items) {
+        if (!(ok = warp_wait(bar(B_K), (uint32_t)(k + 1) & 1u, p.ctl, abort, 94))) break;
+        to_tmem(k_buf(k + 1), C::COL_KT, B_KT);
+      }
       const int key = kt * C::BK + r;
       const float scale = p.scale;
 #pragma unroll 1
