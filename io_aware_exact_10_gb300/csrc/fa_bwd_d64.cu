@@ -137,16 +137,19 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   // decode_grid.  An item loops over the query tiles i0 ... nq-1 of each of
   // the kv_group query heads that share the key/value head, in that order;
   // each role follows the (tile, head) pair of its own position in the loop
-  // with a TileWalk.  A CTA takes items blockIdx.x, blockIdx.x + gridDim.x,
-  // ...: without causal masking or a block mask every item has the same work
-  // and one CTA per SM walks them, so an item's set-up overlaps the previous
-  // item's last tiles instead of costing a CTA launch; otherwise each CTA
-  // takes one item and the hardware scheduler balances them.  The ring
-  // positions and the per-tile barrier phases run on across items (global
-  // tile index U); K, V, their copy into tensor memory and FIN have one
-  // phase per item.
+  // with a TileWalk.  Dense launches have one CTA per SM (G CTAs), and CTA b
+  // takes items b, 2G-1-b, 2G+b, 4G-1-b, ...: every pass over G items visits
+  // them in the other direction, so with causal masking (items heaviest first
+  // within a head group) each CTA pairs heavy items with light ones.  An
+  // item's set-up then overlaps the previous item's last tiles instead of
+  // costing a CTA launch.  Block-sparse launches have one CTA per item (their
+  // work is uneven in no set order) and the hardware scheduler balances
+  // them.  The ring positions and the per-tile barrier phases run on across
+  // items (global tile index U); K, V, their copy into tensor memory and FIN
+  // have one phase per item.
   const int n_items = p.BHkv * p.nkv;
   const int L0 = (int)blockIdx.x, LS = (int)gridDim.x;
+  auto item_at = [&](int k) { return k * LS + ((k & 1) ? LS - 1 - L0 : L0); };  // k-th item
   struct Item {
     int bk, kt, i0;
   };
@@ -273,10 +276,10 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         return true;
       };
       int u = pre, uend = nit;  // global tile index; end of the current item
-      for (int L = L0;;) {
+      for (int L = L0, kk = 0;;) {
         for (; u < uend && ok; ++u) ok = ring(u);
         if (!ok) break;
-        L += LS;
+        L = item_at(++kk);
         if (L >= n_items) break;
         // the next item (index nkv_issued): its K once the previous V is in
         // tensor memory, its first tiles as soon as their slots are free,
@@ -359,7 +362,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       auto q_ph = [](int v) { return (uint32_t)(v / C::QSLOTS) & 1u; };
       bool ok = true;
       int U0 = 0;  // global index of the item's first tile
-      for (int L = L0, k = 0; L < n_items && ok; L += LS, ++k) {
+      for (int L = L0, k = 0; L < n_items && ok; L = item_at(++k)) {
         const int nit_i = L == L0 ? nit : item_nit(item_info(L));
         const uint32_t kp = (uint32_t)k & 1u;
         kMN = sdesc_lo(k_buf(k), 16384);
@@ -452,7 +455,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const uint32_t ds_row = (uint32_t)(cb >> 6) * 16384u + (uint32_t)r * 128u;
     const uint32_t ds_c0 = (uint32_t)((cb & 63) >> 3);
     int U0 = 0;  // global index of the item's first tile
-    for (int L = L0, k = 0; L < n_items && ok; L += LS, ++k) {
+    for (int L = L0, k = 0; L < n_items && ok; L = item_at(++k)) {
     const Item I = L == L0 ? I0 : item_info(L);
     const int kt = I.kt;
     const int nit_i = L == L0 ? nit : item_nit(I);
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     bool ok = warp_wait(bar(B_K), 0, p.ctl, abort, 92);
     if (ok) to_tmem(k_buf(0), C::COL_KT, B_KT);
     int U0 = 0;  // global index of the item's first tile
-    for (int L = L0, k = 0; L < n_items && ok; L += LS, ++k) {
+    for (int L = L0, k = 0; L < n_items && ok; L = item_at(++k)) {
     const Item I = L == L0 ? I0 : item_info(L);
     const int kt = I.kt;
     const int nit_i = L == L0 ? nit : item_nit(I);
@@ -659,7 +662,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     // them only after this warp's V copy for that item
     if (ok && (ok = warp_wait(bar(B_FIN), (uint32_t)k & 1u, p.ctl, abort, 91))) {
       tc_fence_after();
-      if (L + LS < n_items) {
+      if (item_at(k + 1) < n_items) {
         if (!(ok = warp_wait(bar(B_K), (uint32_t)(k + 1) & 1u, p.ctl, abort, 94))) break;
         to_tmem(k_buf(k + 1), C::COL_KT, B_KT);
       }
@@ -721,10 +724,9 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
-  // without causal masking or a block mask every item has the same work:
-  // one CTA per SM walks them; otherwise one CTA per item
+  // dense: one CTA per SM walks the items; block-sparse: one CTA per item
   const long n_items = (long)p.nkv * p.BHkv;
-  const long ctas = (CAUSAL || SPARSE) ? n_items : (n_items < a.num_sms ? n_items : a.num_sms);
+  const long ctas = SPARSE ? n_items : (n_items < a.num_sms ? n_items : a.num_sms);
   dim3 grid((unsigned)ctas);
   kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();
