@@ -44,9 +44,9 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # over its three launches, from one ncu capture (profiles/
 # launches_gpt2_medium_fwd_bwd.md), and the commit of the kernels it measured.
 # The bench line reports it only while the kernel sources are unchanged.
-NCU_TRAFFIC_BYTES = 2145.5e6
-NCU_TRAFFIC_COMMIT = "e56a2e6"
-NCU_TRAFFIC_SOURCES_SHA256 = "0bb9ee65c292f5239aa1fadeddba584141efca772a2d6cd4cd56d0a6a654139e"
+NCU_TRAFFIC_BYTES = 2145.0e6
+NCU_TRAFFIC_COMMIT = "b56903e"
+NCU_TRAFFIC_SOURCES_SHA256 = "95daf98b75b37981851d827673b2afe4b1c4df9c8f8bdeee03f4499c89852842"
 
 
 def kernel_sources_sha256() -> str:
