@@ -9,30 +9,36 @@
 //   dV += P^T dO_i,  dK += dS^T Q_i,  dQ_i = dS K  (added into dQacc).
 //
 // At d = 64 the operands are small enough to software-pipeline the loop:
-// tensor memory holds S^T, dP^T, P^T (bf16), dV, dK and dQ in separate
-// columns.  Per query tile u the MMA warp issues
-//   [P(u) ready]   dV(u), S^T(u+1)
-//   [dS(u) ready]  dP^T(u+1), dK(u), dQ(u)
+// tensor memory holds S^T (then P^T as bf16 pairs), dP^T (then dS^T pairs),
+// dV, dK, dQ, and K and V themselves in separate columns.  Per query tile u
+// the MMA warp issues
+//   [P(u) ready]   dV(u) (A = P^T pairs), S^T(u+1) (A = K)
+//   [dS(u) ready]  dK(u) (A = dS^T pairs), dP^T(u+1) (A = V), dQ(u)
 // so the next tile's S^T and dP^T are computed while the P/dS warps work on
 // the current one, and the P/dS warps run P(u), dS(u), P(u+1), ... with two
 // waits per tile.  The hand-offs rely on a tcgen05.commit tracking every
 // MMA issued before it: "S^T(u+1) done" also says that dV(u) has read the
-// P^T columns, and "dP^T(u) done" that dK(u-2) and dQ(u-2) have read the dS
-// buffer the P/dS warps are about to overwrite.  dK takes dS from shared
-// memory (key rows, query-contiguous: a K-major operand) and dQ takes the
-// same buffer as an M-major operand, so dS^T is never written to tensor
-// memory.  dS is double-buffered in shared memory, Q goes through a 3-slot
-// ring, dO through a 2-slot ring, and the dQ drain stages its reductions in
-// a buffer of its own.  The row statistics of each query tile (-LSE log2 e
-// and -D, written by the preprocess kernel) come with its Q tile.
+// P^T pairs, and "dP^T(u) done" that dK(u-1) has read the dS^T pairs and
+// dQ(u-2) the dS buffer the P/dS warps are about to overwrite.  dQ takes dS
+// from shared memory (query-major), double-buffered.  Q goes through a
+// 3-slot ring, dO through a 2-slot ring, and the dQ drain stages its
+// reductions in a buffer of its own.  The row statistics of each query tile
+// (-LSE log2 e and -D, written by the preprocess kernel) come with its Q
+// tile.
 //
-// Roles (704 threads):
-//   warps 0-15  P / dS: thread = key row = TMEM lane (warp w takes lanes
-//               32 (w % 4) ...); warp w takes query columns [32 g, 32 g + 32)
-//               of the tile, g = w / 4, so each scheduler runs four of them
-//   warps 16-19 dQ drain (thread = query row), then the dK epilogue
-//   warp  20    TMA producer
-//   warp  21    tcgen05 MMA issuer and TMEM owner
+// Dense launches run one CTA per SM over many key tiles (work items), with
+// the ring positions and barrier phases running on across items; the next
+// item's K is loaded early into the V buffer (free once V is in tensor
+// memory).  Block-sparse launches run one CTA per key tile.
+//
+// Roles (448 threads):
+//   warps 0-7   P / dS: thread = key row = TMEM lane (warp w takes lanes
+//               32 (w % 4) ...); warp w takes query columns [64 g, 64 g + 64)
+//               of the tile, g = w / 4
+//   warps 8-11  K and V into tensor memory, dQ drain (thread = query row),
+//               then the dK epilogue
+//   warp  12    TMA producer
+//   warp  13    tcgen05 MMA issuer and TMEM owner
 #include <cuda_bf16.h>
 
 #include "fa_kernels.h"
