@@ -428,7 +428,11 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     const int r = sp * 32 + lane;
     const int cb = h * C::CPT;          // first key column of this thread
     const int ob = h * C::OCPT;         // first O column of this thread
-    if (valid[t]) {
+    // this tile's flags as scalars (a runtime index into the per-tile arrays
+    // would put them in local memory)
+    const bool valid_t = t ? valid[1] : valid[0];
+    const int ntile_t = t ? ntile[1] : ntile[0];
+    if (valid_t) {
       const int qt = qt0 + t;
       const int row = qt * C::BM + r;
       const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
@@ -466,7 +470,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       if constexpr (C::SEPP) {
         const uint32_t tP = tmem + lane_off + C::colP(t);
         int j = SPARSE ? next_bit(tbits, nw, -1) : 0;
-        for (int step = 0; step < ntile[t]; ++step) {
+        for (int step = 0; step < ntile_t; ++step) {
           if (!warp_wait(smem_u32(&bar_s[t]), step & 1, p.ctl, abort, 30)) {
             ok = false;
             break;
@@ -557,7 +561,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         }
       } else {
       int j = SPARSE ? next_bit(tbits, nw, -1) : 0;
-      for (int step = 0; step < ntile[t]; ++step) {
+      for (int step = 0; step < ntile_t; ++step) {
         if (!warp_wait(smem_u32(&bar_s[t]), step & 1, p.ctl, abort, 30)) {
           ok = false;
           break;
@@ -685,7 +689,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         l += lo;
         lr += lro;
       }
-      if (SPARSE && ntile[t] == 0) {
+      if (SPARSE && ntile_t == 0) {
         // no kept block: every row of the tile sees no key (o = 0, lse = -inf)
         if (row < p.Nq) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.Nq + row) * HD + ob);
