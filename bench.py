@@ -43,20 +43,31 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # DRAM bytes (read + write) of one fa_bwd call on the default workload, summed
 # over its three launches, from one ncu capture (profiles/
 # launches_gpt2_medium_fwd_bwd.md), and the commit of the kernels it measured.
-# The bench line reports it only while the kernel sources are unchanged.
+# The bench line reports it only while the code of the fa_bwd call (the
+# backward kernels, their launch layer and shared helpers, comments aside)
+# is the code the capture measured.
 NCU_TRAFFIC_BYTES = 2145.0e6
 NCU_TRAFFIC_COMMIT = "b56903e"
-NCU_TRAFFIC_SOURCES_SHA256 = "95daf98b75b37981851d827673b2afe4b1c4df9c8f8bdeee03f4499c89852842"
+NCU_TRAFFIC_SOURCES_SHA256 = "dda0702d9b698488635de7111967ca639bb85a5a6a52dff7578e860d11a3eb0e"
+BWD_SOURCES = ("fa_api.cu", "fa_bwd.cu", "fa_bwd_d64.cu", "fa_kernels.h", "sm103_ptx.cuh")
+
+
+def strip_comments(text: str) -> str:
+    """C/C++ source without comments and blank lines (trailing spaces cut)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.split("\n") if line.strip())
 
 
 def kernel_sources_sha256() -> str:
+    """Hash of the fa_bwd call's sources with their comments stripped."""
     import hashlib
     csrc = os.path.join(ROOT, "io_aware_exact_10_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in BWD_SOURCES:
+        with open(os.path.join(csrc, name)) as f:
+            h.update(name.encode() + b"\0" + strip_comments(f.read()).encode())
     return h.hexdigest()
 
 
