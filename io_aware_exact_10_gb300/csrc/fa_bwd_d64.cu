@@ -143,14 +143,13 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   // decode_grid.  An item loops over the query tiles i0 ... nq-1 of each of
   // the kv_group query heads that share the key/value head, in that order;
   // each role follows the (tile, head) pair of its own position in the loop
-  // with a TileWalk.  Dense launches have one CTA per SM (G CTAs), and CTA b
-  // takes items b, 2G-1-b, 2G+b, 4G-1-b, ...: every pass over G items visits
-  // them in the other direction, so with causal masking (items heaviest first
-  // within a head group) each CTA pairs heavy items with light ones.  An
-  // item's set-up then overlaps the previous item's last tiles instead of
-  // costing a CTA launch.  Block-sparse launches have one CTA per item (their
-  // work is uneven in no set order) and the hardware scheduler balances
-  // them.  The ring positions and the per-tile barrier phases run on across
+  // with a TileWalk.  Persistent launches (see persistent_launch) have one
+  // CTA per SM (G CTAs), and CTA b takes items b, 2G-1-b, 2G+b, 4G-1-b, ...:
+  // every pass over G items visits them in the other direction, so with
+  // causal masking (items heaviest first within a head group) each CTA pairs
+  // heavy items with light ones.  An item's set-up then overlaps the previous
+  // item's last tiles instead of costing a CTA launch.  Other launches have
+  // one CTA per item, which the hardware scheduler balances.  The ring positions and the per-tile barrier phases run on across
   // items (global tile index U); K, V, their copy into tensor memory and FIN
   // have one phase per item.
   const int n_items = p.BHkv * p.nkv;
@@ -730,9 +729,9 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
-  // dense: one CTA per SM walks the items; block-sparse: one CTA per item
+  // one persistent CTA per SM walks the items, or one CTA per item
   const long n_items = (long)p.nkv * p.BHkv;
-  const long ctas = SPARSE ? n_items : (n_items < a.num_sms ? n_items : a.num_sms);
+  const long ctas = persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms ? a.num_sms : n_items;
   dim3 grid((unsigned)ctas);
   kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();

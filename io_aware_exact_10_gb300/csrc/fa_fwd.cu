@@ -101,11 +101,13 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
   __shared__ __align__(8) uint64_t bar_q[2];
+  __shared__ __align__(8) uint64_t bar_qe[2];  // Q_t free: the last S_t of an item completed
   __shared__ __align__(8) uint64_t bar_full[C::STAGES];
   __shared__ __align__(8) uint64_t bar_empty[C::STAGES];
   __shared__ __align__(8) uint64_t bar_s[2];
   __shared__ __align__(8) uint64_t bar_p[2];
   __shared__ __align__(8) uint64_t bar_o[2];
+  __shared__ __align__(8) uint64_t bar_of[2];  // O_t free: read by the previous item's epilogue
   __shared__ __align__(8) uint64_t bar_sf[2];  // S_t read by its softmax (P in own columns)
   __shared__ __align__(8) uint64_t bar_pf[2];  // PV_t complete (P in own columns)
   __shared__ __align__(8) uint64_t bar_drain;
@@ -120,46 +122,67 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   __shared__ int mcount[3];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One-dimensional grid over (head group, pair rank, head): the CTAs that
-  // share a head's K and V run together and find them in L2, and within a
-  // group the heaviest (causal) query-tile pairs launch first.
-  const GridPos gp = decode_grid((int)blockIdx.x, p.BH, p.npairs, p.group);
-  const int bh = gp.bh;
-  const int bhkv = bh / p.kv_group;  // key/value head of this query head
-  const int qt0 = 2 * (p.npairs - 1 - gp.rank);
-  bool valid[2];
-  int nkv_t[2];
-  for (int t = 0; t < 2; ++t) {
-    valid[t] = qt0 + t < p.nq;
-    // causal: up to the tile of the last key its last row sees
-    nkv_t[t] = !valid[t] ? 0
-                         : (CAUSAL ? min(((qt0 + t) * C::BM + C::BM - 1 + p.coff) / C::BN + 1, p.nkv)
-                                   : p.nkv);
-  }
-  // Key tiles each query tile visits (ntile) and the tiles the pair streams
-  // (nu): dense, tiles 0 .. nkv_t-1 and 0 .. max(nkv_t)-1; block-sparse, the
-  // tiles the mask keeps within those bounds, in ascending order.  The TMA
-  // warp builds the bitsets; every other warp reads the counts after the
-  // CTA-wide sync.
-  int ntile[2] = {nkv_t[0], nkv_t[1]};
-  int nu = max(nkv_t[0], nkv_t[1]);
+  // Work items are the query-tile pairs of every head, in a one-dimensional
+  // order over (head group, pair rank, head): the pairs that share a head's
+  // K and V run together and find them in L2, and within a group the
+  // heaviest (causal) pairs come first.  Persistent launches (see
+  // persistent_launch) have one CTA per SM (G CTAs), and CTA b takes items b,
+  // 2G-1-b, 2G+b, 4G-1-b, ...: each pass over G items runs the other way, so
+  // causal CTAs pair heavy items with light ones, and the next item's Q and
+  // K/V loads and first S overlap the current item's last steps and
+  // epilogue.  Other launches have one CTA per item.  Every role walks the
+  // same items; the ring index and the barrier phases run on across items.
+  const int n_items = p.npairs * p.BH;
+  const int L0 = (int)blockIdx.x, LS = (int)gridDim.x;
+  auto item_at = [&](int k) { return k * LS + ((k & 1) ? LS - 1 - L0 : L0); };  // k-th item
+  struct Item {
+    int bh, bhkv, qt0;
+    bool valid[2];
+    int nkv_t[2];  // causal: key tiles up to the one its last row's last key is in
+    int ntile[2];  // key tiles query tile t visits
+    int nu;        // key tiles the pair streams
+  };
+  auto item_info = [&](int L) {
+    Item I;
+    const GridPos gp = decode_grid(L, p.BH, p.npairs, p.group);
+    I.bh = gp.bh;
+    I.bhkv = gp.bh / p.kv_group;  // key/value head of this query head
+    I.qt0 = 2 * (p.npairs - 1 - gp.rank);
+    #pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      I.valid[t] = I.qt0 + t < p.nq;
+      I.nkv_t[t] = !I.valid[t] ? 0
+                   : (CAUSAL ? min(((I.qt0 + t) * C::BM + C::BM - 1 + p.coff) / C::BN + 1, p.nkv)
+                             : p.nkv);
+      I.ntile[t] = I.nkv_t[t];
+    }
+    I.nu = max(I.nkv_t[0], I.nkv_t[1]);
+    return I;
+  };
+  // Key tiles each query tile visits and the tiles the pair streams: dense,
+  // tiles 0 .. nkv_t-1 and 0 .. max(nkv_t)-1; block-sparse, the tiles the
+  // mask keeps within those bounds, in ascending order.  The TMA warp builds
+  // the bitsets of the CTA's one item; the other warps read the counts after
+  // the CTA-wide sync.
+  Item I0 = item_info(L0);
   const int nw = (p.nkv + 31) >> 5;
   uint32_t* const ubits = mbits + (SPARSE ? 2 * kMaskWords : 0);
   if constexpr (SPARSE) {
     if (warp == C::W_LOAD) {
+      #pragma unroll
       for (int t = 0; t < 2; ++t)
-        mask_bits_warp(p.bmask + (valid[t] ? (size_t)(qt0 + t) * p.nkv : 0), 1, 0,
-                       valid[t] ? nkv_t[t] : 0, nw, mbits + t * kMaskWords, lane);
+        mask_bits_warp(p.bmask + (I0.valid[t] ? (size_t)(I0.qt0 + t) * p.nkv : 0), 1, 0,
+                       I0.valid[t] ? I0.nkv_t[t] : 0, nw, mbits + t * kMaskWords, lane);
       __syncwarp();
       for (int w = lane; w < nw; w += 32) ubits[w] = mbits[w] | mbits[kMaskWords + w];
       __syncwarp();
-      ntile[0] = mask_popc_warp(mbits, nw, lane);
-      ntile[1] = mask_popc_warp(mbits + kMaskWords, nw, lane);
-      nu = mask_popc_warp(ubits, nw, lane);
+      I0.ntile[0] = mask_popc_warp(mbits, nw, lane);
+      I0.ntile[1] = mask_popc_warp(mbits + kMaskWords, nw, lane);
+      I0.nu = mask_popc_warp(ubits, nw, lane);
       if (lane == 0) {
-        mcount[0] = ntile[0];
-        mcount[1] = ntile[1];
-        mcount[2] = nu;
+        mcount[0] = I0.ntile[0];
+        mcount[1] = I0.ntile[1];
+        mcount[2] = I0.nu;
       }
     }
   }
@@ -171,7 +194,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   // no wait (the Q tiles and the first ring slots) before the CTA-wide sync,
   // so their latency overlaps the rest of the set-up.  Ring index it holds
   // K_j (it even) or V_j (it odd) of the pair's (it/2)-th key tile j.
-  auto issue_kv = [&](int it, int j) {
+  auto issue_kv = [&](int it, int j, int bhkv) {
     const int slot = it % C::STAGES;
     const uint32_t bar = smem_u32(&bar_full[slot]);
     mbar_arrive_expect_tx(bar, C::KVTILE);
@@ -179,17 +202,26 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     for (int b = 0; b < C::KB; ++b)
       tma_load_3d(dst + b * C::BN * 128, (it & 1) ? &tv : &tk, bar, b * 64, j * C::BN, bhkv);
   };
-  const int n_it = 2 * nu;                                   // ring uses: K, V of each tile
-  const int pre_it = n_it < C::STAGES ? n_it : C::STAGES;    // issued before the sync
-  int jw = 0;  // the TMA thread's key tile (of ring index it)
+  auto issue_q = [&](int t, const Item& I) {
+    const uint32_t bar = smem_u32(&bar_q[t]);
+    mbar_arrive_expect_tx(bar, C::QTILE);
+    for (int b = 0; b < C::KB; ++b)
+      tma_load_3d(sQ + t * C::QTILE + b * C::BM * 128, &tq, bar, b * 64, (I.qt0 + t) * C::BM, I.bh);
+  };
+  auto live = [](const Item& I, int t) { return I.valid[t] && I.ntile[t] > 0; };
+  const int pre_it = 2 * I0.nu < C::STAGES ? 2 * I0.nu : C::STAGES;  // issued before the sync
+  int jw = 0;  // the TMA thread's key tile (of ring index it; block-sparse)
   if (warp == C::W_LOAD && lane == 0) {
     abort_sh = 0;
+    #pragma unroll
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bar_q[t]), 1);
+      mbar_init(smem_u32(&bar_qe[t]), 1);
       mbar_init(smem_u32(&bar_s[t]), 1);
       mbar_init(smem_u32(&bar_p[t]), 4 * NH);
       for (int sp = 0; sp < 4; ++sp) mbar_init(smem_u32(&bar_x[t][sp]), 64);
       mbar_init(smem_u32(&bar_o[t]), 1);
+      mbar_init(smem_u32(&bar_of[t]), 4 * NH);
       mbar_init(smem_u32(&bar_sf[t]), 4 * NH);
       mbar_init(smem_u32(&bar_pf[t]), 1);
     }
@@ -202,17 +234,13 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
-    for (int t = 0; t < 2; ++t) {
-      if (!valid[t] || ntile[t] == 0) continue;
-      const uint32_t bar = smem_u32(&bar_q[t]);
-      mbar_arrive_expect_tx(bar, C::QTILE);
-      for (int b = 0; b < C::KB; ++b)
-        tma_load_3d(sQ + t * C::QTILE + b * C::BM * 128, &tq, bar, b * 64, (qt0 + t) * C::BM, bh);
-    }
+    #pragma unroll
+    for (int t = 0; t < 2; ++t)
+      if (live(I0, t)) issue_q(t, I0);
     if constexpr (SPARSE) jw = next_bit(ubits, nw, -1);
     for (int it = 0; it < pre_it; ++it) {
-      issue_kv(it, jw);
-      if (it & 1) jw = SPARSE ? next_bit(ubits, nw, jw) : jw + 1;
+      issue_kv(it, SPARSE ? jw : it >> 1, I0.bhkv);
+      if (SPARSE && (it & 1)) jw = next_bit(ubits, nw, jw);
     }
   }
   if (warp == C::W_MMA) {
@@ -224,30 +252,53 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   if constexpr (SPARSE) {
-    ntile[0] = mcount[0];
-    ntile[1] = mcount[1];
-    nu = mcount[2];
+    I0.ntile[0] = mcount[0];
+    I0.ntile[1] = mcount[1];
+    I0.nu = mcount[2];
   }
   if (warp == C::W_LOAD) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
-      int it = pre_it;
+      int it = pre_it;  // ring index, across items
+      int nql[2] = {live(I0, 0) ? 1 : 0, live(I0, 1) ? 1 : 0};  // Q_t loads issued
       bool ok = true;
-      for (; it < n_it; ++it) {
-        const int slot = it % C::STAGES, use = it / C::STAGES;
-        if (use > 0 && !mbar_wait(smem_u32(&bar_empty[slot]), (use - 1) & 1, p.ctl, abort, 10)) {
-          ok = false;
-          break;
+      Item I = I0;
+      int i = pre_it;  // ring use within the item
+      for (int L = L0, kk = 0;;) {
+        for (; i < 2 * I.nu; ++i, ++it) {
+          const int slot = it % C::STAGES, use = it / C::STAGES;
+          if (use > 0 && !mbar_wait(smem_u32(&bar_empty[slot]), (use - 1) & 1, p.ctl, abort, 10)) {
+            ok = false;
+            break;
+          }
+          issue_kv(it, SPARSE ? jw : i >> 1, I.bhkv);
+          if (SPARSE && (i & 1)) jw = next_bit(ubits, nw, jw);
         }
-        issue_kv(it, jw);
-        if (it & 1) jw = SPARSE ? next_bit(ubits, nw, jw) : jw + 1;
+        if (!ok) break;
+        L = item_at(++kk);
+        if (L >= n_items) break;
+        I = item_info(L);
+        // the next item's Q_t, once the MMA no longer reads the previous one
+        #pragma unroll
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!live(I, t)) continue;
+          if (nql[t] > 0 && !mbar_wait(smem_u32(&bar_qe[t]), (nql[t] - 1) & 1, p.ctl, abort, 11)) {
+            ok = false;
+            break;
+          }
+          issue_q(t, I);
+          ++nql[t];
+        }
+        if (!ok) break;
+        i = 0;
       }
       if (!ok) {
         // Abort: let the copies already issued land before the CTA exits.
         for (int s = 0; s < C::STAGES && s < it; ++s)
           mbar_wait_quiet(smem_u32(&bar_full[s]), ((it - 1 - s) / C::STAGES) & 1, 200000000ull);
+        #pragma unroll
         for (int t = 0; t < 2; ++t)
-          if (valid[t] && ntile[t] > 0) mbar_wait_quiet(smem_u32(&bar_q[t]), 0, 200000000ull);
+          if (nql[t] > 0) mbar_wait_quiet(smem_u32(&bar_q[t]), (nql[t] - 1) & 1, 200000000ull);
       }
     }
   } else if (warp == C::W_MMA) {
@@ -262,25 +313,6 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       constexpr uint32_t HI = sdesc_hi(1024);
       constexpr uint32_t QT16 = C::QTILE >> 4, KV16 = C::KVTILE >> 4, BLK16 = (C::BM * 128) >> 4;
       const uint32_t qK = sdesc_lo(sQ, 16), rK = sdesc_lo(sRing, 16), rMN = sdesc_lo(sRing, C::BN * 128);
-      bool ok = true;
-      for (int t = 0; t < 2 && ok; ++t)
-        if (valid[t] && ntile[t] > 0) ok = warp_wait(smem_u32(&bar_q[t]), 0, p.ctl, abort, 20);
-      // Does query tile t use key tile j?  The next key tile of the pair.
-      auto active = [&](int t, int j) -> bool {
-        if constexpr (SPARSE)
-          return ((mbits[t * kMaskWords + (j >> 5)] >> (j & 31)) & 1u) != 0;
-        else
-          return valid[t] && j < nkv_t[t];
-      };
-      auto next_j = [&](int j) -> int {
-        if constexpr (SPARSE)
-          return next_bit(ubits, nw, j);
-        else
-          return j + 1;
-      };
-      // per query tile: S issued, O += P V issued (barrier phases follow them)
-      int cs[2] = {0, 0}, cp[2] = {0, 0};
-
       // S_t = Q_t K^T for the K tile in ring slot `slot`.
       auto issue_s = [&](int t, int slot) {
         const uint32_t a0 = qK + (uint32_t)t * QT16, b0 = rK + (uint32_t)slot * KV16;
@@ -300,119 +332,159 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
                    (acc || k > 0) ? 1u : 0u);
       };
 
-      if constexpr (C::SEPP) {
-        // The pair's q-th key tile u_q has K at ring index 2q, V at 2q + 1.
-        // Per q, with j = u_q and jn = u_{q+1}:
-        //   [S_t read] S_t(jn);  [P_t ready] O_t += P_t V_j
-        int j = SPARSE ? next_bit(ubits, nw, -1) : 0;
-        if (ok && nu > 0) {
-          ok = warp_wait(smem_u32(&bar_full[0]), 0, p.ctl, abort, 21);
-          if (ok) {
-            tc_fence_after();
-            for (int t = 0; t < 2; ++t)
-              if (active(t, j)) {
-                issue_s(t, 0);
-                ++cs[t];
-              }
-            mma_commit_e(lead, smem_u32(&bar_empty[0]));
-          }
-        }
-        for (int q = 0; q < nu && ok; ++q) {
-          const int jn = q + 1 < nu ? next_j(j) : -1;
-          if (q + 1 < nu) {
-            const int ik = 2 * (q + 1), ks = ik % C::STAGES;
-            if (!(ok = warp_wait(smem_u32(&bar_full[ks]), (ik / C::STAGES) & 1, p.ctl, abort, 24))) break;
-            for (int t = 0; t < 2 && ok; ++t) {
-              if (!active(t, jn)) continue;
-              if (cs[t] > 0 && !(ok = warp_wait(smem_u32(&bar_sf[t]), (cs[t] - 1) & 1, p.ctl, abort, 26)))
-                break;
-              tc_fence_after();
-              issue_s(t, ks);
-              ++cs[t];
-            }
-            if (!ok) break;
-            mma_commit_e(lead, smem_u32(&bar_empty[ks]));
-          }
-          const int iv = 2 * q + 1, vs = iv % C::STAGES;
-          if (!(ok = warp_wait(smem_u32(&bar_full[vs]), (iv / C::STAGES) & 1, p.ctl, abort, 22))) break;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (!active(t, j)) continue;
-            if (!(ok = warp_wait(smem_u32(&bar_p[t]), cp[t] & 1, p.ctl, abort, 23))) break;
-            tc_fence_after();
-            issue_pv(t, vs, cp[t] > 0);
-            mma_commit_e(lead, smem_u32(&bar_pf[t]));
-            if (cp[t] == ntile[t] - 1) mma_commit_e(lead, smem_u32(&bar_o[t]));
-            ++cp[t];
-          }
-          if (!ok) break;
-          mma_commit_e(lead, smem_u32(&bar_empty[vs]));
-          j = jn;
-        }
-      } else {
-      // Iteration q takes V of the pair's key tile j = u_{q-1}, then K of
-      // jn = u_q.  S_t(jn) overwrites the columns that O_t += P_t V read, so
-      // it is issued after tile t's last O += P V, which comes earlier in
-      // the same iteration or in an earlier one.
-      int it = 0;
-      int j = SPARSE ? next_bit(ubits, nw, -1) : 0;
-      if (ok && nu > 0) {
-        ok = warp_wait(smem_u32(&bar_full[0]), 0, p.ctl, abort, 21);
-        if (ok) {
+      // Per query tile, across items: S issued, O += P V issued (barrier
+      // phases follow them), Q_t waits, and items whose O_t was committed.
+      int cs[2] = {0, 0}, cp[2] = {0, 0}, nqw[2] = {0, 0}, no[2] = {0, 0};
+      int it0 = 0;  // ring index of the item's first K
+      bool ok = true;
+      for (int L = L0, kk = 0; L < n_items && ok; L = item_at(++kk)) {
+        const Item I = L == L0 ? I0 : item_info(L);
+        #pragma unroll
+        for (int t = 0; t < 2 && ok; ++t)
+          if (live(I, t)) ok = warp_wait(smem_u32(&bar_q[t]), (nqw[t]++) & 1, p.ctl, abort, 20);
+        if (!ok) break;
+        // Does query tile t use key tile j?  The next key tile of the pair.
+        auto active = [&](int t, int j) -> bool {
+          if constexpr (SPARSE)
+            return ((mbits[t * kMaskWords + (j >> 5)] >> (j & 31)) & 1u) != 0;
+          else
+            return I.valid[t] && j < I.nkv_t[t];
+        };
+        auto next_j = [&](int j) -> int {
+          if constexpr (SPARSE)
+            return next_bit(ubits, nw, j);
+          else
+            return j + 1;
+        };
+        int ls[2] = {0, 0}, lp[2] = {0, 0};  // S and O += P V issued in this item
+        // S_t for the K tile in ring slot ks, with the item's Q_t released
+        // after its last S_t.
+        auto s_step = [&](int t, int ks) {
+          issue_s(t, ks);
+          ++cs[t];
+          if (++ls[t] == I.ntile[t]) mma_commit_e(lead, smem_u32(&bar_qe[t]));
+        };
+        // O_t (+)= P_t V for the V tile in ring slot vs.  The item's first one
+        // overwrites O_t: the previous item's epilogue must have read it.
+        auto pv_step = [&](int t, int vs) -> bool {
+          if (lp[t] == 0 && no[t] > 0 &&
+              !warp_wait(smem_u32(&bar_of[t]), (no[t] - 1) & 1, p.ctl, abort, 27))
+            return false;
+          if (!warp_wait(smem_u32(&bar_p[t]), cp[t] & 1, p.ctl, abort, 23)) return false;
           tc_fence_after();
-          for (int t = 0; t < 2; ++t)
-            if (active(t, j)) {
-              issue_s(t, 0);
-              ++cs[t];
+          issue_pv(t, vs, lp[t] > 0);
+          if constexpr (C::SEPP) mma_commit_e(lead, smem_u32(&bar_pf[t]));
+          ++cp[t];
+          if (++lp[t] == I.ntile[t]) {
+            mma_commit_e(lead, smem_u32(&bar_o[t]));
+            ++no[t];
+          }
+          return true;
+        };
+
+        if constexpr (C::SEPP) {
+          // The pair's q-th key tile u_q has K at ring index it0 + 2q, V at
+          // it0 + 2q + 1.  Per q, with j = u_q and jn = u_{q+1}:
+          //   [S_t read] S_t(jn);  [P_t ready] O_t += P_t V_j
+          // S_t overwrites S_t only after the softmax has read it (also the
+          // last S_t of the previous item).
+          int j = SPARSE ? next_bit(ubits, nw, -1) : 0;
+          auto s_after_read = [&](int t, int ks) -> bool {
+            if (cs[t] > 0 && !warp_wait(smem_u32(&bar_sf[t]), (cs[t] - 1) & 1, p.ctl, abort, 26))
+              return false;
+            tc_fence_after();
+            s_step(t, ks);
+            return true;
+          };
+          if (I.nu > 0) {
+            const int ks = it0 % C::STAGES;
+            ok = warp_wait(smem_u32(&bar_full[ks]), (it0 / C::STAGES) & 1, p.ctl, abort, 21);
+            if (ok) {
+              tc_fence_after();
+              #pragma unroll
+              for (int t = 0; t < 2 && ok; ++t)
+                if (active(t, j)) ok = s_after_read(t, ks);
+              if (ok) mma_commit_e(lead, smem_u32(&bar_empty[ks]));
             }
-          mma_commit_e(lead, smem_u32(&bar_empty[0]));
-          it = 1;
-        }
-      }
-      for (int q = 1; q <= nu && ok; ++q) {
-        const int vslot = it % C::STAGES;
-        ok = warp_wait(smem_u32(&bar_full[vslot]), (it / C::STAGES) & 1, p.ctl, abort, 22);
-        ++it;
-        if (!ok) break;
-        tc_fence_after();
-        const bool have_k = q < nu;
-        const int jn = have_k ? next_j(j) : -1;
-        const int kslot = it % C::STAGES, kpar = (it / C::STAGES) & 1;
-        if (have_k) ++it;
-        bool k_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (active(t, j)) {
-            ok = warp_wait(smem_u32(&bar_p[t]), cp[t] & 1, p.ctl, abort, 23);
+          }
+          for (int q = 0; q < I.nu && ok; ++q) {
+            const int jn = q + 1 < I.nu ? next_j(j) : -1;
+            if (q + 1 < I.nu) {
+              const int ik = it0 + 2 * (q + 1), ks = ik % C::STAGES;
+              if (!(ok = warp_wait(smem_u32(&bar_full[ks]), (ik / C::STAGES) & 1, p.ctl, abort, 24))) break;
+              #pragma unroll
+              for (int t = 0; t < 2 && ok; ++t)
+                if (active(t, jn)) ok = s_after_read(t, ks);
+              if (!ok) break;
+              mma_commit_e(lead, smem_u32(&bar_empty[ks]));
+            }
+            const int iv = it0 + 2 * q + 1, vs = iv % C::STAGES;
+            if (!(ok = warp_wait(smem_u32(&bar_full[vs]), (iv / C::STAGES) & 1, p.ctl, abort, 22))) break;
+            #pragma unroll
+            for (int t = 0; t < 2 && ok; ++t)
+              if (active(t, j)) ok = pv_step(t, vs);
+            if (!ok) break;
+            mma_commit_e(lead, smem_u32(&bar_empty[vs]));
+            j = jn;
+          }
+        } else {
+          // Iteration q takes V of the pair's key tile j = u_{q-1}, then K of
+          // jn = u_q.  S_t(jn) overwrites the columns that O_t += P_t V read,
+          // so it is issued after tile t's last O += P V, which comes earlier
+          // in the same iteration or in an earlier one (or item).
+          int it = it0;
+          int j = SPARSE ? next_bit(ubits, nw, -1) : 0;
+          if (I.nu > 0) {
+            ok = warp_wait(smem_u32(&bar_full[it % C::STAGES]), (it / C::STAGES) & 1, p.ctl, abort, 21);
+            if (ok) {
+              tc_fence_after();
+              #pragma unroll
+              for (int t = 0; t < 2; ++t)
+                if (active(t, j)) s_step(t, it % C::STAGES);
+              mma_commit_e(lead, smem_u32(&bar_empty[it % C::STAGES]));
+              ++it;
+            }
+          }
+          for (int q = 1; q <= I.nu && ok; ++q) {
+            const int vslot = it % C::STAGES;
+            ok = warp_wait(smem_u32(&bar_full[vslot]), (it / C::STAGES) & 1, p.ctl, abort, 22);
+            ++it;
             if (!ok) break;
             tc_fence_after();
-            issue_pv(t, vslot, cp[t] > 0);
-            if (cp[t] == ntile[t] - 1) mma_commit_e(lead, smem_u32(&bar_o[t]));
-            ++cp[t];
-          }
-          if (have_k && active(t, jn)) {
-            if (!k_ready) {
-              ok = warp_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 24);
-              if (!ok) break;
-              tc_fence_after();
-              k_ready = true;
+            const bool have_k = q < I.nu;
+            const int jn = have_k ? next_j(j) : -1;
+            const int kslot = it % C::STAGES, kpar = (it / C::STAGES) & 1;
+            if (have_k) ++it;
+            bool k_ready = false;
+            #pragma unroll
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (active(t, j) && !(ok = pv_step(t, vslot))) break;
+              if (have_k && active(t, jn)) {
+                if (!k_ready) {
+                  ok = warp_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 24);
+                  if (!ok) break;
+                  tc_fence_after();
+                  k_ready = true;
+                }
+                s_step(t, kslot);
+              }
             }
-            issue_s(t, kslot);
-            ++cs[t];
-          }
-        }
-        if (!ok) break;
-        mma_commit_e(lead, smem_u32(&bar_empty[vslot]));
-        if (have_k) {
-          if (!k_ready) {
-            ok = warp_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 25);
             if (!ok) break;
+            mma_commit_e(lead, smem_u32(&bar_empty[vslot]));
+            if (have_k) {
+              if (!k_ready) {
+                ok = warp_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 25);
+                if (!ok) break;
+              }
+              mma_commit_e(lead, smem_u32(&bar_empty[kslot]));
+            }
+            j = jn;
           }
-          mma_commit_e(lead, smem_u32(&bar_empty[kslot]));
         }
-        j = jn;
-      }
+        it0 += 2 * I.nu;
       }
       // Drain: every MMA issued above completes before TMEM is released.
-      if (nu > 0) {
+      if (cs[0] + cs[1] > 0) {
         mma_commit_e(lead, smem_u32(&bar_drain));
         mbar_wait_quiet(smem_u32(&bar_drain), 0, 200000000ull);
       }
@@ -428,13 +500,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     const int r = sp * 32 + lane;
     const int cb = h * C::CPT;          // first key column of this thread
     const int ob = h * C::OCPT;         // first O column of this thread
-    // this tile's flags as scalars (a runtime index into the per-tile arrays
-    // would put them in local memory)
-    const bool valid_t = t ? valid[1] : valid[0];
-    const int ntile_t = t ? ntile[1] : ntile[0];
-    if (valid_t) {
-      const int qt = qt0 + t;
-      const int row = qt * C::BM + r;
+    {
       const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
       const uint32_t tS = tmem + lane_off + C::colS(t);
       const uint32_t tO = tmem + lane_off + C::colO(t);
@@ -459,19 +525,30 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       // value O += P V multiplied), so a row dominated by one key gets that
       // key's V row exactly.  With NH = 2 each half keeps partial sums,
       // combined once at the end.
-      float m = -INFINITY, l = 0.f, lr = 0.f;
-      bool ok = true;
-      // Step `step` of this tile handles key tile j: j = step when dense,
-      // the step-th kept tile when block-sparse.  Under a block mask a row may have
-      // seen no key yet (m = -inf); its exponentials then use 0 in place of
-      // m, which gives P = 0 for masked keys instead of -inf - -inf.
+      // Step lstep of an item handles key tile j: j = lstep when dense, the
+      // lstep-th kept tile when block-sparse; gstep counts steps across
+      // items (barrier phases).  Under a block mask a row may have seen no
+      // key yet (m = -inf); its exponentials then use 0 in place of m, which
+      // gives P = 0 for masked keys instead of -inf - -inf.
       const uint32_t* tbits = mbits + t * (SPARSE ? kMaskWords : 0);
       auto m_ref = [](float mv) { return (SPARSE && mv == -INFINITY) ? 0.f : mv; };
+      int gstep = 0, nio = 0;  // steps and epilogues of this tile so far
+      bool ok = true;
+      for (int L = L0, kk = 0; L < n_items && ok; L = item_at(++kk)) {
+      const Item I = L == L0 ? I0 : item_info(L);
+      // this tile's flags as scalars (a runtime index into the item's
+      // arrays would put them in local memory)
+      const bool valid_t = t ? I.valid[1] : I.valid[0];
+      const int ntile_t = t ? I.ntile[1] : I.ntile[0];
+      if (!valid_t) continue;
+      const int bh = I.bh;
+      const int row = (I.qt0 + t) * C::BM + r;
+      float m = -INFINITY, l = 0.f, lr = 0.f;
       if constexpr (C::SEPP) {
         const uint32_t tP = tmem + lane_off + C::colP(t);
         int j = SPARSE ? next_bit(tbits, nw, -1) : 0;
-        for (int step = 0; step < ntile_t; ++step) {
-          if (!warp_wait(smem_u32(&bar_s[t]), step & 1, p.ctl, abort, 30)) {
+        for (int lstep = 0; lstep < ntile_t; ++lstep, ++gstep) {
+          if (!warp_wait(smem_u32(&bar_s[t]), gstep & 1, p.ctl, abort, 30)) {
             ok = false;
             break;
           }
@@ -501,8 +578,9 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
           const float m_new = fmaxf(m, mx * scale2);
           const bool need = m_new > m + kTau;
-          // P_t and O_t: the previous O_t += P_t V must have completed
-          if (step > 0 && !warp_wait(smem_u32(&bar_pf[t]), (step - 1) & 1, p.ctl, abort, 33)) {
+          // P_t and O_t: the previous O_t += P_t V (also of the previous
+          // item) must have completed
+          if (gstep > 0 && !warp_wait(smem_u32(&bar_pf[t]), (gstep - 1) & 1, p.ctl, abort, 33)) {
             ok = false;
             break;
           }
@@ -512,7 +590,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
             if (need) m = m_new;
             l *= alpha;
             lr *= alpha;
-            if (step > 0) {
+            if (lstep > 0) {
 #pragma unroll 1
               for (int c0 = 0; c0 < HD; c0 += 32) {
                 uint32_t ov[32];
@@ -557,12 +635,12 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           if constexpr (SPARSE)
             j = next_bit(tbits, nw, j);
           else
-            j = step + 1;
+            j = lstep + 1;
         }
       } else {
       int j = SPARSE ? next_bit(tbits, nw, -1) : 0;
-      for (int step = 0; step < ntile_t; ++step) {
-        if (!warp_wait(smem_u32(&bar_s[t]), step & 1, p.ctl, abort, 30)) {
+      for (int lstep = 0; lstep < ntile_t; ++lstep, ++gstep) {
+        if (!warp_wait(smem_u32(&bar_s[t]), gstep & 1, p.ctl, abort, 30)) {
           ok = false;
           break;
         }
@@ -611,7 +689,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           if (need) m = m_new;
           l *= alpha;
           lr *= alpha;
-          if (step > 0) {
+          if (lstep > 0) {
             // O_t is complete here: S_t of this step was issued after the
             // previous O_t += P_t V and its commit covers every earlier MMA
             // of the issuing thread.
@@ -677,7 +755,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         if constexpr (SPARSE)
           j = next_bit(tbits, nw, j);
         else
-          j = step + 1;
+          j = lstep + 1;
       }
       }
       // Epilogue: O / lr -> bf16, and LSE = ln 2 * (m + log2 l).
@@ -689,6 +767,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         l += lo;
         lr += lro;
       }
+      if (!ok) break;
       if (SPARSE && ntile_t == 0) {
         // no kept block: every row of the tile sees no key (o = 0, lse = -inf)
         if (row < p.Nq) {
@@ -697,7 +776,8 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           for (int i = 0; i < C::OCPT / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
           if (h == 0) p.lse[(size_t)bh * p.Nq + row] = -INFINITY;
         }
-      } else if (ok && warp_wait(smem_u32(&bar_o[t]), 0, p.ctl, abort, 31)) {
+      } else {
+        if (!(ok = warp_wait(smem_u32(&bar_o[t]), (nio++) & 1, p.ctl, abort, 31))) break;
         tc_fence_after();
         // a row that saw no key (block-sparse only) has lr = 0 and o = 0
         const float inv_l = (SPARSE && !(lr > 0.f)) ? 0.f : 1.0f / lr;
@@ -719,7 +799,12 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           }
         }
         if (h == 0 && row < p.Nq) p.lse[(size_t)bh * p.Nq + row] = (m + __log2f(l)) * kLn2;
+        // O_t has been read: the next item's first O_t += P_t V may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_of[t]));
       }
+      }  // items
     }
   }
 
@@ -754,7 +839,11 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   p.bmask = a.bmask;
   p.scale2 = a.scale * 1.4426950408889634f;
   p.ctl = a.ctl;
-  dim3 grid((unsigned)((long)p.npairs * a.BH));
+  // one persistent CTA per SM walks the pairs, or one CTA per pair
+  // (block-sparse: each builds the bitsets of its own mask rows)
+  const long n_items = (long)p.npairs * a.BH;
+  const long ctas = persistent_launch(CAUSAL, SPARSE, p.npairs) && n_items > a.num_sms ? a.num_sms : n_items;
+  dim3 grid((unsigned)ctas);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, p);
   return cudaGetLastError();
 }
