@@ -147,13 +147,14 @@ static_assert(BwdCfg<128>::SMEM % 16 == 0 && BwdCfg<128>::SMEM + kMaskWords * 4 
 enum : int {
   B_KV = 0, B_QF0 = 1, B_QF1 = 2, B_DOF0 = 3, B_DOF1 = 4, B_QE0 = 5, B_QE1 = 6, B_DOE0 = 7,
   B_DOE1 = 8, B_ST = 9, B_DPT = 10, B_P = 11, B_DS = 12, B_DQF = 13, B_DQE = 14, B_FIN = 15,
-  B_DRAIN = 16, B_WG = 17, B_COUNT = 18
+  B_DRAIN = 16, B_WG = 17, B_DKF = 18, B_COUNT = 19
 };
 // arrival counts: TMA / commit barriers take one arrival; B_P and B_DS one
 // per P/dS warp; B_QE*, B_DOE* and B_DQE one per drain warp (the drain frees
-// the Q and dO slots: it stages dQ in them); B_WG every P/dS thread.
+// the Q and dO slots: it stages dQ in them); B_WG every P/dS thread; B_DKF
+// (dK read out, the next item may overwrite it) one per drain warp.
 __device__ __constant__ const uint32_t kBarCount[B_COUNT] = {1, 1, 1, 1, 1, 4, 4, 4, 4, 1, 1, 8, 8,
-                                                             1, 4, 1, 1, 256};
+                                                             1, 4, 1, 1, 256, 4};
 
 struct BwdParams {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
@@ -199,21 +200,39 @@ __global__ void __launch_bounds__(448, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One-dimensional grid over (head group, key tile, head): the CTAs of a
-  // group's heads run together, share their Q, dO in L2 and add into the same
-  // dQ rows (which then stay in L2).  Key tile 0 (the most work when causal)
-  // of every head in the group comes first.
-  // One CTA per (key/value head, key tile).  It loops over the query tiles
-  // i0 ... nq-1 of each of the kv_group query heads that share the key/value
-  // head, in that order; each role follows the (tile, head) pair of its own
-  // position in the loop with a TileWalk.
-  const GridPos gp = decode_grid((int)blockIdx.x, p.BHkv, p.nkv, p.group);
-  const int bk = gp.bh;
-  const int kt = gp.rank;
-  const int i0 = CAUSAL ? first_query_tile(kt, p.coff) : 0;  // first query tile that sees this key tile
-  // Block-sparse: the TMA warp turns this key tile's mask column (query
-  // tiles i0 .. nq-1) into a bitset after the barrier area; with no kept
-  // tile the CTA only zeroes its dK, dV rows.
+  // Work items are (key/value head, key tile) pairs in a one-dimensional
+  // order over (head group, key tile, head): the items of a group's heads run
+  // together, share their Q, dO in L2 and add into the same dQ rows (which
+  // then stay in L2); key tile 0 (the most work when causal) of every head in
+  // the group comes first.  An item loops over the query tiles i0 ... nq-1 of
+  // each of the kv_group query heads that share the key/value head, in that
+  // order; each role follows the (tile, head) pair of its own position in the
+  // loop with a TileWalk.  Persistent launches (see persistent_launch) have
+  // one CTA per SM (G CTAs), and CTA b takes items b, 2G-1-b, 2G+b, ...:
+  // each pass over G items runs the other way, pairing heavy causal items
+  // with light ones.  Other launches have one CTA per item.  The ring
+  // positions, the per-tile barrier phases and the statistics buffers run on
+  // across items (global tile index U); K, V, FIN and "dK read out" have one
+  // phase per item.
+  const int n_items = p.BHkv * p.nkv;
+  const int L0 = (int)blockIdx.x, LS = (int)gridDim.x;
+  auto item_at = [&](int k) { return k * LS + ((k & 1) ? LS - 1 - L0 : L0); };  // k-th item
+  struct Item {
+    int bk, kt, i0;
+  };
+  auto item_info = [&](int L) {
+    const GridPos gp = decode_grid(L, p.BHkv, p.nkv, p.group);
+    Item I;
+    I.bk = gp.bh;
+    I.kt = gp.rank;
+    I.i0 = CAUSAL ? first_query_tile(I.kt, p.coff) : 0;  // first query tile that sees this key tile
+    return I;
+  };
+  const Item I0 = item_info(L0);
+  const int bk = I0.bk, kt = I0.kt, i0 = I0.i0;
+  // Block-sparse (one item per CTA): the TMA warp turns this key tile's mask
+  // column (query tiles i0 .. nq-1) into a bitset after the barrier area;
+  // with no kept tile the CTA only zeroes its dK, dV rows.
   QuerySeq<SPARSE> qseq{reinterpret_cast<const uint32_t*>(smem + C::SMEM), (p.nq + 31) >> 5, i0, p.nq};
   int nqt = p.nq - i0;  // query tiles per query head
   if constexpr (SPARSE) {
@@ -233,8 +252,15 @@ __global__ void __launch_bounds__(448, 1)
     }
     qseq.first = next_bit(qbits, qseq.nw, -1);
   }
-  const int nit = nqt * p.kv_group;                // query tiles to process
+  const int nit = nqt * p.kv_group;                // query tiles of the first item
   const TileWalk walk0{qseq.first, bk * p.kv_group};
+  // per item (dense items after the first): query tiles and query-tile sequence
+  auto item_nit = [&](const Item& I) { return (p.nq - I.i0) * p.kv_group; };
+  auto item_seq = [&](const Item& I) {
+    QuerySeq<SPARSE> s = qseq;
+    if constexpr (!SPARSE) s.first = I.i0;
+    return s;
+  };
 
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
@@ -246,9 +272,10 @@ __global__ void __launch_bounds__(448, 1)
   // no wait (K, V, and Q and dO of the first two query tiles) before the
   // CTA-wide sync, so their latency overlaps the rest of the set-up.
   TileWalk lw = walk0;  // the TMA thread's position
+  QuerySeq<SPARSE> lseq = qseq;  // and its item's query-tile sequence
   auto issue_qdo = [&](int u) {  // moves to the next tile
     const int st = u & 1, qt = lw.qt, zq = lw.qh;
-    qseq.next(lw);
+    lseq.next(lw);
     mbar_arrive_expect_tx(bar(B_QF0 + st), C::TILE);
     for (int b = 0; b < C::KB; ++b)
       tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, zq);
@@ -286,27 +313,50 @@ __global__ void __launch_bounds__(448, 1)
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
       bool ok = true;
-      int u = pre;
-      for (; u < nit && ok; ++u) {
+      int nkv_issued = 1;  // items whose K, V have been issued
+      // Q_u and dO_u of global tile u, once their ring slots are free
+      auto ring = [&](int u) -> bool {
         const int st = u & 1, use = u >> 1, qt = lw.qt, zq = lw.qh;
-        if (use > 0 && !mbar_wait(bar(B_QE0 + st), (use - 1) & 1, p.ctl, abort, 10)) { ok = false; break; }
+        if (use > 0 && !mbar_wait(bar(B_QE0 + st), (use - 1) & 1, p.ctl, abort, 10)) return false;
         mbar_arrive_expect_tx(bar(B_QF0 + st), C::TILE);
         for (int b = 0; b < C::KB; ++b)
           tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, zq);
         if (use > 0 && !mbar_wait(bar(B_DOE0 + st), (use - 1) & 1, p.ctl, abort, 11)) {
-          ok = false;
-          // the Q load above is in flight; wait for it below
+          // the Q load above is in flight; wait for it here
           mbar_wait_quiet(bar(B_QF0 + st), use & 1, 200000000ull);
-          break;
+          return false;
         }
         mbar_arrive_expect_tx(bar(B_DOF0 + st), C::TILE);
         for (int b = 0; b < C::KB; ++b)
           tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, zq);
-        qseq.next(lw);
+        lseq.next(lw);
+        return true;
+      };
+      int u = pre, uend = nit;  // global tile index; end of the current item
+      for (int L = L0, kk = 0;;) {
+        while (u < uend && (ok = ring(u))) ++u;  // a failed tile is not counted
+        if (!ok) break;
+        L = item_at(++kk);
+        if (L >= n_items) break;
+        // the next item: its first tiles as soon as their slots are free,
+        // then K and V once every MMA of the previous item has completed
+        const Item I = item_info(L);
+        lw = TileWalk{I.i0, I.bk * p.kv_group};
+        lseq = item_seq(I);
+        uend = u + item_nit(I);
+        const int upre = min(uend, u + 2);
+        while (u < upre && (ok = ring(u))) ++u;
+        if (!ok || !(ok = mbar_wait(bar(B_FIN), (nkv_issued - 1) & 1, p.ctl, abort, 12))) break;
+        mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
+        for (int b = 0; b < C::KB; ++b) {
+          tma_load_3d(sK + b * 16384, &tk, bar(B_KV), b * 64, I.kt * C::BK, I.bk);
+          tma_load_3d(sV + b * 16384, &tv, bar(B_KV), b * 64, I.kt * C::BK, I.bk);
+        }
+        ++nkv_issued;
       }
       if (!ok) {
         // Abort: let every copy already issued land before the CTA exits.
-        mbar_wait_quiet(bar(B_KV), 0, 200000000ull);
+        mbar_wait_quiet(bar(B_KV), (nkv_issued - 1) & 1, 200000000ull);
         for (int v = (u >= 2 ? u - 2 : 0); v < u; ++v) {
           mbar_wait_quiet(bar(B_QF0 + (v & 1)), (v >> 1) & 1, 200000000ull);
           mbar_wait_quiet(bar(B_DOF0 + (v & 1)), (v >> 1) & 1, 200000000ull);
@@ -331,9 +381,14 @@ __global__ void __launch_bounds__(448, 1)
       const uint32_t kK = sdesc_lo(sK, 16), kMN = sdesc_lo(sK, 16384), vK = sdesc_lo(sV, 16);
       const uint32_t qK = sdesc_lo(sQ, 16), qMN = sdesc_lo(sQ, 16384);
       const uint32_t doK = sdesc_lo(sDO, 16), doMN = sdesc_lo(sDO, 16384), dsMN = sdesc_lo(sDS, 16384);
-      bool ok = warp_wait_b(bar(B_KV), 0, p.ctl, abort, 20);
-      for (int u = 0; u < nit && ok; ++u) {
-        const int st = u & 1, par = (u >> 1) & 1;
+      bool ok = true;
+      int U0 = 0;  // global index of the item's first tile
+      for (int L = L0, ki = 0; L < n_items && ok; L = item_at(++ki)) {
+      const int nit_i = L == L0 ? nit : item_nit(item_info(L));
+      if (!(ok = warp_wait_b(bar(B_KV), (uint32_t)ki & 1u, p.ctl, abort, 20))) break;
+      for (int u = 0; u < nit_i && ok; ++u) {
+        const int U = U0 + u;
+        const int st = U & 1, par = (U >> 1) & 1;
         const uint32_t so = (uint32_t)st * TILE16;
         const uint32_t acc0 = u > 0 ? 1u : 0u;
         if (!(ok = warp_wait_b(bar(B_QF0 + st), par, p.ctl, abort, 21))) break;
@@ -346,7 +401,7 @@ __global__ void __launch_bounds__(448, 1)
         }
         mma_commit_e(lead, bar(B_ST));
         if (!(ok = warp_wait_b(bar(B_DOF0 + st), par, p.ctl, abort, 22))) break;
-        if (u > 0 && !(ok = warp_wait_b(bar(B_DQE), (u - 1) & 1, p.ctl, abort, 23))) break;
+        if (U > 0 && !(ok = warp_wait_b(bar(B_DQE), (U - 1) & 1, p.ctl, abort, 23))) break;
         tc_fence_after();
         // dP^T = V dO_i^T
 #pragma unroll
@@ -356,13 +411,17 @@ __global__ void __launch_bounds__(448, 1)
         }
         mma_commit_e(lead, bar(B_DPT));
         // dV += P^T dO_i   (A = P^T bf16 in TMEM, B = dO_i query-major)
-        if (!(ok = warp_wait_b(bar(B_P), u & 1, p.ctl, abort, 24))) break;
+        if (!(ok = warp_wait_b(bar(B_P), U & 1, p.ctl, abort, 24))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
           mma_ts_e(lead, tDV, tST + pcol(k), doMN + so + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
         // dK += dS^T Q_i   (A = dS^T bf16 in TMEM)
-        if (!(ok = warp_wait_b(bar(B_DS), u & 1, p.ctl, abort, 25))) break;
+        if (!(ok = warp_wait_b(bar(B_DS), U & 1, p.ctl, abort, 25))) break;
+        // the item's first dK overwrites the previous item's, once the drain
+        // has read it out
+        if (u == 0 && ki > 0 && !(ok = warp_wait_b(bar(B_DKF), (uint32_t)(ki - 1) & 1u, p.ctl, abort, 26)))
+          break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
@@ -373,7 +432,10 @@ __global__ void __launch_bounds__(448, 1)
           mma_ss_e(lead, tDPT, dsMN + 128 * k, HI, kMN + 128 * k, HI, kIdQ, k > 0);
         mma_commit_e(lead, bar(B_DQF));
       }
+      // every MMA of the item: dK, dV final, K and V free for the next item
       if (ok) mma_commit_e(lead, bar(B_FIN));
+      U0 += nit_i;
+      }  // items
       mma_commit_e(lead, bar(B_DRAIN));
       mbar_wait_quiet(bar(B_DRAIN), 0, 200000000ull);
     }
@@ -388,7 +450,6 @@ __global__ void __launch_bounds__(448, 1)
     const int cb = 64 * h;                          // first query column of this thread
     const float scale2 = p.scale2;
     const uint64_t sc2 = f2_pack(scale2, scale2);
-    const size_t rowbase = (size_t)bk * p.Nk;        // key rows (dK, dV)
     // warpgroup 0 stages the negated log2-scaled LSE and negated D of the
     // first query tile
     if (h == 0) {
@@ -400,24 +461,41 @@ __global__ void __launch_bounds__(448, 1)
     // that the wait stays bounded if another warp gives up.
     mbar_arrive(bar(B_WG));
     bool ok = warp_wait_b(bar(B_WG), 0, p.ctl, abort, 34);
-    TileWalk w = walk0;
-    for (int u = 0; u < nit && ok; ++u) {
+    int U0 = 0;  // global index of the item's first tile
+    for (int L = L0, ki = 0; L < n_items && ok; L = item_at(++ki)) {
+    const Item I = L == L0 ? I0 : item_info(L);
+    const int kt = I.kt;
+    const int nit_i = L == L0 ? nit : item_nit(I);
+    const QuerySeq<SPARSE> seq = L == L0 ? qseq : item_seq(I);
+    const size_t rowbase = (size_t)I.bk * p.Nk;      // key rows (dK, dV)
+    // the next item's first tile, whose statistics this item's last tile fetches
+    const int Ln = item_at(ki + 1);
+    const bool has_next = Ln < n_items;
+    TileWalk wn{0, 0};
+    if (has_next) {
+      const Item In = item_info(Ln);
+      wn = TileWalk{item_seq(In).first, In.bk * p.kv_group};
+    }
+    TileWalk w = L == L0 ? walk0 : TileWalk{seq.first, I.bk * p.kv_group};
+    for (int u = 0; u < nit_i && ok; ++u) {
+      const int U = U0 + u;
       const int qt = w.qt;
-      qseq.next(w);  // w now names tile u + 1
-      const float* lse_u = lse_sh + (u & 1) * C::BQ + cb;
-      const float* d_u = d_sh + (u & 1) * C::BQ + cb;
+      seq.next(w);  // w now names tile u + 1 ...
+      if (u + 1 == nit_i) w = wn;  // ... or the next item's first
+      const float* lse_u = lse_sh + (U & 1) * C::BQ + cb;
+      const float* d_u = d_sh + (U & 1) * C::BQ + cb;
       // next tile's statistics, copied asynchronously so that no warp
       // stalls on the global loads; waited for at the end of the iteration
-      float* lse_n = lse_sh + ((u + 1) & 1) * C::BQ + r;
-      float* d_n = d_sh + ((u + 1) & 1) * C::BQ + r;
-      const bool fetch = h == 0 && u + 1 < nit;
+      float* lse_n = lse_sh + ((U + 1) & 1) * C::BQ + r;
+      float* d_n = d_sh + ((U + 1) & 1) * C::BQ + r;
+      const bool fetch = h == 0 && (u + 1 < nit_i || has_next);
       if (fetch) {
         const float* st = p.stats + ((size_t)w.qh * p.nq + w.qt) * 256;
         cp_async_4(smem_u32(lse_n), st + r, 4u);
         cp_async_4(smem_u32(d_n), st + 128 + r, 4u);
         cp_async_commit();
       }
-      if (!(ok = warp_wait_b(bar(B_ST), u & 1, p.ctl, abort, 30))) break;
+      if (!(ok = warp_wait_b(bar(B_ST), U & 1, p.ctl, abort, 30))) break;
       tc_fence_after();
       float pr[64];
       tmem_ld32(tST + cb, *reinterpret_cast<uint32_t(*)[32]>(pr));
@@ -459,9 +537,9 @@ __global__ void __launch_bounds__(448, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P));
       // dS^T = P^T o (dP^T - D), with P^T the bf16 values dV multiplied
-      if (!(ok = warp_wait_b(bar(B_DPT), u & 1, p.ctl, abort, 31))) break;
-      // the dS buffer is the A operand of dQ_{u-1}: wait until it is read
-      if (u > 0 && !(ok = warp_wait_b(bar(B_DQF), (u - 1) & 1, p.ctl, abort, 32))) break;
+      if (!(ok = warp_wait_b(bar(B_DPT), U & 1, p.ctl, abort, 31))) break;
+      // the dS buffer is the A operand of dQ_{U-1}: wait until it is read
+      if (U > 0 && !(ok = warp_wait_b(bar(B_DQF), (U - 1) & 1, p.ctl, abort, 32))) break;
       tc_fence_after();
       const uint32_t srow = sDS + (uint32_t)h * 16384u + (uint32_t)r * 128u;
       const uint32_t sw = (uint32_t)(r & 7);
@@ -509,11 +587,12 @@ __global__ void __launch_bounds__(448, 1)
       // publish the next tile's statistics
       if (fetch) cp_async_wait_all();
       mbar_arrive(bar(B_WG));
-      if (!(ok = warp_wait_b(bar(B_WG), (u + 1) & 1, p.ctl, abort, 35))) break;
+      if (!(ok = warp_wait_b(bar(B_WG), (U + 1) & 1, p.ctl, abort, 35))) break;
     }
     cp_async_wait_all();  // none in flight when a wait above gave up
-    // epilogue: dV rows of this key tile, columns [h*HD/2, (h+1)*HD/2)
-    if (ok && warp_wait_b(bar(B_FIN), 0, p.ctl, abort, 33)) {
+    // epilogue: dV rows of this key tile, columns [h*HD/2, (h+1)*HD/2); the
+    // next item's first dV (after this warp's next P) overwrites them
+    if (ok && (ok = warp_wait_b(bar(B_FIN), (uint32_t)ki & 1u, p.ctl, abort, 33))) {
       tc_fence_after();
       const int key = kt * C::BK + r;
       __nv_bfloat16* dst = p.dv + (rowbase + key) * HD;
@@ -532,6 +611,8 @@ __global__ void __launch_bounds__(448, 1)
         }
       }
     }
+    U0 += nit_i;
+    }  // items
   } else {
     // ---------------------------------------------------------- dQ drain
     // dQ_u (128 query rows x d, fp32) leaves TMEM 64 columns at a time and is
@@ -543,15 +624,22 @@ __global__ void __launch_bounds__(448, 1)
     const int sp = warp & 3;
     const int r = sp * 32 + lane;  // query row within the tile (dQ) / key row (dK)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
-    const size_t rowbase = (size_t)bk * p.Nk;        // key rows (dK, dV)
     const uint32_t sw = (uint32_t)(lane & 7);
     constexpr int BOXES_PER_SLOT = HD / 64;          // 4 KB boxes in a warp's quarter
     bool ok = true;
-    TileWalk w = walk0;
-    for (int u = 0; u < nit; ++u, qseq.next(w)) {
-      if (!(ok = warp_wait_b(bar(B_DQF), u & 1, p.ctl, abort, 40))) break;
+    int U0 = 0;  // global index of the item's first tile
+    for (int L = L0, ki = 0; L < n_items && ok; L = item_at(++ki)) {
+    const Item I = L == L0 ? I0 : item_info(L);
+    const int kt = I.kt;
+    const int nit_i = L == L0 ? nit : item_nit(I);
+    const QuerySeq<SPARSE> seq = L == L0 ? qseq : item_seq(I);
+    const size_t rowbase = (size_t)I.bk * p.Nk;      // key rows (dK, dV)
+    TileWalk w = L == L0 ? walk0 : TileWalk{seq.first, I.bk * p.kv_group};
+    for (int u = 0; u < nit_i; ++u, seq.next(w)) {
+      const int U = U0 + u;
+      if (!(ok = warp_wait_b(bar(B_DQF), U & 1, p.ctl, abort, 40))) break;
       tc_fence_after();
-      const int st = u & 1;
+      const int st = U & 1;
       const uint32_t quarter = (uint32_t)sp * (uint32_t)(C::TILE / 4);
       const uint32_t stage_do = sDO + st * C::TILE + quarter, stage_q = sQ + st * C::TILE + quarter;
       const int y = w.qt * C::BQ + sp * 32, zq = w.qh;
@@ -601,10 +689,9 @@ __global__ void __launch_bounds__(448, 1)
       }
       __syncwarp();
     }
-    if (lane == 0) bulk_wait_group<0>();
-    __syncwarp();
-    // epilogue: dK rows of this key tile (scaled)
-    if (ok && warp_wait_b(bar(B_FIN), 0, p.ctl, abort, 41)) {
+    // epilogue: dK rows of this key tile (scaled); then "dK read out" lets
+    // the next item's first dK overwrite them
+    if (ok && (ok = warp_wait_b(bar(B_FIN), (uint32_t)ki & 1u, p.ctl, abort, 41))) {
       tc_fence_after();
       const int key = kt * C::BK + r;
       __nv_bfloat16* dst = p.dk + (rowbase + key) * HD;
@@ -624,7 +711,15 @@ __global__ void __launch_bounds__(448, 1)
           for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DKF));
     }
+    U0 += nit_i;
+    }  // items
+    // every reduction has landed before the CTA exits
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -660,7 +755,10 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
-  dim3 grid((unsigned)((long)p.nkv * p.BHkv));
+  // one persistent CTA per SM walks the items, or one CTA per item
+  const long n_items = (long)p.nkv * p.BHkv;
+  const long ctas = persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms ? a.num_sms : n_items;
+  dim3 grid((unsigned)ctas);
   kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();
 }

@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       };
       int u = pre, uend = nit;  // global tile index; end of the current item
       for (int L = L0, kk = 0;;) {
-        for (; u < uend && ok; ++u) ok = ring(u);
+        while (u < uend && (ok = ring(u))) ++u;  // a failed tile is not counted
         if (!ok) break;
         L = item_at(++kk);
         if (L >= n_items) break;
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         lseq = item_seq(I);
         uend = u + item_nit(I);
         const int upre = min(uend, u + C::DOSLOTS);
-        for (; u < upre && ok; ++u) ok = ring(u);
+        while (u < upre && (ok = ring(u))) ++u;
         if (!ok || !(ok = mbar_wait(bar(B_FIN), (kn - 1) & 1, p.ctl, abort, 52))) break;
         mbar_arrive_expect_tx(bar(B_V), C::TILE);
         tma_load_3d(v_buf(kn), &tv, bar(B_V), 0, I.kt * C::BK, I.bk);
