@@ -46,9 +46,9 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # The bench line reports it only while the code of the fa_bwd call (the
 # backward kernels, their launch layer and shared helpers, comments aside)
 # is the code the capture measured.
-NCU_TRAFFIC_BYTES = 2145.0e6
-NCU_TRAFFIC_COMMIT = "b56903e"
-NCU_TRAFFIC_SOURCES_SHA256 = "dda0702d9b698488635de7111967ca639bb85a5a6a52dff7578e860d11a3eb0e"
+NCU_TRAFFIC_BYTES = 2144.4e6
+NCU_TRAFFIC_COMMIT = "e8271c0"
+NCU_TRAFFIC_SOURCES_SHA256 = "86e7e21390e89b1851a03ef34a30c24d84fd4218052584a9150cb4f28c81dbd2"
 BWD_SOURCES = ("fa_api.cu", "fa_bwd.cu", "fa_bwd_d64.cu", "fa_kernels.h", "sm103_ptx.cuh")
 
 
