@@ -217,6 +217,58 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          struct CUstream_st* stream);
 
 /*
+ * Host-memory entry points: the forward (fa_fwd_host), or the forward and
+ * the backward (fa_fwd_bwd_host), for inputs and outputs that live in HOST
+ * memory.  The computation is that of fa_fwd_ex and fa_bwd_ex with the same
+ * shapes and arguments (same kernels), so the sources are theirs; the copies
+ * around it are the library's own.
+ *   - q, k, v, dO are HOST pointers to the inputs and o, lse, dq, dk, dv HOST
+ *     pointers to the outputs, with the shapes of fa_fwd_ex / fa_bwd_ex
+ *     (bf16 [B][H][N_q][d] for q, o, dO, dq; bf16 [B][H_kv][N_k][d] for k, v,
+ *     dk, dv; fp32 [B][H][N_q] for lse).  No alignment is required.
+ *   - dev: a DEVICE staging area owned by the caller, 256-byte aligned, of at
+ *     least fa_fwd_host_device_bytes(...) or fa_fwd_bwd_host_device_bytes(...)
+ *     bytes (the latter with the same `chunks`).  It holds the device copy of
+ *     every tensor and the backward workspace; its contents on entry are
+ *     ignored and on exit unspecified.  The *_device_bytes functions return
+ *     0 for an empty problem or invalid sizes.
+ *   - The key/value heads are cut into `chunks` groups of consecutive heads
+ *     (0 = the library's choice, 8; at most 64, at most B * H_kv); a group
+ *     takes its H / H_kv query heads along.  For each group the inputs are
+ *     copied to the device on one internal stream, its kernels run on
+ *     `stream`, and its outputs are copied back on a second internal stream,
+ *     so the copies of one group overlap the kernels and copies of the
+ *     others.  The internal streams and events are created once per device
+ *     and kept until the process exits.
+ *   - Asynchronous like every other call: nothing in `dev` is overwritten
+ *     before the work already on `stream` has finished, and `stream` passes
+ *     this call only once the last output has reached host memory, so
+ *     cudaStreamSynchronize(stream) makes the outputs readable.  The host
+ *     inputs must stay valid and unchanged until then.
+ *   - Host buffers should be page-locked (cudaHostAlloc, cudaHostRegister):
+ *     with pageable memory the copies are correct but do not overlap.
+ *   - Results: o, lse, dk and dv equal those of fa_fwd_ex / fa_bwd_ex on the
+ *     same inputs bit for bit; dq equals them up to the order of its fp32
+ *     additions (which already varies between calls of fa_bwd_ex).
+ *   - Errors: argument errors (the rules of fa_fwd_ex, a null host pointer
+ *     for a non-empty tensor, a misaligned or short staging area) return
+ *     FA_ERR_INVALID_ARG before anything is enqueued.  A CUDA error part way
+ *     returns FA_ERR_LAUNCH or the failing kernel call's status; the outputs
+ *     are then unspecified.  Calls on one device are enqueued one at a time
+ *     (a per-device lock).
+ */
+size_t fa_fwd_host_device_bytes(int B, int H, int H_kv, int N_q, int N_k, int d);
+size_t fa_fwd_bwd_host_device_bytes(int B, int H, int H_kv, int N_q, int N_k, int d,
+                                    int chunks);
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                      void* dev, size_t dev_bytes, int chunks, struct CUstream_st* stream);
+fa_status fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO, void* o,
+                          float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv,
+                          int N_q, int N_k, int d, float scale, int causal, void* dev,
+                          size_t dev_bytes, int chunks, struct CUstream_st* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up on a wait), or
  * FA_ERR_DEVICE when the synchronisation itself reported a CUDA error.

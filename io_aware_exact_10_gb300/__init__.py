@@ -32,8 +32,12 @@ from .binding import (  # noqa: F401
     fa_bwd_workspace_size,
     fa_device_error_word,
     fa_fwd,
+    fa_fwd_bwd_host,
+    fa_fwd_bwd_host_device_bytes,
     fa_fwd_ex,
     fa_fwd_gqa,
+    fa_fwd_host,
+    fa_fwd_host_device_bytes,
     fa_fwd_sparse,
     fa_last_device_error,
     fa_set_wait_timeout_ns,

@@ -216,7 +216,9 @@ __global__ void __launch_bounds__(448, 1)
   // phase per item.
   const int n_items = p.BHkv * p.nkv;
   const int L0 = (int)blockIdx.x, LS = (int)gridDim.x;
-  auto item_at = [&](int k) { return k * LS + ((k & 1) ? LS - 1 - L0 : L0); };  // k-th item
+  // k-th item (k >= 1); a block-sparse CTA has one item, which the compiler
+  // then knows: its item loops run once
+  auto item_at = [&](int k) { return SPARSE ? n_items : k * LS + ((k & 1) ? LS - 1 - L0 : L0); };
   struct Item {
     int bk, kt, i0;
   };

@@ -134,7 +134,9 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   // same items; the ring index and the barrier phases run on across items.
   const int n_items = p.npairs * p.BH;
   const int L0 = (int)blockIdx.x, LS = (int)gridDim.x;
-  auto item_at = [&](int k) { return k * LS + ((k & 1) ? LS - 1 - L0 : L0); };  // k-th item
+  // k-th item (k >= 1); a block-sparse CTA has one item, which the compiler
+  // then knows: its item loops run once
+  auto item_at = [&](int k) { return SPARSE ? n_items : k * LS + ((k & 1) ? LS - 1 - L0 : L0); };
   struct Item {
     int bh, bhkv, qt0;
     bool valid[2];
