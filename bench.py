@@ -49,9 +49,9 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # head groups of the end-to-end leg's host-memory call (copies of one group
 # overlap the kernels of the others)
 E2E_CHUNKS = 8
-NCU_TRAFFIC_BYTES = 2144.4e6
-NCU_TRAFFIC_COMMIT = "e8271c0"
-NCU_TRAFFIC_SOURCES_SHA256 = "86e7e21390e89b1851a03ef34a30c24d84fd4218052584a9150cb4f28c81dbd2"
+NCU_TRAFFIC_BYTES = 2144.5e6
+NCU_TRAFFIC_COMMIT = "4ba4968"
+NCU_TRAFFIC_SOURCES_SHA256 = "00deef6fb9583377d4c45dd5baf7292aa8bb7def8dc73aa52c41929a6bbbb851"
 BWD_SOURCES = ("fa_api.cu", "fa_bwd.cu", "fa_bwd_d64.cu", "fa_kernels.h", "sm103_ptx.cuh")
 
 
