@@ -443,8 +443,87 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def sweep_bytes(N: int, d: int, BH: int, causal: bool) -> dict:
+    """DRAM bytes of one sweep point's forward and main backward kernel: the
+    algorithmic minimum (every input read once, every output written once;
+    for the backward the fp32 dQ accumulator read and written once) and the
+    tiled model, i.e. what the kernels stream if L2 kept nothing between
+    CTAs.  Forward: a CTA holds query tiles 2p, 2p+1 and streams K, V tiles
+    0 .. nu_p - 1 (nu_p = min(2p + 2, nkv) when causal).  Backward: a CTA
+    holds key tile kt, reads its K, V once, writes dK, dV once, and per
+    visited query tile (from kt on when causal) streams Q, dO, 1 KB of row
+    statistics and a read and write of the 128 x d fp32 dQ rows."""
+    tile = 128 * d * 2                      # bf16 128-row tile
+    nt = -(-N // 128)
+    npairs = -(-nt // 2)
+    fwd_min = BH * (8 * N * d + 4 * N)
+    streamed = sum(min(2 * p + 2, nt) if causal else nt for p in range(npairs))
+    fwd_model = BH * (4 * N * d + 4 * N + streamed * 2 * tile)
+    bwd_min = BH * (8 * N * d + 8 * N + 4 * N * d + 8 * N * d)
+    visits = sum(nt - kt if causal else nt for kt in range(nt))
+    bwd_model = BH * (nt * 4 * tile + visits * (2 * tile + 1024 + 2 * 128 * d * 4))
+    return {"fwd_min": fwd_min, "fwd_model": fwd_model, "bwd_kernel_min": bwd_min,
+            "bwd_kernel_model": bwd_model}
+
+
+def sweep_oracle_ms(N: int, d: int, causal: bool):
+    """The fp64 oracle's time for one head's forward + backward at a sweep
+    point: measured on a whole head up to N = 4096, else extrapolated by FLOPs
+    from 64 evenly spaced forward rows.  Returns (ms, how, threads)."""
+    import numpy as np
+    import oracle
+    from io_aware_exact_10_gb300 import workloads as W
+    oracle.build()
+    w1 = W.Workload(f"oracle_N{N}_d{d}", 1, 1, N, d, causal=causal)
+    q, k, v, dO = (t.reshape(N, d).double().numpy() for t in W.make_inputs(w1))
+    head_flops = w1.fwd_flops() + w1.bwd_flops()
+    if N <= 4096:
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, w1.scale, causal)
+        oracle.attn_bwd(q, k, v, dO, w1.scale, causal)
+        return 1e3 * (time.perf_counter() - t0), "one head, forward + backward", oracle.num_threads()
+    rows = np.linspace(0, N - 1, 64).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attn_fwd_rows(q, k, v, rows, w1.scale, causal)
+    dt = time.perf_counter() - t0
+    keys = (rows + 1) if causal else np.full_like(rows, N)
+    sample_flops = float((4 * d * keys).sum())
+    return (1e3 * dt * head_flops / sample_flops,
+            "extrapolated by FLOPs from 64 forward rows of one head", oracle.num_threads())
+
+
+def run_sweep_once(args):
+    """One fa_fwd and one fa_bwd per sweep point, untimed: the driver of the
+    per-point ncu capture (DRAM bytes and tensor-pipe activity per kernel)."""
+    import torch
+    import io_aware_exact_10_gb300 as fa
+    from io_aware_exact_10_gb300 import workloads as W
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    for d in W.SWEEP_D:
+        for N in W.SWEEP_N:
+            w = W.sweep(N, d)
+            B, H = w.B, w.H
+            q, k, v, dO = W.make_inputs_on_device(w, dev)
+            o = torch.empty_like(q)
+            lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            wsb = fa.fa_bwd_workspace_size(B, H, N, d)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            fa.fa_fwd(q, k, v, o, lse, B, H, N, d, w.scale, 1, stream)
+            fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, w.scale, 1, ws, wsb, stream)
+            if fa.fa_last_device_error(stream) != fa.FA_OK:
+                raise RuntimeError("device error during the sweep")
+            print(f"N={N} d={d} B={B} H={H}: one fa_fwd, one fa_bwd", flush=True)
+            del q, k, v, dO, o, lse, dq, dk, dv, ws
+
+
 def run_sweep(args):
-    """Forward and forward+backward TFLOP/s per sweep point (one JSON line)."""
+    """Forward and forward+backward TFLOP/s per sweep point (one JSON line),
+    with each point's byte model and the oracle's time for one head."""
     import torch
     import io_aware_exact_10_gb300 as fa
     from io_aware_exact_10_gb300 import workloads as W
@@ -487,9 +566,15 @@ def run_sweep(args):
                 res[name] = {"ms": ms, "tflops": fl / ms / 1e9, "pct_of_peak": 100 * fl / ms / 1e9 / peak}
             if fa.fa_last_device_error(stream) != fa.FA_OK:
                 raise RuntimeError("device error during the sweep")
-            points.append({"N": N, "d": d, "B": B, "H": H, **res})
+            points.append({"N": N, "d": d, "B": B, "H": H, **res,
+                           "bytes": sweep_bytes(N, d, B * H, True)})
             del q, k, v, dO, o, lse, dq, dk, dv, ws
     clk = clocks.stop()
+    # the oracle on the host cores, after the GPU timing (one head per point)
+    for pt in points:
+        ms, how, threads = sweep_oracle_ms(pt["N"], pt["d"], True)
+        pt["oracle"] = {"ms_per_head": ms, "sample": how, "cores": threads,
+                        "ms_all_heads": ms * pt["B"] * pt["H"]}
     print(json.dumps({"metric": "attention fwd / fwd+bwd TFLOP/s vs N (causal, H=16, B*N=65536)",
                       "unit": "TFLOP/s", "peak": peak, "steps": args.steps,
                       "warmup": args.warmup, "data": "synthetic (seeded on the device)",
@@ -595,12 +680,17 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="gpt2_medium")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-once", action="store_true",
+                    help="one untimed fa_fwd and fa_bwd per sweep point (ncu capture driver)")
     ap.add_argument("--compare", action="store_true",
                     help="standard attention (S, P in device memory) against this library")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from io_aware_exact_10_gb300 import workloads as W
+    if args.sweep_once:
+        run_sweep_once(args)
+        return
     if args.sweep:
         run_sweep(args)
         return

@@ -24,3 +24,28 @@ def test_config_names_the_shape():
     assert c["block_pattern"] == "local3_global1_random0.05" and 0.10 < c["blocks_kept"] < 0.13
     c = bench.config_of(W.GPT2_MEDIUM)
     assert "N_k" not in c and "H_kv" not in c and "block_pattern" not in c
+
+
+def test_sweep_byte_model_counts_visited_tiles():
+    """The sweep's tiled byte model equals a brute-force count of the tiles
+    the kernels visit (causal: key j visible to query i iff j <= i), and never
+    falls below the algorithmic minimum; one pair of query tiles against two
+    key tiles streams each input exactly once."""
+    import bench
+    for N, d, causal in ((256, 64, True), (512, 64, False), (1000, 128, True), (4096, 128, True),
+                         (384, 64, True)):
+        nt = -(-N // 128)
+        tile = 128 * d * 2
+        fwd_tiles = 0
+        for p in range(-(-nt // 2)):
+            last_row = min(N, (2 * p + 2) * 128) - 1
+            fwd_tiles += sum(1 for j in range(nt) if not causal or j * 128 <= last_row)
+        bwd_visits = sum(1 for kt in range(nt) for qt in range(nt)
+                         if not causal or kt * 128 <= min(N, qt * 128 + 128) - 1)
+        b = bench.sweep_bytes(N, d, 3, causal)
+        assert b["fwd_model"] == 3 * (4 * N * d + 4 * N + fwd_tiles * 2 * tile)
+        assert b["bwd_kernel_model"] == 3 * (nt * 4 * tile + bwd_visits * (2 * tile + 1024 + 1024 * d))
+        assert b["fwd_model"] >= b["fwd_min"] - 3 * (4 * (nt * 128 - N) * d) * 2
+        assert b["bwd_kernel_model"] >= b["bwd_kernel_min"]
+    b = bench.sweep_bytes(256, 64, 1, True)
+    assert b["fwd_model"] == b["fwd_min"]
