@@ -19,6 +19,9 @@
  *   - Tensors q, k, v, o, dO, dq, dk, dv are DEVICE pointers to contiguous
  *     bf16 arrays of shape [B][H][N][d] (d innermost).  lse is a device
  *     pointer to fp32 [B][H][N].  Every pointer must be 16-byte aligned.
+ *     (The host-memory entry points fa_fwd_host and fa_fwd_bwd_host take
+ *     HOST pointers instead, with no alignment rule, and a device staging
+ *     area; see their section.)
  *   - d must be 64 or 128.  N >= 1 is any length up to 2^30 (the last tile
  *     is masked).  B, H >= 1.  B == 0, H == 0 or N == 0 is an empty problem:
  *     FA_OK, no work.  B * H * ceil(N / 128) must be at most 2^27 - 1 (grid
