@@ -346,34 +346,23 @@ def run_ours(args, w):
     bwd_tf = w.bwd_flops() / (bwd_ms * 1e-3) / 1e12
     fwd_tf = w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
 
-    # ---- end to end: pinned host inputs -> device -> fwd + bwd -> host outputs.
-    # Dense workloads go through the host-memory entry point, which pipelines
-    # the copies of each head group against the kernels of the others;
-    # block-sparse ones (no host entry point) copy, compute and copy back.
+    # ---- end to end: pinned host inputs -> device -> fwd + bwd -> host outputs,
+    # through the host-memory entry point, which pipelines the copies of each
+    # head group against the kernels of the others (a block mask, resident on
+    # the device like the dense path's, applies to every group).
     hq, hk, hv, hdO = (t.cpu().pin_memory() for t in (q, k, v, dO))
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     hdq = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     hdk, hdv = (torch.empty(k.shape, dtype=k.dtype).pin_memory() for _ in range(2))
     e2e_chunks = E2E_CHUNKS
-    if bmask is None:
-        stage_bytes = fa.fa_fwd_bwd_host_device_bytes(B, H, Hkv, N, Nk, d, e2e_chunks)
-        stage = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
-        e2e_path = f"fa_fwd_bwd_host, {e2e_chunks} head groups"
+    stage_bytes = fa.fa_fwd_bwd_host_device_bytes(B, H, Hkv, N, Nk, d, e2e_chunks)
+    stage = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
+    e2e_path = f"fa_fwd_bwd_host, {e2e_chunks} head groups"
 
-        def e2e_step():
-            fa.fa_fwd_bwd_host(hq, hk, hv, hdO, ho, hl, hdq, hdk, hdv, B, H, Hkv, N, Nk, d,
-                               w.scale, causal, stage, stage_bytes, e2e_chunks, stream)
-    else:
-        e2e_path = "copies + fa_fwd_sparse + fa_bwd_sparse + copies, one stream"
-
-        def e2e_step():
-            for h, dd in ((hq, q), (hk, k), (hv, v), (hdO, dO)):
-                dd.copy_(h, non_blocking=True)
-            fwd()
-            bwd()
-            for h, dd in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
-                h.copy_(dd, non_blocking=True)
+    def e2e_step():
+        fa.fa_fwd_bwd_host(hq, hk, hv, hdO, ho, hl, hdq, hdk, hdv, B, H, Hkv, N, Nk, d, w.scale,
+                           causal, stage, stage_bytes, e2e_chunks, stream, block_mask=bmask)
 
     e2e_steps = max(3, min(args.steps, 20))
     e2e_step()

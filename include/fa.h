@@ -222,9 +222,13 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
 /*
  * Host-memory entry points: the forward (fa_fwd_host), or the forward and
  * the backward (fa_fwd_bwd_host), for inputs and outputs that live in HOST
- * memory.  The computation is that of fa_fwd_ex and fa_bwd_ex with the same
- * shapes and arguments (same kernels), so the sources are theirs; the copies
- * around it are the library's own.
+ * memory.  The computation is that of fa_fwd_sparse and fa_bwd_sparse with
+ * the same shapes and arguments (same kernels; with block_mask == NULL, that
+ * of fa_fwd_ex and fa_bwd_ex), so the sources are theirs; the copies around
+ * it are the library's own.
+ *   - block_mask: NULL, or a DEVICE pointer to the block mask of
+ *     fa_fwd_sparse (same layout and limits), shared by every head and so by
+ *     every group.
  *   - q, k, v, dO are HOST pointers to the inputs and o, lse, dq, dk, dv HOST
  *     pointers to the outputs, with the shapes of fa_fwd_ex / fa_bwd_ex
  *     (bf16 [B][H][N_q][d] for q, o, dO, dq; bf16 [B][H_kv][N_k][d] for k, v,
@@ -250,8 +254,8 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  *     inputs must stay valid and unchanged until then.
  *   - Host buffers should be page-locked (cudaHostAlloc, cudaHostRegister):
  *     with pageable memory the copies are correct but do not overlap.
- *   - Results: o, lse, dk and dv equal those of fa_fwd_ex / fa_bwd_ex on the
- *     same inputs bit for bit; dq equals them up to the order of its fp32
+ *   - Results: o, lse, dk and dv equal those of the device entry points on
+ *     the same inputs bit for bit; dq equals them up to the order of its fp32
  *     additions (which already varies between calls of fa_bwd_ex).
  *   - Errors: argument errors (the rules of fa_fwd_ex, a null host pointer
  *     for a non-empty tensor, a misaligned or short staging area) return
@@ -265,11 +269,13 @@ size_t fa_fwd_bwd_host_device_bytes(int B, int H, int H_kv, int N_q, int N_k, in
                                     int chunks);
 fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
-                      void* dev, size_t dev_bytes, int chunks, struct CUstream_st* stream);
+                      const unsigned char* block_mask, void* dev, size_t dev_bytes, int chunks,
+                      struct CUstream_st* stream);
 fa_status fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO, void* o,
                           float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv,
-                          int N_q, int N_k, int d, float scale, int causal, void* dev,
-                          size_t dev_bytes, int chunks, struct CUstream_st* stream);
+                          int N_q, int N_k, int d, float scale, int causal,
+                          const unsigned char* block_mask, void* dev, size_t dev_bytes,
+                          int chunks, struct CUstream_st* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error

@@ -69,10 +69,10 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_host_device_bytes.restype = sz
         L.fa_fwd_bwd_host_device_bytes.argtypes = [i, i, i, i, i, i, i]
         L.fa_fwd_bwd_host_device_bytes.restype = sz
-        L.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, i, vp]
+        L.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, sz, i, vp]
         L.fa_fwd_host.restype = i
         L.fa_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i,
-                                      vp, sz, i, vp]
+                                      vp, vp, sz, i, vp]
         L.fa_fwd_bwd_host.restype = i
         L.fa_last_device_error.argtypes = [vp]
         L.fa_last_device_error.restype = i
@@ -244,25 +244,28 @@ def fa_fwd_bwd_host_device_bytes(B, H, H_kv, N_q, N_k, d, chunks=0) -> int:
 
 
 def fa_fwd_host(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, dev, dev_bytes,
-                chunks=0, stream=None, check=True) -> int:
+                chunks=0, stream=None, check=True, block_mask=None) -> int:
     """fa_fwd_host(...) -> status: q, k, v, o, lse are HOST buffers (torch CPU
-    tensors, ideally pinned, or raw addresses); dev is the device staging area."""
+    tensors, ideally pinned, or raw addresses); dev is the device staging area;
+    block_mask an optional DEVICE block mask (as for fa_fwd_sparse)."""
     s = lib().fa_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
                           int(H_kv), int(N_q), int(N_k), int(d), float(scale), int(causal),
-                          _ptr(dev), int(dev_bytes), int(chunks), _stream(stream))
+                          _ptr(block_mask), _ptr(dev), int(dev_bytes), int(chunks),
+                          _stream(stream))
     if check:
         _check(s, "fa_fwd_host")
     return s
 
 
 def fa_fwd_bwd_host(q, k, v, dO, o, lse, dq, dk, dv, B, H, H_kv, N_q, N_k, d, scale, causal,
-                    dev, dev_bytes, chunks=0, stream=None, check=True) -> int:
+                    dev, dev_bytes, chunks=0, stream=None, check=True, block_mask=None) -> int:
     """fa_fwd_bwd_host(...) -> status: forward and backward with every tensor in
-    HOST memory; copies of one head group overlap the kernels of the others."""
+    HOST memory; copies of one head group overlap the kernels of the others.
+    block_mask: optional DEVICE block mask (as for fa_fwd_sparse)."""
     s = lib().fa_fwd_bwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(o), _ptr(lse),
                               _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(H_kv), int(N_q),
-                              int(N_k), int(d), float(scale), int(causal), _ptr(dev),
-                              int(dev_bytes), int(chunks), _stream(stream))
+                              int(N_k), int(d), float(scale), int(causal), _ptr(block_mask),
+                              _ptr(dev), int(dev_bytes), int(chunks), _stream(stream))
     if check:
         _check(s, "fa_fwd_bwd_host")
     return s

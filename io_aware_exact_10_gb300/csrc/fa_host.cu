@@ -2,7 +2,8 @@
 // heads are cut into groups, and each group's copies to the device, its
 // kernels and its copies back run on three streams, so the copies of one
 // group overlap the kernels and copies of its neighbours.  The kernels are
-// the ones fa_fwd_ex / fa_bwd_ex launch; nothing here computes.
+// the ones fa_fwd_sparse / fa_bwd_sparse launch (with a NULL mask, those of
+// fa_fwd_ex / fa_bwd_ex); nothing here computes.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -71,8 +72,11 @@ bool sizes_ok(int B, int H, int H_kv, int N_q, int N_k, int d) {
   if (B > 0 && H > 0 && (H_kv < 1 || H_kv > H || H % H_kv != 0)) return false;
   return true;
 }
-bool args_ok(int B, int H, int H_kv, int N_q, int N_k, int d, float scale, int causal) {
+bool args_ok(int B, int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+             const unsigned char* block_mask) {
   if (!sizes_ok(B, H, H_kv, N_q, N_k, d)) return false;
+  // a block mask has at most 4096 blocks per side (as for fa_fwd_sparse)
+  if (block_mask && ((N_q + 127) / 128 > 4096 || (N_k + 127) / 128 > 4096)) return false;
   if (causal != 0 && causal != 1) return false;
   if (!(std::isfinite(scale) && scale > 0.f)) return false;
   if (B > 0 && H > 0 && N_q > 0 && (N_k == 0 || (causal && N_k < N_q))) return false;
@@ -127,9 +131,9 @@ void group_range(long long n_kv, int n, int c, long long* lo, long long* hi) {
 
 fa_status run(const void* q, const void* k, const void* v, const void* dO, void* o, float* lse,
               void* dq, void* dk, void* dv, int B, int H, int H_kv, int N_q, int N_k, int d,
-              float scale, int causal, void* dev, size_t dev_bytes, int chunks,
-              cudaStream_t stream, bool backward) {
-  if (!args_ok(B, H, H_kv, N_q, N_k, d, scale, causal)) return FA_ERR_INVALID_ARG;
+              float scale, int causal, const unsigned char* block_mask, void* dev,
+              size_t dev_bytes, int chunks, cudaStream_t stream, bool backward) {
+  if (!args_ok(B, H, H_kv, N_q, N_k, d, scale, causal, block_mask)) return FA_ERR_INVALID_ARG;
   if (B == 0 || H == 0) return FA_OK;
   const long long n_kv = (long long)B * H_kv;
   const int G = H / H_kv;
@@ -184,17 +188,19 @@ fa_status run(const void* q, const void* k, const void* v, const void* dO, void*
     if (ok) ck(cudaEventRecord(P->in_ev[c], P->in));
     if (ok) ck(cudaStreamWaitEvent(stream, P->in_ev[c], 0));
     if (!ok) break;
-    // its kernels, on the caller's stream
-    st = fa_fwd_ex(base + L.q + qo, base + L.k + ko, base + L.v + ko, base + L.o + qo,
-                   reinterpret_cast<float*>(base + ldev), 1, nh, nk, N_q, N_k, d, scale, causal,
-                   stream);
+    // its kernels, on the caller's stream (the block mask, shared by every
+    // head, applies to each group as it is; NULL is the dense computation)
+    st = fa_fwd_sparse(base + L.q + qo, base + L.k + ko, base + L.v + ko, base + L.o + qo,
+                       reinterpret_cast<float*>(base + ldev), 1, nh, nk, N_q, N_k, d, scale,
+                       causal, block_mask, stream);
     if (st != FA_OK) break;
     ck(cudaEventRecord(P->fwd_ev[c], stream));
     if (backward && ok) {
-      st = fa_bwd_ex(base + L.q + qo, base + L.k + ko, base + L.v + ko, base + L.o + qo,
-                     reinterpret_cast<const float*>(base + ldev), base + L.dO + qo,
-                     base + L.dq + qo, base + L.dk + ko, base + L.dv + ko, 1, nh, nk, N_q, N_k, d,
-                     scale, causal, base + L.ws, fa_bwd_workspace_size(1, nh, N_q, d), stream);
+      st = fa_bwd_sparse(base + L.q + qo, base + L.k + ko, base + L.v + ko, base + L.o + qo,
+                         reinterpret_cast<const float*>(base + ldev), base + L.dO + qo,
+                         base + L.dq + qo, base + L.dk + ko, base + L.dv + ko, 1, nh, nk, N_q,
+                         N_k, d, scale, causal, block_mask, base + L.ws,
+                         fa_bwd_workspace_size(1, nh, N_q, d), stream);
       if (st != FA_OK) break;
       ck(cudaEventRecord(P->bwd_ev[c], stream));
     }
@@ -245,17 +251,20 @@ size_t fa_fwd_bwd_host_device_bytes(int B, int H, int H_kv, int N_q, int N_k, in
 
 fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
-                      void* dev, size_t dev_bytes, int chunks, struct CUstream_st* stream) {
+                      const unsigned char* block_mask, void* dev, size_t dev_bytes, int chunks,
+                      struct CUstream_st* stream) {
   return run(q, k, v, nullptr, o, lse, nullptr, nullptr, nullptr, B, H, H_kv, N_q, N_k, d, scale,
-             causal, dev, dev_bytes, chunks, reinterpret_cast<cudaStream_t>(stream), false);
+             causal, block_mask, dev, dev_bytes, chunks, reinterpret_cast<cudaStream_t>(stream),
+             false);
 }
 
 fa_status fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO, void* o,
                           float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv,
-                          int N_q, int N_k, int d, float scale, int causal, void* dev,
-                          size_t dev_bytes, int chunks, struct CUstream_st* stream) {
-  return run(q, k, v, dO, o, lse, dq, dk, dv, B, H, H_kv, N_q, N_k, d, scale, causal, dev,
-             dev_bytes, chunks, reinterpret_cast<cudaStream_t>(stream), true);
+                          int N_q, int N_k, int d, float scale, int causal,
+                          const unsigned char* block_mask, void* dev, size_t dev_bytes,
+                          int chunks, struct CUstream_st* stream) {
+  return run(q, k, v, dO, o, lse, dq, dk, dv, B, H, H_kv, N_q, N_k, d, scale, causal, block_mask,
+             dev, dev_bytes, chunks, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 }  // extern "C"

@@ -90,6 +90,51 @@ def test_host_forward_only():
     assert torch.equal(ho, o.cpu()) and torch.equal(hl, lse.cpu())
 
 
+def test_host_block_sparse():
+    """A block mask passes through to every group: the host call equals the
+    block-sparse device entry points, and the oracle on two groups."""
+    import numpy as np
+    B, H, H_kv, N, d = 2, 4, 2, 640, 128
+    q, k, v, dO = gqa_inputs(B, H, H_kv, N, d, seed=17)
+    scale = d ** -0.5
+    nt = -(-N // 128)
+    rng = np.random.default_rng(5)
+    mask = (rng.random((nt, nt)) < 0.5) | np.eye(nt, dtype=bool)
+    mask[2, :] = False  # a query block that sees no key: o = 0, lse = -inf
+    m_dev = torch.from_numpy(mask.astype(np.uint8)).cuda()
+    hq, hk, hv, hdO = (pinned(t) for t in (q, k, v, dO))
+    ho, hdq = torch.empty_like(hq).pin_memory(), torch.empty_like(hq).pin_memory()
+    hl = torch.empty((B, H, N)).pin_memory()
+    hdk, hdv = torch.empty_like(hk).pin_memory(), torch.empty_like(hv).pin_memory()
+    nbytes = fa.fa_fwd_bwd_host_device_bytes(B, H, H_kv, N, N, d, 3)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    fa.fa_fwd_bwd_host(hq, hk, hv, hdO, ho, hl, hdq, hdk, hdv, B, H, H_kv, N, N, d, scale, True,
+                       buf, nbytes, 3, block_mask=m_dev)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == fa.FA_OK
+    out = {"o": ho, "lse": hl, "dq": hdq, "dk": hdk, "dv": hdv}
+    qd, kd, vd, dOd = (t.cuda() for t in (q, k, v, dO))
+    o, lse = fa.forward(qd, kd, vd, scale, True, block_mask=m_dev)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dOd, scale, True, block_mask=m_dev)
+    torch.cuda.synchronize()
+    same_as_device(out, {"o": o.cpu(), "lse": lse.cpu(), "dq": dq.cpu(), "dk": dk.cpu(),
+                         "dv": dv.cpu()})
+    assert torch.isneginf(hl[:, :, 256:384]).all() and not ho[:, :, 256:384].any()
+    import oracle
+    from parity import f64, rel_fro, TOL_GRAD, TOL_O
+    G = H // H_kv
+    for b, hk_ in ((0, 1), (1, 0)):
+        hs = slice(hk_ * G, hk_ * G + G)
+        o_ref, _ = oracle.attn_fwd(f64(q[b, hs]), f64(k[b, hk_:hk_ + 1]), f64(v[b, hk_:hk_ + 1]),
+                                   scale, True, block_mask=mask)
+        assert float(np.abs(f64(ho[b, hs]) - o_ref).max()) <= TOL_O
+        _, dk_ref, dv_ref = oracle.attn_bwd(f64(q[b, hs]), f64(k[b, hk_:hk_ + 1]),
+                                            f64(v[b, hk_:hk_ + 1]), f64(dO[b, hs]), scale, True,
+                                            block_mask=mask)
+        assert rel_fro(f64(hdk[b, hk_]), dk_ref[0]) <= TOL_GRAD
+        assert rel_fro(f64(hdv[b, hk_]), dv_ref[0]) <= TOL_GRAD
+
+
 def test_host_no_query_rows_zeroes_key_gradients():
     B, H, H_kv, Nk, d = 1, 4, 2, 300, 64
     _, k, v, _ = gqa_inputs(B, H, H_kv, 1, d, seed=3, N_k=Nk)

@@ -60,13 +60,14 @@ def test_argument_errors_before_any_device_call(L):
     sc = ctypes.c_float(0.125)
 
     def fb(B=1, H=4, H_kv=2, Nq=128, Nk=128, d=64, causal=0, scale=sc, dev=DEV, nbytes=1 << 40,
-           ptr=H_, dq=None):
+           ptr=H_, dq=None, mask=None):
         dq = ptr if dq is None else dq
         return L.fa_fwd_bwd_host(ptr, ptr, ptr, ptr, ptr, ptr, dq, ptr, ptr, B, H, H_kv, Nq, Nk, d,
-                                 scale, causal, dev, nbytes, 0, None)
+                                 scale, causal, mask, dev, nbytes, 0, None)
 
-    def ff(B=1, H=4, H_kv=2, Nq=128, Nk=128, d=64, causal=0, dev=DEV, nbytes=1 << 40, ptr=H_):
-        return L.fa_fwd_host(ptr, ptr, ptr, ptr, ptr, B, H, H_kv, Nq, Nk, d, sc, causal, dev,
+    def ff(B=1, H=4, H_kv=2, Nq=128, Nk=128, d=64, causal=0, dev=DEV, nbytes=1 << 40, ptr=H_,
+           mask=None):
+        return L.fa_fwd_host(ptr, ptr, ptr, ptr, ptr, B, H, H_kv, Nq, Nk, d, sc, causal, mask, dev,
                              nbytes, 0, None)
 
     # valid arguments reach the device lookup (none here)
@@ -85,5 +86,9 @@ def test_argument_errors_before_any_device_call(L):
     # a null host pointer for a tensor that has elements
     assert fb(ptr=None) == INV and ff(ptr=None) == INV
     assert fb(dq=0) == INV
+    # a block mask is limited to 4096 blocks per side, as for fa_fwd_sparse
+    big = 4096 * 128 + 1
+    assert fb(Nq=big, Nk=big, mask=DEV) == INV and ff(Nq=128, Nk=big, mask=DEV) == INV
+    assert fb(Nq=big, Nk=big) == NODEV and fb(mask=DEV) == NODEV
     # empty problems: nothing to do
     assert fb(B=0) == OK and fb(H=0) == OK and ff(B=0) == OK
