@@ -42,6 +42,10 @@
  *     fa_last_device_error() reads.
  *   - Thread safety: calls on distinct streams may come from distinct host
  *     threads.
+ *   - CUDA graphs: every compute entry point, the host-memory ones included,
+ *     may be captured on a stream and replayed; a replay computes on what the
+ *     buffers hold then.  Make one eager call on the device first (it looks
+ *     up the device and the driver's tensor-map encoder once).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
