@@ -219,11 +219,16 @@ fa_status run(const void* q, const void* k, const void* v, const void* dO, void*
       d2h(dv, L.dv, ko, kn);
     }
   }
-  // The caller's stream passes this call only when the last copy back has
-  // landed: synchronising it makes the host outputs readable.
-  if (ok) ck(cudaEventRecord(P->done, P->out));
-  if (ok) ck(cudaStreamWaitEvent(stream, P->done, 0));
-  if (!ok) {
+  // The caller's stream passes this call only when both copy streams have
+  // drained: synchronising it makes the host outputs readable.  Joined even
+  // after a failure part way, so that no copy enqueued above can still touch
+  // the staging area when later work on `stream` writes it.  (A wait takes
+  // the event as last recorded, so one event serves both joins.)
+  const bool joined = cudaEventRecord(P->done, P->out) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, P->done, 0) == cudaSuccess &&
+                      cudaEventRecord(P->done, P->in) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, P->done, 0) == cudaSuccess;
+  if (!ok || !joined) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
   }
