@@ -74,8 +74,15 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def ncu_traffic():
-    """The captured traffic if the kernel sources still match the capture."""
+# the workload the traffic capture ran (the default bench line's)
+NCU_TRAFFIC_WORKLOAD = "gpt2_medium_B64_H16_N1024_d64"
+
+
+def ncu_traffic(workload_name: str = NCU_TRAFFIC_WORKLOAD):
+    """The captured traffic, for the workload the capture ran and while the
+    kernel sources still match the capture; else None."""
+    if workload_name != NCU_TRAFFIC_WORKLOAD:
+        return None
     if NCU_TRAFFIC_SOURCES_SHA256 and kernel_sources_sha256() == NCU_TRAFFIC_SOURCES_SHA256:
         return NCU_TRAFFIC_BYTES
     return None
@@ -414,7 +421,7 @@ def run_ours(args, w):
             "frac": bwd_tf / peak,
             "frac_sustained": bwd_tf / peak_sus,
             "peak_source": f"{peak_src} bf16 burst ({PEAKS_PATH if peak_src == 'measured' else 'recipe fallback'})",
-            "traffic": ncu_traffic(),
+            "traffic": ncu_traffic(w.name),
         },
         "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,

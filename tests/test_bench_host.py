@@ -13,6 +13,10 @@ def test_traffic_follows_the_backward_sources(monkeypatch):
     sources matches the capture, and dropped (null) once it does not."""
     monkeypatch.setattr(bench, "NCU_TRAFFIC_SOURCES_SHA256", bench.kernel_sources_sha256())
     assert bench.ncu_traffic() == bench.NCU_TRAFFIC_BYTES
+    assert bench.ncu_traffic(W.GPT2_MEDIUM.name) == bench.NCU_TRAFFIC_BYTES
+    # the capture belongs to one workload: other lines report no traffic
+    assert bench.ncu_traffic(W.GQA_CAUSAL.name) is None
+    assert bench.ncu_traffic(W.SPARSE_LOCAL_GLOBAL.name) is None
     monkeypatch.setattr(bench, "NCU_TRAFFIC_SOURCES_SHA256", "0" * 64)
     assert bench.ncu_traffic() is None
 
