@@ -462,10 +462,11 @@ def sweep_bytes(N: int, d: int, BH: int, causal: bool) -> dict:
             "bwd_kernel_model": bwd_model}
 
 
-def sweep_oracle_ms(N: int, d: int, causal: bool):
-    """The fp64 oracle's time for one head's forward + backward at a sweep
-    point: measured on a whole head up to N = 4096, else extrapolated by FLOPs
-    from 64 evenly spaced forward rows.  Returns (ms, how, threads)."""
+def sweep_cpu_baseline(N: int, d: int, causal: bool):
+    """The sweep's CPU baseline: the fp64 oracle's time for one head's forward
+    + backward at a sweep point, measured on a whole head up to N = 4096, else
+    extrapolated by FLOPs from 64 evenly spaced forward rows.  Returns (ms,
+    how, threads)."""
     import numpy as np
     import oracle
     from io_aware_exact_10_gb300 import workloads as W
@@ -566,11 +567,11 @@ def run_sweep(args):
                            "bytes": sweep_bytes(N, d, B * H, True)})
             del q, k, v, dO, o, lse, dq, dk, dv, ws
     clk = clocks.stop()
-    # the oracle on the host cores, after the GPU timing (one head per point)
+    # the CPU baseline (the oracle on the host cores), after the GPU timing
     for pt in points:
-        ms, how, threads = sweep_oracle_ms(pt["N"], pt["d"], True)
-        pt["oracle"] = {"ms_per_head": ms, "sample": how, "cores": threads,
-                        "ms_all_heads": ms * pt["B"] * pt["H"]}
+        ms, how, threads = sweep_cpu_baseline(pt["N"], pt["d"], True)
+        pt["cpu_baseline"] = {"kind": "oracle", "ms_per_head": ms, "sample": how,
+                              "cores": threads, "ms_all_heads": ms * pt["B"] * pt["H"]}
     print(json.dumps({"metric": "attention fwd / fwd+bwd TFLOP/s vs N (causal, H=16, B*N=65536)",
                       "unit": "TFLOP/s", "peak": peak, "steps": args.steps,
                       "warmup": args.warmup, "data": "synthetic (seeded on the device)",
