@@ -578,6 +578,70 @@ def run_sweep(args):
                       "clocks": clk, "sweep": points}), flush=True)
 
 
+def run_tile_sweep(args):
+    """Query rows per CTA (Br) of the forward, the block-size axis of the
+    paper review's Fig. 2 that the kernels can vary as built: a CTA holds two
+    128-row query tiles of a head (Br = 256) when the head has two or more.
+    Viewing every query tile as its own query head (N_q = 128, H' = H N/128
+    query heads on the H key/value heads) gives each CTA one tile (Br = 128)
+    with the same arithmetic per row, so o and lse must match bit for bit;
+    K and V are then streamed once per 128 query rows instead of per 256.
+    Non-causal only (causal masking aligns on each head's last row).  Prints
+    one JSON line: forward time and TFLOP/s per (N, d, Br)."""
+    import torch
+    import io_aware_exact_10_gb300 as fa
+    from io_aware_exact_10_gb300 import workloads as W
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peaks, _ = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    points = []
+    for d in W.SWEEP_D:
+        for N in (1024, 4096, 16384):
+            w = W.sweep(N, d, causal=False)
+            B, H = w.B, w.H
+            q, k, v = W.make_inputs_on_device(w, dev, with_grad=False)
+            nt = N // 128
+            res = {}
+            outs = {}
+            for br in (256, 128):
+                o = torch.empty_like(q)
+                lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+                if br == 256:
+                    f = lambda: fa.fa_fwd(q, k, v, o, lse, B, H, N, d, w.scale, 0, stream)
+                else:  # every query tile its own query head of the same key/value head
+                    f = lambda: fa.fa_fwd_ex(q, k, v, o, lse, B, H * nt, H, 128, N, d, w.scale,
+                                             0, stream)
+                for _ in range(args.warmup):
+                    f()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(args.steps):
+                    f()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / args.steps
+                tf = w.fwd_flops() / ms / 1e9
+                kv_bytes = B * H * 2 * N * d * 2 * (N // br if br <= N else 1)
+                res[f"br{br}"] = {"ms": ms, "tflops": tf, "pct_of_peak": 100 * tf / peak,
+                                  "kv_streamed_gb": kv_bytes / 1e9}
+                outs[br] = (o, lse)
+            if fa.fa_last_device_error(stream) != fa.FA_OK:
+                raise RuntimeError("device error during the tile sweep")
+            if not (torch.equal(outs[256][0], outs[128][0]) and torch.equal(outs[256][1], outs[128][1])):
+                raise RuntimeError(f"Br = 128 and Br = 256 disagree at N={N}, d={d}")
+            points.append({"N": N, "d": d, "B": B, "H": H, **res})
+            del q, k, v, outs
+    print(json.dumps({"metric": "attention fwd TFLOP/s vs query rows per CTA (non-causal)",
+                      "unit": "TFLOP/s", "peak": peak, "steps": args.steps,
+                      "warmup": args.warmup, "identical_outputs": True, "points": points}),
+          flush=True)
+
+
 def run_compare(args, w):
     """Standard attention against this library on one workload (the
     comparison of the paper review's Fig. 2): a forward+backward step of
@@ -677,6 +741,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="gpt2_medium")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--tile-sweep", action="store_true",
+                    help="forward time against query rows per CTA (128 or 256), non-causal")
     ap.add_argument("--sweep-once", action="store_true",
                     help="one untimed fa_fwd and fa_bwd per sweep point (ncu capture driver)")
     ap.add_argument("--compare", action="store_true",
@@ -687,6 +753,9 @@ def main():
     from io_aware_exact_10_gb300 import workloads as W
     if args.sweep_once:
         run_sweep_once(args)
+        return
+    if args.tile_sweep:
+        run_tile_sweep(args)
         return
     if args.sweep:
         run_sweep(args)

@@ -164,3 +164,19 @@ def test_sweep(N, d):
     rows = np.concatenate([[0, N - 1], np.random.default_rng(N).choice(N, 46, replace=False)])
     check_rows(q, k, v, out, w.scale, True, seeded_heads(w.B, w.H, 2, seed=N + 1), rows)
     check_invariants(dO, out)
+
+
+@pytest.mark.parametrize("B,H,N,d", [(2, 2, 1024, 64), (1, 2, 512, 128)])
+def test_one_query_tile_per_cta_matches_two(B, H, N, d):
+    """The tile-size sweep's Br = 128 layout (every 128-row query tile its own
+    query head of the same key/value head, non-causal) computes each row as
+    the standard Br = 256 layout does: o and lse bit for bit."""
+    g = torch.Generator().manual_seed(N + d)
+    q, k, v = (torch.randn((B, H, N, d), generator=g).to(torch.bfloat16).cuda() for _ in range(3))
+    scale = d ** -0.5
+    o, lse = fa.forward(q, k, v, scale, False)
+    nt = N // 128
+    o1, lse1 = torch.empty_like(q), torch.empty((B, H, N), device="cuda")
+    fa.fa_fwd_ex(q, k, v, o1, lse1, B, H * nt, H, 128, N, d, scale, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o1) and torch.equal(lse, lse1)
