@@ -53,3 +53,21 @@ def test_sweep_byte_model_counts_visited_tiles():
         assert b["bwd_kernel_model"] >= b["bwd_kernel_min"]
     b = bench.sweep_bytes(256, 64, 1, True)
     assert b["fwd_model"] == b["fwd_min"]
+
+
+def test_tile_sweep_layout_is_the_same_attention():
+    """The tile sweep's Br = 128 layout views every 128-row query tile as its
+    own query head (N_q = 128) of the original key/value head, through the
+    grouped-head and cross-length rules (query head h' uses key/value head
+    h' // G).  Non-causal, that is the same attention: the oracle on both
+    layouts agrees to rounding."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(3)
+    B, H, N, d = 1, 2, 384, 16
+    q, k, v = (rng.standard_normal((B, H, N, d)) for _ in range(3))
+    o, lse = oracle.attn_fwd(q, k, v, 0.25, False)
+    nt = N // 128
+    o2, lse2 = oracle.attn_fwd(q.reshape(B, H * nt, 128, d), k, v, 0.25, False)
+    assert np.allclose(o2.reshape(o.shape), o, rtol=0, atol=1e-12)
+    assert np.allclose(lse2.reshape(lse.shape), lse, rtol=0, atol=1e-12)
