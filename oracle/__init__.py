@@ -13,6 +13,9 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
   torch's CPU ``scaled_dot_product_attention`` in fp64.
 * ``attn_bwd`` -- pinned: central finite differences of the forward on tiny
   shapes, exact gradient invariants, and torch autograd in fp64.
+* ``attn_bwd_rows`` (dq of chosen query rows, dk and dv of chosen key rows of
+  one head) -- pinned: the full ``attn_bwd`` on those rows, and torch
+  autograd in fp64 on those rows, with equal and unequal lengths.
 
 Planted mistakes (``tests/test_oracle_mutants.py``) check that the pins catch
 a dropped term, a wrong sign, a wrong index or a transposed operand.
@@ -20,6 +23,7 @@ a dropped term, a wrong sign, a wrong index or a transposed operand.
 from .oracle import (  # noqa: F401
     OracleLib,
     attn_bwd,
+    attn_bwd_rows,
     attn_fwd,
     attn_fwd_rows,
     build,

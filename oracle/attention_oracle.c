@@ -69,6 +69,8 @@
  * q, o, dO, dq have BH heads of Nq rows, k, v, dk, dv BH / G heads of Nk
  * rows; lse and the per-row statistics are [BH][Nq].  BH = B*H independent
  * query heads.
+ * oracle_attn_fwd_rows and oracle_attn_bwd_rows compute the same formulas
+ * for chosen rows of one head (sampled checks of long sequences).
  * Parallelism: OpenMP over (head, row) for the row-wise passes and over
  * (head, key) for the key-wise pass.  No blocking, no online softmax, no
  * reordering beyond the loops of the definition.
@@ -276,4 +278,95 @@ void oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
         }
         lse[t] = m + log(l);
     }
+}
+
+/*
+ * Backward for chosen rows of one head (for checks at sizes where the full
+ * backward would take too long): dq of the query rows qrows[0 .. Rq) and dk,
+ * dv of the key rows krows[0 .. Rk), with the formulas of oracle_attn_bwd
+ * restricted to those outputs.  One head, no grouping, no block mask; causal
+ * with Nq != Nk aligns the last query with the last key as above.
+ * q, dO: [Nq][d]; k, v: [Nk][d]; dq: [Rq][d]; dk, dv: [Rk][d].
+ *
+ * dk_j and dv_j sum over every query row i that sees key j, so the row
+ * statistics m_i, l_i and D_i are computed for each such row (and for the
+ * rows of qrows); no statistic is taken from elsewhere.
+ */
+void oracle_attn_bwd_rows(const double *q, const double *k, const double *v, const double *dO,
+                          const int *qrows, int Rq, const int *krows, int Rk,
+                          double *dq, double *dk, double *dv,
+                          int Nq, int Nk, int d, double scale, int causal) {
+    const Mask mkv = make_mask(causal, Nq, Nk, NULL, 1, 1), *mk = &mkv;
+    double *m = (double *)malloc(sizeof(double) * (size_t)(Nq > 0 ? Nq : 1));
+    double *l = (double *)malloc(sizeof(double) * (size_t)(Nq > 0 ? Nq : 1));
+    double *D = (double *)malloc(sizeof(double) * (size_t)(Nq > 0 ? Nq : 1));
+    unsigned char *need = (unsigned char *)calloc((size_t)(Nq > 0 ? Nq : 1), 1);
+    /* a statistic that is used without having been computed shows as NaN */
+    for (int i = 0; i < Nq; ++i) m[i] = l[i] = D[i] = NAN;
+
+    /* rows whose statistics are used: the rows of qrows, and every row that
+     * sees at least one key of krows */
+    for (int t = 0; t < Rq; ++t) need[qrows[t]] = 1;
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < Nq; ++i) {
+        for (int t = 0; t < Rk && !need[i]; ++t)
+            if (visible(mk, i, krows[t])) need[i] = 1;
+    }
+
+    /* m_i, l_i (safe softmax) and D_i = sum_j p_ij dp_ij of those rows */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int i = 0; i < Nq; ++i) {
+        if (!need[i]) continue;
+        const double *dOi = dO + (long)i * d;
+        row_stats(q, k, i, Nk, mk, d, scale, &m[i], &l[i]);
+        double Di = 0.0;
+        for (long j = 0; j < Nk; ++j) {
+            if (!visible(mk, i, j)) continue;
+            double p = exp(score(q + (long)i * d, k + j * d, d, scale) - m[i]) / l[i];
+            double dp = 0.0;
+            for (int c = 0; c < d; ++c) dp += dOi[c] * v[j * d + c];
+            Di += p * dp;
+        }
+        D[i] = Di;
+    }
+
+    /* dq_i = scale * sum_j ds_ij k_j for the rows of qrows */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < Rq; ++t) {
+        const long i = qrows[t];
+        const double *dOi = dO + i * d;
+        double *dqi = dq + (long)t * d;
+        for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+        for (long j = 0; j < Nk; ++j) {
+            if (!visible(mk, i, j)) continue;
+            double p = exp(score(q + i * d, k + j * d, d, scale) - m[i]) / l[i];
+            double dp = 0.0;
+            for (int c = 0; c < d; ++c) dp += dOi[c] * v[j * d + c];
+            double ds = p * (dp - D[i]);
+            for (int c = 0; c < d; ++c) dqi[c] += scale * ds * k[j * d + c];
+        }
+    }
+
+    /* dv_j = sum_i p_ij dO_i and dk_j = scale * sum_i ds_ij q_i for the keys of krows */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < Rk; ++t) {
+        const long j = krows[t];
+        double *dvj = dv + (long)t * d, *dkj = dk + (long)t * d;
+        for (int c = 0; c < d; ++c) { dvj[c] = 0.0; dkj[c] = 0.0; }
+        for (long i = 0; i < Nq; ++i) {
+            if (!visible(mk, i, j)) continue;
+            double p = exp(score(q + i * d, k + j * d, d, scale) - m[i]) / l[i];
+            double dp = 0.0;
+            for (int c = 0; c < d; ++c) dp += dO[i * d + c] * v[j * d + c];
+            double ds = p * (dp - D[i]);
+            for (int c = 0; c < d; ++c) {
+                dvj[c] += p * dO[i * d + c];
+                dkj[c] += scale * ds * q[i * d + c];
+            }
+        }
+    }
+    free(m);
+    free(l);
+    free(D);
+    free(need);
 }

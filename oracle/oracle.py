@@ -105,6 +105,9 @@ class OracleLib:
         lib.oracle_attn_fwd_rows.argtypes = [dp, dp, dp, ip, ci, dp, dp,
                                              ci, ci, ci, cd, ci]
         lib.oracle_attn_fwd_rows.restype = None
+        lib.oracle_attn_bwd_rows.argtypes = [dp, dp, dp, dp, ip, ci, ip, ci, dp, dp, dp,
+                                             ci, ci, ci, cd, ci]
+        lib.oracle_attn_bwd_rows.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ci
         self._lib = lib
@@ -192,6 +195,35 @@ class OracleLib:
             _ptr(o), _ptr(lse), N, Nk, d, float(scale), int(bool(causal)))
         return o, lse
 
+    def attn_bwd_rows(self, q, k, v, dO, qrows, krows, scale: float, causal: bool):
+        """Backward for selected rows of ONE head: q, dO are [Nq, d], k, v
+        are [Nk, d].
+
+        Returns (dq [Rq, d] for the query rows ``qrows``, dk [Rk, d] and
+        dv [Rk, d] for the key rows ``krows``), equal to those rows of
+        attn_bwd's outputs.
+        """
+        q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+        N, d = q.shape
+        if dO.shape != q.shape:
+            raise ValueError(f"dO {dO.shape} must be shaped like q {q.shape}")
+        Nk = _kv_rows(N, k[None], v[None], d, causal)
+        qr = np.ascontiguousarray(np.asarray(qrows, dtype=np.int32))
+        kr = np.ascontiguousarray(np.asarray(krows, dtype=np.int32))
+        if qr.size and (qr.min() < 0 or qr.max() >= N):
+            raise ValueError("query row out of range")
+        if kr.size and (kr.min() < 0 or kr.max() >= Nk):
+            raise ValueError("key row out of range")
+        dq = np.empty((qr.shape[0], d), dtype=np.float64)
+        dk = np.empty((kr.shape[0], d), dtype=np.float64)
+        dv = np.empty((kr.shape[0], d), dtype=np.float64)
+        ip = ctypes.POINTER(ctypes.c_int)
+        self._lib.oracle_attn_bwd_rows(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(dO), qr.ctypes.data_as(ip), qr.shape[0],
+            kr.ctypes.data_as(ip), kr.shape[0], _ptr(dq), _ptr(dk), _ptr(dv),
+            N, Nk, d, float(scale), int(bool(causal)))
+        return dq, dk, dv
+
 
 _default = None
 
@@ -217,3 +249,7 @@ def attn_bwd(q, k, v, dO, scale, causal, return_D=False, block_mask=None, block=
 
 def attn_fwd_rows(q, k, v, rows, scale, causal):
     return default().attn_fwd_rows(q, k, v, rows, scale, causal)
+
+
+def attn_bwd_rows(q, k, v, dO, qrows, krows, scale, causal):
+    return default().attn_bwd_rows(q, k, v, dO, qrows, krows, scale, causal)

@@ -319,6 +319,53 @@ def check_torch_autograd(orc):
         assert np.allclose(dv, tv.grad.numpy(), atol=1e-11, rtol=0)
 
 
+def _rows_cases():
+    """(Nq, Nk, causal) shapes for the backward rows entry: equal lengths
+    with and without the causal mask, fewer queries than keys (causal,
+    bottom-right aligned) and more queries than keys (unmasked)."""
+    return ((33, 33, False), (33, 33, True), (20, 45, True), (40, 17, False))
+
+
+def check_bwd_rows_entry(orc):
+    """The backward rows entry equals the full backward on those rows: dq of
+    the chosen query rows, dk and dv of the chosen key rows."""
+    r = _rng(14)
+    d = 8
+    for Nq, Nk, causal in _rows_cases():
+        q, dO = (r.normal(size=(Nq, d)) for _ in range(2))
+        k, v = (r.normal(size=(Nk, d)) for _ in range(2))
+        qrows = [0, 3, Nq // 2, Nq - 1]
+        krows = [0, 1, Nk // 3, Nk - 2, Nk - 1]
+        dq, dk, dv = orc.attn_bwd(q, k, v, dO, 0.45, causal)
+        dq_r, dk_r, dv_r = orc.attn_bwd_rows(q, k, v, dO, qrows, krows, 0.45, causal)
+        assert np.allclose(dq_r, dq[qrows], atol=1e-13, rtol=0), (Nq, Nk, causal)
+        assert np.allclose(dk_r, dk[krows], atol=1e-13, rtol=0), (Nq, Nk, causal)
+        assert np.allclose(dv_r, dv[krows], atol=1e-13, rtol=0), (Nq, Nk, causal)
+
+
+def check_bwd_rows_torch(orc):
+    """The backward rows entry against torch autograd in fp64 (explicit
+    mask: key j visible to query i iff j <= i + Nk - Nq when causal) on the
+    chosen rows, to 1e-11."""
+    import torch
+    r = _rng(15)
+    d = 8
+    for Nq, Nk, causal in _rows_cases():
+        q, dO = (r.normal(size=(Nq, d)) for _ in range(2))
+        k, v = (r.normal(size=(Nk, d)) for _ in range(2))
+        tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (q, k, v))
+        s = (tq @ tk.T) * 0.6
+        if causal:
+            s = s.masked_fill(~_bottom_right_mask(Nq, Nk), float("-inf"))
+        (torch.softmax(s, dim=-1) @ tv).backward(torch.from_numpy(dO))
+        qrows = [1, Nq // 3, Nq - 1]
+        krows = [Nk // 2 + 1, Nk - 1]  # no key 0 (which every causal row sees)
+        dq_r, dk_r, dv_r = orc.attn_bwd_rows(q, k, v, dO, qrows, krows, 0.6, causal)
+        assert np.allclose(dq_r, tq.grad.numpy()[qrows], atol=1e-11, rtol=0), (Nq, Nk, causal)
+        assert np.allclose(dk_r, tk.grad.numpy()[krows], atol=1e-11, rtol=0), (Nq, Nk, causal)
+        assert np.allclose(dv_r, tv.grad.numpy()[krows], atol=1e-11, rtol=0), (Nq, Nk, causal)
+
+
 # ----------------------------------------------------------------------------
 # grouped key/value heads (GQA / MQA)
 # ----------------------------------------------------------------------------
@@ -597,7 +644,8 @@ FWD_CHECKS = (check_four_scores, check_rows_sum_to_one, check_softmax_of_scores,
               check_identical_keys, check_causal_row0, check_zero_queries,
               check_dominant_key, check_blocked_online_softmax,
               check_multi_head_independent, check_rows_entry, check_torch_sdpa_fwd)
-BWD_CHECKS = (check_finite_differences, check_gradient_invariants, check_torch_autograd)
+BWD_CHECKS = (check_finite_differences, check_gradient_invariants, check_torch_autograd,
+              check_bwd_rows_entry, check_bwd_rows_torch)
 GQA_CHECKS = (check_gqa_torch, check_gqa_finite_differences)
 CROSS_CHECKS = (check_cross_torch, check_cross_causal_is_suffix, check_cross_finite_differences)
 SPARSE_CHECKS = (check_block_sparse_torch, check_block_sparse_empty_rows,

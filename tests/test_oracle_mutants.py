@@ -36,6 +36,13 @@ MUTANTS = {
         "dp += dOh[i * d + c] * vh[(long)j * d + c];",
         "dp += dOh[(long)j * d + c] * vh[i * d + c];"),
     "key_pass_D_dropped": ("double ds = p * (dp - D[r]);", "double ds = p * dp;"),
+    # the backward rows entry
+    "bwd_rows_dk_wrong_operand": ("dkj[c] += scale * ds * q[i * d + c];",
+                                  "dkj[c] += scale * ds * k[j * d + c];"),
+    "bwd_rows_D_dropped": ("double ds = p * (dp - D[i]);", "double ds = p * dp;"),
+    "bwd_rows_query_index": ("const long i = qrows[t];", "const long i = t;"),
+    "bwd_rows_stats_top_left": ("if (visible(mk, i, krows[t])) need[i] = 1;",
+                                "if (krows[t] <= i) need[i] = 1;"),
     # grouped key/value heads
     "gqa_kv_head_modulo": ("*kh = k + (h / group) * hk, *vh = v + (h / group) * hk;",
                            "*kh = k + (h % group) * hk, *vh = v + (h % group) * hk;"),
