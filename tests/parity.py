@@ -7,6 +7,8 @@ The oracle runs in fp64 on the same bf16-rounded inputs widened to fp64.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -16,6 +18,18 @@ import oracle
 TOL_O = 2e-2
 TOL_LSE = 1e-3
 TOL_GRAD = 3e-2
+
+# Worst error of every comparison made in this process, for the margin
+# report (tests/conftest.py prints it and, when FA_PARITY_REPORT names a
+# file, writes it there as JSON lines).
+MARGINS: list = []
+
+
+def record(what: str, err: float, tol: float, **extra) -> None:
+    """Note the worst error `err` of one comparison (`what`: the tensor and
+    the kind of check) against its tolerance, under the running test's id."""
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    MARGINS.append({"test": test, "what": what, "err": float(err), "tol": float(tol), **extra})
 
 
 def f64(t) -> np.ndarray:
@@ -61,11 +75,17 @@ def check_heads(q, k, v, dO, out, scale, causal, heads, bwd=True):
                 e = rel_fro(f64(out[name][b, h]), r)
                 assert e <= TOL_GRAD, f"{name} rel-Frobenius {e} at head {(b, h)}"
                 worst[name] = max(worst[name], e)
+    record("o max-abs", worst["o"], TOL_O, heads=len(heads))
+    record("lse max-abs", worst["lse"], TOL_LSE, heads=len(heads))
+    if bwd:
+        for name in ("dq", "dk", "dv"):
+            record(f"{name} rel-Frobenius", worst[name], TOL_GRAD, heads=len(heads))
     return worst
 
 
 def check_rows(q, k, v, out, scale, causal, heads, rows):
     """O and LSE on selected query rows of selected heads (any size)."""
+    wo = wl = 0.0
     for b, h in heads:
         o_r, lse_r = oracle.attn_fwd_rows(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), rows,
                                           scale, causal)
@@ -73,6 +93,29 @@ def check_rows(q, k, v, out, scale, causal, heads, rows):
         el = float(np.abs(f64(out["lse"][b, h][rows]) - lse_r).max())
         assert eo <= TOL_O, f"O max-abs {eo} at head {(b, h)} rows"
         assert el <= TOL_LSE, f"LSE max-abs {el} at head {(b, h)} rows"
+        wo, wl = max(wo, eo), max(wl, el)
+    record("o max-abs (rows)", wo, TOL_O, heads=len(heads), rows=len(rows))
+    record("lse max-abs (rows)", wl, TOL_LSE, heads=len(heads), rows=len(rows))
+
+
+def check_bwd_rows(q, k, v, dO, out, scale, causal, heads, qrows, krows):
+    """dq on selected query rows and dk, dv on selected key rows of selected
+    heads (any size), against the oracle's backward rows entry: relative
+    Frobenius error over the selected rows of each tensor, per head."""
+    worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
+    for b, h in heads:
+        refs = oracle.attn_bwd_rows(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), f64(dO[b, h]),
+                                    qrows, krows, scale, causal)
+        for name, rows, r in zip(("dq", "dk", "dv"), (qrows, krows, krows), refs):
+            g = f64(out[name][b, h][rows])
+            assert np.isfinite(g).all(), f"{name} not finite at head {(b, h)} rows"
+            e = rel_fro(g, r)
+            assert e <= TOL_GRAD, f"{name} rel-Frobenius {e} at head {(b, h)} rows"
+            worst[name] = max(worst[name], e)
+    for name in ("dq", "dk", "dv"):
+        record(f"{name} rel-Frobenius (rows)", worst[name], TOL_GRAD, heads=len(heads),
+               rows=len(qrows if name == "dq" else krows))
+    return worst
 
 
 def check_invariants(dO, out, tol=3e-2):
@@ -90,6 +133,8 @@ def check_invariants(dO, out, tol=3e-2):
     err_k = (dk.sum(dim=2).norm(dim=-1) / fro(dk)).max().item()
     assert err_v <= tol, f"sum dv != sum dO: {err_v}"
     assert err_k <= tol, f"sum dk != 0: {err_k}"
+    record("sum_j dv_j - sum_i dO_i (all heads)", err_v, tol)
+    record("sum_j dk_j (all heads)", err_k, tol)
     return err_v, err_k
 
 
@@ -116,6 +161,7 @@ def check_groups(q, k, v, dO, out, scale, causal, kv_heads):
     that head, against the oracle run on the group."""
     H, H_kv = q.shape[1], k.shape[1]
     G = H // H_kv
+    worst = {"o": 0.0, "lse": 0.0, "dq": 0.0, "dk": 0.0, "dv": 0.0}
     for b, hk in kv_heads:
         hs = slice(hk * G, hk * G + G)
         qg, dOg = f64(q[b, hs]), f64(dO[b, hs])
@@ -129,6 +175,14 @@ def check_groups(q, k, v, dO, out, scale, causal, kv_heads):
         for g in range(G):
             e = rel_fro(f64(out["dq"][b, hk * G + g]), dq_ref[g])
             assert e <= TOL_GRAD, f"dq rel-Frobenius {e} at query head {(b, hk * G + g)}"
+            worst["dq"] = max(worst["dq"], e)
         for name, r in (("dk", dk_ref[0]), ("dv", dv_ref[0])):
             e = rel_fro(f64(out[name][b, hk]), r)
             assert e <= TOL_GRAD, f"{name} rel-Frobenius {e} at key/value head {(b, hk)}"
+            worst[name] = max(worst[name], e)
+        worst["o"], worst["lse"] = max(worst["o"], eo), max(worst["lse"], el)
+    record("o max-abs", worst["o"], TOL_O, kv_heads=len(kv_heads))
+    record("lse max-abs", worst["lse"], TOL_LSE, kv_heads=len(kv_heads))
+    for name in ("dq", "dk", "dv"):
+        record(f"{name} rel-Frobenius", worst[name], TOL_GRAD, kv_heads=len(kv_heads))
+    return worst

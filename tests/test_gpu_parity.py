@@ -11,7 +11,8 @@ import torch
 
 import io_aware_exact_10_gb300 as fa
 from io_aware_exact_10_gb300 import workloads as W
-from parity import (check_heads, check_invariants, check_rows, f64, run_gpu, seeded_heads)
+from parity import (check_bwd_rows, check_heads, check_invariants, check_rows, f64, run_gpu,
+                    seeded_heads)
 
 pytestmark = pytest.mark.gpu
 
@@ -148,19 +149,32 @@ def test_stress(causal):
     check_invariants(dO, out)
 
 
+def sampled_rows(N, n, seed):
+    """n distinct rows of [0, N): the first and last rows of the first two
+    tiles and of the sequence, the middle one, and seeded random rows."""
+    fixed = [r for r in (0, 1, 127, 128, N // 2, N - 2, N - 1) if 0 <= r < N]
+    rest = np.setdiff1d(np.arange(N), fixed)
+    pick = np.random.default_rng(seed).choice(rest, n - len(fixed), replace=False)
+    return np.sort(np.concatenate([fixed, pick])).astype(np.int64)
+
+
 @pytest.mark.parametrize("d", W.SWEEP_D)
 @pytest.mark.parametrize("N", W.SWEEP_N)
 def test_sweep(N, d):
-    """Sequence-length sweep (H=16, B*N=65536, causal): one head in full up to
-    N=4096 (forward to 8192), 48 rows on two heads beyond, identities on all."""
+    """Sequence-length sweep (H=16, B*N=65536, causal): one head in full,
+    forward and backward, up to N=8192; beyond that, on one head, dq on 48
+    query rows and dk, dv on 48 key rows (the key rows include the first
+    tile's, whose sums run over every query).  O and LSE on 48 rows of two
+    more heads, and the gradient identities on every head."""
     w = W.sweep(N, d)
     q, k, v, dO = W.make_inputs(w)
     out = run_gpu(q, k, v, dO, w.scale, True)
     head = seeded_heads(w.B, w.H, 1, seed=N)
-    if N <= 4096:
+    if N <= 8192:
         check_heads(q, k, v, dO, out, w.scale, True, head)
-    elif N <= 8192:
-        check_heads(q, k, v, dO, out, w.scale, True, head, bwd=False)
+    else:
+        check_bwd_rows(q, k, v, dO, out, w.scale, True, head, sampled_rows(N, 48, N + 2),
+                       sampled_rows(N, 48, N + 3))
     rows = np.concatenate([[0, N - 1], np.random.default_rng(N).choice(N, 46, replace=False)])
     check_rows(q, k, v, out, w.scale, True, seeded_heads(w.B, w.H, 2, seed=N + 1), rows)
     check_invariants(dO, out)

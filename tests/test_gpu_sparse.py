@@ -12,7 +12,7 @@ import torch
 
 import io_aware_exact_10_gb300 as fa
 import oracle
-from parity import TOL_GRAD, TOL_LSE, TOL_O, f64, gqa_inputs, rel_fro
+from parity import TOL_GRAD, TOL_LSE, TOL_O, f64, gqa_inputs, record, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +33,7 @@ def check_sparse(q, k, v, dO, out, scale, causal, bm):
     B, H, Nq, d = q.shape
     H_kv = k.shape[1]
     G = H // H_kv
+    worst = {"o": 0.0, "lse": 0.0, "dq": 0.0, "dk": 0.0, "dv": 0.0}
     for b in range(B):
         for hk in range(H_kv):
             hs = slice(hk * G, hk * G + G)
@@ -43,20 +44,28 @@ def check_sparse(q, k, v, dO, out, scale, causal, bm):
             assert np.all(np.isfinite(o_g)), "non-finite O"
             eo = float(np.abs(o_g - o_ref).max())
             assert eo <= TOL_O, f"O max-abs {eo} at {(b, hk)}"
+            worst["o"] = max(worst["o"], eo)
             empty = np.isneginf(lse_ref)
             assert np.array_equal(np.isneginf(lse_g), empty), f"-inf LSE rows differ at {(b, hk)}"
             if (~empty).any():
                 el = float(np.abs(lse_g[~empty] - lse_ref[~empty]).max())
                 assert el <= TOL_LSE, f"LSE max-abs {el} at {(b, hk)}"
+                worst["lse"] = max(worst["lse"], el)
             refs = oracle.attn_bwd(qg, kg, vg, dOg, scale, causal, block_mask=bm)
             for g in range(G):
                 e = rel_fro(f64(out["dq"][b, hk * G + g]), refs[0][g])
                 assert e <= TOL_GRAD, f"dq rel-Frobenius {e} at query head {(b, hk * G + g)}"
+                worst["dq"] = max(worst["dq"], e)
             for name, r in (("dk", refs[1][0]), ("dv", refs[2][0])):
                 gv = f64(out[name][b, hk])
                 assert np.all(np.isfinite(gv)), f"non-finite {name}"
                 e = rel_fro(gv, r)
                 assert e <= TOL_GRAD, f"{name} rel-Frobenius {e} at {(b, hk)}"
+                worst[name] = max(worst[name], e)
+    record("o max-abs", worst["o"], TOL_O)
+    record("lse max-abs", worst["lse"], TOL_LSE)
+    for name in ("dq", "dk", "dv"):
+        record(f"{name} rel-Frobenius", worst[name], TOL_GRAD)
 
 
 def random_mask(Nq, Nk, density, seed, keep_col0=True):
