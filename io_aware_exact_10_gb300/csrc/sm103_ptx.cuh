@@ -77,17 +77,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with an explicit bound on how long the thread may be suspended in
+// it (ns); without one the hardware picks its own limit.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait bounds below this are honoured to within a poll: each try_wait may
+// suspend for at most kShortSuspendNs and the clock is read after every one.
+// Longer bounds (the default is 2 s) read the clock every 64 polls.
+constexpr unsigned long long kShortBoundNs = 1000000ull;
+constexpr uint32_t kShortSuspendNs = 256u;
+
 // Wait until the phase with the given parity of `bar` has completed.  The wait
 // is bounded: it gives up when `*abort` is raised by another thread of the CTA,
 // or after ctl.timeout_ns, in which case it records kErrTimeout with `site`
 // and raises `*abort` itself.  Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
                                           volatile int* abort, uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const bool short_bound = ctl.timeout_ns < kShortBoundNs;
+  if (short_bound ? mbar_try_wait_hint(bar, parity, kShortSuspendNs) : mbar_try_wait(bar, parity))
+    return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (short_bound ? mbar_try_wait_hint(bar, parity, kShortSuspendNs) : mbar_try_wait(bar, parity))
+      return true;
+    if ((it & 63u) == 0 || short_bound) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > ctl.timeout_ns) {
         record_error(ctl, kErrTimeout, site);
