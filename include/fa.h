@@ -42,7 +42,8 @@
  *     fa_last_device_error() reads.
  *   - Thread safety: calls on distinct streams may come from distinct host
  *     threads.
- *   - CUDA graphs: every compute entry point, the host-memory ones included,
+ *   - CUDA graphs: fa_fwd, fa_fwd_gqa, fa_fwd_ex, fa_fwd_sparse, fa_bwd,
+ *     fa_bwd_gqa, fa_bwd_ex, fa_bwd_sparse and the host-memory entry points
  *     may be captured on a stream and replayed; a replay computes on what the
  *     buffers hold then.  Make one eager call on the device first (it looks
  *     up the device and the driver's tensor-map encoder once).
@@ -192,6 +193,22 @@ fa_status fa_bwd_sparse(const void* q, const void* k, const void* v, const void*
                         int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
                         const unsigned char* block_mask, void* workspace,
                         size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * Forward with a chosen key tile: fa_fwd_ex computed with K and V streamed in
+ * tiles of key_tile keys (64 or 128; fa_fwd_ex uses 128).  Same arguments,
+ * outputs and errors as fa_fwd_ex, plus key_tile: any other value returns
+ * FA_ERR_UNSUPPORTED before anything is launched.  The results of the two
+ * tile sizes agree to rounding (the online softmax sums the keys in another
+ * grouping); fa_bwd_ex accepts the o and lse of either.  This is the block-
+ * size axis of the IO analysis: FlashAttention: exact attention made fast by
+ * counting memory traffic, "The decisive evidence" (Fig. 2, runtime against
+ * block size); the pages' block-size rule itself (Flash Attention, "Memory &
+ * Performance Analysis") is not used.
+ */
+fa_status fa_fwd_tiled(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                       int key_tile, struct CUstream_st* stream);
 
 /*
  * Backward with no workspace argument and no allocation.  The paper has no

@@ -39,6 +39,7 @@ from .binding import (  # noqa: F401
     fa_fwd_host,
     fa_fwd_host_device_bytes,
     fa_fwd_sparse,
+    fa_fwd_tiled,
     fa_last_device_error,
     fa_set_wait_timeout_ns,
     fa_strerror,

@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_ex.restype = i
         L.fa_fwd_sparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp]
         L.fa_fwd_sparse.restype = i
+        L.fa_fwd_tiled.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+        L.fa_fwd_tiled.restype = i
         L.fa_bwd_sparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i,
                                     vp, vp, sz, vp]
         L.fa_bwd_sparse.restype = i
@@ -204,6 +206,18 @@ def fa_fwd_sparse(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, block
                             _ptr(block_mask), _stream(stream))
     if check:
         _check(s, "fa_fwd_sparse")
+    return s
+
+
+def fa_fwd_tiled(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, key_tile,
+                 stream=None, check=True) -> int:
+    """fa_fwd_tiled(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, key_tile,
+    stream) -> status: fa_fwd_ex with K/V tiles of key_tile (64 or 128) keys."""
+    s = lib().fa_fwd_tiled(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                           int(H_kv), int(N_q), int(N_k), int(d), float(scale), int(causal),
+                           int(key_tile), _stream(stream))
+    if check:
+        _check(s, "fa_fwd_tiled")
     return s
 
 

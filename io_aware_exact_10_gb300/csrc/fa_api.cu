@@ -87,12 +87,13 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
-// bf16 [BH][N][d] viewed as a 3-D tensor (d, N, BH); box of 64 columns x 128
-// rows, 128-byte swizzle (the layout the tcgen05 descriptors expect).
-bool encode_bf16_3d(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
+// bf16 [BH][N][d] viewed as a 3-D tensor (d, N, BH); box of 64 columns x
+// `rows` rows (128, or 64 for 64-key tiles), 128-byte swizzle (the layout the
+// tcgen05 descriptors expect).
+bool encode_bf16_3d(CUtensorMap* m, const void* ptr, int BH, int N, int d, int rows = 128) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -150,6 +151,12 @@ bool mask_fits(int Nq, int Nk) {
 // whole 128-row tiles
 size_t stats_floats(int BH, int N) { return (size_t)BH * (size_t)((N + 127) / 128) * 256; }
 
+// The forward behind fa_fwd_sparse (128-key tiles, optional block mask)
+// and fa_fwd_tiled (dense, 64- or 128-key tiles).
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                   const unsigned char* block_mask, int key_tile, struct CUstream_st* stream);
+
 }  // namespace
 
 extern "C" {
@@ -174,6 +181,24 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
                         const unsigned char* block_mask, struct CUstream_st* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, block_mask, 128, stream);
+}
+
+fa_status fa_fwd_tiled(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                       int key_tile, struct CUstream_st* stream) {
+  if (key_tile != 64 && key_tile != 128) return FA_ERR_UNSUPPORTED;
+  return fwd_impl(q, k, v, o, lse, B, H, H_kv, N_q, N_k, d, scale, causal, nullptr, key_tile,
+                  stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int H_kv, int N_q, int N_k, int d, float scale, int causal,
+                   const unsigned char* block_mask, int key_tile, struct CUstream_st* stream) {
   bool empty = false;
   fa_status s = check_common(B, H, H_kv, N_q, N_k, d, scale, causal, &empty);
   if (s != FA_OK || empty) return s;
@@ -185,9 +210,10 @@ fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, void* o, fl
   if (!get_encoder()) return FA_ERR_LAUNCH;
   fa::FwdLaunch a;
   const int BH = B * H, BHkv = B * H_kv;
-  if (!encode_bf16_3d(&a.tq, q, BH, N_q, d) || !encode_bf16_3d(&a.tk, k, BHkv, N_k, d) ||
-      !encode_bf16_3d(&a.tv, v, BHkv, N_k, d))
+  if (!encode_bf16_3d(&a.tq, q, BH, N_q, d) || !encode_bf16_3d(&a.tk, k, BHkv, N_k, d, key_tile) ||
+      !encode_bf16_3d(&a.tv, v, BHkv, N_k, d, key_tile))
     return FA_ERR_INVALID_ARG;
+  a.key_tile = key_tile;
   a.o = o;
   a.lse = lse;
   a.BH = BH;
@@ -207,6 +233,10 @@ fa_status fa_fwd_sparse(const void* q, const void* k, const void* v, void* o, fl
   }
   return FA_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   bool empty = false;

@@ -41,28 +41,36 @@ constexpr float kTau = 8.0f;
 constexpr int kSplit = 1;  // softmax warpgroups per query tile (2 measured no faster)
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int HD, int NH>
+template <int HD, int NH, int BN_ = 128>
 struct FwdCfg {
   static constexpr int BM = 128;                  // query rows per tile
-  static constexpr int BN = 128;                  // keys per K/V tile
+  static constexpr int BN = BN_;                  // keys per K/V tile (128, or 64)
   static constexpr int KB = HD / 64;              // 64-column (128-byte) blocks per row
   static constexpr int QTILE = BM * HD * 2;       // bytes of one Q tile
   static constexpr int KVTILE = BN * HD * 2;      // bytes of one K or V tile
-  static constexpr int STAGES = HD == 128 ? 4 : 8;
+  // the ring holds 128 KB of K/V tiles whatever their size
+  static constexpr int STAGES = (HD == 128 ? 4 : 8) * (128 / BN);
   static constexpr int SMEM = 2 * QTILE + STAGES * KVTILE + 1024;
   // NH warpgroups share each query tile's softmax, each taking 128 / NH of
   // the key columns; then come the TMA warp and the MMA warp.
   static constexpr int WS = 8 * NH;               // softmax warps
   static constexpr int W_LOAD = WS, W_MMA = WS + 1;
   static constexpr int THREADS = (WS + 2) * 32;
-  static constexpr int CPT = 128 / NH;            // key columns per softmax thread
+  static constexpr int CPT = BN / NH;             // key columns per softmax thread
   static constexpr int OCPT = HD / NH;            // O columns per softmax thread
   static constexpr uint32_t TMEM_COLS = 512;
-  // P in columns of its own (d = 64 only: S, P and O of two tiles fill the 512)
+  // P in columns of its own (d = 64 only: with 128-key tiles, S, P and O of
+  // two tiles fill the 512)
   static constexpr bool SEPP = HD == 64 && NH == 1;
-  static constexpr uint32_t colS(int t) { return (uint32_t)t * 128; }
-  static constexpr uint32_t colP(int t) { return SEPP ? 256 + (uint32_t)t * 64 : (uint32_t)t * 128; }
-  static constexpr uint32_t colO(int t) { return SEPP ? 384 + (uint32_t)t * 64 : 256 + (uint32_t)t * HD; }
+  static constexpr uint32_t colS(int t) { return (uint32_t)t * BN; }
+  static constexpr uint32_t colP(int t) {
+    return SEPP ? 2 * BN + (uint32_t)t * (BN / 2) : (uint32_t)t * BN;
+  }
+  static constexpr uint32_t colO(int t) {
+    return SEPP ? 3 * BN + (uint32_t)t * HD : 2 * BN + (uint32_t)t * HD;
+  }
+  static_assert(BN == 128 || (BN == 64 && NH == 1), "64-key tiles: one softmax warpgroup per tile");
+  static_assert(colO(1) + HD <= TMEM_COLS, "tensor memory plan");
 };
 
 struct FwdParams {
@@ -92,11 +100,12 @@ __device__ __forceinline__ uint32_t p_col(int k) {
   return NH == 1 ? (uint32_t)(k * 8) : (uint32_t)(k * 8 + (k >= 4 ? 32 : 0));
 }
 
-template <int HD, bool CAUSAL, int NH, bool SPARSE>
+template <int HD, bool CAUSAL, int NH, bool SPARSE, int BN = 128>
 __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  using C = FwdCfg<HD, NH>;
+  using C = FwdCfg<HD, NH, BN>;
+  static_assert(BN == 128 || !SPARSE, "block masks are over 128 x 128 blocks");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
@@ -313,15 +322,18 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       constexpr uint32_t kIdPV = idesc_bf16(128, HD, false, true);
       // descriptor halves (sdesc_lo / sdesc_hi) of Q tile 0 and ring slot 0
       constexpr uint32_t HI = sdesc_hi(1024);
-      constexpr uint32_t QT16 = C::QTILE >> 4, KV16 = C::KVTILE >> 4, BLK16 = (C::BM * 128) >> 4;
+      // 64-column blocks of a Q tile (128 rows) and of a K tile (BN rows), in 16-byte units
+      constexpr uint32_t QT16 = C::QTILE >> 4, KV16 = C::KVTILE >> 4, QBLK16 = (C::BM * 128) >> 4,
+                         KBLK16 = (C::BN * 128) >> 4;
       const uint32_t qK = sdesc_lo(sQ, 16), rK = sdesc_lo(sRing, 16), rMN = sdesc_lo(sRing, C::BN * 128);
       // S_t = Q_t K^T for the K tile in ring slot `slot`.
       auto issue_s = [&](int t, int slot) {
         const uint32_t a0 = qK + (uint32_t)t * QT16, b0 = rK + (uint32_t)slot * KV16;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (uint32_t)(k / 4) * BLK16 + (uint32_t)(k % 4) * 2;
-          mma_ss_e(lead, tmem + C::colS(t), a0 + off, HI, b0 + off, HI, kIdS, k > 0);
+          const uint32_t koff = (uint32_t)(k % 4) * 2;
+          mma_ss_e(lead, tmem + C::colS(t), a0 + (uint32_t)(k / 4) * QBLK16 + koff, HI,
+                   b0 + (uint32_t)(k / 4) * KBLK16 + koff, HI, kIdS, k > 0);
         }
         mma_commit_e(lead, smem_u32(&bar_s[t]));
       };
@@ -555,25 +567,25 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
             break;
           }
           tc_fence_after();
-          int lim = 128;
+          int lim = C::BN;
           if (CAUSAL) lim = min(lim, row + p.coff + 1 - j * C::BN);
           if (!CAUSAL && tail && j == p.nkv - 1) lim = p.Nk - j * C::BN;
           // The whole row of S into registers; S_t may then be overwritten.
-          float sv[128];
+          float sv[C::BN];
 #pragma unroll
-          for (int c = 0; c < 128; c += 32) tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(sv + c));
+          for (int c = 0; c < C::BN; c += 32) tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(sv + c));
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bar_sf[t]));
-          if (lim < 128) {
+          if (lim < C::BN) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
+            for (int c = 0; c < C::BN; ++c)
               if (c >= lim) sv[c] = -INFINITY;
           }
           float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int c = 0; c < 128; c += 8) {
+          for (int c = 0; c < C::BN; c += 8) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) mc[e] = fmax3(mc[e], sv[c + 2 * e], sv[c + 2 * e + 1]);
           }
@@ -612,7 +624,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-mr, -mr);
           uint64_t l2 = f2_pack(0.f, 0.f);
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
+          for (int c0 = 0; c0 < C::BN; c0 += 32) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -652,7 +664,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         // may be <= 0: a tile past the row's last key.  Without a block mask
         // key 0 is in every row's first tile, so the running max is finite
         // from there on.
-        int lim = 128;
+        int lim = C::BN;
         if (CAUSAL) lim = min(lim, row + p.coff + 1 - j * C::BN);
         if (!CAUSAL && tail && j == p.nkv - 1) lim = p.Nk - j * C::BN;
         // Pass 1: max over this thread's columns, 64 at a time (pass 2 reads
@@ -664,7 +676,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           tmem_ld32(tS + cb + c64, *reinterpret_cast<uint32_t(*)[32]>(sv));
           tmem_ld32(tS + cb + c64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
           tmem_wait_ld();
-          if (lim < 128) {
+          if (lim < C::BN) {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (cb + c64 + c >= lim) sv[c] = -INFINITY;
@@ -727,7 +739,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           float* sv = sbuf[(c0 / 32) & 1];
           if (c0 + 32 < C::CPT)
             tmem_ld32(tS + cb + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sbuf[((c0 / 32) + 1) & 1]));
-          if (lim < 128) {
+          if (lim < C::BN) {
 #pragma unroll
             for (int c = 0; c < 32; ++c)
               if (cb + c0 + c >= lim) sv[c] = -INFINITY;
@@ -819,11 +831,11 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   }
 }
 
-template <int HD, bool CAUSAL, bool SPARSE>
+template <int HD, bool CAUSAL, bool SPARSE, int BN = 128>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   constexpr int NH = kSplit;
-  using C = FwdCfg<HD, NH>;
-  auto kern = fa_fwd_kernel<HD, CAUSAL, NH, SPARSE>;
+  using C = FwdCfg<HD, NH, BN>;
+  auto kern = fa_fwd_kernel<HD, CAUSAL, NH, SPARSE, BN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   FwdParams p;
@@ -853,6 +865,13 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
+  if (a.key_tile == 64) {  // dense only (the caller checks)
+    if (a.d == 128)
+      return a.causal ? launch_fwd_t<128, true, false, 64>(a, stream)
+                      : launch_fwd_t<128, false, false, 64>(a, stream);
+    return a.causal ? launch_fwd_t<64, true, false, 64>(a, stream)
+                    : launch_fwd_t<64, false, false, 64>(a, stream);
+  }
   if (a.bmask) {
     if (a.d == 128)
       return a.causal ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, false, true>(a, stream);

@@ -14,7 +14,7 @@ namespace fa {
 // Everything a forward launch needs; tensor maps are encoded by the caller.
 struct FwdLaunch {
   CUtensorMap tq;               // bf16 [BH][Nq][d], box {64, 128, 1}, 128-byte swizzle
-  CUtensorMap tk, tv;           // bf16 [BH / group][Nk][d], same box
+  CUtensorMap tk, tv;           // bf16 [BH / group][Nk][d], box {64, key_tile, 1}
   void* o;                      // bf16 [BH][Nq][d]
   float* lse;                   // fp32 [BH][Nq]
   int BH, Nq, Nk, d;            // causal requires Nk >= Nq (bottom-right aligned)
@@ -23,6 +23,7 @@ struct FwdLaunch {
   float scale;
   int causal;
   const uint8_t* bmask;         // block mask [ceil(Nq/128)][ceil(Nk/128)], or null (dense)
+  int key_tile = 128;           // keys per K/V tile: 128, or 64 (dense only)
   KernelCtl ctl;
 };
 

@@ -144,3 +144,17 @@ def test_cross_length_argument_errors(L):
     assert b(0, 100, 1) == NODEV  # zeroes dk, dv on the device
     assert L.fa_bwd_ex(A, A, A, A, A, A, A, A, None, 1, 4, 2, 0, 100, 64, sc, 0, A, 0,
                        None) == INV  # ... which must then be valid pointers
+
+
+def test_key_tile_argument(L):
+    """fa_fwd_tiled takes 64- or 128-key tiles; other sizes are refused before
+    any device work, valid ones pass validation (and stop at the device)."""
+    import io_aware_exact_10_gb300 as fa
+    sc = ctypes.c_float(0.125)
+    f = lambda kt, d=64: L.fa_fwd_tiled(A, A, A, A, A, 1, 2, 2, 256, 256, d, sc, 1, kt, None)
+    for kt in (0, 32, 96, 127, 256, -64):
+        assert f(kt) == fa.FA_ERR_UNSUPPORTED, kt
+    for kt in (64, 128):
+        assert f(kt) == fa.FA_ERR_NO_DEVICE, kt
+        assert f(kt, d=128) == fa.FA_ERR_NO_DEVICE, kt
+    assert f(64, d=96) == fa.FA_ERR_UNSUPPORTED
