@@ -592,6 +592,35 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
           const float m_new = fmaxf(m, mx * scale2);
           const bool need = m_new > m + kTau;
+          const bool any_need = __any_sync(0xffffffffu, need);
+          const float alpha = need ? ex2(m - m_new) : 1.0f;
+          if (need) m = m_new;
+          l *= alpha;
+          lr *= alpha;
+          const float mr = m_ref(m);
+          {
+            const float pmax = ex2(fmaf(mx, scale2, -mr));
+            lr += __uint_as_float(pack_bf16(pmax, 0.f) << 16) - pmax;
+          }
+          // P = exp2(scale2 * s - m) as bf16 pairs in registers: this runs
+          // while O_t += P_t V of the previous step may still read P_t
+          const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-mr, -mr);
+          uint64_t l2 = f2_pack(0.f, 0.f);
+          uint32_t pk[C::BN / 2];
+#pragma unroll
+          for (int i = 0; i < C::BN / 2; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), sc2, nm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            pk[i] = pack_bf16(p0, p1);
+            l2 = f2_add(l2, f2_pack(p0, p1));
+          }
+          {
+            float a0, a1;
+            f2_unpack(l2, a0, a1);
+            l += a0 + a1;
+            lr += a0 + a1;
+          }
           // P_t and O_t: the previous O_t += P_t V (also of the previous
           // item) must have completed
           if (gstep > 0 && !warp_wait(smem_u32(&bar_pf[t]), (gstep - 1) & 1, p.ctl, abort, 33)) {
@@ -599,48 +628,19 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
             break;
           }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2(m - m_new) : 1.0f;
-            if (need) m = m_new;
-            l *= alpha;
-            lr *= alpha;
-            if (lstep > 0) {
+#pragma unroll
+          for (int c0 = 0; c0 < C::BN / 2; c0 += 16)
+            tmem_st16(tP + c0, *reinterpret_cast<uint32_t(*)[16]>(pk + c0));
+          if (any_need && lstep > 0) {
 #pragma unroll 1
-              for (int c0 = 0; c0 < HD; c0 += 32) {
-                uint32_t ov[32];
-                tmem_ld32(tO + c0, ov);
-                tmem_wait_ld();
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+              uint32_t ov[32];
+              tmem_ld32(tO + c0, ov);
+              tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                tmem_st32(tO + c0, ov);
-              }
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              tmem_st32(tO + c0, ov);
             }
-          }
-          const float mr = m_ref(m);
-          {
-            const float pmax = ex2(fmaf(mx, scale2, -mr));
-            lr += __uint_as_float(pack_bf16(pmax, 0.f) << 16) - pmax;
-          }
-          const uint64_t sc2 = f2_pack(scale2, scale2), nm2 = f2_pack(-mr, -mr);
-          uint64_t l2 = f2_pack(0.f, 0.f);
-#pragma unroll
-          for (int c0 = 0; c0 < C::BN; c0 += 32) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float x0, x1;
-              f2_unpack(f2_fma(f2_pack(sv[c0 + 2 * i], sv[c0 + 2 * i + 1]), sc2, nm2), x0, x1);
-              const float p0 = ex2(x0), p1 = ex2(x1);
-              pk[i] = pack_bf16(p0, p1);
-              l2 = f2_add(l2, f2_pack(p0, p1));
-            }
-            tmem_st16(tP + c0 / 2, pk);
-          }
-          {
-            float a0, a1;
-            f2_unpack(l2, a0, a1);
-            l += a0 + a1;
-            lr += a0 + a1;
           }
           tmem_wait_st();
           tc_fence_before();
