@@ -5,10 +5,13 @@
                     [--workload NAME] [--sweep]
 
 A step is one pass of the whole hot path over one batch: fa_fwd (O, LSE) then
-fa_bwd (D preprocess, the backward kernel, dQ conversion).  The workload is the
-GPT-2-medium attention shape of the paper's Figure 2 (B=64, H=16, N=1024,
-d=64, non-causal, bf16, seeded synthetic N(0,1) inputs).  Its inputs (4 x 134
-MB) exceed the 129 MB L2, so no L2 flush is needed between steps.
+fa_bwd (D preprocess, the backward kernel, dQ conversion).  The default
+workload is long-context causal training attention (B=4, H=32, N=8192,
+d=128, causal, bf16, seeded synthetic N(0,1) inputs), a shape with N >= 4096
+and d = 128, where the forward and backward are compared with the tensor
+peak.  Its inputs (4 x 268 MB) exceed the 129 MB L2, so no L2 flush is
+needed between steps.  --workload gpt2_medium gives the GPT-2-medium
+attention shape of the paper review's Figure 2 (B=64, H=16, N=1024, d=64).
 
 Printed (rank 0, one JSON line): fwd+bwd TFLOP/s with FLOPs counted as
 4*B*H*N^2*d for the forward and 2.5x that for the backward (recomputation
@@ -20,8 +23,9 @@ With --gpus N > 1 (launched under torch.distributed.run) every rank processes
 its own copy of the workload (attention heads are independent: weak scaling,
 no data-path collective); the time is the max over ranks and the value sums
 the work of all ranks.  --impl reference times the fp64 CPU oracle instead.
---workload picks another workload of io_aware_exact_10_gb300.workloads (the
-default line stays the GPT-2-medium one).  --sweep times the sequence-length
+--workload picks another workload of io_aware_exact_10_gb300.workloads.
+--once runs one untimed fa_fwd and fa_bwd of the workload (with --batch to
+cut B): the driver of a small ncu capture.  --sweep times the sequence-length
 sweep (N = 512 ... 32768, d = 64 and 128, H = 16, B*N = 65536, causal):
 forward and forward+backward TFLOP/s per point, printed as one JSON line.
 """
@@ -40,19 +44,23 @@ sys.path.insert(0, ROOT)
 
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-# DRAM bytes (read + write) of one fa_bwd call on the default workload, summed
-# over its three launches, from one ncu capture (profiles/
-# launches_gpt2_medium_fwd_bwd.md), and the commit of the kernels it measured.
-# The bench line reports it only while the code of the fa_bwd call (the
-# backward kernels, their launch layer and shared helpers, comments aside)
-# is the code the capture measured.
 # head groups of the end-to-end leg's host-memory call (copies of one group
 # overlap the kernels of the others)
 E2E_CHUNKS = 8
-NCU_TRAFFIC_BYTES = 2144.5e6
-NCU_TRAFFIC_COMMIT = "4ba4968"
-NCU_TRAFFIC_SOURCES_SHA256 = "00deef6fb9583377d4c45dd5baf7292aa8bb7def8dc73aa52c41929a6bbbb851"
+# DRAM bytes (read + write) of one fa_bwd call, summed over its three
+# launches, per workload, from one ncu capture of `bench.py --once`, with the
+# hash of the sources it measured.  A capture on a smaller batch (capture_B)
+# is scaled to the workload's B: the heads are independent, so the bytes
+# grow in proportion.  The bench line reports a figure only while the code
+# of the fa_bwd call (the backward kernels, their launch layer and shared
+# helpers, comments aside) is the code the capture measured.
+NCU_TRAFFIC = {
+    "gpt2_medium_B64_H16_N1024_d64": {
+        "bytes": 2144.5e6, "capture_B": 64,
+        "sources_sha256": "00deef6fb9583377d4c45dd5baf7292aa8bb7def8dc73aa52c41929a6bbbb851"},
+}
 BWD_SOURCES = ("fa_api.cu", "fa_bwd.cu", "fa_bwd_d64.cu", "fa_kernels.h", "sm103_ptx.cuh")
+DEFAULT_WORKLOAD = "long_causal"
 
 
 def strip_comments(text: str) -> str:
@@ -74,18 +82,14 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
-# the workload the traffic capture ran (the default bench line's)
-NCU_TRAFFIC_WORKLOAD = "gpt2_medium_B64_H16_N1024_d64"
-
-
-def ncu_traffic(workload_name: str = NCU_TRAFFIC_WORKLOAD):
-    """The captured traffic, for the workload the capture ran and while the
-    kernel sources still match the capture; else None."""
-    if workload_name != NCU_TRAFFIC_WORKLOAD:
+def ncu_traffic(w):
+    """The captured DRAM bytes of one fa_bwd call on workload w, scaled from
+    the capture's batch to w.B, while the kernel sources still match the
+    capture; else None."""
+    t = NCU_TRAFFIC.get(w.name)
+    if not t or kernel_sources_sha256() != t["sources_sha256"]:
         return None
-    if NCU_TRAFFIC_SOURCES_SHA256 and kernel_sources_sha256() == NCU_TRAFFIC_SOURCES_SHA256:
-        return NCU_TRAFFIC_BYTES
-    return None
+    return t["bytes"] * w.B / t["capture_B"]
 
 
 def load_peaks():
@@ -146,6 +150,19 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def oracle_heads(w, flops: float, most: int) -> int:
+    """Heads of workload w whose forward + backward add up to about `flops`
+    (at least 1, at most `most`): the fp64 oracle runs at a few tens of
+    GFLOP/s on the host cores, so 1e11 flop is a few seconds."""
+    one = W_head_flops(w)
+    return max(1, min(most, int(flops // one)))
+
+
+def W_head_flops(w) -> float:
+    """Forward + backward FLOPs of one query head of w."""
+    return (w.fwd_flops() + w.bwd_flops()) / (w.B * w.H)
+
+
 def cpu_oracle_sample(w, cpu_inputs, n_heads: int):
     """Time the fp64 oracle (fwd + bwd) on the first n_heads heads of the
     workload's inputs; returns (seconds, flops of the sample, threads)."""
@@ -180,7 +197,7 @@ def run_reference(args, w):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    heads_per_step = 8
+    heads_per_step = oracle_heads(w, 1.0e11, 8)
     import oracle
     from io_aware_exact_10_gb300 import workloads as W
     oracle.build()
@@ -391,7 +408,7 @@ def run_ours(args, w):
         return
 
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
-    cpu_heads = int(os.environ.get("FA_BENCH_CPU_HEADS", "128"))
+    cpu_heads = int(os.environ.get("FA_BENCH_CPU_HEADS", oracle_heads(w, 4.0e11, 128)))
     cpu_s, cpu_flops, cores = cpu_oracle_sample(w, cpu_inputs, cpu_heads)
 
     line = {
@@ -421,12 +438,13 @@ def run_ours(args, w):
             "frac": bwd_tf / peak,
             "frac_sustained": bwd_tf / peak_sus,
             "peak_source": f"{peak_src} bf16 burst ({PEAKS_PATH if peak_src == 'measured' else 'recipe fallback'})",
-            "traffic": ncu_traffic(w.name),
+            "traffic": ncu_traffic(w),
         },
         "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "path": e2e_path},
         "gpu_launches": 4 * args.steps,
+        "bars": bars_of(w, fwd_tf, bwd_tf, peak),
         "clocks": clk,
         "cpu_baseline": {"value": cpu_flops / cpu_s / 1e12, "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle",
@@ -437,6 +455,46 @@ def run_ours(args, w):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def bars_of(w, fwd_tf: float, bwd_tf: float, peak: float):
+    """The throughput bars, stated for N >= 4096 and d = 128: the forward at
+    >= 60 % and the backward at >= 40 % of the dense bf16 tensor peak (None
+    for other shapes)."""
+    if w.d != 128 or w.N < 4096:
+        return None
+    return {"fwd_min_pct": 60.0, "bwd_min_pct": 40.0,
+            "fwd_pct": 100.0 * fwd_tf / peak, "bwd_pct": 100.0 * bwd_tf / peak,
+            "fwd_met": fwd_tf >= 0.6 * peak, "bwd_met": bwd_tf >= 0.4 * peak}
+
+
+def run_once(args, w):
+    """One untimed fa_fwd and fa_bwd of workload w (B cut to --batch when
+    given), drawn on the device: the driver of a small ncu capture."""
+    import dataclasses
+    import torch
+    import io_aware_exact_10_gb300 as fa
+    from io_aware_exact_10_gb300 import workloads as W
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch)
+    B, H, Hkv, N, Nk, d = w.B, w.H, w.kv_heads, w.N, w.kv_len, w.d
+    q, k, v, dO = W.make_inputs_on_device(w, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsb = fa.fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    fa.fa_fwd_ex(q, k, v, o, lse, B, H, Hkv, N, Nk, d, w.scale, int(w.causal), stream)
+    fa.fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, Nk, d, w.scale, int(w.causal),
+                 ws, wsb, stream)
+    if fa.fa_last_device_error(stream) != fa.FA_OK:
+        raise RuntimeError("device error")
+    print(f"{w.name} B={B}: one fa_fwd, one fa_bwd", flush=True)
 
 
 def sweep_bytes(N: int, d: int, BH: int, causal: bool) -> dict:
@@ -578,16 +636,32 @@ def run_sweep(args):
                       "clocks": clk, "sweep": points}), flush=True)
 
 
+TILE_LAYOUTS = ((256, 128), (256, 64), (128, 128), (128, 64))  # (Br, Bc)
+
+
+def tile_layout_call(fa, q, k, v, o, lse, w, br, bc, causal, stream):
+    """One forward of workload w's shape with Br query rows per CTA and Bc
+    keys per K/V tile.  Br = 256 is the normal layout (a CTA holds two
+    128-row query tiles of a head).  Br = 128 views every 128-row query tile
+    as its own query head (N_q = 128, H N / 128 query heads on the H
+    key/value heads): each CTA holds one tile, with the same arithmetic per
+    row (non-causal only, since causal masking aligns on each head's last
+    row).  Bc = 64 is fa_fwd_tiled's 64-key tile."""
+    B, H, N, d = w.B, w.H, w.N, w.d
+    if br == 256:
+        return fa.fa_fwd_tiled(q, k, v, o, lse, B, H, H, N, N, d, w.scale, causal, bc, stream)
+    nt = N // 128
+    return fa.fa_fwd_tiled(q, k, v, o, lse, B, H * nt, H, 128, N, d, w.scale, 0, bc, stream)
+
+
 def run_tile_sweep(args):
-    """Query rows per CTA (Br) of the forward, the block-size axis of the
-    paper review's Fig. 2 that the kernels can vary as built: a CTA holds two
-    128-row query tiles of a head (Br = 256) when the head has two or more.
-    Viewing every query tile as its own query head (N_q = 128, H' = H N/128
-    query heads on the H key/value heads) gives each CTA one tile (Br = 128)
-    with the same arithmetic per row, so o and lse must match bit for bit;
-    K and V are then streamed once per 128 query rows instead of per 256.
-    Non-causal only (causal masking aligns on each head's last row).  Prints
-    one JSON line: forward time and TFLOP/s per (N, d, Br)."""
+    """Forward time against the two tile sizes of the paper review's Fig. 2
+    (middle panel: runtime against block size): query rows per CTA (Br = 128
+    or 256) and keys per K/V tile (Bc = 64 or 128), non-causal, plus the Bc
+    axis causal at Br = 256.  Layouts with the same Bc give o and lse bit for
+    bit equal; the two Bc agree to rounding.  Prints one JSON line: forward
+    time and TFLOP/s per (N, d, Br, Bc), with the K/V bytes a no-reuse model
+    says each layout streams (a model, not a counter)."""
     import torch
     import io_aware_exact_10_gb300 as fa
     from io_aware_exact_10_gb300 import workloads as W
@@ -599,47 +673,81 @@ def run_tile_sweep(args):
     peaks, _ = load_peaks()
     peak = float(peaks["bf16_tflops"])
     points = []
+    max_dev = {"o": 0.0, "lse": 0.0}
     for d in W.SWEEP_D:
         for N in (1024, 4096, 16384):
-            w = W.sweep(N, d, causal=False)
-            B, H = w.B, w.H
-            q, k, v = W.make_inputs_on_device(w, dev, with_grad=False)
-            nt = N // 128
-            res = {}
-            outs = {}
-            for br in (256, 128):
-                o = torch.empty_like(q)
-                lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-                if br == 256:
-                    f = lambda: fa.fa_fwd(q, k, v, o, lse, B, H, N, d, w.scale, 0, stream)
-                else:  # every query tile its own query head of the same key/value head
-                    f = lambda: fa.fa_fwd_ex(q, k, v, o, lse, B, H * nt, H, 128, N, d, w.scale,
-                                             0, stream)
-                for _ in range(args.warmup):
-                    f()
-                torch.cuda.synchronize()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(args.steps):
-                    f()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                ms = e0.elapsed_time(e1) / args.steps
-                tf = w.fwd_flops() / ms / 1e9
-                kv_bytes = B * H * 2 * N * d * 2 * (N // br if br <= N else 1)
-                res[f"br{br}"] = {"ms": ms, "tflops": tf, "pct_of_peak": 100 * tf / peak,
-                                  "kv_streamed_gb": kv_bytes / 1e9}
-                outs[br] = (o, lse)
-            if fa.fa_last_device_error(stream) != fa.FA_OK:
-                raise RuntimeError("device error during the tile sweep")
-            if not (torch.equal(outs[256][0], outs[128][0]) and torch.equal(outs[256][1], outs[128][1])):
-                raise RuntimeError(f"Br = 128 and Br = 256 disagree at N={N}, d={d}")
-            points.append({"N": N, "d": d, "B": B, "H": H, **res})
-            del q, k, v, outs
-    print(json.dumps({"metric": "attention fwd TFLOP/s vs query rows per CTA (non-causal)",
+            for causal in (False, True):
+                w = W.sweep(N, d, causal=causal)
+                B, H = w.B, w.H
+                q, k, v = W.make_inputs_on_device(w, dev, with_grad=False)
+                res, outs = {}, {}
+                layouts = TILE_LAYOUTS if not causal else ((256, 128), (256, 64))
+                for br, bc in layouts:
+                    o = torch.empty_like(q)
+                    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+                    f = lambda: tile_layout_call(fa, q, k, v, o, lse, w, br, bc, int(causal), stream)
+                    for _ in range(args.warmup):
+                        f()
+                    torch.cuda.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(args.steps):
+                        f()
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    ms = e0.elapsed_time(e1) / args.steps
+                    tf = w.fwd_flops() / ms / 1e9
+                    # K and V bytes the CTAs ask for from L2 or DRAM if nothing
+                    # were reused between CTAs (each streams its head's K and V
+                    # once, or up to its last visible tile when causal)
+                    kv_model = B * H * 2 * N * d * 2 * (N // br if br <= N else 1)
+                    if causal:
+                        kv_model = kv_model // 2
+                    res[f"br{br}_bc{bc}"] = {"ms": ms, "tflops": tf, "pct_of_peak": 100 * tf / peak,
+                                             "kv_model_gb": kv_model / 1e9}
+                    outs[(br, bc)] = (o, lse)
+                    del o, lse, f
+                if fa.fa_last_device_error(stream) != fa.FA_OK:
+                    raise RuntimeError("device error during the tile sweep")
+                for bc in (128, 64):
+                    if (128, bc) in outs and not (torch.equal(outs[(256, bc)][0], outs[(128, bc)][0])
+                                                  and torch.equal(outs[(256, bc)][1], outs[(128, bc)][1])):
+                        raise RuntimeError(f"Br = 128 and Br = 256 disagree at N={N}, d={d}, Bc={bc}")
+                do = (outs[(256, 64)][0].float() - outs[(256, 128)][0].float()).abs().max().item()
+                dl = (outs[(256, 64)][1] - outs[(256, 128)][1]).abs().max().item()
+                if do > 2e-2 or dl > 1e-3:
+                    raise RuntimeError(f"Bc = 64 and Bc = 128 differ beyond rounding at N={N}, d={d}")
+                max_dev["o"], max_dev["lse"] = max(max_dev["o"], do), max(max_dev["lse"], dl)
+                points.append({"N": N, "d": d, "B": B, "H": H, "causal": causal, **res})
+                del q, k, v, outs
+    print(json.dumps({"metric": "attention fwd TFLOP/s vs query rows per CTA (Br) and keys per "
+                                "K/V tile (Bc)",
                       "unit": "TFLOP/s", "peak": peak, "steps": args.steps,
-                      "warmup": args.warmup, "identical_outputs": True, "points": points}),
+                      "warmup": args.warmup, "same_bc_bitwise_equal": True,
+                      "bc64_vs_bc128_max_abs": max_dev, "points": points}),
           flush=True)
+
+
+def run_tile_once(args):
+    """One untimed forward per tile layout at N = 4096, d = 128 (B = 16,
+    H = 16, non-causal): the driver of the per-layout ncu capture."""
+    import torch
+    import io_aware_exact_10_gb300 as fa
+    from io_aware_exact_10_gb300 import workloads as W
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    w = W.sweep(4096, 128, causal=False)
+    q, k, v = W.make_inputs_on_device(w, dev, with_grad=False)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    for br, bc in TILE_LAYOUTS:
+        tile_layout_call(fa, q, k, v, o, lse, w, br, bc, 0, stream)
+        print(f"Br={br} Bc={bc}: one forward", flush=True)
+    if fa.fa_last_device_error(stream) != fa.FA_OK:
+        raise RuntimeError("device error")
 
 
 def run_compare(args, w):
@@ -739,10 +847,17 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="gpt2_medium")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--once", action="store_true",
+                    help="one untimed fa_fwd and fa_bwd of the workload (ncu capture driver)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="with --once: the workload's B cut to this value")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--tile-sweep", action="store_true",
-                    help="forward time against query rows per CTA (128 or 256), non-causal")
+                    help="forward time against query rows per CTA (128 or 256) and keys per "
+                         "K/V tile (64 or 128)")
+    ap.add_argument("--tile-once", action="store_true",
+                    help="one untimed forward per tile layout at N=4096, d=128 (ncu capture driver)")
     ap.add_argument("--sweep-once", action="store_true",
                     help="one untimed fa_fwd and fa_bwd per sweep point (ncu capture driver)")
     ap.add_argument("--compare", action="store_true",
@@ -757,10 +872,16 @@ def main():
     if args.tile_sweep:
         run_tile_sweep(args)
         return
+    if args.tile_once:
+        run_tile_once(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
     w = W.WORKLOADS[args.workload]
+    if args.once:
+        run_once(args, w)
+        return
     if args.compare:
         run_compare(args, w)
         return

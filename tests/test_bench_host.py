@@ -9,16 +9,32 @@ def test_strip_comments():
 
 
 def test_traffic_follows_the_backward_sources(monkeypatch):
-    """The captured traffic is reported while the hash of the backward's
-    sources matches the capture, and dropped (null) once it does not."""
-    monkeypatch.setattr(bench, "NCU_TRAFFIC_SOURCES_SHA256", bench.kernel_sources_sha256())
-    assert bench.ncu_traffic() == bench.NCU_TRAFFIC_BYTES
-    assert bench.ncu_traffic(W.GPT2_MEDIUM.name) == bench.NCU_TRAFFIC_BYTES
+    """The captured traffic is reported for the workload it was captured on,
+    scaled from the capture's batch to the workload's, while the hash of the
+    backward's sources matches the capture, and dropped (null) once it does
+    not."""
+    sha = bench.kernel_sources_sha256()
+    table = {W.LONG_CAUSAL.name: {"bytes": 1000.0, "capture_B": 1, "sources_sha256": sha}}
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", table)
+    assert bench.ncu_traffic(W.LONG_CAUSAL) == 1000.0 * W.LONG_CAUSAL.B
     # the capture belongs to one workload: other lines report no traffic
-    assert bench.ncu_traffic(W.GQA_CAUSAL.name) is None
-    assert bench.ncu_traffic(W.SPARSE_LOCAL_GLOBAL.name) is None
-    monkeypatch.setattr(bench, "NCU_TRAFFIC_SOURCES_SHA256", "0" * 64)
-    assert bench.ncu_traffic() is None
+    assert bench.ncu_traffic(W.GQA_CAUSAL) is None
+    assert bench.ncu_traffic(W.SPARSE_LOCAL_GLOBAL) is None
+    table[W.LONG_CAUSAL.name]["sources_sha256"] = "0" * 64
+    assert bench.ncu_traffic(W.LONG_CAUSAL) is None
+
+
+def test_default_line_is_the_long_causal_d128_workload():
+    """The default bench line runs B=4, H=32, N=8192, d=128, causal, where
+    the forward and backward bars are stated, and reports them."""
+    w = W.WORKLOADS[bench.DEFAULT_WORKLOAD]
+    assert (w.B, w.H, w.N, w.d, w.causal) == (4, 32, 8192, 128, True)
+    b = bench.bars_of(w, 1200.0, 700.0, 2000.0)
+    assert b["fwd_met"] and not b["bwd_met"] and abs(b["bwd_pct"] - 35.0) < 1e-9
+    assert bench.bars_of(W.GPT2_MEDIUM, 1.0, 1.0, 2.0) is None
+    # the oracle samples stay bounded: a few heads of the long workload
+    assert 1 <= bench.oracle_heads(w, 1.0e11, 8) <= 2
+    assert bench.oracle_heads(W.GPT2_MEDIUM, 4.0e11, 128) == 128
 
 
 def test_config_names_the_shape():
