@@ -194,3 +194,22 @@ def test_one_query_tile_per_cta_matches_two(B, H, N, d):
     fa.fa_fwd_ex(q, k, v, o1, lse1, B, H * nt, H, 128, N, d, scale, 0)
     torch.cuda.synchronize()
     assert torch.equal(o, o1) and torch.equal(lse, lse1)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_longest_sequence(d):
+    """B=1, H=2, N=131072, causal: 1024 key tiles per head (launches of one
+    CTA per tile; dK and dV of the first key tiles accumulate over 131072
+    queries).  On one head: O, LSE and dq on 48 query rows spread over the
+    sequence, dk and dv on 48 key rows among the last 1024 (the oracle's
+    statistics are then needed for those rows only); gradient identities on
+    both heads."""
+    N = 131072
+    w = W.Workload(f"longest_N{N}_d{d}", 1, 2, N, d, causal=True, seed=d + 1)
+    q, k, v, dO = W.make_inputs(w)
+    out = run_gpu(q, k, v, dO, w.scale, True)
+    rows = sampled_rows(N, 48, 11)
+    check_rows(q, k, v, out, w.scale, True, [(0, 1)], rows)
+    krows = np.sort(N - 1024 + np.random.default_rng(12).choice(1024, 48, replace=False))
+    check_bwd_rows(q, k, v, dO, out, w.scale, True, [(0, 1)], rows, krows)
+    check_invariants(dO, out)
