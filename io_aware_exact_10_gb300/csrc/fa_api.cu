@@ -88,8 +88,8 @@ bool get_encoder() {
 }
 
 // bf16 [BH][N][d] viewed as a 3-D tensor (d, N, BH); box of 64 columns x
-// `rows` rows (128, or 64 for 64-key tiles), 128-byte swizzle (the layout the
-// tcgen05 descriptors expect).
+// `rows` rows (128; 64 for 64-key tiles; 32 for one warp's rows of O),
+// 128-byte swizzle (the layout the tcgen05 descriptors expect).
 bool encode_bf16_3d(CUtensorMap* m, const void* ptr, int BH, int N, int d, int rows = 128) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
@@ -211,7 +211,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   fa::FwdLaunch a;
   const int BH = B * H, BHkv = B * H_kv;
   if (!encode_bf16_3d(&a.tq, q, BH, N_q, d) || !encode_bf16_3d(&a.tk, k, BHkv, N_k, d, key_tile) ||
-      !encode_bf16_3d(&a.tv, v, BHkv, N_k, d, key_tile))
+      !encode_bf16_3d(&a.tv, v, BHkv, N_k, d, key_tile) || !encode_bf16_3d(&a.to, o, BH, N_q, d, 32))
     return FA_ERR_INVALID_ARG;
   a.key_tile = key_tile;
   a.o = o;

@@ -175,9 +175,10 @@ struct BwdParams {
 // has already read: queries 0-63 -> columns 0-31, queries 64-127 -> 64-95.
 __device__ __forceinline__ uint32_t pcol(int k) { return (uint32_t)((k >> 2) * 64 + (k & 3) * 8); }
 
+template <bool TEST_FIRST = true>
 __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
                                             volatile int* abort, uint32_t site) {
-  const bool ok = mbar_wait(bar, parity, ctl, abort, site);
+  const bool ok = mbar_wait<TEST_FIRST>(bar, parity, ctl, abort, site);
   return __all_sync(0xffffffffu, ok);
 }
 

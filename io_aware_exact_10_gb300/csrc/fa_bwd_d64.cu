@@ -116,9 +116,10 @@ struct BwdParams64 {
   KernelCtl ctl;
 };
 
+template <bool TEST_FIRST = true>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
                                           volatile int* abort, uint32_t site) {
-  const bool ok = mbar_wait(bar, parity, ctl, abort, site);
+  const bool ok = mbar_wait<TEST_FIRST>(bar, parity, ctl, abort, site);
   return __all_sync(0xffffffffu, ok);
 }
 

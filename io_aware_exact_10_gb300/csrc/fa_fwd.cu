@@ -41,7 +41,7 @@ constexpr float kTau = 8.0f;
 constexpr int kSplit = 1;  // softmax warpgroups per query tile (2 measured no faster)
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int HD, int NH, int BN_ = 128>
+template <int HD, int NH, int BN_ = 128, bool STG = false>
 struct FwdCfg {
   static constexpr int BM = 128;                  // query rows per tile
   static constexpr int BN = BN_;                  // keys per K/V tile (128, or 64)
@@ -50,7 +50,12 @@ struct FwdCfg {
   static constexpr int KVTILE = BN * HD * 2;      // bytes of one K or V tile
   // the ring holds 128 KB of K/V tiles whatever their size
   static constexpr int STAGES = (HD == 128 ? 4 : 8) * (128 / BN);
-  static constexpr int SMEM = 2 * QTILE + STAGES * KVTILE + 1024;
+  // Q buffers per query tile: two in the staged kernels (d = 64, persistent
+  // launches), so that the next item's Q loads while the current item's S
+  // still read theirs and the epilogue can stage O in the finished one (at
+  // d = 128 the ring leaves no room for a second pair)
+  static constexpr int QBUF = STG ? 2 : 1;
+  static constexpr int SMEM = 2 * QBUF * QTILE + STAGES * KVTILE + 1024;
   // NH warpgroups share each query tile's softmax, each taking 128 / NH of
   // the key columns; then come the TMA warp and the MMA warp.
   static constexpr int WS = 8 * NH;               // softmax warps
@@ -86,9 +91,10 @@ struct FwdParams {
 };
 
 // Warp-uniform bounded wait: every lane polls, all agree on the outcome.
+template <bool TEST_FIRST = true>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
                                           volatile int* abort, uint32_t site) {
-  const bool ok = mbar_wait(bar, parity, ctl, abort, site);
+  const bool ok = mbar_wait<TEST_FIRST>(bar, parity, ctl, abort, site);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -100,17 +106,25 @@ __device__ __forceinline__ uint32_t p_col(int k) {
   return NH == 1 ? (uint32_t)(k * 8) : (uint32_t)(k * 8 + (k >= 4 ? 32 : 0));
 }
 
-template <int HD, bool CAUSAL, int NH, bool SPARSE, int BN = 128>
+template <int HD, bool CAUSAL, int NH, bool SPARSE, int BN = 128, bool STG = false>
 __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  using C = FwdCfg<HD, NH, BN>;
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                  const FwdParams p) {
+  using C = FwdCfg<HD, NH, BN, STG>;
+  static_assert(!STG || (HD == 64 && !SPARSE), "staged kernels: dense d = 64");
+  // First poll of every wait a non-blocking test at d = 64 (measured 4-5 % faster there);
+  // at d = 128 the plain suspending wait (the test measured 1-2 % slower).
+  constexpr bool TF = HD == 64;
   static_assert(BN == 128 || !SPARSE, "block masks are over 128 x 128 blocks");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
 
-  __shared__ __align__(8) uint64_t bar_q[2];
-  __shared__ __align__(8) uint64_t bar_qe[2];  // Q_t free: the last S_t of an item completed
+  // Q buffer b of tile t: index 2 b + t.  It is free again once the last S of
+  // its item has completed (one Q buffer per tile), or, with two, once the
+  // item's epilogue has staged O in it and the TMA store has read it.
+  __shared__ __align__(8) uint64_t bar_q[2 * C::QBUF];
+  __shared__ __align__(8) uint64_t bar_qe[2 * C::QBUF];
   __shared__ __align__(8) uint64_t bar_full[C::STAGES];
   __shared__ __align__(8) uint64_t bar_empty[C::STAGES];
   __shared__ __align__(8) uint64_t bar_s[2];
@@ -199,7 +213,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   }
 
   const uint32_t sQ = smem_u32(smem);
-  const uint32_t sRing = sQ + 2 * C::QTILE;
+  const uint32_t sRing = sQ + 2 * C::QBUF * C::QTILE;
 
   // The TMA thread initialises the barriers and issues the copies that need
   // no wait (the Q tiles and the first ring slots) before the CTA-wide sync,
@@ -213,11 +227,12 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     for (int b = 0; b < C::KB; ++b)
       tma_load_3d(dst + b * C::BN * 128, (it & 1) ? &tv : &tk, bar, b * 64, j * C::BN, bhkv);
   };
-  auto issue_q = [&](int t, const Item& I) {
-    const uint32_t bar = smem_u32(&bar_q[t]);
+  auto issue_q = [&](int t, const Item& I, int qb) {
+    const int qi = 2 * qb + t;
+    const uint32_t bar = smem_u32(&bar_q[qi]);
     mbar_arrive_expect_tx(bar, C::QTILE);
     for (int b = 0; b < C::KB; ++b)
-      tma_load_3d(sQ + t * C::QTILE + b * C::BM * 128, &tq, bar, b * 64, (I.qt0 + t) * C::BM, I.bh);
+      tma_load_3d(sQ + qi * C::QTILE + b * C::BM * 128, &tq, bar, b * 64, (I.qt0 + t) * C::BM, I.bh);
   };
   auto live = [](const Item& I, int t) { return I.valid[t] && I.ntile[t] > 0; };
   const int pre_it = 2 * I0.nu < C::STAGES ? 2 * I0.nu : C::STAGES;  // issued before the sync
@@ -226,8 +241,10 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     abort_sh = 0;
     #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&bar_q[t]), 1);
-      mbar_init(smem_u32(&bar_qe[t]), 1);
+      for (int qb = 0; qb < C::QBUF; ++qb) {
+        mbar_init(smem_u32(&bar_q[2 * qb + t]), 1);
+        mbar_init(smem_u32(&bar_qe[2 * qb + t]), C::QBUF == 2 ? 4 : 1);
+      }
       mbar_init(smem_u32(&bar_s[t]), 1);
       mbar_init(smem_u32(&bar_p[t]), 4 * NH);
       for (int sp = 0; sp < 4; ++sp) mbar_init(smem_u32(&bar_x[t][sp]), 64);
@@ -245,9 +262,10 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
+    if (C::QBUF == 2) tma_prefetch_desc(&to);
     #pragma unroll
     for (int t = 0; t < 2; ++t)
-      if (live(I0, t)) issue_q(t, I0);
+      if (live(I0, t)) issue_q(t, I0, 0);
     if constexpr (SPARSE) jw = next_bit(ubits, nw, -1);
     for (int it = 0; it < pre_it; ++it) {
       issue_kv(it, SPARSE ? jw : it >> 1, I0.bhkv);
@@ -278,7 +296,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       for (int L = L0, kk = 0;;) {
         for (; i < 2 * I.nu; ++i, ++it) {
           const int slot = it % C::STAGES, use = it / C::STAGES;
-          if (use > 0 && !mbar_wait(smem_u32(&bar_empty[slot]), (use - 1) & 1, p.ctl, abort, 10)) {
+          if (use > 0 && !mbar_wait<TF>(smem_u32(&bar_empty[slot]), (use - 1) & 1, p.ctl, abort, 10)) {
             ok = false;
             break;
           }
@@ -293,11 +311,13 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         #pragma unroll
         for (int t = 0; t < 2 && ok; ++t) {
           if (!live(I, t)) continue;
-          if (nql[t] > 0 && !mbar_wait(smem_u32(&bar_qe[t]), (nql[t] - 1) & 1, p.ctl, abort, 11)) {
+          const int qb = nql[t] % C::QBUF;
+          if (nql[t] >= C::QBUF &&
+              !mbar_wait<TF>(smem_u32(&bar_qe[2 * qb + t]), ((nql[t] - C::QBUF) / C::QBUF) & 1, p.ctl, abort, 11)) {
             ok = false;
             break;
           }
-          issue_q(t, I);
+          issue_q(t, I, qb);
           ++nql[t];
         }
         if (!ok) break;
@@ -309,7 +329,8 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           mbar_wait_quiet(smem_u32(&bar_full[s]), ((it - 1 - s) / C::STAGES) & 1, 200000000ull);
         #pragma unroll
         for (int t = 0; t < 2; ++t)
-          if (nql[t] > 0) mbar_wait_quiet(smem_u32(&bar_q[t]), (nql[t] - 1) & 1, 200000000ull);
+          for (int n = nql[t] > C::QBUF ? nql[t] - C::QBUF : 0; n < nql[t]; ++n)
+            mbar_wait_quiet(smem_u32(&bar_q[2 * (n % C::QBUF) + t]), (n / C::QBUF) & 1, 200000000ull);
       }
     }
   } else if (warp == C::W_MMA) {
@@ -327,8 +348,9 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
                          KBLK16 = (C::BN * 128) >> 4;
       const uint32_t qK = sdesc_lo(sQ, 16), rK = sdesc_lo(sRing, 16), rMN = sdesc_lo(sRing, C::BN * 128);
       // S_t = Q_t K^T for the K tile in ring slot `slot`.
+      int qb[2] = {0, 0};  // the item's Q buffer of each tile
       auto issue_s = [&](int t, int slot) {
-        const uint32_t a0 = qK + (uint32_t)t * QT16, b0 = rK + (uint32_t)slot * KV16;
+        const uint32_t a0 = qK + (uint32_t)(2 * qb[t] + t) * QT16, b0 = rK + (uint32_t)slot * KV16;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint32_t koff = (uint32_t)(k % 4) * 2;
@@ -355,7 +377,11 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         const Item I = L == L0 ? I0 : item_info(L);
         #pragma unroll
         for (int t = 0; t < 2 && ok; ++t)
-          if (live(I, t)) ok = warp_wait(smem_u32(&bar_q[t]), (nqw[t]++) & 1, p.ctl, abort, 20);
+          if (live(I, t)) {
+            qb[t] = nqw[t] % C::QBUF;
+            ok = warp_wait<TF>(smem_u32(&bar_q[2 * qb[t] + t]), (nqw[t] / C::QBUF) & 1, p.ctl, abort, 20);
+            ++nqw[t];
+          }
         if (!ok) break;
         // Does query tile t use key tile j?  The next key tile of the pair.
         auto active = [&](int t, int j) -> bool {
@@ -376,15 +402,15 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         auto s_step = [&](int t, int ks) {
           issue_s(t, ks);
           ++cs[t];
-          if (++ls[t] == I.ntile[t]) mma_commit_e(lead, smem_u32(&bar_qe[t]));
+          if (++ls[t] == I.ntile[t] && C::QBUF == 1) mma_commit_e(lead, smem_u32(&bar_qe[t]));
         };
         // O_t (+)= P_t V for the V tile in ring slot vs.  The item's first one
         // overwrites O_t: the previous item's epilogue must have read it.
         auto pv_step = [&](int t, int vs) -> bool {
           if (lp[t] == 0 && no[t] > 0 &&
-              !warp_wait(smem_u32(&bar_of[t]), (no[t] - 1) & 1, p.ctl, abort, 27))
+              !warp_wait<TF>(smem_u32(&bar_of[t]), (no[t] - 1) & 1, p.ctl, abort, 27))
             return false;
-          if (!warp_wait(smem_u32(&bar_p[t]), cp[t] & 1, p.ctl, abort, 23)) return false;
+          if (!warp_wait<TF>(smem_u32(&bar_p[t]), cp[t] & 1, p.ctl, abort, 23)) return false;
           tc_fence_after();
           issue_pv(t, vs, lp[t] > 0);
           if constexpr (C::SEPP) mma_commit_e(lead, smem_u32(&bar_pf[t]));
@@ -404,7 +430,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           // last S_t of the previous item).
           int j = SPARSE ? next_bit(ubits, nw, -1) : 0;
           auto s_after_read = [&](int t, int ks) -> bool {
-            if (cs[t] > 0 && !warp_wait(smem_u32(&bar_sf[t]), (cs[t] - 1) & 1, p.ctl, abort, 26))
+            if (cs[t] > 0 && !warp_wait<TF>(smem_u32(&bar_sf[t]), (cs[t] - 1) & 1, p.ctl, abort, 26))
               return false;
             tc_fence_after();
             s_step(t, ks);
@@ -412,7 +438,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           };
           if (I.nu > 0) {
             const int ks = it0 % C::STAGES;
-            ok = warp_wait(smem_u32(&bar_full[ks]), (it0 / C::STAGES) & 1, p.ctl, abort, 21);
+            ok = warp_wait<TF>(smem_u32(&bar_full[ks]), (it0 / C::STAGES) & 1, p.ctl, abort, 21);
             if (ok) {
               tc_fence_after();
               #pragma unroll
@@ -425,7 +451,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
             const int jn = q + 1 < I.nu ? next_j(j) : -1;
             if (q + 1 < I.nu) {
               const int ik = it0 + 2 * (q + 1), ks = ik % C::STAGES;
-              if (!(ok = warp_wait(smem_u32(&bar_full[ks]), (ik / C::STAGES) & 1, p.ctl, abort, 24))) break;
+              if (!(ok = warp_wait<TF>(smem_u32(&bar_full[ks]), (ik / C::STAGES) & 1, p.ctl, abort, 24))) break;
               #pragma unroll
               for (int t = 0; t < 2 && ok; ++t)
                 if (active(t, jn)) ok = s_after_read(t, ks);
@@ -433,7 +459,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
               mma_commit_e(lead, smem_u32(&bar_empty[ks]));
             }
             const int iv = it0 + 2 * q + 1, vs = iv % C::STAGES;
-            if (!(ok = warp_wait(smem_u32(&bar_full[vs]), (iv / C::STAGES) & 1, p.ctl, abort, 22))) break;
+            if (!(ok = warp_wait<TF>(smem_u32(&bar_full[vs]), (iv / C::STAGES) & 1, p.ctl, abort, 22))) break;
             #pragma unroll
             for (int t = 0; t < 2 && ok; ++t)
               if (active(t, j)) ok = pv_step(t, vs);
@@ -449,7 +475,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           int it = it0;
           int j = SPARSE ? next_bit(ubits, nw, -1) : 0;
           if (I.nu > 0) {
-            ok = warp_wait(smem_u32(&bar_full[it % C::STAGES]), (it / C::STAGES) & 1, p.ctl, abort, 21);
+            ok = warp_wait<TF>(smem_u32(&bar_full[it % C::STAGES]), (it / C::STAGES) & 1, p.ctl, abort, 21);
             if (ok) {
               tc_fence_after();
               #pragma unroll
@@ -461,7 +487,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           }
           for (int q = 1; q <= I.nu && ok; ++q) {
             const int vslot = it % C::STAGES;
-            ok = warp_wait(smem_u32(&bar_full[vslot]), (it / C::STAGES) & 1, p.ctl, abort, 22);
+            ok = warp_wait<TF>(smem_u32(&bar_full[vslot]), (it / C::STAGES) & 1, p.ctl, abort, 22);
             ++it;
             if (!ok) break;
             tc_fence_after();
@@ -475,7 +501,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
               if (active(t, j) && !(ok = pv_step(t, vslot))) break;
               if (have_k && active(t, jn)) {
                 if (!k_ready) {
-                  ok = warp_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 24);
+                  ok = warp_wait<TF>(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 24);
                   if (!ok) break;
                   tc_fence_after();
                   k_ready = true;
@@ -487,7 +513,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
             mma_commit_e(lead, smem_u32(&bar_empty[vslot]));
             if (have_k) {
               if (!k_ready) {
-                ok = warp_wait(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 25);
+                ok = warp_wait<TF>(smem_u32(&bar_full[kslot]), kpar, p.ctl, abort, 25);
                 if (!ok) break;
               }
               mma_commit_e(lead, smem_u32(&bar_empty[kslot]));
@@ -530,7 +556,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         const int slot = xph & 1;
         xch[t][slot][h][r] = v;
         mbar_arrive(xbar);  // every lane: releases its own write
-        const bool okx = warp_wait(xbar, xph & 1, p.ctl, abort, 32);
+        const bool okx = warp_wait<TF>(xbar, xph & 1, p.ctl, abort, 32);
         ++xph;
         return okx ? xch[t][slot][h ^ 1][r] : NAN;
       };
@@ -547,6 +573,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       const uint32_t* tbits = mbits + t * (SPARSE ? kMaskWords : 0);
       auto m_ref = [](float mv) { return (SPARSE && mv == -INFINITY) ? 0.f : mv; };
       int gstep = 0, nio = 0;  // steps and epilogues of this tile so far
+      int nlq = 0;             // live items of this tile so far
       bool ok = true;
       for (int L = L0, kk = 0; L < n_items && ok; L = item_at(++kk)) {
       const Item I = L == L0 ? I0 : item_info(L);
@@ -555,6 +582,9 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       const bool valid_t = t ? I.valid[1] : I.valid[0];
       const int ntile_t = t ? I.ntile[1] : I.ntile[0];
       if (!valid_t) continue;
+      // this item's Q buffer (the loads count the tile's live items too)
+      const int qbi = nlq % C::QBUF;
+      if (ntile_t > 0) ++nlq;
       const int bh = I.bh;
       const int row = (I.qt0 + t) * C::BM + r;
       float m = -INFINITY, l = 0.f, lr = 0.f;
@@ -562,7 +592,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         const uint32_t tP = tmem + lane_off + C::colP(t);
         int j = SPARSE ? next_bit(tbits, nw, -1) : 0;
         for (int lstep = 0; lstep < ntile_t; ++lstep, ++gstep) {
-          if (!warp_wait(smem_u32(&bar_s[t]), gstep & 1, p.ctl, abort, 30)) {
+          if (!warp_wait<TF>(smem_u32(&bar_s[t]), gstep & 1, p.ctl, abort, 30)) {
             ok = false;
             break;
           }
@@ -623,7 +653,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           }
           // P_t and O_t: the previous O_t += P_t V (also of the previous
           // item) must have completed
-          if (gstep > 0 && !warp_wait(smem_u32(&bar_pf[t]), (gstep - 1) & 1, p.ctl, abort, 33)) {
+          if (gstep > 0 && !warp_wait<TF>(smem_u32(&bar_pf[t]), (gstep - 1) & 1, p.ctl, abort, 33)) {
             ok = false;
             break;
           }
@@ -654,7 +684,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
       } else {
       int j = SPARSE ? next_bit(tbits, nw, -1) : 0;
       for (int lstep = 0; lstep < ntile_t; ++lstep, ++gstep) {
-        if (!warp_wait(smem_u32(&bar_s[t]), gstep & 1, p.ctl, abort, 30)) {
+        if (!warp_wait<TF>(smem_u32(&bar_s[t]), gstep & 1, p.ctl, abort, 30)) {
           ok = false;
           break;
         }
@@ -791,10 +821,52 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           if (h == 0) p.lse[(size_t)bh * p.Nq + row] = -INFINITY;
         }
       } else {
-        if (!(ok = warp_wait(smem_u32(&bar_o[t]), (nio++) & 1, p.ctl, abort, 31))) break;
+        if (!(ok = warp_wait<TF>(smem_u32(&bar_o[t]), (nio++) & 1, p.ctl, abort, 31))) break;
         tc_fence_after();
         // a row that saw no key (block-sparse only) has lr = 0 and o = 0
         const float inv_l = (SPARSE && !(lr > 0.f)) ? 0.f : 1.0f / lr;
+        // O through shared memory when another item follows on this CTA:
+        // each warp stages its 32 rows (128-byte swizzled, the TMA store's
+        // layout) in this item's Q buffer, which the item's last S has
+        // finished reading (bar_o follows it), and one TMA store writes them
+        // as whole lines.  Per-thread row stores touch 32 lines per
+        // instruction and hold the shared-memory pipe while the next item's
+        // first S needs it; a CTA's last item (every item of a one-item
+        // launch) keeps them, which measured faster there.
+        if (C::QBUF == 2 && item_at(kk + 1) < n_items) {
+          uint8_t* stg = smem + (size_t)(2 * qbi + t) * C::QTILE + (size_t)sp * 4096 + (size_t)lane * 128;
+#pragma unroll
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c0, ov);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<uint4*>(stg + (((c0 / 8 + i) ^ (lane & 7)) * 16)) =
+                  make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+          if (row < p.Nq) p.lse[(size_t)bh * p.Nq + row] = (m + __log2f(l)) * kLn2;
+          // O_t has been read: the next item's first O_t += P_t V may overwrite it
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&bar_of[t]));
+            const int row0 = (I.qt0 + t) * C::BM + sp * 32;
+            if (row0 < p.Nq) {
+              tma_store_3d(&to, smem_u32(stg), 0, row0, bh);
+              bulk_commit_group();
+              bulk_wait_group_read<0>();
+            }
+            mbar_arrive(smem_u32(&bar_qe[2 * qbi + t]));  // the Q buffer is free again
+          }
+          __syncwarp();
+          continue;
+        }
         __nv_bfloat16* orow = p.o + ((size_t)bh * p.Nq + row) * HD;
 #pragma unroll 1
         for (int c0 = 0; c0 < C::OCPT; c0 += 32) {
@@ -816,7 +888,10 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
         // O_t has been read: the next item's first O_t += P_t V may overwrite it
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_of[t]));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&bar_of[t]));
+          if (C::QBUF == 2) mbar_arrive(smem_u32(&bar_qe[2 * qbi + t]));  // the Q buffer is free again
+        }
       }
       }  // items
     }
@@ -831,13 +906,20 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   }
 }
 
-template <int HD, bool CAUSAL, bool SPARSE, int BN = 128>
-cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
-  constexpr int NH = kSplit;
-  using C = FwdCfg<HD, NH, BN>;
-  auto kern = fa_fwd_kernel<HD, CAUSAL, NH, SPARSE, BN>;
+template <int HD, bool CAUSAL, bool SPARSE, int BN, bool STG>
+cudaError_t launch_fwd_k(const FwdParams& p, const FwdLaunch& a, long ctas, cudaStream_t stream) {
+  using C = FwdCfg<HD, kSplit, BN, STG>;
+  auto kern = fa_fwd_kernel<HD, CAUSAL, kSplit, SPARSE, BN, STG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)ctas);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, a.to, p);
+  return cudaGetLastError();
+}
+
+template <int HD, bool CAUSAL, bool SPARSE, int BN = 128>
+cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
+  using C = FwdCfg<HD, kSplit, BN>;
   FwdParams p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
@@ -856,10 +938,15 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   // one persistent CTA per SM walks the pairs, or one CTA per pair
   // (block-sparse: each builds the bitsets of its own mask rows)
   const long n_items = (long)p.npairs * a.BH;
-  const long ctas = persistent_launch(CAUSAL, SPARSE, p.npairs) && n_items > a.num_sms ? a.num_sms : n_items;
-  dim3 grid((unsigned)ctas);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tq, a.tk, a.tv, p);
-  return cudaGetLastError();
+  const bool persistent = persistent_launch(CAUSAL, SPARSE, p.npairs) && n_items > a.num_sms;
+  const long ctas = persistent ? a.num_sms : n_items;
+  // d = 64 persistent launches of short items (at most 16 key tiles) stage O
+  // through shared memory: there the epilogue is a large share of an item.
+  // The staged kernel's step loop measured 2 % slower at 32 key tiles and
+  // 5 % on one-item launches, which keep the other instantiation.
+  if constexpr (HD == 64 && !SPARSE)
+    if (persistent && p.nkv * BN <= 2048) return launch_fwd_k<HD, CAUSAL, SPARSE, BN, true>(p, a, ctas, stream);
+  return launch_fwd_k<HD, CAUSAL, SPARSE, BN, false>(p, a, ctas, stream);
 }
 
 }  // namespace

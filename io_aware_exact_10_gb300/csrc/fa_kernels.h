@@ -15,6 +15,7 @@ namespace fa {
 struct FwdLaunch {
   CUtensorMap tq;               // bf16 [BH][Nq][d], box {64, 128, 1}, 128-byte swizzle
   CUtensorMap tk, tv;           // bf16 [BH / group][Nk][d], box {64, key_tile, 1}
+  CUtensorMap to;               // bf16 [BH][Nq][d] output, box {64, 32, 1} (d = 64 stores)
   void* o;                      // bf16 [BH][Nq][d]
   float* lse;                   // fp32 [BH][Nq]
   int BH, Nq, Nk, d;            // causal requires Nk >= Nq (bottom-right aligned)

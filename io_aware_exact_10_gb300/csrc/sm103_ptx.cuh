@@ -77,6 +77,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // try_wait with an explicit bound on how long the thread may be suspended in
 // it (ns); without one the hardware picks its own limit.
 __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
@@ -101,8 +114,15 @@ constexpr uint32_t kShortSuspendNs = 256u;
 // is bounded: it gives up when `*abort` is raised by another thread of the CTA,
 // or after ctl.timeout_ns, in which case it records kErrTimeout with `site`
 // and raises `*abort` itself.  Returns false when it gave up.
+// With TEST_FIRST the first poll is a non-blocking test (a shared-memory
+// round trip, ~50 cycles measured), which answers a phase that has already
+// completed before anything that depends on the bound is read.  Where the
+// phase usually completes a little later (hand-offs between partner warps),
+// the extra test only delays the suspending wait.
+template <bool TEST_FIRST = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const KernelCtl& ctl,
                                           volatile int* abort, uint32_t site) {
+  if (TEST_FIRST && mbar_test_wait(bar, parity)) return true;
   const bool short_bound = ctl.timeout_ns < kShortBoundNs;
   if (short_bound ? mbar_try_wait_hint(bar, parity, kShortSuspendNs) : mbar_try_wait(bar, parity))
     return true;

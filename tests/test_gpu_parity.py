@@ -54,6 +54,19 @@ def test_small_shapes(B, H, N, d, causal):
     check_heads(q, k, v, dO, out, w.scale, causal, heads)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_d64_ragged(causal):
+    """d = 64 with more query-tile pairs than SMs (the persistent launch, whose
+    CTAs stage O through shared memory for every item but their last) and a
+    ragged last tile whose last three warps hold no row (N = 900 = 7 * 128 +
+    4): six seeded heads in full, identities on all 160."""
+    w = W.Workload("persistent_d64", 8, 20, 900, 64, causal=causal, seed=77)
+    q, k, v, dO = W.make_inputs(w)
+    out = run_gpu(q, k, v, dO, w.scale, causal)
+    check_heads(q, k, v, dO, out, w.scale, causal, seeded_heads(w.B, w.H, 6, seed=8))
+    check_invariants(dO, out)
+
+
 def test_nonstandard_scale():
     """scale is an argument, not fixed to 1/sqrt(d)."""
     q, k, v, dO = W.make_inputs(W.Workload("s", 1, 2, 384, 64, causal=True, seed=3))
