@@ -60,8 +60,8 @@ NCU_TRAFFIC = {
         "sources_sha256": "00deef6fb9583377d4c45dd5baf7292aa8bb7def8dc73aa52c41929a6bbbb851"},
     # profiles/fa_bwd_call_long_causal_traffic.md (B = 1, scaled by B)
     "long_causal_B4_H32_N8192_d128": {
-        "bytes": 1002741760.0, "capture_B": 1,
-        "sources_sha256": "831a67b9ef24359e370cef6fbdf8ffbce4dbfa78c2bd9562ca091b1db55637b9"},
+        "bytes": 1003028736.0, "capture_B": 1,
+        "sources_sha256": "36b3576298c44ee80b60bfb8761908ab5f95bb4acd4c7c830da3fd5914427395"},
 }
 BWD_SOURCES = ("fa_api.cu", "fa_bwd.cu", "fa_bwd_d64.cu", "fa_kernels.h", "sm103_ptx.cuh")
 DEFAULT_WORKLOAD = "long_causal"

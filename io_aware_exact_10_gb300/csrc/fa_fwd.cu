@@ -98,6 +98,27 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const K
   return __all_sync(0xffffffffu, ok);
 }
 
+// Phases of up to three barriers tested in one shared-memory round trip: the
+// tests are issued back to back and combined before the result is read
+// (a completed phase costs ~250 cycles of round trip inside the busy kernel;
+// three separate tests pay it three times).
+__device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
+                                           uint32_t p2) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "and.pred q0, q0, q1;\n\t"
+      "and.pred q0, q0, q2;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t}"
+      : "=r"(ok)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return ok != 0;
+}
+
 // TMEM column (relative to S_t) of the bf16 pairs of P for K-step k (16 keys
 // of the P V contraction).  Each softmax warpgroup packs its keys into the
 // first half of its own, already read, column range.
@@ -116,6 +137,14 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
   // First poll of every wait a non-blocking test at d = 64 (measured 4-5 % faster there);
   // at d = 128 the plain suspending wait (the test measured 1-2 % slower).
   constexpr bool TF = HD == 64;
+  // The d = 64 MMA loop's waits: 0 = each barrier tested on its own; 2 = a
+  // tile's K or V landing tested with its S read (or P stored) in one round
+  // trip; 3 = both tiles' barriers and the K or V landing in one.  Chosen per
+  // kernel by measurement (alternating runs on one GPU): 3 on one-item and
+  // long-item launches (+2-3 % at N = 4096-16384 causal, +20 % with 64-key
+  // tiles), 2 on the staged kernel with 64-key tiles (+17 %), 0 on the staged
+  // kernel with 128-key tiles (1-2 % ahead of both).
+  constexpr int BATCH = STG ? (BN == 64 ? 2 : 0) : 3;
   static_assert(BN == 128 || !SPARSE, "block masks are over 128 x 128 blocks");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -429,6 +458,83 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           // S_t overwrites S_t only after the softmax has read it (also the
           // last S_t of the previous item).
           int j = SPARSE ? next_bit(ubits, nw, -1) : 0;
+          if constexpr (BATCH >= 2) {
+          // S_0(jn), S_1(jn) once K(jn) has landed and both S have been read:
+          // one round trip tests all three.
+          auto s_pair = [&](int ks, uint32_t kpar, bool a0, bool a1) -> bool {
+            const uint32_t kb = smem_u32(&bar_full[ks]);
+            const bool w0 = a0 && cs[0] > 0, w1 = a1 && cs[1] > 0;
+            const uint32_t f0 = smem_u32(&bar_sf[0]), f1 = smem_u32(&bar_sf[1]);
+            const uint32_t q0 = (uint32_t)(cs[0] - 1) & 1u, q1 = (uint32_t)(cs[1] - 1) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_test3(kb, kpar, w0 ? f0 : kb, w0 ? q0 : kpar, w1 ? f1 : kb,
+                                                     w1 ? q1 : kpar))) {
+              if (!warp_wait<TF>(kb, kpar, p.ctl, abort, 24)) return false;
+              if (w0 && !warp_wait<TF>(f0, q0, p.ctl, abort, 26)) return false;
+              if (w1 && !warp_wait<TF>(f1, q1, p.ctl, abort, 26)) return false;
+            }
+            tc_fence_after();
+            if (a0) s_step(0, ks);
+            if (a1) s_step(1, ks);
+            return true;
+          };
+          // O_0 += P_0 V_j, O_1 += P_1 V_j once V_j has landed and both P are
+          // stored (the item's first P V also waits for the epilogue to free O_t).
+          auto pv_pair = [&](int vs, uint32_t vpar, bool a0, bool a1) -> bool {
+            #pragma unroll
+            for (int t = 0; t < 2; ++t)
+              if ((t ? a1 : a0) && lp[t] == 0 && no[t] > 0 &&
+                  !warp_wait<TF>(smem_u32(&bar_of[t]), (no[t] - 1) & 1, p.ctl, abort, 27))
+                return false;
+            const uint32_t vb = smem_u32(&bar_full[vs]);
+            const uint32_t g0 = smem_u32(&bar_p[0]), g1 = smem_u32(&bar_p[1]);
+            const uint32_t q0 = (uint32_t)cp[0] & 1u, q1 = (uint32_t)cp[1] & 1u;
+            if (!__all_sync(0xffffffffu, mbar_test3(vb, vpar, a0 ? g0 : vb, a0 ? q0 : vpar, a1 ? g1 : vb,
+                                                     a1 ? q1 : vpar))) {
+              if (!warp_wait<TF>(vb, vpar, p.ctl, abort, 22)) return false;
+              if (a0 && !warp_wait<TF>(g0, q0, p.ctl, abort, 23)) return false;
+              if (a1 && !warp_wait<TF>(g1, q1, p.ctl, abort, 23)) return false;
+            }
+            tc_fence_after();
+            #pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!(t ? a1 : a0)) continue;
+              issue_pv(t, vs, lp[t] > 0);
+              mma_commit_e(lead, smem_u32(&bar_pf[t]));
+              ++cp[t];
+              if (++lp[t] == I.ntile[t]) {
+                mma_commit_e(lead, smem_u32(&bar_o[t]));
+                ++no[t];
+              }
+            }
+            return true;
+          };
+          // both tiles behind one test, or each tile behind its own
+          auto s_all = [&](int ks, uint32_t kpar, bool a0, bool a1) -> bool {
+            if (BATCH == 3) return s_pair(ks, kpar, a0, a1);
+            return (!a0 || s_pair(ks, kpar, true, false)) && (!a1 || s_pair(ks, kpar, false, true));
+          };
+          auto pv_all = [&](int vs, uint32_t vpar, bool a0, bool a1) -> bool {
+            if (BATCH == 3) return pv_pair(vs, vpar, a0, a1);
+            return (!a0 || pv_pair(vs, vpar, true, false)) && (!a1 || pv_pair(vs, vpar, false, true));
+          };
+          if (I.nu > 0) {
+            const int ks = it0 % C::STAGES;
+            ok = s_all(ks, (uint32_t)(it0 / C::STAGES) & 1u, active(0, j), active(1, j));
+            if (ok) mma_commit_e(lead, smem_u32(&bar_empty[ks]));
+          }
+          for (int q = 0; q < I.nu && ok; ++q) {
+            const int jn = q + 1 < I.nu ? next_j(j) : -1;
+            if (q + 1 < I.nu) {
+              const int ik = it0 + 2 * (q + 1), ks = ik % C::STAGES;
+              if (!(ok = s_all(ks, (uint32_t)(ik / C::STAGES) & 1u, active(0, jn), active(1, jn)))) break;
+              mma_commit_e(lead, smem_u32(&bar_empty[ks]));
+            }
+            const int iv = it0 + 2 * q + 1, vs = iv % C::STAGES;
+            if (!(ok = pv_all(vs, (uint32_t)(iv / C::STAGES) & 1u, active(0, j), active(1, j)))) break;
+            mma_commit_e(lead, smem_u32(&bar_empty[vs]));
+            j = jn;
+          }
+          } else {
           auto s_after_read = [&](int t, int ks) -> bool {
             if (cs[t] > 0 && !warp_wait<TF>(smem_u32(&bar_sf[t]), (cs[t] - 1) & 1, p.ctl, abort, 26))
               return false;
@@ -466,6 +572,7 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
             if (!ok) break;
             mma_commit_e(lead, smem_u32(&bar_empty[vs]));
             j = jn;
+          }
           }
         } else {
           // Iteration q takes V of the pair's key tile j = u_{q-1}, then K of
