@@ -312,7 +312,8 @@ fa_status fa_bwd_sparse(const void* q, const void* k, const void* v, const void*
   a.stats = static_cast<float*>(workspace);
   a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                       round256(stats_floats(BH, N_q) * sizeof(float)));
-  if (!encode_f32_3d(&a.tdq, a.dq_acc, BH, N_q, d)) return FA_ERR_INVALID_ARG;
+  if (!encode_f32_3d(&a.tdq, a.dq_acc, BH, N_q, d) || !encode_bf16_3d(&a.tdk, dk, BHkv, N_k, d, 32))
+    return FA_ERR_INVALID_ARG;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;

@@ -127,7 +127,8 @@ template <bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     fa_bwd_d64_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                      const __grid_constant__ CUtensorMap tdq, const BwdParams64 p) {
+                      const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
+                      const BwdParams64 p) {
   using C = Cfg64;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     tma_prefetch_desc(&tv);
     tma_prefetch_desc(&tdo);
     tma_prefetch_desc(&tdq);
+    tma_prefetch_desc(&tdk);
     // K and Q_0 first: S^T of the first tile needs only those two
     mbar_arrive_expect_tx(bar(B_K), C::TILE);
     tma_load_3d(sK, &tk, bar(B_K), 0, kt * C::BK, bk);
@@ -627,7 +629,6 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int kt = I.kt;
     const int nit_i = L == L0 ? nit : item_nit(I);
     const QuerySeq<SPARSE> seq = L == L0 ? qseq : item_seq(I);
-    const size_t rowbase = (size_t)I.bk * p.Nk;      // key rows (dK, dV)
     if (!(ok = warp_wait(bar(B_V), (uint32_t)k & 1u, p.ctl, abort, 93))) break;
     to_tmem(v_buf(k), C::COL_VT, B_VT);
     TileWalk w = L == L0 ? walk0 : TileWalk{seq.first, I.bk * p.kv_group};
@@ -674,8 +675,13 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         if (!(ok = warp_wait(bar(B_K), (uint32_t)(k + 1) & 1u, p.ctl, abort, 94))) break;
         to_tmem(k_buf(k + 1), C::COL_KT, B_KT);
       }
-      const int key = kt * C::BK + r;
+      // The warp's 32 rows go out through its staging area (128-byte
+      // swizzled, as the TMA store reads them) in one store of whole lines,
+      // once the area's last dQ boxes have been read; per-thread row stores
+      // would touch 32 lines per instruction.
       const float scale = p.scale;
+      if (lane == 0) bulk_wait_group_read<0>();
+      __syncwarp();
 #pragma unroll 1
       for (int c0 = 0; c0 < C::HD; c0 += 32) {
         uint32_t v[32];
@@ -685,11 +691,19 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
-        if (key < p.Nk) {
-          uint4* d4 = reinterpret_cast<uint4*>(p.dk + (rowbase + key) * C::HD + c0);
+        const uint32_t row = stage + (uint32_t)lane * 128u;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        for (int i = 0; i < 4; ++i)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((((uint32_t)(c0 / 8 + i)) ^ sw) << 4)),
+                       "r"(pk[4 * i]), "r"(pk[4 * i + 1]), "r"(pk[4 * i + 2]), "r"(pk[4 * i + 3])
+                       : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int key0 = kt * C::BK + sp * 32;
+      if (lane == 0 && key0 < p.Nk) {
+        tma_store_3d(&tdk, stage, 0, key0, I.bk);
+        bulk_commit_group();
       }
     }
     U0 += nit_i;
@@ -736,7 +750,7 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   const long n_items = (long)p.nkv * p.BHkv;
   const long ctas = persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms ? a.num_sms : n_items;
   dim3 grid((unsigned)ctas);
-  kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
+  kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, a.tdk, p);
   return cudaGetLastError();
 }
 

@@ -33,6 +33,7 @@ struct BwdLaunch {
   CUtensorMap tq, tdo;          // bf16 [BH][Nq][d], box {64, 128, 1}, 128-byte swizzle
   CUtensorMap tk, tv;           // bf16 [BH / group][Nk][d], same box
   CUtensorMap tdq;              // fp32 dQacc [BH][Nq][d], box {32, 32, 1}, 128-byte swizzle
+  CUtensorMap tdk;              // bf16 dk [BH / group][Nk][d], box {64, 32, 1} (d = 64 stores)
   const void* o;                // bf16 [BH][Nq][d]
   const void* dO;               // bf16 [BH][Nq][d]
   const float* lse;             // fp32 [BH][Nq]
