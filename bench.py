@@ -55,13 +55,14 @@ E2E_CHUNKS = 8
 # of the fa_bwd call (the backward kernels, their launch layer and shared
 # helpers, comments aside) is the code the capture measured.
 NCU_TRAFFIC = {
+    # captured on the whole workload (B = 64)
     "gpt2_medium_B64_H16_N1024_d64": {
-        "bytes": 2144.5e6, "capture_B": 64,
-        "sources_sha256": "00deef6fb9583377d4c45dd5baf7292aa8bb7def8dc73aa52c41929a6bbbb851"},
-    # profiles/fa_bwd_call_long_causal_traffic.md (B = 1, scaled by B)
+        "bytes": 2148681216.0, "capture_B": 64,
+        "sources_sha256": "aaf11900baf367d2a114f4c7669c19b16e24a1b030a471cb2b2e528d40b73adf"},
+    # captured at B = 1, scaled by B (the heads are independent)
     "long_causal_B4_H32_N8192_d128": {
-        "bytes": 1003028736.0, "capture_B": 1,
-        "sources_sha256": "36b3576298c44ee80b60bfb8761908ab5f95bb4acd4c7c830da3fd5914427395"},
+        "bytes": 1002817792.0, "capture_B": 1,
+        "sources_sha256": "aaf11900baf367d2a114f4c7669c19b16e24a1b030a471cb2b2e528d40b73adf"},
 }
 BWD_SOURCES = ("fa_api.cu", "fa_bwd.cu", "fa_bwd_d64.cu", "fa_kernels.h", "sm103_ptx.cuh")
 DEFAULT_WORKLOAD = "long_causal"

@@ -8,7 +8,8 @@ FA_ERR_TIMEOUT with the site of the wait in the per-device error word, lets
 the copies and tensor-core operations it has issued complete, frees its
 tensor memory and returns.  Nothing is injected: the same kernels run on
 valid inputs, only the bound differs.  Each main kernel (forward, the d = 64
-and the d = 128 backward) is made to give up once on one small problem; the
+and the d = 128 backward) is made to give up once on a small problem, and
+the persistent d = 64 kernels on one with more work items than SMs; the
 status is read back, the bound restored, and a normal call on the same
 device then matches the oracle.
 """
@@ -43,11 +44,15 @@ def gives_up(fn):
     return st, word
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_wait_bound_runs_out_then_a_normal_call_succeeds(d):
+@pytest.mark.parametrize("B,H,N,d", [
+    (1, 2, 4096, 64), (1, 2, 4096, 128),
+    # more work items than SMs: the persistent kernels, at d = 64 the
+    # forward that stages O through its second Q buffers
+    (8, 20, 1024, 64)])
+def test_wait_bound_runs_out_then_a_normal_call_succeeds(B, H, N, d):
     # long enough that the pipelines' producers wait for free slots (a wait
     # that ends within one poll of the barrier cannot run out)
-    w = W.Workload("timeout", 1, 2, 4096, d, causal=False, seed=40 + d)
+    w = W.Workload("timeout", B, H, N, d, causal=False, seed=40 + d + N)
     cpu = W.make_inputs(w)
     q, k, v, dO = (t.cuda() for t in cpu)
 
