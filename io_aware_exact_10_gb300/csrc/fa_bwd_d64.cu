@@ -29,7 +29,8 @@
 // Dense launches run one CTA per SM over many key tiles (work items), with
 // the ring positions and barrier phases running on across items; the next
 // item's K is loaded early into the V buffer (free once V is in tensor
-// memory).  Block-sparse launches run one CTA per key tile.
+// memory), and copied into tensor memory by the drain warps once the item's
+// last S^T has completed.  Block-sparse launches run one CTA per key tile.
 //
 // Roles (448 threads):
 //   warps 0-7   P / dS: thread = key row = TMEM lane (warp w takes lanes
@@ -93,15 +94,15 @@ static_assert(Cfg64::NG == 2 || Cfg64::NG == 4, "32 or 64 query columns per P/dS
 // barrier indices
 enum : int {
   B_K = 0, B_V, B_QF0, B_QF1, B_QF2, B_QE0, B_QE1, B_QE2, B_DOF0, B_DOF1, B_DOE0, B_DOE1,
-  B_ST, B_P, B_DPT, B_DS, B_DQF, B_DQE, B_FIN, B_DRAIN, B_KT, B_VT, B_COUNT
+  B_ST, B_P, B_DPT, B_DS, B_DQF, B_DQE, B_FIN, B_DRAIN, B_KT, B_VT, B_DKR, B_COUNT
 };
 static_assert(B_COUNT <= Cfg64::NBAR, "barrier area");
 // arrival counts: TMA and tcgen05.commit barriers take one arrival; P and DS
-// one per P/dS warp; DQE, KT and VT one per drain warp.
+// one per P/dS warp; DQE, KT, VT and DKR one per drain warp.
 __device__ __constant__ const uint32_t kBarCount64[B_COUNT] = {
     1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1,           // K, V, QF*, QE*, DOF*, DOE*
     1, Cfg64::NPW, 1, Cfg64::NPW, 1, 4, 1, 1,     // ST, P, DPT, DS, DQF, DQE, FIN, DRAIN
-    4, 4};                                        // KT, VT (K, V copied to tensor memory)
+    4, 4, 4};  // KT, VT (K, V copied to tensor memory), DKR (dK read out by the drain)
 
 struct BwdParams64 {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
@@ -123,7 +124,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const K
   return __all_sync(0xffffffffu, ok);
 }
 
-template <bool CAUSAL, bool SPARSE>
+// XV (persistent launches): the drain copies the next item's V into tensor
+// memory before its dK epilogue, and the MMA warp's first dK of an item waits
+// for that epilogue's reads (DKR) instead of following the V copy.
+template <bool CAUSAL, bool SPARSE, bool XV = false>
 __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     fa_bwd_d64_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -417,6 +421,10 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
           // dS(u) is in shared memory, its transpose in the dP^T columns
           if (!(ok = warp_wait(bar(B_DS), U & 1, p.ctl, abort, 69))) break;
           tc_fence_after();
+          // the item's first dK overwrites the previous item's: the drain has
+          // read that out (it copies the next V before its dK epilogue)
+          if (XV && u == 0 && k > 0 && !(ok = warp_wait(bar(B_DKR), (uint32_t)(k - 1) & 1u, p.ctl, abort, 68)))
+            break;
           // dK += dS^T Q_u   (A = dS^T bf16 pairs in TMEM, B = Q_u query-major)
 #pragma unroll
           for (int k2 = 0; k2 < C::BQ / 16; ++k2)
@@ -629,10 +637,25 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     const int kt = I.kt;
     const int nit_i = L == L0 ? nit : item_nit(I);
     const QuerySeq<SPARSE> seq = L == L0 ? qseq : item_seq(I);
-    if (!(ok = warp_wait(bar(B_V), (uint32_t)k & 1u, p.ctl, abort, 93))) break;
-    to_tmem(v_buf(k), C::COL_VT, B_VT);
+    if (!XV || k == 0) {  // with XV later items' V is copied at the end of the item before
+      if (!(ok = warp_wait(bar(B_V), (uint32_t)k & 1u, p.ctl, abort, 93))) break;
+      to_tmem(v_buf(k), C::COL_VT, B_VT);
+    }
     TileWalk w = L == L0 ? walk0 : TileWalk{seq.first, I.bk * p.kv_group};
+    const bool has_next = item_at(k + 1) < n_items;
     for (int u = 0; u < nit_i && ok; ++u, seq.next(w)) {
+      // The next item's K goes into tensor memory as soon as the item's last
+      // S^T (the last MMA that reads the K columns) has completed and that K
+      // has landed, so the next item's first S^T need not wait for this
+      // item's last dQ, its drain and the dK epilogue.  Nothing issues the
+      // next S^T before this copy, so the S^T barrier cannot run past it.
+      if (has_next && u + 1 == nit_i) {
+        if (!(ok = warp_wait(bar(B_ST), (uint32_t)(U0 + u) & 1u, p.ctl, abort, 95) &&
+                   warp_wait(bar(B_K), (uint32_t)(k + 1) & 1u, p.ctl, abort, 94)))
+          break;
+        tc_fence_after();
+        to_tmem(k_buf(k + 1), C::COL_KT, B_KT);
+      }
       if (!(ok = warp_wait(bar(B_DQF), (U0 + u) & 1, p.ctl, abort, 90))) break;
       tc_fence_after();
       uint32_t v[64];
@@ -666,14 +689,14 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
         bulk_commit_group();
       }
     }
-    // epilogue: dK rows of this key tile (scaled), after the next item's K
-    // copy (its first S^T waits for it); the next item's first dK overwrites
-    // them only after this warp's V copy for that item
+    // epilogue: the next item's V into tensor memory first (its first dP^T
+    // waits for it), then the dK rows of this key tile (scaled); the next
+    // item's first dK waits for DKR, which follows their reads
     if (ok && (ok = warp_wait(bar(B_FIN), (uint32_t)k & 1u, p.ctl, abort, 91))) {
       tc_fence_after();
-      if (item_at(k + 1) < n_items) {
-        if (!(ok = warp_wait(bar(B_K), (uint32_t)(k + 1) & 1u, p.ctl, abort, 94))) break;
-        to_tmem(k_buf(k + 1), C::COL_KT, B_KT);
+      if (XV && has_next) {
+        if (!(ok = warp_wait(bar(B_V), (uint32_t)(k + 1) & 1u, p.ctl, abort, 93))) break;
+        to_tmem(v_buf(k + 1), C::COL_VT, B_VT);
       }
       // The warp's 32 rows go out through its staging area (128-byte
       // swizzled, as the TMA store reads them) in one store of whole lines,
@@ -698,8 +721,11 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
                        "r"(pk[4 * i]), "r"(pk[4 * i + 1]), "r"(pk[4 * i + 2]), "r"(pk[4 * i + 3])
                        : "memory");
       }
+      // dK has been read out of tensor memory: the next item's first dK may overwrite it
+      tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
+      if (XV && lane == 0) mbar_arrive(bar(B_DKR));
       const int key0 = kt * C::BK + sp * 32;
       if (lane == 0 && key0 < p.Nk) {
         tma_store_3d(&tdk, stage, 0, key0, I.bk);
@@ -722,14 +748,22 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   }
 }
 
-template <bool CAUSAL, bool SPARSE>
-cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
+template <bool CAUSAL, bool SPARSE, bool XV>
+cudaError_t launch_k(const BwdLaunch& a, const BwdParams64& p, long ctas, cudaStream_t stream) {
   using C = Cfg64;
-  auto kern = fa_bwd_d64_kernel<CAUSAL, SPARSE>;
+  auto kern = fa_bwd_d64_kernel<CAUSAL, SPARSE, XV>;
   // block-sparse: the mask column's bitset and its count follow the layout
   const int smem_bytes = C::SMEM + (SPARSE ? kMaskWords * 4 + 16 : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)ctas);
+  kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, a.tdk, p);
+  return cudaGetLastError();
+}
+
+template <bool CAUSAL, bool SPARSE>
+cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
+  using C = Cfg64;
   BwdParams64 p;
   p.stats = a.stats;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
@@ -748,10 +782,14 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   p.ctl = a.ctl;
   // one persistent CTA per SM walks the items, or one CTA per item
   const long n_items = (long)p.nkv * p.BHkv;
-  const long ctas = persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms ? a.num_sms : n_items;
-  dim3 grid((unsigned)ctas);
-  kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, a.tdk, p);
-  return cudaGetLastError();
+  const bool persistent = persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms;
+  const long ctas = persistent ? a.num_sms : n_items;
+  // the cross-item V copy pays where CTAs run several items (+6 % on the
+  // GPT-2 backward); one-item launches keep the other instantiation, which
+  // measured 1-2 % faster for them
+  if constexpr (!SPARSE)
+    if (persistent) return launch_k<CAUSAL, SPARSE, true>(a, p, ctas, stream);
+  return launch_k<CAUSAL, SPARSE, false>(a, p, ctas, stream);
 }
 
 }  // namespace
