@@ -77,3 +77,18 @@ def test_gqa_long_causal_sampled():
     err_v = ((dv.sum(dim=2) - sdo).norm(dim=-1) / fro(dv)).max().item()
     err_k = (dk.sum(dim=2).norm(dim=-1) / fro(dk)).max().item()
     assert err_v <= 3e-2 and err_k <= 3e-2, (err_v, err_k)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_d64_grouped_cross(causal):
+    """d = 64 with grouped key/value heads, more queries than fit one tile
+    pair and keys that differ in length (N_q = 640, N_k = 1000), on enough
+    heads that both main kernels run persistent CTAs over several items: the
+    forward staging O through shared memory, the backward copying the next
+    item's K and V into tensor memory before the current item ends.  Three
+    key/value groups in full."""
+    B, H, H_kv, Nq, Nk, d = 8, 16, 4, 640, 1000, 64
+    q, k, v, dO = gqa_inputs(B, H, H_kv, Nq, d, seed=88 + causal, N_k=Nk)
+    scale = d ** -0.5
+    out = run_gpu(q, k, v, dO, scale, causal)
+    check_groups(q, k, v, dO, out, scale, causal, [(0, 0), (3, 2), (7, 3)])
