@@ -54,13 +54,14 @@ def test_small_shapes(B, H, N, d, causal):
     check_heads(q, k, v, dO, out, w.scale, causal, heads)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_persistent_d64_ragged(causal):
-    """d = 64 with more query-tile pairs than SMs (the persistent launch, whose
-    CTAs stage O through shared memory for every item but their last) and a
-    ragged last tile whose last three warps hold no row (N = 900 = 7 * 128 +
-    4): six seeded heads in full, identities on all 160."""
-    w = W.Workload("persistent_d64", 8, 20, 900, 64, causal=causal, seed=77)
+def test_persistent_staged_ragged(causal, d):
+    """More query-tile pairs than SMs and short heads (persistent launches;
+    at d = 64 the CTAs stage O through shared memory for every item but
+    their last) and a ragged last tile whose last three warps hold no row
+    (N = 900 = 7 * 128 + 4): six seeded heads in full, identities on all 160."""
+    w = W.Workload("persistent_staged", 8, 20, 900, d, causal=causal, seed=77 + d)
     q, k, v, dO = W.make_inputs(w)
     out = run_gpu(q, k, v, dO, w.scale, causal)
     check_heads(q, k, v, dO, out, w.scale, causal, seeded_heads(w.B, w.H, 6, seed=8))
