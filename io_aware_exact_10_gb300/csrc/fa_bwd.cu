@@ -608,9 +608,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
         if (key < p.Nk) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          st_global_64B(dst + c0, pk);
         }
       }
     }
@@ -709,9 +707,7 @@ __global__ void __launch_bounds__(448, 1)
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
         if (key < p.Nk) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          st_global_64B(dst + c0, pk);
         }
       }
       tc_fence_before();

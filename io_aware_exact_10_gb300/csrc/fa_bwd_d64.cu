@@ -578,6 +578,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     // epilogue: dV rows of this key tile, columns [DVC g, DVC g + DVC); the
     // next item's first dV (computed after this warp's next P) overwrites them
     constexpr int DVC = C::HD / C::NG;
+    static_assert(DVC % 32 == 0, "whole 64-byte pieces of a dV row per thread");
     if (ok && (ok = warp_wait(bar(B_FIN), (uint32_t)k & 1u, p.ctl, abort, 86))) {
       tc_fence_after();
       const int key = kt * C::BK + r;
@@ -594,7 +595,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
       if (key < p.Nk) {
         uint4* d4 = reinterpret_cast<uint4*>(p.dv + (rowbase + key) * C::HD + DVC * g);
 #pragma unroll
-        for (int i = 0; i < DVC / 8; ++i) d4[i] = make_uint4(pkv[4 * i], pkv[4 * i + 1], pkv[4 * i + 2], pkv[4 * i + 3]);
+        for (int i = 0; i < DVC / 32; ++i) st_global_64B(d4 + 4 * i, pkv + 16 * i);
       }
     }
     U0 += nit_i;

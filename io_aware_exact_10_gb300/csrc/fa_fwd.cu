@@ -985,10 +985,13 @@ __global__ void __launch_bounds__((8 * NH + 2) * 32, 1)
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
           if (row < p.Nq) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + ob + c0);
+            if constexpr (STG) {  // the staged-store kernel measured faster with 16-byte stores here
+              uint4* dst = reinterpret_cast<uint4*>(orow + ob + c0);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            } else {
+              st_global_64B(orow + ob + c0, pk);
+            }
           }
         }
         if (h == 0 && row < p.Nq) p.lse[(size_t)bh * p.Nq + row] = (m + __log2f(l)) * kLn2;

@@ -500,6 +500,27 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+// 64 contiguous bytes (16 words) from one thread to global memory: two
+// 32-byte stores (whole sectors) where the address allows, else four 16-byte
+// ones.  A thread writing its own row touches 32 rows per warp instruction;
+// full sectors halve the instructions and leave no partial sector writes.
+__device__ __forceinline__ void st_global_64B(void* dst, const uint32_t* w) {
+  if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                     reinterpret_cast<char*>(dst) + 32),
+                 "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
+                 "r"(w[15])
+                 : "memory");
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+}
+
 // max of three fp32 values (sm_100+)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
