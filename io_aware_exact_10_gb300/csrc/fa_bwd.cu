@@ -147,14 +147,15 @@ static_assert(BwdCfg<128>::SMEM % 16 == 0 && BwdCfg<128>::SMEM + kMaskWords * 4 
 enum : int {
   B_KV = 0, B_QF0 = 1, B_QF1 = 2, B_DOF0 = 3, B_DOF1 = 4, B_QE0 = 5, B_QE1 = 6, B_DOE0 = 7,
   B_DOE1 = 8, B_ST = 9, B_DPT = 10, B_P = 11, B_DS = 12, B_DQF = 13, B_DQE = 14, B_FIN = 15,
-  B_DRAIN = 16, B_WG = 17, B_DKF = 18, B_COUNT = 19
+  B_DRAIN = 16, B_WG = 17, B_DKF = 18, B_DS0 = 19, B_COUNT = 20
 };
-// arrival counts: TMA / commit barriers take one arrival; B_P and B_DS one
-// per P/dS warp; B_QE*, B_DOE* and B_DQE one per drain warp (the drain frees
+// arrival counts: TMA / commit barriers take one arrival; B_P, B_DS0 (the
+// first half of each warp's dS^T in TMEM) and B_DS one per P/dS warp; B_QE*, B_DOE* and B_DQE one per drain warp (the drain frees
 // the Q and dO slots: it stages dQ in them); B_WG every P/dS thread; B_DKF
 // (dK read out, the next item may overwrite it) one per drain warp.
+static_assert(B_COUNT <= BwdCfg<128>::NBAR, "barrier slots");
 __device__ __constant__ const uint32_t kBarCount[B_COUNT] = {1, 1, 1, 1, 1, 4, 4, 4, 4, 1, 1, 8, 8,
-                                                             1, 4, 1, 1, 256, 4};
+                                                             1, 4, 1, 1, 256, 4, 8};
 
 struct BwdParams {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
@@ -419,16 +420,27 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
           mma_ts_e(lead, tDV, tST + pcol(k), doMN + so + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
-        // dK += dS^T Q_i   (A = dS^T bf16 in TMEM)
-        if (!(ok = warp_wait_b(bar(B_DS), U & 1, p.ctl, abort, 25))) break;
+        // dK += dS^T Q_i   (A = dS^T bf16 in TMEM), in two halves: the
+        // K-steps of the queries whose dS^T the P/dS warps write first (0-31
+        // and 64-95: steps 0, 1, 4, 5) run while the warps compute the rest
+        if (!(ok = warp_wait_b(bar(B_DS0), U & 1, p.ctl, abort, 27))) break;
         // the item's first dK overwrites the previous item's, once the drain
         // has read it out
         if (u == 0 && ki > 0 && !(ok = warp_wait_b(bar(B_DKF), (uint32_t)(ki - 1) & 1u, p.ctl, abort, 26)))
           break;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < C::BQ / 16; ++k)
+        for (int j = 0; j < 4; ++j) {
+          const int k = (j >> 1) * 4 + (j & 1);
           mma_ts_e(lead, tDK, tDPT + pcol(k), qMN + so + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
+        }
+        if (!(ok = warp_wait_b(bar(B_DS), U & 1, p.ctl, abort, 25))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int k = (j >> 1) * 4 + (j & 1) + 2;
+          mma_ts_e(lead, tDK, tDPT + pcol(k), qMN + so + 128 * k, HI, kIdG, 1u);
+        }
         // dQ_i = dS K   (M = queries, N = d, K = keys; A = dS smem query-major, B = K key-major)
 #pragma unroll
         for (int k = 0; k < C::BK / 16; ++k)
@@ -581,6 +593,12 @@ __global__ void __launch_bounds__(448, 1)
                        "r"(pk[4 * cc]), "r"(pk[4 * cc + 1]), "r"(pk[4 * cc + 2]), "r"(pk[4 * cc + 3])
                        : "memory");
         }
+        if (c0 == 0) {  // the first 32 queries' dS^T is in TMEM: dK may take them
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_DS0));
+        }
       }
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -620,8 +638,10 @@ __global__ void __launch_bounds__(448, 1)
     // added into dQacc by TMA bulk reductions of 32-row x 32-column boxes
     // (128-byte swizzled).  The boxes are staged in the ring slots of Q_u and
     // dO_u, which no MMA reads once dQ_u is complete: this warp's quarter of
-    // the dO_u slot holds the first HD/64 boxes, its quarter of the Q_u slot
-    // the rest.  The drain then releases both slots to the TMA producer.
+    // the Q_u slot holds the first HD/64 boxes, its quarter of the dO_u slot
+    // the rest.  The drain releases each slot to the TMA producer once the
+    // reductions have read it, the Q slot (needed first: the next S^T in it
+    // precedes the next dP^T) after the first half.
     const int sp = warp & 3;
     const int r = sp * 32 + lane;  // query row within the tile (dQ) / key row (dK)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
@@ -658,7 +678,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           const int box = 2 * hh + bb;             // columns [32 box, 32 box + 32)
-          const uint32_t base = (box < BOXES_PER_SLOT ? stage_do : stage_q) +
+          const uint32_t base = (box < BOXES_PER_SLOT ? stage_q : stage_do) +
                                 (uint32_t)(box % BOXES_PER_SLOT) * 4096u;
           const uint32_t row = base + (uint32_t)lane * 128u;
 #pragma unroll
@@ -675,17 +695,20 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
           for (int bb = 0; bb < 2; ++bb) {
             const int box = 2 * hh + bb;
-            const uint32_t base = (box < BOXES_PER_SLOT ? stage_do : stage_q) +
+            const uint32_t base = (box < BOXES_PER_SLOT ? stage_q : stage_do) +
                                   (uint32_t)(box % BOXES_PER_SLOT) * 4096u;
             tma_reduce_add_3d(&tdq, base, box * 32, y, zq);
           }
           bulk_commit_group();
         }
       }
-      // once the boxes have been read, the Q_u and dO_u slots may be refilled
+      // once their boxes have been read, the Q_u and dO_u slots may be
+      // refilled (one bulk group per 64 columns: the first fills the Q slot)
+      static_assert(HD / 64 == 2, "one bulk group per ring slot");
       if (lane == 0) {
-        bulk_wait_group_read<0>();
+        bulk_wait_group_read<1>();
         mbar_arrive(bar(B_QE0 + st));
+        bulk_wait_group_read<0>();
         mbar_arrive(bar(B_DOE0 + st));
       }
       __syncwarp();
