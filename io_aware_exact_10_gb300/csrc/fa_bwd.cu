@@ -24,7 +24,8 @@
 //   warps 0-7   P / dS: thread = key row = TMEM lane; warps 0-3 take query
 //               columns 0-63 of the tile, warps 4-7 columns 64-127
 //   warps 8-11  dQ drain (thread = query row = TMEM lane), then dK epilogue
-//   warp  12    TMA producer (K, V once; then Q_i, dO_i through 2-slot rings)
+//   warp  12    TMA producer (K, V once; then Q_i, dO_i through rings of two
+//               slots each, or of three for Q and one for dO)
 //   warp  13    tcgen05 MMA issuer and TMEM owner
 // Tensor memory (512 columns): ST (S^T, then P^T bf16) | DPT (dP^T, then dS^T
 // bf16, then dQ) | dV | dK.  The bf16 pairs of P^T and dS^T for queries 0-63
@@ -33,7 +34,7 @@
 //   S^T = K Q_i^T -> ST;  dP^T = V dO_i^T -> DPT;  dV += P^T dO_i;
 //   dK += dS^T Q_i;  dQ_i = dS K -> DPT.
 // dS is also written to shared memory (query-major) as the A operand of dQ;
-// dQ is staged for its bulk reductions in the Q_u and dO_u ring slots.
+// dQ is staged for its bulk reductions in ring slots of Q_u (and dO_u).
 #include <cuda_bf16.h>
 
 #include "fa_kernels.h"
@@ -127,13 +128,14 @@ struct BwdCfg {
   // dynamic shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
-  static constexpr int OFF_Q = OFF_V + TILE;        // 2 slots
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE;   // 2 slots
-  static constexpr int OFF_DS = OFF_DO + 2 * TILE;
+  // four ring slots for Q and dO: two each, or (persistent launches) three
+  // for Q and one for dO
+  static constexpr int OFF_Q = OFF_V + TILE;
+  static constexpr int OFF_DS = OFF_Q + 4 * TILE;
   static constexpr int OFF_LSE = OFF_DS + DS_BYTES; // 2 x 128 floats (-LSE * log2 e)
   static constexpr int OFF_D = OFF_LSE + 2 * BQ * 4;  // 2 x 128 floats (-D)
   static constexpr int OFF_BAR = OFF_D + 2 * BQ * 4;
-  static constexpr int NBAR = 20;
+  static constexpr int NBAR = 24;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static constexpr int THREADS = 448;
   static constexpr int W_LOAD = 12, W_MMA = 13;  // warps 0-7: P / dS; 8-11: dQ drain
@@ -145,17 +147,19 @@ static_assert(BwdCfg<128>::SMEM % 16 == 0 && BwdCfg<128>::SMEM + kMaskWords * 4 
 
 // barrier indices
 enum : int {
-  B_KV = 0, B_QF0 = 1, B_QF1 = 2, B_DOF0 = 3, B_DOF1 = 4, B_QE0 = 5, B_QE1 = 6, B_DOE0 = 7,
-  B_DOE1 = 8, B_ST = 9, B_DPT = 10, B_P = 11, B_DS = 12, B_DQF = 13, B_DQE = 14, B_FIN = 15,
-  B_DRAIN = 16, B_WG = 17, B_DKF = 18, B_DS0 = 19, B_COUNT = 20
+  B_KV = 0, B_QF0 = 1, B_DOF0 = 4, B_QE0 = 6, B_DOE0 = 9,  // up to 3 Q, 2 dO slots
+  B_ST = 11, B_DPT = 12, B_P = 13, B_DS = 14, B_DQF = 15, B_DQE = 16, B_FIN = 17,
+  B_DRAIN = 18, B_WG = 19, B_DKF = 20, B_DS0 = 21, B_COUNT = 22
 };
 // arrival counts: TMA / commit barriers take one arrival; B_P, B_DS0 (the
-// first half of each warp's dS^T in TMEM) and B_DS one per P/dS warp; B_QE*, B_DOE* and B_DQE one per drain warp (the drain frees
-// the Q and dO slots: it stages dQ in them); B_WG every P/dS thread; B_DKF
-// (dK read out, the next item may overwrite it) one per drain warp.
+// first half of each warp's dS^T in TMEM) and B_DS one per P/dS warp; B_QE*,
+// B_DOE* and B_DQE one per drain warp (the drain frees the slots it stages
+// dQ in), except that with one dO slot B_DOE0 is the commit after dV (the
+// last MMA that reads dO); B_WG every P/dS thread; B_DKF (dK read out, the
+// next item may overwrite it) one per drain warp.
 static_assert(B_COUNT <= BwdCfg<128>::NBAR, "barrier slots");
-__device__ __constant__ const uint32_t kBarCount[B_COUNT] = {1, 1, 1, 1, 1, 4, 4, 4, 4, 1, 1, 8, 8,
-                                                             1, 4, 1, 1, 256, 4, 8};
+__device__ __constant__ const uint32_t kBarCount[B_COUNT] = {1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 4,
+                                                             1, 1, 8, 8, 1, 4, 1, 1, 256, 4, 8};
 
 struct BwdParams {
   const float* stats;  // per tile: -LSE log2 e (128), -D (128)
@@ -183,7 +187,10 @@ __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, const
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int HD, bool CAUSAL, bool SPARSE>
+// R3: three Q slots and one dO slot, the dO slot refilled once dV has read
+// it and dQ staged in two halves in the Q slot (persistent launches);
+// otherwise two slots of each, dQ staged in the Q and dO slots of its tile.
+template <int HD, bool CAUSAL, bool SPARSE, bool R3 = false>
 __global__ void __launch_bounds__(448, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -266,31 +273,44 @@ __global__ void __launch_bounds__(448, 1)
     return s;
   };
 
+  constexpr int QSLOTS = R3 ? 3 : 2;
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V, sQ = s0 + C::OFF_Q,
-                 sDO = s0 + C::OFF_DO, sDS = s0 + C::OFF_DS;
+                 sDO = sQ + QSLOTS * C::TILE, sDS = s0 + C::OFF_DS;
+  // ring slots and barrier phases of global tile u
+  // (u >= 0)
+  auto qslot = [](int u) { return R3 ? (int)((uint32_t)u % 3u) : (u & 1); };
+  auto qphase = [](int u) { return (R3 ? (uint32_t)u / 3u : (uint32_t)u >> 1) & 1u; };
+  auto doslot = [](int u) { return R3 ? 0 : (u & 1); };
+  auto dophase = [](int u) { return (uint32_t)(R3 ? u : (u >> 1)) & 1u; };
   float* lse_sh = reinterpret_cast<float*>(smem + C::OFF_LSE);
   float* d_sh = reinterpret_cast<float*>(smem + C::OFF_D);
 
   // The TMA thread initialises the barriers and issues the copies that need
-  // no wait (K, V, and Q and dO of the first two query tiles) before the
+  // no wait (K, V, and Q and dO of the first query tiles) before the
   // CTA-wide sync, so their latency overlaps the rest of the set-up.
   TileWalk lw = walk0;  // the TMA thread's position
   QuerySeq<SPARSE> lseq = qseq;  // and its item's query-tile sequence
-  auto issue_qdo = [&](int u) {  // moves to the next tile
-    const int st = u & 1, qt = lw.qt, zq = lw.qh;
-    lseq.next(lw);
+  auto issue_q = [&](int u) {
+    const int st = qslot(u);
     mbar_arrive_expect_tx(bar(B_QF0 + st), C::TILE);
     for (int b = 0; b < C::KB; ++b)
-      tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, zq);
+      tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, lw.qt * C::BQ, lw.qh);
+  };
+  auto issue_do = [&](int u) {  // then moves to the next tile
+    const int st = doslot(u);
     mbar_arrive_expect_tx(bar(B_DOF0 + st), C::TILE);
     for (int b = 0; b < C::KB; ++b)
-      tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, zq);
+      tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, lw.qt * C::BQ, lw.qh);
+    lseq.next(lw);
   };
-  const int pre = nit < 2 ? nit : 2;  // query tiles issued before the sync
+  // tiles issued before the sync; with one dO slot the second tile's dO
+  // waits for the first tile's dV
+  constexpr int PRE = R3 ? 1 : 2;
+  const int pre = nit < PRE ? nit : PRE;
   if (warp == C::W_LOAD && lane == 0) {
     *abort = 0;
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), kBarCount[i]);
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), R3 && i == B_DOE0 ? 1u : kBarCount[i]);
     fence_barrier_init();
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
@@ -302,7 +322,10 @@ __global__ void __launch_bounds__(448, 1)
       tma_load_3d(sK + b * 16384, &tk, bar(B_KV), b * 64, kt * C::BK, bk);
       tma_load_3d(sV + b * 16384, &tv, bar(B_KV), b * 64, kt * C::BK, bk);
     }
-    for (int u = 0; u < pre; ++u) issue_qdo(u);
+    for (int u = 0; u < pre; ++u) {
+      issue_q(u);
+      issue_do(u);
+    }
   }
   if (warp == C::W_MMA) {
     tmem_alloc(smem_u32(tmem_base_sh), C::TMEM_COLS);
@@ -318,22 +341,20 @@ __global__ void __launch_bounds__(448, 1)
     if (lane == 0) {
       bool ok = true;
       int nkv_issued = 1;  // items whose K, V have been issued
-      // Q_u and dO_u of global tile u, once their ring slots are free
+      // Q_u and dO_u of global tile u, once their ring slots are free: a
+      // slot's previous tile (u - QSLOTS for Q, u - 1 or u - 2 for dO) has
+      // released it (phase of that tile on the slot's barrier)
       auto ring = [&](int u) -> bool {
-        const int st = u & 1, use = u >> 1, qt = lw.qt, zq = lw.qh;
-        if (use > 0 && !mbar_wait(bar(B_QE0 + st), (use - 1) & 1, p.ctl, abort, 10)) return false;
-        mbar_arrive_expect_tx(bar(B_QF0 + st), C::TILE);
-        for (int b = 0; b < C::KB; ++b)
-          tma_load_3d(sQ + st * C::TILE + b * 16384, &tq, bar(B_QF0 + st), b * 64, qt * C::BQ, zq);
-        if (use > 0 && !mbar_wait(bar(B_DOE0 + st), (use - 1) & 1, p.ctl, abort, 11)) {
+        const int qs = qslot(u), ds = doslot(u);
+        if (u >= QSLOTS && !mbar_wait(bar(B_QE0 + qs), qphase(u) ^ 1u, p.ctl, abort, 10)) return false;
+        issue_q(u);
+        const int ud = u - (R3 ? 1 : 2);  // the dO slot's previous tile
+        if (ud >= 0 && !mbar_wait(bar(B_DOE0 + ds), dophase(ud), p.ctl, abort, 11)) {
           // the Q load above is in flight; wait for it here
-          mbar_wait_quiet(bar(B_QF0 + st), use & 1, 200000000ull);
+          mbar_wait_quiet(bar(B_QF0 + qs), qphase(u), 200000000ull);
           return false;
         }
-        mbar_arrive_expect_tx(bar(B_DOF0 + st), C::TILE);
-        for (int b = 0; b < C::KB; ++b)
-          tma_load_3d(sDO + st * C::TILE + b * 16384, &tdo, bar(B_DOF0 + st), b * 64, qt * C::BQ, zq);
-        lseq.next(lw);
+        issue_do(u);
         return true;
       };
       int u = pre, uend = nit;  // global tile index; end of the current item
@@ -342,13 +363,15 @@ __global__ void __launch_bounds__(448, 1)
         if (!ok) break;
         L = item_at(++kk);
         if (L >= n_items) break;
-        // the next item: its first tiles as soon as their slots are free,
-        // then K and V once every MMA of the previous item has completed
+        // the next item: its first tiles (as many as there are dO slots: a
+        // later dO waits for a dV of the new item) as soon as their slots
+        // are free, then K and V once every MMA of the previous item has
+        // completed
         const Item I = item_info(L);
         lw = TileWalk{I.i0, I.bk * p.kv_group};
         lseq = item_seq(I);
         uend = u + item_nit(I);
-        const int upre = min(uend, u + 2);
+        const int upre = min(uend, u + PRE);
         while (u < upre && (ok = ring(u))) ++u;
         if (!ok || !(ok = mbar_wait(bar(B_FIN), (nkv_issued - 1) & 1, p.ctl, abort, 12))) break;
         mbar_arrive_expect_tx(bar(B_KV), 2 * C::TILE);
@@ -361,10 +384,11 @@ __global__ void __launch_bounds__(448, 1)
       if (!ok) {
         // Abort: let every copy already issued land before the CTA exits.
         mbar_wait_quiet(bar(B_KV), (nkv_issued - 1) & 1, 200000000ull);
-        for (int v = (u >= 2 ? u - 2 : 0); v < u; ++v) {
-          mbar_wait_quiet(bar(B_QF0 + (v & 1)), (v >> 1) & 1, 200000000ull);
-          mbar_wait_quiet(bar(B_DOF0 + (v & 1)), (v >> 1) & 1, 200000000ull);
-        }
+        // (a slot's earlier loads completed before it was refilled)
+        for (int v = (u >= QSLOTS ? u - QSLOTS : 0); v < u; ++v)
+          mbar_wait_quiet(bar(B_QF0 + qslot(v)), qphase(v), 200000000ull);
+        for (int v = (u >= PRE ? u - PRE : 0); v < u; ++v)
+          mbar_wait_quiet(bar(B_DOF0 + doslot(v)), dophase(v), 200000000ull);
       }
     }
   } else if (warp == C::W_MMA) {
@@ -392,10 +416,9 @@ __global__ void __launch_bounds__(448, 1)
       if (!(ok = warp_wait_b(bar(B_KV), (uint32_t)ki & 1u, p.ctl, abort, 20))) break;
       for (int u = 0; u < nit_i && ok; ++u) {
         const int U = U0 + u;
-        const int st = U & 1, par = (U >> 1) & 1;
-        const uint32_t so = (uint32_t)st * TILE16;
+        const uint32_t so = (uint32_t)qslot(U) * TILE16, sd = (uint32_t)doslot(U) * TILE16;
         const uint32_t acc0 = u > 0 ? 1u : 0u;
-        if (!(ok = warp_wait_b(bar(B_QF0 + st), par, p.ctl, abort, 21))) break;
+        if (!(ok = warp_wait_b(bar(B_QF0 + qslot(U)), qphase(U), p.ctl, abort, 21))) break;
         tc_fence_after();
         // S^T = K Q_i^T   (M = keys, N = queries, K = d; both K-major)
 #pragma unroll
@@ -404,14 +427,14 @@ __global__ void __launch_bounds__(448, 1)
           mma_ss_e(lead, tST, kK + off, HI, qK + so + off, HI, kIdS, k > 0);
         }
         mma_commit_e(lead, bar(B_ST));
-        if (!(ok = warp_wait_b(bar(B_DOF0 + st), par, p.ctl, abort, 22))) break;
+        if (!(ok = warp_wait_b(bar(B_DOF0 + doslot(U)), dophase(U), p.ctl, abort, 22))) break;
         if (U > 0 && !(ok = warp_wait_b(bar(B_DQE), (U - 1) & 1, p.ctl, abort, 23))) break;
         tc_fence_after();
         // dP^T = V dO_i^T
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint32_t off = (uint32_t)(k / 4) * 1024 + (uint32_t)(k % 4) * 2;
-          mma_ss_e(lead, tDPT, vK + off, HI, doK + so + off, HI, kIdS, k > 0);
+          mma_ss_e(lead, tDPT, vK + off, HI, doK + sd + off, HI, kIdS, k > 0);
         }
         mma_commit_e(lead, bar(B_DPT));
         // dV += P^T dO_i   (A = P^T bf16 in TMEM, B = dO_i query-major)
@@ -419,7 +442,8 @@ __global__ void __launch_bounds__(448, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::BQ / 16; ++k)
-          mma_ts_e(lead, tDV, tST + pcol(k), doMN + so + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
+          mma_ts_e(lead, tDV, tST + pcol(k), doMN + sd + 128 * k, HI, kIdG, k > 0 ? 1u : acc0);
+        if (R3) mma_commit_e(lead, bar(B_DOE0));  // dO_i read: the next dO may load
         // dK += dS^T Q_i   (A = dS^T bf16 in TMEM), in two halves: the
         // K-steps of the queries whose dS^T the P/dS warps write first (0-31
         // and 64-95: steps 0, 1, 4, 5) run while the warps compute the rest
@@ -636,17 +660,19 @@ __global__ void __launch_bounds__(448, 1)
     // ---------------------------------------------------------- dQ drain
     // dQ_u (128 query rows x d, fp32) leaves TMEM 64 columns at a time and is
     // added into dQacc by TMA bulk reductions of 32-row x 32-column boxes
-    // (128-byte swizzled).  The boxes are staged in the ring slots of Q_u and
-    // dO_u, which no MMA reads once dQ_u is complete: this warp's quarter of
-    // the Q_u slot holds the first HD/64 boxes, its quarter of the dO_u slot
-    // the rest.  The drain releases each slot to the TMA producer once the
-    // reductions have read it, the Q slot (needed first: the next S^T in it
-    // precedes the next dP^T) after the first half.
+    // (128-byte swizzled), staged in ring slots that no MMA reads once dQ_u
+    // is complete.  Each warp's quarter of a slot holds two boxes (64
+    // columns of its rows).  Two dO slots: the first half goes to the Q_u
+    // slot, which is released as soon as the reductions have read it (the
+    // next S^T needs it before the next dP^T needs a dO slot), the second to
+    // the dO_u slot.  One dO slot: both halves go to the Q_u slot, the second
+    // once the first has been read; both leave TMEM before that wait, so the
+    // columns are free as early.
     const int sp = warp & 3;
     const int r = sp * 32 + lane;  // query row within the tile (dQ) / key row (dK)
     const uint32_t lane_off = (uint32_t)(sp * 32) << 16;
     const uint32_t sw = (uint32_t)(lane & 7);
-    constexpr int BOXES_PER_SLOT = HD / 64;          // 4 KB boxes in a warp's quarter
+    static_assert(HD / 64 == 2, "two 64-column halves, one bulk group each");
     bool ok = true;
     int U0 = 0;  // global index of the item's first tile
     for (int L = L0, ki = 0; L < n_items && ok; L = item_at(++ki)) {
@@ -660,9 +686,9 @@ __global__ void __launch_bounds__(448, 1)
       const int U = U0 + u;
       if (!(ok = warp_wait_b(bar(B_DQF), U & 1, p.ctl, abort, 40))) break;
       tc_fence_after();
-      const int st = U & 1;
-      const uint32_t quarter = (uint32_t)sp * (uint32_t)(C::TILE / 4);
-      const uint32_t stage_do = sDO + st * C::TILE + quarter, stage_q = sQ + st * C::TILE + quarter;
+      const uint32_t quarter = (uint32_t)sp * (uint32_t)(C::TILE / 4);  // 8 KB
+      const uint32_t stage_q = sQ + qslot(U) * C::TILE + quarter;
+      const uint32_t stage_2 = R3 ? stage_q : sDO + doslot(U) * C::TILE + quarter;
       const int y = w.qt * C::BQ + sp * 32, zq = w.qh;
 #pragma unroll
       for (int hh = 0; hh < HD / 64; ++hh) {
@@ -675,12 +701,15 @@ __global__ void __launch_bounds__(448, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_DQE));  // dQ's TMEM columns are free again
         }
+        if (R3 && hh > 0) {  // the first half's boxes must have been read
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+        }
+        const uint32_t stage = hh == 0 ? stage_q : stage_2;
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
-          const int box = 2 * hh + bb;             // columns [32 box, 32 box + 32)
-          const uint32_t base = (box < BOXES_PER_SLOT ? stage_q : stage_do) +
-                                (uint32_t)(box % BOXES_PER_SLOT) * 4096u;
-          const uint32_t row = base + (uint32_t)lane * 128u;
+          // box 2 hh + bb: columns [64 hh + 32 bb, 64 hh + 32 bb + 32)
+          const uint32_t row = stage + (uint32_t)bb * 4096u + (uint32_t)lane * 128u;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const int col = bb * 32 + c * 4;
@@ -693,23 +722,22 @@ __global__ void __launch_bounds__(448, 1)
         __syncwarp();
         if (lane == 0) {
 #pragma unroll
-          for (int bb = 0; bb < 2; ++bb) {
-            const int box = 2 * hh + bb;
-            const uint32_t base = (box < BOXES_PER_SLOT ? stage_q : stage_do) +
-                                  (uint32_t)(box % BOXES_PER_SLOT) * 4096u;
-            tma_reduce_add_3d(&tdq, base, box * 32, y, zq);
-          }
+          for (int bb = 0; bb < 2; ++bb)
+            tma_reduce_add_3d(&tdq, stage + (uint32_t)bb * 4096u, (2 * hh + bb) * 32, y, zq);
           bulk_commit_group();
         }
       }
-      // once their boxes have been read, the Q_u and dO_u slots may be
-      // refilled (one bulk group per 64 columns: the first fills the Q slot)
-      static_assert(HD / 64 == 2, "one bulk group per ring slot");
+      // once their boxes have been read, the slots may be refilled
       if (lane == 0) {
-        bulk_wait_group_read<1>();
-        mbar_arrive(bar(B_QE0 + st));
-        bulk_wait_group_read<0>();
-        mbar_arrive(bar(B_DOE0 + st));
+        if constexpr (R3) {
+          bulk_wait_group_read<0>();
+          mbar_arrive(bar(B_QE0 + qslot(U)));
+        } else {
+          bulk_wait_group_read<1>();
+          mbar_arrive(bar(B_QE0 + qslot(U)));
+          bulk_wait_group_read<0>();
+          mbar_arrive(bar(B_DOE0 + doslot(U)));
+        }
       }
       __syncwarp();
     }
@@ -756,11 +784,6 @@ __global__ void __launch_bounds__(448, 1)
 template <int HD, bool CAUSAL, bool SPARSE>
 cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   using C = BwdCfg<HD>;
-  auto kern = fa_bwd_kernel<HD, CAUSAL, SPARSE>;
-  // block-sparse: the mask column's bitset and its count follow the layout
-  const int smem_bytes = C::SMEM + (SPARSE ? kMaskWords * 4 + 16 : 0);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-  if (e != cudaSuccess) return e;
   BwdParams p;
   p.stats = a.stats;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
@@ -777,9 +800,18 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
-  // one persistent CTA per SM walks the items, or one CTA per item
+  // one persistent CTA per SM walks the items (with the three-Q-slot ring,
+  // measured faster there), or one CTA per item
   const long n_items = (long)p.nkv * p.BHkv;
-  const long ctas = persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms ? a.num_sms : n_items;
+  const bool pers = persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms;
+  const long ctas = pers ? a.num_sms : n_items;
+  auto kern = fa_bwd_kernel<HD, CAUSAL, SPARSE, false>;
+  if constexpr (!SPARSE)
+    if (pers) kern = fa_bwd_kernel<HD, CAUSAL, SPARSE, true>;
+  // block-sparse: the mask column's bitset and its count follow the layout
+  const int smem_bytes = C::SMEM + (SPARSE ? kMaskWords * 4 + 16 : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)ctas);
   kern<<<grid, C::THREADS, smem_bytes, stream>>>(a.tq, a.tk, a.tv, a.tdo, a.tdq, p);
   return cudaGetLastError();

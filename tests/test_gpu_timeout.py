@@ -9,7 +9,7 @@ the copies and tensor-core operations it has issued complete, frees its
 tensor memory and returns.  Nothing is injected: the same kernels run on
 valid inputs, only the bound differs.  Each main kernel (forward, the d = 64
 and the d = 128 backward) is made to give up once on a small problem, and
-the persistent d = 64 kernels on one with more work items than SMs; the
+the persistent kernels on one with more work items than SMs; the
 status is read back, the bound restored, and a normal call on the same
 device then matches the oracle.
 """
@@ -47,8 +47,9 @@ def gives_up(fn):
 @pytest.mark.parametrize("B,H,N,d", [
     (1, 2, 4096, 64), (1, 2, 4096, 128),
     # more work items than SMs: the persistent kernels, at d = 64 the
-    # forward that stages O through its second Q buffers
-    (8, 20, 1024, 64)])
+    # forward that stages O through its second Q buffers, at d = 128 the
+    # backward with three Q slots and one dO slot
+    (8, 20, 1024, 64), (8, 20, 1024, 128)])
 def test_wait_bound_runs_out_then_a_normal_call_succeeds(B, H, N, d):
     # long enough that the pipelines' producers wait for free slots (a wait
     # that ends within one poll of the barrier cannot run out)
