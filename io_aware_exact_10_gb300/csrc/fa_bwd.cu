@@ -187,10 +187,11 @@ __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, const
   return __all_sync(0xffffffffu, ok);
 }
 
-// R3: three Q slots and one dO slot, the dO slot refilled once dV has read
-// it and dQ staged in two halves in the Q slot (persistent launches);
-// otherwise two slots of each, dQ staged in the Q and dO slots of its tile.
-template <int HD, bool CAUSAL, bool SPARSE, bool R3 = false>
+// SCHED 0: one CTA per item, two Q and two dO slots, dQ staged in the Q and
+// dO slots of its tile.  SCHED 1 and 2: persistent CTAs (2: causal, in units
+// of two key tiles) with three Q slots and one dO slot, the dO slot refilled
+// once dV has read it and dQ staged in two halves in the Q slot.
+template <int HD, bool CAUSAL, bool SPARSE, int SCHED = 0>
 __global__ void __launch_bounds__(448, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(448, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
+  constexpr bool R3 = SCHED >= 1, PAIRS = SCHED == 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Work items are (key/value head, key tile) pairs in a one-dimensional
   // order over (head group, key tile, head): the items of a group's heads run
@@ -219,23 +221,38 @@ __global__ void __launch_bounds__(448, 1)
   // loop with a TileWalk.  Persistent launches (see persistent_launch) have
   // one CTA per SM (G CTAs), and CTA b takes items b, 2G-1-b, 2G+b, ...:
   // each pass over G items runs the other way, pairing heavy causal items
-  // with light ones.  Other launches have one CTA per item.  The ring
-  // positions, the per-tile barrier phases and the statistics buffers run on
-  // across items (global tile index U); K, V, FIN and "dK read out" have one
-  // phase per item.
+  // with light ones.  Persistent causal launches over square heads with many
+  // key tiles (SCHED 2) instead walk units of two key tiles of one head, j
+  // and nkv-1-j, which see nq + 1 query tiles together whatever j: unit u
+  // is (head u / (nkv/2), j = u mod nkv/2), CTA b takes units b, b+G, ...,
+  // and item 2u + s is the unit's heavy (s = 0) or light (s = 1) key tile.
+  // Other launches have one CTA per item.  The ring positions, the per-tile
+  // barrier phases and the statistics buffers run on across items (global
+  // tile index U); K, V, FIN and "dK read out" have one phase per item.
   const int n_items = p.BHkv * p.nkv;
-  const int L0 = (int)blockIdx.x, LS = (int)gridDim.x;
-  // k-th item (k >= 1); a block-sparse CTA has one item, which the compiler
-  // then knows: its item loops run once
-  auto item_at = [&](int k) { return SPARSE ? n_items : k * LS + ((k & 1) ? LS - 1 - L0 : L0); };
+  const int B0 = (int)blockIdx.x, LS = (int)gridDim.x;
+  // k-th item of this CTA (n_items or more: none); a block-sparse CTA has one
+  // item, which the compiler then knows: its item loops run once
+  auto item_at = [&](int k) {
+    if (SPARSE) return k == 0 ? B0 : n_items;
+    if (PAIRS) return 2 * (B0 + (k >> 1) * LS) + (k & 1);
+    return k * LS + ((k & 1) ? LS - 1 - B0 : B0);
+  };
+  const int L0 = item_at(0);
   struct Item {
     int bk, kt, i0;
   };
   auto item_info = [&](int L) {
-    const GridPos gp = decode_grid(L, p.BHkv, p.nkv, p.group);
     Item I;
-    I.bk = gp.bh;
-    I.kt = gp.rank;
+    if (PAIRS) {
+      const int hk = p.nkv >> 1, unit = L >> 1, h = unit / hk, j = unit - h * hk;
+      I.bk = h;
+      I.kt = (L & 1) ? p.nkv - 1 - j : j;
+    } else {
+      const GridPos gp = decode_grid(L, p.BHkv, p.nkv, p.group);
+      I.bk = gp.bh;
+      I.kt = gp.rank;
+    }
     I.i0 = CAUSAL ? first_query_tile(I.kt, p.coff) : 0;  // first query tile that sees this key tile
     return I;
   };
@@ -801,13 +818,25 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
   // one persistent CTA per SM walks the items (with the three-Q-slot ring,
-  // measured faster there), or one CTA per item
+  // measured faster there), or one CTA per item.  Causal launches over
+  // square heads with an even number of key tiles, more than persistent
+  // launches take otherwise and at most 64, go persistent in units of two
+  // key tiles of equal total work when the units fill their last wave of
+  // CTAs to 95 % or more (measured: +4 % at 32 key tiles per head, +1.5 %
+  // at 64, -0.5 % at 128).
   const long n_items = (long)p.nkv * p.BHkv;
-  const bool pers = persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms;
+  const long units = n_items / 2, waves = (units + a.num_sms - 1) / a.num_sms;
+  const bool pairs = CAUSAL && !SPARSE && a.Nq == a.Nk && p.nkv % 2 == 0 && p.nkv <= 64 &&
+                     !persistent_launch(CAUSAL, SPARSE, p.nkv) && units >= a.num_sms &&
+                     units * 20 >= waves * a.num_sms * 19;
+  const bool pers = pairs || (persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms);
   const long ctas = pers ? a.num_sms : n_items;
-  auto kern = fa_bwd_kernel<HD, CAUSAL, SPARSE, false>;
-  if constexpr (!SPARSE)
-    if (pers) kern = fa_bwd_kernel<HD, CAUSAL, SPARSE, true>;
+  auto kern = fa_bwd_kernel<HD, CAUSAL, SPARSE, 0>;
+  if constexpr (!SPARSE) {
+    if (pers) kern = fa_bwd_kernel<HD, CAUSAL, SPARSE, 1>;
+    if constexpr (CAUSAL)
+      if (pairs) kern = fa_bwd_kernel<HD, CAUSAL, SPARSE, 2>;
+  }
   // block-sparse: the mask column's bitset and its count follow the layout
   const int smem_bytes = C::SMEM + (SPARSE ? kMaskWords * 4 + 16 : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);

@@ -44,32 +44,33 @@ def gives_up(fn):
     return st, word
 
 
-@pytest.mark.parametrize("B,H,N,d", [
-    (1, 2, 4096, 64), (1, 2, 4096, 128),
+@pytest.mark.parametrize("B,H,N,d,causal", [
+    (1, 2, 4096, 64, False), (1, 2, 4096, 128, False),
     # more work items than SMs: the persistent kernels, at d = 64 the
     # forward that stages O through its second Q buffers, at d = 128 the
-    # backward with three Q slots and one dO slot
-    (8, 20, 1024, 64), (8, 20, 1024, 128)])
-def test_wait_bound_runs_out_then_a_normal_call_succeeds(B, H, N, d):
+    # backward with three Q slots and one dO slot, and (causal) that
+    # backward walking units of two key tiles
+    (8, 20, 1024, 64, False), (8, 20, 1024, 128, False), (2, 20, 4096, 128, True)])
+def test_wait_bound_runs_out_then_a_normal_call_succeeds(B, H, N, d, causal):
     # long enough that the pipelines' producers wait for free slots (a wait
     # that ends within one poll of the barrier cannot run out)
-    w = W.Workload("timeout", B, H, N, d, causal=False, seed=40 + d + N)
+    w = W.Workload("timeout", B, H, N, d, causal=causal, seed=40 + d + N)
     cpu = W.make_inputs(w)
     q, k, v, dO = (t.cuda() for t in cpu)
 
     # forward
-    st, word = gives_up(lambda: fa.forward(q, k, v, w.scale, False))
+    st, word = gives_up(lambda: fa.forward(q, k, v, w.scale, causal))
     assert st == fa.FA_ERR_TIMEOUT, (st, hex(word))
     assert word & 0xFF == 4  # the timeout code, then the site and the block index
 
     # backward, on a forward computed with the normal bound
-    o, lse = fa.forward(q, k, v, w.scale, False)
+    o, lse = fa.forward(q, k, v, w.scale, causal)
     torch.cuda.synchronize()
     assert fa.fa_last_device_error() == fa.FA_OK
-    st, word = gives_up(lambda: fa.backward(q, k, v, o, lse, dO, w.scale, False))
+    st, word = gives_up(lambda: fa.backward(q, k, v, o, lse, dO, w.scale, causal))
     assert st == fa.FA_ERR_TIMEOUT, (st, hex(word))
 
     # the device is still usable: a normal forward and backward match the oracle
-    out = run_gpu(*cpu, w.scale, False)
-    check_heads(*cpu, out, w.scale, False, [(0, 0), (0, 1)])
+    out = run_gpu(*cpu, w.scale, causal)
+    check_heads(*cpu, out, w.scale, causal, [(0, 0), (0, 1)])
     assert fa.fa_last_device_error() == fa.FA_OK
