@@ -223,10 +223,8 @@ __global__ void __launch_bounds__(448, 1)
   // each pass over G items runs the other way, pairing heavy causal items
   // with light ones.  Persistent causal launches over square heads with many
   // key tiles (SCHED 2) instead walk units of two key tiles of one head, j
-  // and nkv-1-j, which see nq + 1 query tiles together whatever j: unit u
-  // is (head u / (nkv/2), j = u mod nkv/2), CTA b takes units b, b+G, ...,
-  // and item 2u + s is the unit's heavy (s = 0) or light (s = 1) key tile.
-  // Other launches have one CTA per item.  The ring positions, the per-tile
+  // and nkv-1-j, which see nq + 1 query tiles together whatever j (see
+  // decode_pair).  Other launches have one CTA per item.  The ring positions, the per-tile
   // barrier phases and the statistics buffers run on across items (global
   // tile index U); K, V, FIN and "dK read out" have one phase per item.
   const int n_items = p.BHkv * p.nkv;
@@ -243,16 +241,10 @@ __global__ void __launch_bounds__(448, 1)
     int bk, kt, i0;
   };
   auto item_info = [&](int L) {
+    const GridPos gp = PAIRS ? decode_pair(L, p.nkv) : decode_grid(L, p.BHkv, p.nkv, p.group);
     Item I;
-    if (PAIRS) {
-      const int hk = p.nkv >> 1, unit = L >> 1, h = unit / hk, j = unit - h * hk;
-      I.bk = h;
-      I.kt = (L & 1) ? p.nkv - 1 - j : j;
-    } else {
-      const GridPos gp = decode_grid(L, p.BHkv, p.nkv, p.group);
-      I.bk = gp.bh;
-      I.kt = gp.rank;
-    }
+    I.bk = gp.bh;
+    I.kt = gp.rank;
     I.i0 = CAUSAL ? first_query_tile(I.kt, p.coff) : 0;  // first query tile that sees this key tile
     return I;
   };
@@ -818,17 +810,11 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
   // one persistent CTA per SM walks the items (with the three-Q-slot ring,
-  // measured faster there), or one CTA per item.  Causal launches over
-  // square heads with an even number of key tiles, more than persistent
-  // launches take otherwise and at most 64, go persistent in units of two
-  // key tiles of equal total work when the units fill their last wave of
-  // CTAs to 95 % or more (measured: +4 % at 32 key tiles per head, +1.5 %
-  // at 64, -0.5 % at 128).
+  // measured faster there), or one CTA per item; long square causal
+  // launches in units of two key tiles (pair_launch; measured +4 % at 32 key
+  // tiles per head, +1.5 % at 64, -0.5 % at 128)
   const long n_items = (long)p.nkv * p.BHkv;
-  const long units = n_items / 2, waves = (units + a.num_sms - 1) / a.num_sms;
-  const bool pairs = CAUSAL && !SPARSE && a.Nq == a.Nk && p.nkv % 2 == 0 && p.nkv <= 64 &&
-                     !persistent_launch(CAUSAL, SPARSE, p.nkv) && units >= a.num_sms &&
-                     units * 20 >= waves * a.num_sms * 19;
+  const bool pairs = pair_launch(CAUSAL, SPARSE, a.Nq == a.Nk, p.nkv, n_items, a.num_sms);
   const bool pers = pairs || (persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms);
   const long ctas = pers ? a.num_sms : n_items;
   auto kern = fa_bwd_kernel<HD, CAUSAL, SPARSE, 0>;

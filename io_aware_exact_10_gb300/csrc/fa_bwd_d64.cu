@@ -127,7 +127,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const K
 // XV (persistent launches): the drain copies the next item's V into tensor
 // memory before its dK epilogue, and the MMA warp's first dK of an item waits
 // for that epilogue's reads (DKR) instead of following the V copy.
-template <bool CAUSAL, bool SPARSE, bool XV = false>
+template <bool CAUSAL, bool SPARSE, bool XV = false, bool PAIRS = false>
 __global__ void __launch_bounds__(Cfg64::THREADS, 1)
     fa_bwd_d64_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -153,21 +153,28 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   // CTA per SM (G CTAs), and CTA b takes items b, 2G-1-b, 2G+b, 4G-1-b, ...:
   // every pass over G items visits them in the other direction, so with
   // causal masking (items heaviest first within a head group) each CTA pairs
-  // heavy items with light ones.  An item's set-up then overlaps the previous
-  // item's last tiles instead of costing a CTA launch.  Other launches have
-  // one CTA per item, which the hardware scheduler balances.  The ring positions and the per-tile barrier phases run on across
-  // items (global tile index U); K, V, their copy into tensor memory and FIN
-  // have one phase per item.
+  // heavy items with light ones.  Long square causal launches (PAIRS) walk
+  // units of two key tiles of equal total work instead (see decode_pair).
+  // An item's set-up then overlaps the previous item's last tiles instead of
+  // costing a CTA launch.  Other launches have one CTA per item, which the
+  // hardware scheduler balances.  The ring positions and the per-tile
+  // barrier phases run on across items (global tile index U); K, V, their
+  // copy into tensor memory and FIN have one phase per item.
   const int n_items = p.BHkv * p.nkv;
-  const int L0 = (int)blockIdx.x, LS = (int)gridDim.x;
-  // k-th item (k >= 1); a block-sparse CTA has one item, which the compiler
-  // then knows: its item loops run once
-  auto item_at = [&](int k) { return SPARSE ? n_items : k * LS + ((k & 1) ? LS - 1 - L0 : L0); };
+  const int B0 = (int)blockIdx.x, LS = (int)gridDim.x;
+  // k-th item of this CTA (n_items or more: none); a block-sparse CTA has
+  // one item, which the compiler then knows: its item loops run once
+  auto item_at = [&](int k) {
+    if (SPARSE) return k == 0 ? B0 : n_items;
+    if (PAIRS) return 2 * (B0 + (k >> 1) * LS) + (k & 1);
+    return k * LS + ((k & 1) ? LS - 1 - B0 : B0);
+  };
+  const int L0 = item_at(0);
   struct Item {
     int bk, kt, i0;
   };
   auto item_info = [&](int L) {
-    const GridPos gp = decode_grid(L, p.BHkv, p.nkv, p.group);
+    const GridPos gp = PAIRS ? decode_pair(L, p.nkv) : decode_grid(L, p.BHkv, p.nkv, p.group);
     Item I;
     I.bk = gp.bh;
     I.kt = gp.rank;
@@ -749,10 +756,10 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 1)
   }
 }
 
-template <bool CAUSAL, bool SPARSE, bool XV>
+template <bool CAUSAL, bool SPARSE, bool XV, bool PAIRS = false>
 cudaError_t launch_k(const BwdLaunch& a, const BwdParams64& p, long ctas, cudaStream_t stream) {
   using C = Cfg64;
-  auto kern = fa_bwd_d64_kernel<CAUSAL, SPARSE, XV>;
+  auto kern = fa_bwd_d64_kernel<CAUSAL, SPARSE, XV, PAIRS>;
   // block-sparse: the mask column's bitset and its count follow the layout
   const int smem_bytes = C::SMEM + (SPARSE ? kMaskWords * 4 + 16 : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
@@ -781,13 +788,17 @@ cudaError_t launch_t(const BwdLaunch& a, cudaStream_t stream) {
   p.scale = a.scale;
   p.scale2 = a.scale * kLog2e;
   p.ctl = a.ctl;
-  // one persistent CTA per SM walks the items, or one CTA per item
+  // one persistent CTA per SM walks the items, or one CTA per item; long
+  // square causal launches in units of two key tiles (pair_launch)
   const long n_items = (long)p.nkv * p.BHkv;
-  const bool persistent = persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms;
+  const bool pairs = pair_launch(CAUSAL, SPARSE, a.Nq == a.Nk, p.nkv, n_items, a.num_sms);
+  const bool persistent = pairs || (persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms);
   const long ctas = persistent ? a.num_sms : n_items;
   // the cross-item V copy pays where CTAs run several items (+6 % on the
   // GPT-2 backward); one-item launches keep the other instantiation, which
   // measured 1-2 % faster for them
+  if constexpr (CAUSAL && !SPARSE)
+    if (pairs) return launch_k<CAUSAL, SPARSE, true, true>(a, p, ctas, stream);
   if constexpr (!SPARSE)
     if (persistent) return launch_k<CAUSAL, SPARSE, true>(a, p, ctas, stream);
   return launch_k<CAUSAL, SPARSE, false>(a, p, ctas, stream);

@@ -192,6 +192,32 @@ __host__ __device__ inline GridPos decode_grid(int L, int BH, int tiles, int gro
   return r;
 }
 
+// Persistent causal launches over square heads (query and key tiles alike)
+// may instead walk units of two tiles of one head, j and tiles-1-j, whose
+// causal work sums to the same for every j: unit u is (head u / (tiles/2),
+// j = u mod tiles/2), and item 2u + s its tile j (s = 0, the heavier) or
+// tiles-1-j (s = 1).  CTA b of G takes units b, b + G, b + 2G, ...
+__host__ __device__ inline GridPos decode_pair(int L, int tiles) {
+  const int hk = tiles >> 1, unit = L >> 1, h = unit / hk, j = unit - h * hk;
+  GridPos r;
+  r.bh = h;
+  r.rank = (L & 1) ? tiles - 1 - j : j;
+  return r;
+}
+
+// Whether a launch takes the paired schedule: causal, dense, square, an even
+// number of tiles per head between persistent_launch's limit and 64 (beyond,
+// the one-CTA-per-item launch measured as fast), and units that fill the
+// last wave of CTAs to 95 % or more.
+inline bool pair_launch(bool causal, bool sparse, bool square, int tiles_per_head, long items,
+                        int num_sms) {
+  if (!causal || sparse || !square || tiles_per_head % 2 != 0 || tiles_per_head > 64 ||
+      persistent_launch(causal, sparse, tiles_per_head))
+    return false;
+  const long units = items / 2, waves = (units + num_sms - 1) / num_sms;
+  return units >= num_sms && units * 20 >= waves * num_sms * 19;
+}
+
 // Each returns cudaSuccess or the launch error; nothing is synchronised.
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream);
