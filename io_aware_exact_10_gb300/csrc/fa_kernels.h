@@ -206,12 +206,12 @@ __host__ __device__ inline GridPos decode_pair(int L, int tiles) {
 }
 
 // Whether a launch takes the paired schedule: causal, dense, square, an even
-// number of tiles per head between persistent_launch's limit and 64 (beyond,
-// the one-CTA-per-item launch measured as fast), and units that fill the
-// last wave of CTAs to 95 % or more.
+// number of tiles per head between persistent_launch's limit and max_tiles
+// (the kernel's measured break-even), and units that fill the last wave of
+// CTAs to 95 % or more.
 inline bool pair_launch(bool causal, bool sparse, bool square, int tiles_per_head, long items,
-                        int num_sms) {
-  if (!causal || sparse || !square || tiles_per_head % 2 != 0 || tiles_per_head > 64 ||
+                        int num_sms, int max_tiles) {
+  if (!causal || sparse || !square || tiles_per_head % 2 != 0 || tiles_per_head > max_tiles ||
       persistent_launch(causal, sparse, tiles_per_head))
     return false;
   const long units = items / 2, waves = (units + num_sms - 1) / num_sms;
