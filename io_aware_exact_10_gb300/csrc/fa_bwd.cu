@@ -545,9 +545,21 @@ __global__ void __launch_bounds__(448, 1)
       }
       if (!(ok = warp_wait_b(bar(B_ST), U & 1, p.ctl, abort, 30))) break;
       tc_fence_after();
+      // statistics four at a time (one 16-byte broadcast load per two pairs),
+      // the first chunk's while the TMEM loads are in flight
+      auto load_stats = [](const float* src, uint64_t (&dst)[16]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + 4 * i);
+          dst[2 * i] = v.x;
+          dst[2 * i + 1] = v.y;
+        }
+      };
       float pr[64];
       tmem_ld32(tST + cb, *reinterpret_cast<uint32_t(*)[32]>(pr));
       tmem_ld32(tST + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(pr + 32));
+      uint64_t nlp[16];
+      load_stats(lse_u, nlp);
       tmem_wait_ld();
       // P^T[r][q] = exp2(scale2 * S^T - LSE2_q); causal: zero where query
       // qt*128 + q does not see key kt*128 + r, i.e. q < r + (kt - qt)*128 - coff.
@@ -558,14 +570,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t pk[16];
-        // statistics four at a time (one 16-byte broadcast load per two pairs)
-        uint64_t nlp[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(lse_u + c0 + 4 * i);
-          nlp[2 * i] = v.x;
-          nlp[2 * i + 1] = v.y;
-        }
+        if (c0 > 0) load_stats(lse_u + c0, nlp);
         // two queries per paired FMA: scale2 * s - LSE2 (the shared copy holds -LSE2)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -585,9 +590,10 @@ __global__ void __launch_bounds__(448, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P));
       // dS^T = P^T o (dP^T - D), with P^T the bf16 values dV multiplied
+      // The dS buffer is the A operand of dQ_{U-1}, which has completed
+      // when dP^T_U has: the MMA warp issues dP^T_U after it, and the commit
+      // behind B_DPT covers every MMA issued before.
       if (!(ok = warp_wait_b(bar(B_DPT), U & 1, p.ctl, abort, 31))) break;
-      // the dS buffer is the A operand of dQ_{U-1}: wait until it is read
-      if (U > 0 && !(ok = warp_wait_b(bar(B_DQF), (U - 1) & 1, p.ctl, abort, 32))) break;
       tc_fence_after();
       const uint32_t srow = sDS + (uint32_t)h * 16384u + (uint32_t)r * 128u;
       const uint32_t sw = (uint32_t)(r & 7);
@@ -597,15 +603,10 @@ __global__ void __launch_bounds__(448, 1)
         uint32_t dp[32], pp[16];
         tmem_ld32(tDPT + cb + c0, dp);
         tmem_ld16(tST + cb + c0 / 2, pp);
+        uint64_t ndp[16];
+        load_stats(d_u + c0, ndp);  // while the TMEM loads are in flight
         tmem_wait_ld();
         uint32_t pk[16];
-        uint64_t ndp[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(d_u + c0 + 4 * i);
-          ndp[2 * i] = v.x;
-          ndp[2 * i + 1] = v.y;
-        }
         // two queries per paired add and multiply: (dP - D) * P (the shared
         // copy holds -D)
 #pragma unroll
