@@ -57,12 +57,12 @@ E2E_CHUNKS = 8
 NCU_TRAFFIC = {
     # captured on the whole workload (B = 64)
     "gpt2_medium_B64_H16_N1024_d64": {
-        "bytes": 2151340800.0, "capture_B": 64,
-        "sources_sha256": "3cb5603437fce17ee3c1c7ef890ab4429cbb9889345d10a99675727db9001493"},
+        "bytes": 2152624384.0, "capture_B": 64,
+        "sources_sha256": "8db46b3cfcd96cc6a996de77c953a2c749460ce14e54d016e973b3b0b7bfec6e"},
     # captured at B = 1, scaled by B (the heads are independent)
     "long_causal_B4_H32_N8192_d128": {
-        "bytes": 1011032576.0, "capture_B": 1,
-        "sources_sha256": "3cb5603437fce17ee3c1c7ef890ab4429cbb9889345d10a99675727db9001493"},
+        "bytes": 1007949824.0, "capture_B": 1,
+        "sources_sha256": "8db46b3cfcd96cc6a996de77c953a2c749460ce14e54d016e973b3b0b7bfec6e"},
 }
 BWD_SOURCES = ("fa_api.cu", "fa_bwd.cu", "fa_bwd_d64.cu", "fa_kernels.h", "sm103_ptx.cuh")
 DEFAULT_WORKLOAD = "long_causal"
