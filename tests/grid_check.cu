@@ -20,6 +20,15 @@ int main(int argc, char** argv) {
     printf("%d\n", fa::head_group(atoi(argv[2]), atoi(argv[3]), atoi(argv[4])));
   } else if (what[0] == 'p') {  // persistent_launch causal sparse tiles
     printf("%d\n", (int)fa::persistent_launch(atoi(argv[2]) != 0, atoi(argv[3]) != 0, atoi(argv[4])));
+  } else if (what[0] == 'u') {  // decode_pair BH tiles -> one "bh rank" line per L
+    const int BH = atoi(argv[2]), tiles = atoi(argv[3]);
+    for (int L = 0; L < BH * tiles; ++L) {
+      const fa::GridPos p = fa::decode_pair(L, tiles);
+      printf("%d %d\n", p.bh, p.rank);
+    }
+  } else if (what[0] == 'l') {  // pair_launch causal sparse square tiles items sms max_tiles
+    printf("%d\n", (int)fa::pair_launch(atoi(argv[2]) != 0, atoi(argv[3]) != 0, atoi(argv[4]) != 0,
+                                       atoi(argv[5]), atol(argv[6]), atoi(argv[7]), atoi(argv[8])));
   }
   return 0;
 }

@@ -55,3 +55,36 @@ def test_head_group_and_persistence_rule(harness):
     rule = lambda c, s, t: harness("p", c, s, t)[0][0]
     assert rule(0, 0, 64) == 1 and rule(1, 0, 16) == 1 and rule(1, 0, 17) == 0
     assert rule(0, 1, 4) == 0 and rule(1, 1, 4) == 0
+
+
+@pytest.mark.parametrize("BH,tiles", [(1, 2), (3, 32), (40, 64), (7, 18)])
+def test_decode_pair_units_cover_every_item_with_equal_causal_work(harness, BH, tiles):
+    """Item 2u + s is key tile j (s = 0) or tiles-1-j (s = 1) of head
+    u / (tiles/2), j = u mod tiles/2: every (head, tile) appears once, and
+    under a square causal mask (key tile kt sees tiles - kt query tiles) every
+    unit sees tiles + 1 query tiles."""
+    pos = harness("u", BH, tiles)
+    assert sorted(map(tuple, pos)) == [(h, r) for h in range(BH) for r in range(tiles)]
+    for u in range(BH * tiles // 2):
+        (h0, r0), (h1, r1) = pos[2 * u], pos[2 * u + 1]
+        assert h0 == h1 == u // (tiles // 2) and r0 == u % (tiles // 2) and r1 == tiles - 1 - r0
+        assert (tiles - r0) + (tiles - r1) == tiles + 1
+
+
+def test_pair_launch_rule(harness):
+    """Causal, dense and square only; tile counts between the persistent
+    rule's limit (16) and the kernel's maximum, even; units at least one per
+    SM and filling the last wave of CTAs to 95 % or more."""
+    rule = lambda *a: harness("l", *a)[0][0]
+    # the long causal bench shape: 128 heads x 64 key tiles, 4096 units on 152 SMs (27 waves, 99.8 %)
+    assert rule(1, 0, 1, 64, 128 * 64, 152, 64) == 1
+    assert rule(0, 0, 1, 64, 128 * 64, 152, 64) == 0       # not causal
+    assert rule(1, 1, 1, 64, 128 * 64, 152, 64) == 0       # block-sparse
+    assert rule(1, 0, 0, 64, 128 * 64, 152, 64) == 0       # query and key lengths differ
+    assert rule(1, 0, 1, 16, 4096 * 16, 152, 64) == 0      # the persistent rule covers it
+    assert rule(1, 0, 1, 63, 128 * 63, 152, 64) == 0       # odd tile count
+    assert rule(1, 0, 1, 128, 64 * 128, 152, 64) == 0      # beyond the kernel's maximum
+    assert rule(1, 0, 1, 128, 64 * 128, 152, 128) == 1
+    assert rule(1, 0, 1, 32, 16 * 32, 152, 64) == 0        # 256 units: 2 waves, 84 % full
+    assert rule(1, 0, 1, 32, 8 * 32, 152, 64) == 0         # 128 units: fewer than SMs
+    assert rule(1, 0, 1, 32, 128 * 32, 152, 64) == 1       # 2048 units: 14 waves, 96 % full
