@@ -48,9 +48,11 @@ def gives_up(fn):
     (1, 2, 4096, 64, False), (1, 2, 4096, 128, False),
     # more work items than SMs: the persistent kernels, at d = 64 the
     # forward that stages O through its second Q buffers, at d = 128 the
-    # backward with three Q slots and one dO slot, and (causal) that
-    # backward walking units of two key tiles
-    (8, 20, 1024, 64, False), (8, 20, 1024, 128, False), (2, 20, 4096, 128, True)])
+    # backward with three Q slots and one dO slot, and (causal, 19 heads of 16
+    # units: two full waves on 152 SMs) both backward kernels walking units
+    # of two key tiles
+    (8, 20, 1024, 64, False), (8, 20, 1024, 128, False),
+    (1, 19, 4096, 64, True), (1, 19, 4096, 128, True)])
 def test_wait_bound_runs_out_then_a_normal_call_succeeds(B, H, N, d, causal):
     # long enough that the pipelines' producers wait for free slots (a wait
     # that ends within one poll of the barrier cannot run out)
