@@ -826,9 +826,9 @@ cudaError_t launch_bwd_main(const BwdLaunch& a, cudaStream_t stream) {
   // one persistent CTA per SM walks the items (with the three-Q-slot ring,
   // measured faster there), or one CTA per item; long square causal
   // launches in units of two key tiles (pair_launch; measured +4 % at 32 key
-  // tiles per head, +1.5 % at 64, -0.5 % at 128)
+  // tiles per head, +1.5 % at 64, +1.3 % at 128, -0.9 % at 256)
   const long n_items = (long)p.nkv * p.BHkv;
-  const bool pairs = pair_launch(CAUSAL, SPARSE, a.Nq == a.Nk, p.nkv, n_items, a.num_sms, 64);
+  const bool pairs = pair_launch(CAUSAL, SPARSE, a.Nq == a.Nk, p.nkv, n_items, a.num_sms, 128);
   const bool pers = pairs || (persistent_launch(CAUSAL, SPARSE, p.nkv) && n_items > a.num_sms);
   const long ctas = pers ? a.num_sms : n_items;
   auto kern = fa_bwd_kernel<HD, CAUSAL, SPARSE, 0>;
